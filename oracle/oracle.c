@@ -1,0 +1,248 @@
+/*
+ * oracle.c -- plain fp64 CPU oracle for the paged INT8 group-64 KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by tests/, the smoke check and the
+ * benchmark's CPU-baseline leg; never by the CUDA product path. Shares no code
+ * with it. See oracle.h for the definitions and the readings of the pages.
+ *
+ * Written for obviousness, not speed: each step follows the definition in the
+ * order it is stated, with no blocking, fusion or reordering. The only
+ * parallelism is an OpenMP loop over independent units (tokens, query rows).
+ *
+ * Build: gcc -O2 -fno-fast-math -ffp-contract=off -fopenmp -shared -fPIC
+ */
+#include "oracle.h"
+
+#include <fenv.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define GROUP 64 /* channels per quantization group ("INT8 group-64") */
+
+static void ensure_round_to_nearest(void) {
+  if (fegetround() != FE_TONEAREST) fesetround(FE_TONEAREST);
+}
+
+double oracle_bf16_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+uint16_t oracle_double_to_bf16(double x) {
+  /* bf16: 8 significant bits, exponent range of fp32, subnormal quantum 2^-133. */
+  ensure_round_to_nearest();
+  if (isnan(x)) return 0x7fc0;
+  double r;
+  if (x == 0.0) {
+    r = x;
+  } else {
+    int e;
+    double m = frexp(x, &e); /* x = m * 2^e, 0.5 <= |m| < 1 */
+    if (e - 1 < -126) {
+      r = nearbyint(ldexp(x, 133)) * ldexp(1.0, -133);
+    } else {
+      r = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+    }
+    if (fabs(r) >= ldexp(1.0, 128)) r = copysign(INFINITY, x);
+  }
+  float f = (float)r; /* exact: r is a bf16 value */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(u >> 16);
+}
+
+void oracle_round_bf16(const double* x, size_t n, uint16_t* out) {
+  for (size_t i = 0; i < n; ++i) out[i] = oracle_double_to_bf16(x[i]);
+}
+
+float oracle_quantize_group(const uint16_t* x, int n, int8_t* q) {
+  ensure_round_to_nearest();
+  /* absmax of the group (bf16 widens exactly) */
+  double a = 0.0;
+  for (int i = 0; i < n; ++i) {
+    double v = fabs(oracle_bf16_to_double(x[i]));
+    if (v > a) a = v;
+  }
+  /* s = a / 127 in fp32. The fp64 quotient rounded once more to fp32 is the
+   * correctly rounded fp32 quotient (53 >= 2*24 + 2). */
+  float s = (a == 0.0) ? 1.0f : (float)(a / 127.0);
+  for (int i = 0; i < n; ++i) {
+    /* fp32 quotient x / s, again exact through fp64 */
+    float r = (float)(oracle_bf16_to_double(x[i]) / (double)s);
+    double k = nearbyint((double)r); /* ties to even */
+    if (k > 127.0) k = 127.0;
+    if (k < -127.0) k = -127.0;
+    q[i] = (int8_t)k;
+  }
+  return s;
+}
+
+size_t oracle_chunk_bytes(int page_size, int head_dim) {
+  size_t P = (size_t)page_size, D = (size_t)head_dim, g = D / GROUP;
+  return P * D + P * g * sizeof(float) + P * D + P * g * sizeof(float);
+}
+
+size_t oracle_pool_bytes(int num_pages, int page_size, int num_kv_heads, int head_dim) {
+  return (size_t)num_pages * (size_t)num_kv_heads * oracle_chunk_bytes(page_size, head_dim);
+}
+
+/* Addresses inside one (page, head) chunk. */
+typedef struct {
+  int8_t* kc;
+  float* ks;
+  int8_t* vc;
+  float* vs;
+} chunk_ptrs;
+
+static chunk_ptrs chunk_at(const uint8_t* pool, int page, int head, int num_kv_heads, int P, int D) {
+  size_t g = (size_t)D / GROUP;
+  uint8_t* base = (uint8_t*)pool + ((size_t)page * num_kv_heads + head) * oracle_chunk_bytes(P, D);
+  chunk_ptrs c;
+  c.kc = (int8_t*)base;
+  c.ks = (float*)(base + (size_t)P * D);
+  c.vc = (int8_t*)(base + (size_t)P * D + (size_t)P * g * sizeof(float));
+  c.vs = (float*)(base + 2 * (size_t)P * D + (size_t)P * g * sizeof(float));
+  return c;
+}
+
+int oracle_kv_append(uint8_t* pool, int num_pages, int page_size, int num_kv_heads, int head_dim,
+                     const int32_t* block_table, int max_pages, const int32_t* start_pos,
+                     const int32_t* cu_new, int B, const uint16_t* k, const uint16_t* v) {
+  const int P = page_size, D = head_dim, H = num_kv_heads, g = D / GROUP;
+  const int total = cu_new[B];
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(+ : bad)
+  for (int j = 0; j < total; ++j) {
+    /* which sequence owns new row j */
+    int b = 0;
+    while (b + 1 <= B && cu_new[b + 1] <= j) ++b;
+    long pos = (long)start_pos[b] + (j - cu_new[b]);
+    if (pos < 0 || pos >= (long)max_pages * P) { ++bad; continue; }
+    int page = block_table[(size_t)b * max_pages + pos / P];
+    if (page < 0 || page >= num_pages) { ++bad; continue; }
+    int slot = (int)(pos % P);
+    for (int h = 0; h < H; ++h) {
+      chunk_ptrs c = chunk_at(pool, page, h, H, P, D);
+      const uint16_t* krow = k + ((size_t)j * H + h) * D;
+      const uint16_t* vrow = v + ((size_t)j * H + h) * D;
+      for (int gr = 0; gr < g; ++gr) {
+        c.ks[(size_t)slot * g + gr] = oracle_quantize_group(krow + gr * GROUP, GROUP, c.kc + (size_t)slot * D + gr * GROUP);
+        c.vs[(size_t)slot * g + gr] = oracle_quantize_group(vrow + gr * GROUP, GROUP, c.vc + (size_t)slot * D + gr * GROUP);
+      }
+    }
+  }
+  return bad;
+}
+
+int oracle_attention_row(const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                         int head_dim, const int32_t* block_table, int max_pages,
+                         const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                         const uint16_t* q, double sm_scale, int b, int t, int i,
+                         int key_begin, int key_end, double* o, double* lse) {
+  const int P = page_size, D = head_dim, Hq = num_q_heads, H = num_kv_heads, g = D / GROUP;
+  for (int c = 0; c < D; ++c) o[c] = 0.0;
+  *lse = -INFINITY;
+  if (b < 0 || b >= B || t < 0 || t >= T || i < 0 || i >= Hq || Hq % H != 0) return 1;
+  const int G = Hq / H;   /* q-heads per kv-head */
+  const int h = i / G;    /* q-head i reads kv-head i / G */
+  const long L = ctx_lens[b];
+  if (L < T || L > (long)max_pages * P) return 1;
+  const long last = L - T + t; /* last key this query column may see */
+  long n0 = key_begin < 0 ? 0 : key_begin;
+  long n1 = (long)key_end < last + 1 ? (long)key_end : last + 1;
+  if (n1 <= n0) return 0;
+
+  const uint16_t* qrow = q + (((size_t)b * T + t) * Hq + i) * D;
+  double* z = (double*)malloc(sizeof(double) * (size_t)(n1 - n0));
+  double* kd = (double*)malloc(sizeof(double) * (size_t)D);
+  if (!z || !kd) { free(z); free(kd); return 1; }
+  int err = 0;
+
+  /* scores z_n = tau * sum_c q_c * khat_{n,c}, khat = code * scale (exact in fp64) */
+  for (long n = n0; n < n1; ++n) {
+    int page = block_table[(size_t)b * max_pages + n / P];
+    if (page < 0 || page >= num_pages) { err = 1; break; }
+    int slot = (int)(n % P);
+    chunk_ptrs c = chunk_at(pool, page, h, H, P, D);
+    for (int ch = 0; ch < D; ++ch)
+      kd[ch] = (double)c.kc[(size_t)slot * D + ch] * (double)c.ks[(size_t)slot * g + ch / GROUP];
+    double dot = 0.0;
+    for (int ch = 0; ch < D; ++ch) dot += oracle_bf16_to_double(qrow[ch]) * kd[ch];
+    z[n - n0] = sm_scale * dot;
+  }
+  if (err) { free(z); free(kd); return 1; }
+
+  /* softmax over the visible keys, then the weighted mean of vhat */
+  double m = -INFINITY;
+  for (long n = n0; n < n1; ++n) if (z[n - n0] > m) m = z[n - n0];
+  double l = 0.0;
+  for (long n = n0; n < n1; ++n) {
+    double w = exp(z[n - n0] - m);
+    int page = block_table[(size_t)b * max_pages + n / P];
+    int slot = (int)(n % P);
+    chunk_ptrs c = chunk_at(pool, page, h, H, P, D);
+    for (int ch = 0; ch < D; ++ch)
+      o[ch] += w * ((double)c.vc[(size_t)slot * D + ch] * (double)c.vs[(size_t)slot * g + ch / GROUP]);
+    l += w;
+  }
+  for (int ch = 0; ch < D; ++ch) o[ch] /= l;
+  *lse = m + log(l);
+  free(z);
+  free(kd);
+  return 0;
+}
+
+int oracle_paged_attention(const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                           int head_dim, const int32_t* block_table, int max_pages,
+                           const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                           const uint16_t* q, double sm_scale, double* out, double* lse) {
+  const long rows = (long)B * T * num_q_heads;
+  const int D = head_dim;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+  for (long r = 0; r < rows; ++r) {
+    int i = (int)(r % num_q_heads);
+    int t = (int)((r / num_q_heads) % T);
+    int b = (int)(r / ((long)num_q_heads * T));
+    double row_lse;
+    bad += oracle_attention_row(pool, num_pages, page_size, num_kv_heads, head_dim, block_table,
+                                max_pages, ctx_lens, B, T, num_q_heads, q, sm_scale, b, t, i, 0,
+                                0x7fffffff, out + (size_t)r * D, &row_lse);
+    if (lse) lse[r] = row_lse;
+  }
+  return bad;
+}
+
+void oracle_combine(const float* part_o, const float* part_lse, int S, int R, int D, double* out) {
+  for (int r = 0; r < R; ++r) {
+    double m = -INFINITY;
+    for (int s = 0; s < S; ++s)
+      if ((double)part_lse[(size_t)s * R + r] > m) m = part_lse[(size_t)s * R + r];
+    double* o = out + (size_t)r * D;
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    if (m == -INFINITY) continue; /* no visible key in any split */
+    double wsum = 0.0;
+    for (int s = 0; s < S; ++s) {
+      double ls = part_lse[(size_t)s * R + r];
+      if (ls == -INFINITY) continue;
+      double w = exp(ls - m);
+      for (int c = 0; c < D; ++c) o[c] += w * (double)part_o[((size_t)s * R + r) * D + c];
+      wsum += w;
+    }
+    for (int c = 0; c < D; ++c) o[c] /= wsum;
+  }
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
