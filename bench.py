@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of one step of the paged INT8 KV-cache hot path on GB300.
+
+A step is one pass of the whole path over one batch: kv_cache_append of the
+step's new K/V rows (quantize + scatter), then split-KV paged attention and
+its log-sum-exp combine. Inputs are seeded and synthetic (see
+quantized_paged_kv_cache_gb300/workloads.py); the cache history is appended
+once, untimed, before the timed region.
+
+Prints one JSON line. `value` is algorithmic bytes per second (int8 K/V codes
++ fp32 group scales + bf16 Q + bf16 O of the attention, plus the append's bf16
+reads and int8/fp32 writes) over all ranks; `us_per_call` is the step time.
+`--impl reference` times the fp64 CPU oracle on the same workload instead.
+
+Multi-GPU: every rank runs an independent replica (no data-path collective);
+the step time is the max over ranks and `value` sums the ranks' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged INT8-KV decode attention: µs/call and KV GB/s as % of GB300 HBM peak"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c1_decode",
+                    help="tiny | c1_decode | c8_verify | long_context | mix")
+    ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
+    ap.add_argument("--num-ctas", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_paged_kv_cache_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(d, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """dram read+write bytes per launch of the attention kernel from the committed
+    ncu summary, only if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(f"{workload}/{kernel}")
+    if not ent or ent.get("source_sha") != source_hash():
+        return None
+    return ent.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples over the load window around the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons), "window": "load window containing the timed region"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def setup_gpu(w, device, replicas, num_ctas, kernel):
+    import torch
+
+    import quantized_paged_kv_cache_gb300 as nk
+    from quantized_paged_kv_cache_gb300 import workloads as wl
+
+    bt = wl.block_table(w).to(device)
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    base = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, device=device, fill=0)
+    hist, _ = wl.history_and_step(w)
+    for b in range(w.B):
+        pos = 0
+        while pos < hist[b]:
+            n = min(16384, hist[b] - pos)
+            k, v = wl.kv_rows(w, b, pos, n, device=device)
+            nk.kv_append(base, bt[b:b + 1].contiguous(), torch.tensor([pos], dtype=torch.int32, device=device),
+                         torch.tensor([0, n], dtype=torch.int32, device=device), k, v, status=status)
+            pos += n
+    pools = [base] + [nk.KVPool(base.storage.clone(), w.num_pages, w.P, w.Hkv, w.D) for _ in range(replicas - 1)]
+    starts, _ = wl.history_and_step(w)
+    k, v, sp, cu = wl.append_batch(w, starts, [w.append_len] * w.B, device=device)
+    q = wl.queries(w, device=device)
+    nct = num_ctas
+    ws_bytes = nk.decode_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D, nct)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    out = torch.empty_like(q)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"history append flagged device status {int(status.item())}")
+    return dict(bt=bt, ctx=ctx, status=status, pools=pools, k=k, v=v, sp=sp.to(device), cu=cu.to(device), q=q,
+                ws=ws, out=out, nct=nct, kernel=kernel)
+
+
+def run_ours(args, w, rank, world, device):
+    import torch
+
+    import quantized_paged_kv_cache_gb300 as nk
+
+    pool_bytes = nk.kv_pool_bytes(w.num_pages, w.P, w.Hkv, w.D)
+    replicas = 1 if pool_bytes >= 2 * L2_BYTES else int(-(-2 * L2_BYTES // pool_bytes)) + 1
+    S = setup_gpu(w, device, replicas, args.num_ctas, args.kernel)
+    dec = nk.paged_decode_attn if args.kernel == "mma" else nk.paged_decode_attn_simt
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev_a=None, ev_b=None):
+        pool = S["pools"][i % replicas]
+        nk.kv_append(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        dec(pool, S["q"], S["bt"], S["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
+            out=S["out"], status=S["status"], stream=stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    # keep the GPU loaded ~0.5 s so the clock samples cover the timed region
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    t_end = time.perf_counter() + 0.5
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+
+    K = args.steps
+    evs_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    evs_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for j in range(K):
+        step(j, evs_a[j], evs_b[j])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = e0.elapsed_time(e1)
+    attn_ms = [a.elapsed_time(b) for a, b in zip(evs_a, evs_b)]
+    if int(S["status"].item()) != 0:
+        raise RuntimeError(f"device status {int(S['status'].item())} during the benchmark")
+
+    ms = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    step_bytes = w.attn_bytes() + w.append_bytes()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, S, dec, replicas, step_bytes, world, device)
+
+    return dict(ms=ms, attn_ms=attn_ms, clocks=clocks, step_bytes=step_bytes, replicas=replicas,
+                pool_bytes=pool_bytes, e2e=e2e, nct=S["nct"])
+
+
+def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
+    """The same step through the public API from pinned host buffers: every
+    step copies its inputs (new K/V rows, Q, positions, lengths) host->device,
+    runs append + attention, and reads the output back device->host."""
+    import torch
+
+    import quantized_paged_kv_cache_gb300 as nk
+
+    h = {name: S[name].cpu().pin_memory() for name in ("k", "v", "q", "sp", "cu", "ctx")}
+    dev = {name: torch.empty_like(S[name]) for name in h}
+    out_h = torch.empty(S["out"].shape, dtype=S["out"].dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    bi = sum(t.numel() * t.element_size() for t in h.values())
+    bo = out_h.numel() * out_h.element_size()
+
+    def step(i):
+        for name in h:
+            dev[name].copy_(h[name], non_blocking=True)
+        pool = S["pools"][i % replicas]
+        nk.kv_append(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], status=S["status"], stream=stream)
+        dec(pool, dev["q"], S["bt"], dev["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
+            out=S["out"], status=S["status"], stream=stream)
+        out_h.copy_(S["out"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    K = args.steps
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for j in range(K):
+        step(j)
+    el = (time.perf_counter() - t0) * 1e3 / K
+    if world > 1:
+        t = torch.tensor([el], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        el = float(t.item())
+    return {"value": round(step_bytes * world / (el * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "ms_per_step": round(el, 5), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "sync": "host waits for each step's output"}
+
+
+# ---------------------------------------------------------------------------
+# the oracle (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleStep:
+    """The fp64 oracle on a bounded sample of the workload: the step's append
+    of every new row, and the attention of `rows` query rows (all rows of the
+    first kv-heads) over their full contexts."""
+
+    def __init__(self, w, max_rows=None):
+        import numpy as np
+        import torch
+
+        import oracle
+        from quantized_paged_kv_cache_gb300 import workloads as wl
+
+        self.w, self.oracle, self.np = w, oracle, np
+        self.bt = wl.block_table(w)
+        self.pool = oracle.new_pool(w.num_pages, w.P, w.Hkv, w.D)
+        hist, _ = wl.history_and_step(w)
+        for b in range(w.B):
+            pos = 0
+            while pos < hist[b]:
+                n = min(16384, hist[b] - pos)
+                k, v = wl.kv_rows(w, b, pos, n, device="cpu")
+                oracle.kv_append(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt[b:b + 1], [pos], [0, n], k, v)
+                pos += n
+        starts, _ = wl.history_and_step(w)
+        self.k, self.v, self.sp, self.cu = wl.append_batch(w, starts, [w.append_len] * w.B, device="cpu")
+        self.q = wl.queries(w, device="cpu")
+        all_rows = [(b, t, i) for b in range(w.B) for t in range(w.T) for i in range(w.Hq)]
+        self.rows = all_rows if max_rows is None else all_rows[:max_rows]
+        self.frac_rows = len(self.rows) / len(all_rows)
+        self.threads = oracle.num_threads()
+        # algorithmic bytes of this sample: the whole append, and the KV bytes
+        # each sampled row's kv-head stream would read, pro rata per row
+        self.bytes = w.append_bytes() + w.attn_bytes() * self.frac_rows
+        del torch
+
+    def __call__(self):
+        w, oracle = self.w, self.oracle
+        oracle.kv_append(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, self.sp, self.cu, self.k, self.v)
+        if self.frac_rows == 1.0:
+            oracle.paged_attention(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T, w.Hq,
+                                   w.sm_scale)
+        else:
+            for (b, t, i) in self.rows:
+                oracle.attention_row(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T,
+                                     w.Hq, w.sm_scale, b, t, i)
+
+    def sample_text(self):
+        return (f"{len(self.rows)} of {self.w.B * self.w.T * self.w.Hq} query rows over their full contexts "
+                f"+ the step's whole append ({self.w.append_rows()} rows); bytes counted pro rata")
+
+
+def pick_rows(w, budget_s=2.0):
+    """Rows for a bounded oracle step: roughly budget_s of single-row work per
+    thread at ~2 ns per key-channel (fp64), never fewer than one kv-head group."""
+    import oracle
+
+    threads = max(1, oracle.num_threads())
+    per_row = max(w.ctx_lens) * w.D * 2e-9
+    rows = max(w.G, int(budget_s * threads / max(per_row, 1e-9)))
+    total = w.B * w.T * w.Hq
+    return None if rows >= total else rows
+
+
+def cpu_baseline(w):
+    st = OracleStep(w, pick_rows(w, budget_s=4.0))
+    st()  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        st()
+        n += 1
+        if time.perf_counter() - t0 > 8.0 or n >= 3:
+            break
+    el = (time.perf_counter() - t0) / n
+    return {"value": round(st.bytes / el / 1e9, 4), "unit": "GB/s", "cores": st.threads, "kind": "oracle",
+            "sample": st.sample_text(), "s_per_step": round(el, 4)}
+
+
+def run_reference(args, w):
+    st = OracleStep(w, pick_rows(w, budget_s=0.5))
+    for _ in range(max(args.warmup, 3)):
+        st()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st()
+    el = (time.perf_counter() - t0) / args.steps
+    val = st.bytes / el / 1e9
+    cb = {"value": round(val, 4), "unit": "GB/s", "cores": st.threads, "kind": "oracle", "sample": st.sample_text()}
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, "host"), "cpu_baseline": cb,
+            "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def config_dict(w, l2):
+    return {"workload": w.name, "B": w.B, "T": w.T, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
+            "page_size": w.P, "ctx_lens": w.ctx_lens if w.B <= 8 else f"{w.B} seqs", "append_rows": w.append_rows(),
+            "l2": l2}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from quantized_paged_kv_cache_gb300 import workloads as wl
+
+    w = wl.make(args.config)
+    if args.impl == "reference":
+        if rank == 0:
+            line = json.dumps(run_reference(args, w))
+            print(line, flush=True)
+            if args.out:
+                with open(args.out, "a") as f:
+                    f.write(line + "\n")
+        return 0
+
+    import torch
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    r = run_ours(args, w, rank, world, device)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    peaks, src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    attn_us = statistics.mean(r["attn_ms"]) * 1e3
+    achieved = w.attn_bytes() / (attn_us * 1e-6) / 1e9
+    traffic = ncu_traffic(w.name, args.kernel)
+    us = r["ms"] * 1e3
+    gbs = r["step_bytes"] * world / (r["ms"] * 1e-3) / 1e9
+    l2 = (f"rotating {r['replicas']} pool copies ({r['replicas'] * r['pool_bytes'] / 2**20:.0f} MiB) > 2x L2"
+          if r["replicas"] > 1 else f"pool {r['pool_bytes'] / 2**20:.0f} MiB > 2x L2")
+    out = {
+        "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(r["ms"], 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8 KV, f16 MMA operands, f32 accumulate", "data": "synthetic",
+        "config": config_dict(w, l2),
+        "us_per_call": round(us, 3), "attn_us_per_call": round(attn_us, 3),
+        "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
+        "kernel": args.kernel, "num_ctas": r["nct"] or "default",
+        "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": 3 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "paged_decode split kernel + combine (one nk_paged_decode_attn call)",
+                     "peak_source": f"{src} hbm_gbs", "bytes_per_launch": w.attn_bytes()},
+    }
+    if not args.no_cpu_baseline and world == 1:
+        out["cpu_baseline"] = cpu_baseline(w)
+    line = json.dumps(out)
+    print(line, flush=True)
+    if args.out:
+        with open(args.out, "a") as f:
+            f.write(line + "\n")
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * nk.h -- C ABI of the paged INT8 group-64 KV cache for one GB300 (sm_103a).
+ *
+ * Three operations, all enqueued on a caller-supplied CUDA stream:
+ *   nk_kv_append          quantize new bf16 K/V rows into 64-channel int8 groups
+ *                         and scatter them into pages ("NInfer-3090" README,
+ *                         introduction: the kv_cache_append Op owns KV
+ *                         quantization; "RotorQuant KV (rk8v4)": values are
+ *                         stored from the represented bf16 source directly;
+ *                         "NInfer" README, capability list: INT8 group-64 KV).
+ *   nk_paged_decode_attn  GQA decode / small-T verify attention over the paged
+ *                         cache, dequantizing inside the kernel, split over
+ *                         pages and merged by a log-sum-exp combine
+ *                         ("NInfer-3090" README, "Choosing a KV format":
+ *                         attention re-reads the whole cache every step;
+ *                         "Decode after the small-T kernels": a verify round
+ *                         covers draft+1 token columns per sequence).
+ *   nk_attn_combine       the log-sum-exp merge of split partial results, on
+ *                         its own.
+ *
+ * Conventions for every entry point
+ *   - Pointers named *_dev are device pointers; everything else is host.
+ *   - bf16 tensors are raw 16-bit bf16 bit patterns in device memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - The library allocates no memory and never synchronizes. All buffers
+ *     (pool, tables, Q, outputs, workspace, status word) belong to the caller.
+ *   - Host-checkable argument errors return an NK_ERR_* code before anything
+ *     is launched. Errors in device-resident data (a page id outside the
+ *     pool, a position beyond the block table, ctx_len < T or > max_ctx) are
+ *     reported by OR-ing NK_DEVFLAG_* bits into *status_dev (when it is not
+ *     NULL); the affected unit is skipped and its output left unspecified.
+ *     Nothing traps. A launch failure returns NK_ERR_CUDA.
+ *
+ * Quantization (one (token, kv-head, 64-channel group) at a time; the pages
+ * name the format but not the rule, and this is the rule implemented):
+ *   a = max |x|;  s = fp32(a / 127) (IEEE division), s = 1 when a = 0;
+ *   q = clamp(round_half_even(fp32(x / s)), -127, 127).
+ *
+ * KV pool layout (one contiguous chunk per (page, kv-head), all offsets
+ * multiples of 16 bytes):
+ *   chunk = Kc[P][D] int8 | Ks[P][D/64] fp32 | Vc[P][D] int8 | Vs[P][D/64] fp32
+ *   pool  = chunk[num_pages][num_kv_heads]
+ * Position n of sequence b lives in page block_table[b][n / P], slot n % P.
+ * At P = 64, D = 256 a chunk is 34,816 bytes (544 bytes per token and head).
+ *
+ * Attention semantics: Q is [B][T][Hq][D] bf16. ctx_len[b] counts every
+ * token of sequence b including its T query tokens, whose K/V must already be
+ * appended. Query column t (0-based) sees keys 0 .. ctx_len[b] - T + t; q-head
+ * i reads kv-head i / (Hq / Hkv). Scores are sm_scale * q.k; the softmax and
+ * LSE use natural exponentials. Output O is [B][T][Hq][D] bf16 (round to
+ * nearest even).
+ */
+#ifndef NK_H
+#define NK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NK_OK = 0,
+  NK_ERR_NULL = 1,        /* a required pointer is NULL */
+  NK_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+  NK_ERR_UNSUPPORTED = 3, /* a size this build has no kernel for */
+  NK_ERR_WORKSPACE = 4,   /* the workspace is too small */
+  NK_ERR_CUDA = 5,        /* a CUDA call failed (launch or attribute) */
+  NK_ERR_DEVICE_DATA = 6, /* used by callers to report a nonzero status word */
+  NK_ERR_TIMEOUT = 7      /* used by callers to report NK_DEVFLAG_TIMEOUT */
+} nk_status;
+
+/* Bits OR-ed into *status_dev by the kernels. */
+#define NK_DEVFLAG_BAD_PAGE 0x1u    /* block-table entry outside [0, num_pages) */
+#define NK_DEVFLAG_BAD_POS 0x2u     /* append position outside the block table */
+#define NK_DEVFLAG_BAD_CTX 0x4u     /* ctx_len < T, > max_ctx or > table capacity */
+#define NK_DEVFLAG_TIMEOUT 0x8u     /* a bounded wait on an async copy gave up */
+#define NK_DEVFLAG_RANGE 0x10u      /* a Q value or an output left the fp16 range of the
+                                       tensor-core path (|Q| > 65504, or p * Vs > 65504) */
+
+/* Limits of this build. */
+#define NK_GROUP 64      /* channels per quantization group */
+#define NK_MAX_T 8       /* query tokens per sequence (decode + MTP verify) */
+#define NK_MAX_HEAD_DIM 256
+
+/* A KV pool: `base_dev` points at num_pages * num_kv_heads chunks laid out
+ * as above (16-byte aligned; 1024-byte alignment is recommended). */
+typedef struct nk_kv_pool {
+  void* base_dev;
+  int32_t num_pages;
+  int32_t page_size;    /* P: multiple of 16, 16..256 */
+  int32_t num_kv_heads; /* Hkv >= 1 */
+  int32_t head_dim;     /* D: 64, 128 or 256 */
+} nk_kv_pool;
+
+/* Bytes of one (page, kv-head) chunk, and of a whole pool. 0 for bad sizes. */
+size_t nk_kv_chunk_bytes(int32_t page_size, int32_t head_dim);
+size_t nk_kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * nk_kv_append -- quantize and scatter new K/V rows.
+ *   block_table_dev  int32 [B][max_pages_per_seq] physical page ids. Every
+ *                    page a new position falls in must already be assigned.
+ *   start_pos_dev    int32 [B]: position of sequence b's first new row.
+ *   cu_new_dev       int32 [B+1]: new rows of sequence b are rows
+ *                    cu_new[b] .. cu_new[b+1]-1 of k/v (cu_new[0] = 0,
+ *                    cu_new[B] = total_new).
+ *   k_dev, v_dev     bf16 [total_new][Hkv][D].
+ * Writes codes and scales of every (row, kv-head) into the pool. Rows whose
+ * position or page id is out of range are skipped and flagged. Two new rows
+ * that map to the same slot race (undefined which one wins).
+ */
+int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                 const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                 const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream);
+
+/*
+ * Work split of nk_paged_decode_attn. The flat list of (sequence, kv-head,
+ * page) items is cut into `num_ctas` near-equal contiguous ranges, one per
+ * CTA; each (CTA, (sequence, kv-head)) overlap produces one partial result,
+ * so there are at most num_ctas + B*Hkv - 1 partials. num_ctas <= 0 picks the
+ * default (a multiple of the device's SM count, capped by the work).
+ */
+int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size);
+
+/* Workspace bytes nk_paged_decode_attn needs for this shape and CTA count:
+ * fp32 partial outputs [num_ctas + B*Hkv][T*G][D] and their LSEs. */
+size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t num_ctas);
+
+/*
+ * nk_paged_decode_attn -- split-KV GQA attention over the paged cache.
+ *   q_dev          bf16 [B][T][Hq][D]
+ *   ctx_lens_dev   int32 [B], each in [T, max_ctx]
+ *   max_ctx        host-side upper bound of ctx_lens (sizes the work split)
+ *   num_ctas       <= 0 for the default
+ *   workspace_dev  nk_decode_workspace_bytes(...) bytes, 256-byte aligned;
+ *                  scratch, contents on entry do not matter
+ *   out_dev        bf16 [B][T][Hq][D]
+ * Runs the split kernel (tensor-core path) and then the combine on `stream`.
+ */
+int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                         int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                         int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                         void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
+                         void* stream);
+
+/* Same contract and result, computed by the fp32 CUDA-core kernel that the
+ * tensor-core path is measured against. */
+int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                              int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                              int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                              void* workspace_dev, size_t workspace_bytes, void* out_dev,
+                              int32_t* status_dev, void* stream);
+
+/*
+ * nk_attn_combine -- log-sum-exp merge of S partial results.
+ *   part_o_dev    fp32 [S][R][D]: each partial normalized by its own softmax sum
+ *   part_lse_dev  fp32 [S][R]: natural-log LSE of the partial's scaled scores,
+ *                 -inf for a partial that saw no key (weight 0)
+ *   out_dev       bf16 [R][D] = sum_s w_s * O_s / sum_s w_s, w_s = exp(lse_s - max lse)
+ * A row whose partials are all empty is written as zeros.
+ */
+int nk_attn_combine(const float* part_o_dev, const float* part_lse_dev, int32_t num_splits, int32_t rows,
+                    int32_t head_dim, void* out_dev, void* stream);
+
+/* Static string for an nk_status code. */
+const char* nk_status_string(int code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int nk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NK_H */

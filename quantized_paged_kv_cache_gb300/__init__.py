@@ -1,0 +1,151 @@
+"""Paged INT8 group-64 KV cache for one GB300: append, split-KV decode attention, combine.
+
+The functions below mirror the C ABI in ``include/nk.h`` one to one and take
+torch tensors that already live on the GPU. They only marshal arguments: the
+work runs in the library's CUDA kernels on the current CUDA stream. Nothing
+here synchronizes; errors in device data are reported through the optional
+int32 ``status`` tensor (``NK_DEVFLAG_*`` bits).
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+from ._lib import NKError, lib, nk_kv_pool, status_string  # noqa: F401
+
+NK_DEVFLAG_BAD_PAGE = 0x1
+NK_DEVFLAG_BAD_POS = 0x2
+NK_DEVFLAG_BAD_CTX = 0x4
+NK_DEVFLAG_TIMEOUT = 0x8
+GROUP = 64
+MAX_T = 8
+
+__all__ = [
+    "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_ctas",
+    "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "attn_combine", "status_string",
+]
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is not None:
+        return int(getattr(stream, "cuda_stream", stream))
+    import torch
+
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise NKError(rc, where)
+
+
+def _need_cuda(*tensors) -> None:
+    for t in tensors:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (there is no CPU path)")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def kv_chunk_bytes(page_size: int, head_dim: int) -> int:
+    return int(lib().nk_kv_chunk_bytes(page_size, head_dim))
+
+
+def kv_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().nk_kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+@dataclass
+class KVPool:
+    """A caller-owned pool: ``storage`` is a uint8 CUDA tensor of
+    ``kv_pool_bytes(...)`` bytes laid out as [page][kv-head][chunk]."""
+
+    storage: "object"
+    num_pages: int
+    page_size: int
+    num_kv_heads: int
+    head_dim: int
+
+    @classmethod
+    def empty(cls, num_pages, page_size, num_kv_heads, head_dim, device="cuda", fill: int | None = None):
+        import torch
+
+        n = kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
+        st = torch.empty(n, dtype=torch.uint8, device=device)
+        if fill is not None:
+            st.fill_(fill)
+        return cls(st, num_pages, page_size, num_kv_heads, head_dim)
+
+    def c_struct(self) -> nk_kv_pool:
+        _need_cuda(self.storage)
+        return nk_kv_pool(self.storage.data_ptr(), self.num_pages, self.page_size, self.num_kv_heads, self.head_dim)
+
+
+def kv_append(pool: KVPool, block_table, start_pos, cu_new, k, v, status=None, stream=None) -> None:
+    """Quantize k/v rows (bf16 [total_new][Hkv][D]) into the pool (nk_kv_append)."""
+    _need_cuda(block_table, start_pos, cu_new, k, v, status)
+    B = int(start_pos.numel())
+    total = int(k.shape[0]) if k.dim() > 0 else 0
+    ps = pool.c_struct()
+    rc = lib().nk_kv_append(ctypes.byref(ps), _ptr(block_table), int(block_table.shape[-1]), _ptr(start_pos),
+                            _ptr(cu_new), B, total, _ptr(k), _ptr(v), _ptr(status), _stream(stream))
+    _check(rc, "nk_kv_append")
+
+
+def decode_default_ctas(B: int, num_kv_heads: int, max_ctx: int, page_size: int) -> int:
+    return int(lib().nk_decode_default_ctas(B, num_kv_heads, max_ctx, page_size))
+
+
+def decode_workspace_bytes(B: int, T: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           num_ctas: int = 0) -> int:
+    return int(lib().nk_decode_workspace_bytes(B, T, num_q_heads, num_kv_heads, head_dim, num_ctas))
+
+
+def _decode(fn, name, pool, q, block_table, ctx_lens, sm_scale, max_ctx, num_ctas, workspace, out, status, stream):
+    import torch
+
+    _need_cuda(q, block_table, ctx_lens, workspace, out, status)
+    B, T, Hq, D = (int(s) for s in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = decode_workspace_bytes(B, T, Hq, pool.num_kv_heads, D, num_ctas)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    ps = pool.c_struct()
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = fn(ctypes.byref(ps), _ptr(q), _ptr(block_table), int(block_table.shape[-1]), _ptr(ctx_lens), B, T, Hq,
+            float(sm_scale), int(max_ctx), int(num_ctas), _ptr(workspace), wbytes, _ptr(out), _ptr(status),
+            _stream(stream))
+    _check(rc, name)
+    return out
+
+
+def paged_decode_attn(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int, num_ctas: int = 0,
+                      workspace=None, out=None, status=None, stream=None):
+    """Split-KV paged attention on tensor cores (nk_paged_decode_attn); returns out bf16 [B][T][Hq][D]."""
+    return _decode(lib().nk_paged_decode_attn, "nk_paged_decode_attn", pool, q, block_table, ctx_lens, sm_scale,
+                   max_ctx, num_ctas, workspace, out, status, stream)
+
+
+def paged_decode_attn_simt(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int,
+                           num_ctas: int = 0, workspace=None, out=None, status=None, stream=None):
+    """Same result from the fp32 CUDA-core kernel (nk_paged_decode_attn_simt)."""
+    return _decode(lib().nk_paged_decode_attn_simt, "nk_paged_decode_attn_simt", pool, q, block_table, ctx_lens,
+                   sm_scale, max_ctx, num_ctas, workspace, out, status, stream)
+
+
+def attn_combine(part_o, part_lse, out=None, stream=None):
+    """LSE merge of partials: part_o fp32 [S][R][D], part_lse fp32 [S][R] -> bf16 [R][D] (nk_attn_combine)."""
+    import torch
+
+    _need_cuda(part_o, part_lse, out)
+    S, R, D = (int(s) for s in part_o.shape)
+    if out is None:
+        out = torch.empty((R, D), dtype=torch.bfloat16, device=part_o.device)
+    rc = lib().nk_attn_combine(_ptr(part_o), _ptr(part_lse), S, R, D, _ptr(out), _stream(stream))
+    _check(rc, "nk_attn_combine")
+    return out

@@ -1,0 +1,82 @@
+"""ctypes binding of ``libnk.so`` (argument marshalling only).
+
+Every computation runs in the CUDA kernels behind the C ABI declared in
+``include/nk.h``; this module only turns torch tensors into device pointers,
+picks the current CUDA stream and raises on a nonzero status. There is no
+CPU path: if the library cannot be loaded (or built), every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NKError(RuntimeError):
+    """A nonzero nk_status returned by the C ABI."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: nk status {code} ({status_string(code)})")
+
+
+class nk_kv_pool(ctypes.Structure):
+    _fields_ = [
+        ("base_dev", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+    ]
+
+
+EXPORTS = (
+    "nk_kv_chunk_bytes",
+    "nk_kv_pool_bytes",
+    "nk_kv_append",
+    "nk_decode_default_ctas",
+    "nk_decode_workspace_bytes",
+    "nk_paged_decode_attn",
+    "nk_paged_decode_attn_simt",
+    "nk_attn_combine",
+    "nk_status_string",
+    "nk_version",
+)
+
+
+def lib() -> ctypes.CDLL:
+    """Load libnk.so, building it first when the sources are newer."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError("libnk.so is missing and could not be built")
+            L = ctypes.CDLL(path)
+            P, I32, Z, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+            pool_p = ctypes.POINTER(nk_kv_pool)
+            L.nk_kv_chunk_bytes.argtypes, L.nk_kv_chunk_bytes.restype = [I32, I32], Z
+            L.nk_kv_pool_bytes.argtypes, L.nk_kv_pool_bytes.restype = [I32, I32, I32, I32], Z
+            L.nk_kv_append.argtypes = [pool_p, P, I32, P, P, I32, I32, P, P, P, P]
+            L.nk_kv_append.restype = ctypes.c_int
+            L.nk_decode_default_ctas.argtypes, L.nk_decode_default_ctas.restype = [I32, I32, I32, I32], I32
+            L.nk_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, I32]
+            L.nk_decode_workspace_bytes.restype = Z
+            dec = [pool_p, P, P, I32, P, I32, I32, I32, F, I32, I32, P, Z, P, P, P]
+            L.nk_paged_decode_attn.argtypes, L.nk_paged_decode_attn.restype = dec, ctypes.c_int
+            L.nk_paged_decode_attn_simt.argtypes, L.nk_paged_decode_attn_simt.restype = dec, ctypes.c_int
+            L.nk_attn_combine.argtypes = [P, P, I32, I32, I32, P, P]
+            L.nk_attn_combine.restype = ctypes.c_int
+            L.nk_status_string.argtypes, L.nk_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+            L.nk_version.argtypes, L.nk_version.restype = [], ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().nk_status_string(int(code)).decode()

@@ -1,0 +1,206 @@
+// nk_api.cu -- the C ABI (declared in include/nk.h): argument checks, the
+// work split of the decode path, and kernel launches. No allocation, no
+// synchronization; every launch goes on the caller's stream.
+#include <math.h>
+
+#include "nk_decode.cuh"
+
+namespace nk {
+cudaError_t launch_kv_append(const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
+                             const int32_t* cu_new, int B, int total_new, const void* k, const void* v,
+                             int32_t* status, cudaStream_t stream);
+}
+
+using namespace nk;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool pool_ok(const nk_kv_pool* pool, int* err) {
+  if (!pool || !pool->base_dev) { *err = NK_ERR_NULL; return false; }
+  const int P = pool->page_size, D = pool->head_dim;
+  if (pool->num_pages < 1 || pool->num_kv_heads < 1 || P < 16 || P > 256 || P % 16 != 0 ||
+      !(D == 64 || D == 128 || D == 256) || !aligned(pool->base_dev, 16)) {
+    *err = NK_ERR_SHAPE;
+    return false;
+  }
+  return true;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return 0; }
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int64_t max_items(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P) {
+  return (int64_t)B * Hkv * ((max_ctx + P - 1) / P);
+}
+
+int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per_sm) {
+  const int sms = sm_count();
+  // at most two CTAs per SM: the default workspace size assumes that bound
+  const int k = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
+  int64_t n = (int64_t)(sms > 0 ? sms : 148) * k;
+  const int64_t w = max_items(B, Hkv, max_ctx, P);
+  if (w < n) n = w;
+  if (n < 1) n = 1;
+  return (int32_t)n;
+}
+
+int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
+                 int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                 void* workspace, size_t workspace_bytes, void* out, int32_t* status, void* stream, bool simt) {
+  int err = NK_OK;
+  if (!pool_ok(pool, &err)) return err;
+  if (B < 0 || T < 1 || T > NK_MAX_T || Hq < 1) return NK_ERR_SHAPE;
+  if (B == 0) return NK_OK;
+  if (!q || !bt || !ctx || !out) return NK_ERR_NULL;
+  const int Hkv = pool->num_kv_heads, D = pool->head_dim, P = pool->page_size;
+  if (Hq % Hkv != 0) return NK_ERR_SHAPE;
+  const int G = Hq / Hkv;
+  if (B > kMaxBatch) return NK_ERR_UNSUPPORTED;
+  if (max_pages < 1 || max_ctx < T || (int64_t)max_ctx > (int64_t)max_pages * P) return NK_ERR_SHAPE;
+  if (!isfinite(sm_scale)) return NK_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(out, 16)) return NK_ERR_SHAPE;
+  if (simt) {
+    if (G > 8) return NK_ERR_UNSUPPORTED;
+  } else {
+    if (!decode_mma_supported(D, T, G, P)) return NK_ERR_UNSUPPORTED;
+  }
+  const int per_sm = simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G);
+  const int32_t n = num_ctas > 0 ? num_ctas : default_ctas(B, Hkv, max_ctx, P, per_sm);
+  const size_t need = nk_decode_workspace_bytes(B, T, Hq, Hkv, D, n);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return NK_ERR_WORKSPACE;
+  if (workspace && !aligned(workspace, 16)) return NK_ERR_WORKSPACE;
+
+  DecodeParams p;
+  p.pool = reinterpret_cast<const uint8_t*>(pool->base_dev);
+  p.num_pages = pool->num_pages;
+  p.P = P;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.lay = ChunkLayout::make(P, D);
+  p.q = reinterpret_cast<const uint16_t*>(q);
+  p.bt = bt;
+  p.max_pages = max_pages;
+  p.ctx = ctx;
+  p.B = B;
+  p.T = T;
+  p.Hq = Hq;
+  p.G = G;
+  p.sm_scale = sm_scale;
+  p.scale2 = sm_scale * kLog2e;
+  p.max_ctx = max_ctx;
+  p.n_ctas = n;
+  const int64_t slots = (int64_t)n + (int64_t)B * Hkv;
+  p.part_o = reinterpret_cast<float*>(workspace);
+  p.part_lse = p.part_o + slots * G * T * D;
+  p.out = reinterpret_cast<uint16_t*>(out);
+  p.status = status;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = simt ? launch_decode_simt(p, st) : launch_decode_mma(p, st);
+  if (e != cudaSuccess) return NK_ERR_CUDA;
+  e = launch_decode_combine(p, st);
+  if (e != cudaSuccess) return NK_ERR_CUDA;
+  return NK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t nk_kv_chunk_bytes(int32_t page_size, int32_t head_dim) {
+  if (page_size < 1 || head_dim < kGroup || head_dim % kGroup != 0) return 0;
+  return (size_t)ChunkLayout::make(page_size, head_dim).chunk;
+}
+
+size_t nk_kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_pages < 0 || num_kv_heads < 1) return 0;
+  return (size_t)num_pages * (size_t)num_kv_heads * nk_kv_chunk_bytes(page_size, head_dim);
+}
+
+int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                 const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                 const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream) {
+  int err = NK_OK;
+  if (!pool_ok(pool, &err)) return err;
+  if (B < 0 || total_new < 0 || max_pages_per_seq < 1) return NK_ERR_SHAPE;
+  if (B == 0 || total_new == 0) return NK_OK;
+  if (!block_table_dev || !start_pos_dev || !cu_new_dev || !k_dev || !v_dev) return NK_ERR_NULL;
+  if (!aligned(k_dev, 16) || !aligned(v_dev, 16)) return NK_ERR_SHAPE;
+  if ((int64_t)total_new * pool->num_kv_heads * (pool->head_dim / 16) > ((int64_t)1 << 40)) return NK_ERR_SHAPE;
+  const cudaError_t e = launch_kv_append(*pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B,
+                                         total_new, k_dev, v_dev, status_dev,
+                                         reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;
+}
+
+int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {
+  if (B < 1 || num_kv_heads < 1 || max_ctx < 1 || page_size < 1) return 1;
+  return default_ctas(B, num_kv_heads, max_ctx, page_size, 1);
+}
+
+size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t num_ctas) {
+  if (B < 1 || T < 1 || num_kv_heads < 1 || num_q_heads < num_kv_heads || head_dim < 1) return 0;
+  if (num_ctas < 1) num_ctas = (sm_count() > 0 ? sm_count() : 148) * 2;
+  const int64_t G = num_q_heads / num_kv_heads;
+  const int64_t slots = (int64_t)num_ctas + (int64_t)B * num_kv_heads;
+  const int64_t rows = slots * G * T;
+  const int64_t bytes = rows * head_dim * 4 + rows * 4;
+  return (size_t)((bytes + 255) / 256 * 256);
+}
+
+int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                         int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                         int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                         size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream) {
+  return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, false);
+}
+
+int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                              int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                              int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                              void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
+                              void* stream) {
+  return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, true);
+}
+
+int nk_attn_combine(const float* part_o_dev, const float* part_lse_dev, int32_t num_splits, int32_t rows,
+                    int32_t head_dim, void* out_dev, void* stream) {
+  if (num_splits < 0 || rows < 0) return NK_ERR_SHAPE;
+  if (!(head_dim == 64 || head_dim == 128 || head_dim == 256)) return NK_ERR_UNSUPPORTED;
+  if (rows == 0) return NK_OK;
+  if (!part_o_dev || !part_lse_dev || !out_dev) return NK_ERR_NULL;
+  if (!aligned(part_o_dev, 16) || !aligned(out_dev, 16)) return NK_ERR_SHAPE;
+  const cudaError_t e = launch_attn_combine(part_o_dev, part_lse_dev, num_splits, rows, head_dim,
+                                            reinterpret_cast<uint16_t*>(out_dev),
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;
+}
+
+const char* nk_status_string(int code) {
+  switch (code) {
+    case NK_OK: return "ok";
+    case NK_ERR_NULL: return "a required pointer is NULL";
+    case NK_ERR_SHAPE: return "a size is out of range, inconsistent or misaligned";
+    case NK_ERR_UNSUPPORTED: return "no kernel for this shape";
+    case NK_ERR_WORKSPACE: return "workspace missing or too small";
+    case NK_ERR_CUDA: return "a CUDA call failed";
+    case NK_ERR_DEVICE_DATA: return "device-resident data out of range (see the status word)";
+    case NK_ERR_TIMEOUT: return "a bounded wait on an asynchronous copy gave up";
+    default: return "unknown status";
+  }
+}
+
+int nk_version(void) { return 100; }
+
+}  // extern "C"

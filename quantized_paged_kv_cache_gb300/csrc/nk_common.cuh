@@ -1,0 +1,147 @@
+// nk_common.cuh -- shared device helpers of the CUDA library (not of the oracle).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nk.h"
+
+namespace nk {
+
+constexpr int kGroup = NK_GROUP;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Byte offsets inside one (page, kv-head) chunk:
+//   Kc[P][D] int8 | Ks[P][D/64] fp32 | Vc[P][D] int8 | Vs[P][D/64] fp32
+struct ChunkLayout {
+  int64_t chunk;  // bytes per (page, head)
+  int64_t ks;     // offset of Ks
+  int64_t vc;     // offset of Vc
+  int64_t vs;     // offset of Vs
+  __host__ __device__ static ChunkLayout make(int P, int D) {
+    ChunkLayout c;
+    const int64_t g = D / kGroup;
+    c.ks = (int64_t)P * D;
+    c.vc = c.ks + (int64_t)P * g * 4;
+    c.vs = c.vc + (int64_t)P * D;
+    c.chunk = c.vs + (int64_t)P * g * 4;
+    return c;
+  }
+};
+
+__device__ __forceinline__ void flag(int32_t* status, uint32_t bits) {
+  if (status) atomicOr(reinterpret_cast<unsigned int*>(status), bits);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// ---------------------------------------------------------------------------
+// Work split shared by the decode kernels and their combine.
+// Unit u = (b, h) = (u / Hkv, u % Hkv) owns ceil(ctx_len[b] / P) pages (0 if
+// ctx_len[b] is invalid). Units are laid end to end into W page items; CTA c
+// of n takes items [floor(c W / n), floor((c+1) W / n)). Each overlap of a CTA
+// range with a unit is one segment, stored as partial slot c + u.
+// ---------------------------------------------------------------------------
+struct SplitShape {
+  int B, Hkv, P, T, max_ctx, max_pages;
+};
+
+__device__ __forceinline__ int unit_pages(const SplitShape& s, const int32_t* ctx_lens, int b) {
+  const int L = ctx_lens[b];
+  if (L < s.T || L > s.max_ctx || (int64_t)L > (int64_t)s.max_pages * s.P) return 0;
+  return (L + s.P - 1) / s.P;
+}
+
+__device__ __forceinline__ int64_t cta_begin(int64_t W, int n, int c) { return (int64_t)c * W / n; }
+
+// Largest CTA index whose range starts at or before item x (x < W).
+__device__ __forceinline__ int cta_of_item(int64_t W, int n, int64_t x) {
+  return (int)(((x + 1) * (int64_t)n - 1) / W);
+}
+
+}  // namespace nk
+
+namespace nk {
+
+constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shared memory)
+
+// Block-wide exclusive prefix of per-sequence page counts:
+// pre[b] = sum_{b' < b} pages(b'), pre[B] = total. Needs blockDim.x == 256 and
+// B <= kMaxBatch; every thread of the block must call it.
+__device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int32_t* ctx_lens, int* pre,
+                                                  int* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int v[4];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int b = tid * 4 + i;
+    v[i] = (b < s.B) ? unit_pages(s, ctx_lens, b) : 0;
+    sum += v[i];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < wid; ++w) wbase += warp_tot[w];
+  int run = wbase + incl - sum;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int b = tid * 4 + i;
+    if (b < s.B) pre[b] = run;
+    run += v[i];
+  }
+  if (tid == blockDim.x - 1) pre[s.B] = run;
+  __syncthreads();
+}
+
+// Segment of unit items handled by one CTA.
+struct Segment {
+  int b, h, u;           // sequence, kv-head, unit index b*Hkv + h
+  int page_begin;        // first logical page of the segment within the sequence
+  int page_end;          // one past the last
+  bool whole;            // the segment covers the whole unit (single partial)
+};
+
+// Iterate the segments of CTA c: call first with x = cta_begin; returns false
+// when the range is exhausted. `x` advances past the returned segment.
+__device__ __forceinline__ bool next_segment(const SplitShape& s, const int* pre, int64_t& x, int64_t x_end,
+                                             Segment& seg) {
+  if (x >= x_end) return false;
+  // sequence b with pre[b]*Hkv <= x < pre[b+1]*Hkv (skip empty sequences)
+  int lo = 0, hi = s.B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)pre[mid] * s.Hkv <= x) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int pages = pre[b + 1] - pre[b];
+  const int64_t off = x - (int64_t)pre[b] * s.Hkv;
+  const int h = (int)(off / pages);
+  const int p0 = (int)(off % pages);
+  const int64_t unit_end = (int64_t)pre[b] * s.Hkv + (int64_t)(h + 1) * pages;
+  const int64_t e = unit_end < x_end ? unit_end : x_end;
+  seg.b = b;
+  seg.h = h;
+  seg.u = b * s.Hkv + h;
+  seg.page_begin = p0;
+  seg.page_end = p0 + (int)(e - x);
+  seg.whole = (p0 == 0) && (seg.page_end == pages);
+  x = e;
+  return true;
+}
+
+}  // namespace nk

@@ -1,0 +1,46 @@
+// nk_decode.cuh -- parameters and launchers shared by the decode kernels.
+#pragma once
+
+#include "nk_common.cuh"
+
+namespace nk {
+
+struct DecodeParams {
+  const uint8_t* pool;
+  int num_pages, P, Hkv, D;
+  ChunkLayout lay;
+  const uint16_t* q;      // bf16 [B][T][Hq][D]
+  const int32_t* bt;      // [B][max_pages]
+  int max_pages;
+  const int32_t* ctx;     // [B]
+  int B, T, Hq, G;
+  float sm_scale;
+  float scale2;           // sm_scale * log2(e)
+  int max_ctx;
+  int n_ctas;
+  float* part_o;          // [n_ctas + B*Hkv][T*G][D]
+  float* part_lse;        // [n_ctas + B*Hkv][T*G]
+  uint16_t* out;          // bf16 [B][T][Hq][D]
+  int32_t* status;
+  __host__ __device__ SplitShape shape() const { return SplitShape{B, Hkv, P, T, max_ctx, max_pages}; }
+};
+
+// Flag invalid ctx lengths once (block 0 of a kernel).
+__device__ __forceinline__ void flag_bad_ctx(const DecodeParams& p) {
+  if (blockIdx.x != 0) return;
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const int L = p.ctx[b];
+    if (L < p.T || L > p.max_ctx || (int64_t)L > (int64_t)p.max_pages * p.P) flag(p.status, NK_DEVFLAG_BAD_CTX);
+  }
+}
+
+cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_attn_combine(const float* part_o, const float* part_lse, int S, int R, int D, uint16_t* out,
+                                cudaStream_t stream);
+int decode_simt_ctas_per_sm(int D, int G);
+int decode_mma_ctas_per_sm(int D, int T, int G);
+bool decode_mma_supported(int D, int T, int G, int P);
+
+}  // namespace nk

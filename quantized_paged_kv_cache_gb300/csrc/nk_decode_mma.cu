@@ -1,0 +1,82 @@
+// nk_decode_mma.cu -- host side of the tensor-core decode kernel: shape
+// support, the TMA descriptor of the pool, and dispatch to the instances
+// compiled per head_dim (nk_decode_mma_d*.cu).
+#include "nk_decode_mma.cuh"
+
+namespace nk {
+namespace mma {
+
+// Warps per team (channel split) for a head_dim and a number of 8-row tiles:
+// chosen so one warp's Q fragments and output accumulator stay near 150
+// registers.
+int channel_split(int D, int NT) {
+  if (D == 256) return NT <= 1 ? 1 : (NT <= 3 ? 2 : 4);
+  if (D == 128) return NT <= 3 ? 1 : 2;
+  return 1;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    else
+      (void)cudaGetLastError();
+  }
+  return fn;
+}
+
+// 4-D view of the pool's code bytes: [D channels][P keys][K|V][page*Hkv + h],
+// boxes of [min(D,128)][P][2][1] with the matching shared-memory swizzle.
+cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.P, 2, (cuuint64_t)p.num_pages * p.Hkv};
+  cuuint64_t strides[3] = {(cuuint64_t)p.D, (cuuint64_t)p.lay.vc, (cuuint64_t)p.lay.chunk};
+  cuuint32_t box[4] = {(cuuint32_t)(p.D < 128 ? p.D : 128), (cuuint32_t)p.P, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.pool), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        p.D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_d256(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st);
+cudaError_t launch_d128(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st);
+cudaError_t launch_d64(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st);
+
+}  // namespace mma
+
+bool decode_mma_supported(int D, int T, int G, int P) {
+  const int M = G * T;
+  if (M < 1 || M > 48 || P % 16 != 0 || P > 256) return false;
+  if (!(D == 64 || D == 128 || D == 256)) return false;
+  const int NT = (M + 7) / 8;
+  const mma::Geometry g = mma::geometry(D, NT, mma::channel_split(D, NT), P, kMaxBatch);
+  return g.stages >= 2;
+}
+
+int decode_mma_ctas_per_sm(int, int, int) { return 1; }
+
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
+  CUtensorMap map;
+  cudaError_t e = mma::make_pool_map(p, &map);
+  if (e != cudaSuccess) return e;
+  const int NT = (p.G * p.T + 7) / 8;
+  if (p.D == 256) return mma::launch_d256(map, p, NT, stream);
+  if (p.D == 128) return mma::launch_d128(map, p, NT, stream);
+  return mma::launch_d64(map, p, NT, stream);
+}
+
+}  // namespace nk

@@ -1,0 +1,672 @@
+// nk_decode_mma.cuh -- split-KV paged attention over the INT8 group-64 cache
+// on tensor cores (mma.sync m16n8k16, fp16 operands, fp32 accumulate).
+//
+// Attention re-reads the whole cache every step ("NInfer-3090" README,
+// "Choosing a KV format"), so the kernel is built to stream pages at HBM
+// speed; decode and MTP-verify rounds attend T = draft+1 columns per sequence
+// ("Decode after the small-T kernels"). The dequantization happens inside the
+// dot products: the int8 codes enter the MMAs exactly (as fp16), the group
+// scales are applied to fp32 partial sums.
+//
+// CTA layout (256 threads = 8 warps, two per SM sub-partition, so a thread
+// may hold up to 255 registers):
+//   * Loads: lane 0 of warp 0 walks the CTA's page items (sequence,
+//     kv-head, page) and, per page, issues TMA tile loads of the K and V code
+//     tiles (128-byte swizzled, [128 channels][P keys][K|V] boxes straight out
+//     of the pool by physical page id) plus 1-D bulk copies of the two scale
+//     arrays into a ring of shared-memory stages, signalled by mbarriers. It
+//     issues opportunistically before each of its own blocks (a stage whose
+//     readers are done is refilled at once) and blocks only when its own next
+//     page, or a page another warp needs before a segment ends, is missing.
+//   * Consumers: teams of CS warps. A team owns 16-key blocks of the stream
+//     (block j goes to team j % NTEAMS); its CS warps split the head_dim
+//     channels (DW = D/CS each, whole 64-channel groups), so each warp keeps
+//     only its slice of Q (as MMA B fragments) and of the output accumulator.
+//     Per block and warp:
+//       QK   S^T[key][row] = K[key][ch] Q^T[ch][row], one fp32 accumulator per
+//            64-channel group, scaled by Ks * sm_scale * log2(e) and summed
+//            (swap-AB: keys are the MMA M dimension, the G*T query rows the N
+//            dimension, so M = 24 needs no padding); K fragments come from
+//            ldmatrix on the swizzled tile and are widened int8 -> fp16 with a
+//            byte permute and one half2 subtract.
+//       team exchange of the partial scores (CS > 1) through shared memory,
+//            summed in a fixed order so every warp of the team holds identical
+//            scores.
+//       online softmax in base 2 (running max and sum per row; the
+//            accumulator is rescaled only when a row's max grows).
+//       PV   O^T[ch][row] += V^T[ch][key] P'^T[key][row] with
+//            P' = p * Vs[key][group] split into fp16 hi + lo parts (two MMAs)
+//            so the product keeps ~22 bits; V^T fragments come from
+//            ldmatrix.trans, P'^T fragments from movmatrix of the score tile.
+//     At the end of a segment (the CTA's share of one (sequence, kv-head))
+//     the teams merge through shared memory in a fixed order and the CTA
+//     writes the bf16 output (whole unit) or an fp32 partial plus LSE.
+// Every wait on an mbarrier is bounded; a timeout sets NK_DEVFLAG_TIMEOUT.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+
+#include "nk_decode.cuh"
+
+namespace nk {
+namespace mma {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = kConsumerWarps * 32;
+constexpr int kSmemLimit = 232448;  // opt-in shared memory per block on sm_100/103
+constexpr unsigned long long kWaitCycles = 4000000000ull;  // ~2 s at 2 GHz
+
+struct Geometry {
+  int stage_bytes;   // one page: K|V boxes, then Ks, Vs (rounded to 1 KB)
+  int stages;
+  int xch_off, xch_bytes;
+  int merge_off, merge_bytes;
+  int pre_off;
+  int bar_off;
+  int total;
+};
+
+__host__ __device__ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// Shared-memory plan. Needs D, NT, CS, P (and B for the prefix array).
+__host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B) {
+  Geometry g;
+  const int nteams = kConsumerWarps / CS;
+  const int kv_bytes = 2 * P * D;
+  const int sc_bytes = 2 * P * (D / kGroup) * 4;
+  g.stage_bytes = round_up(kv_bytes + sc_bytes, 1024);
+  g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
+  const int mrows = NT * 8;
+  g.merge_bytes = mrows * (D + 4) * 4 + 2 * nteams * mrows * 4;
+  const int pre_bytes = round_up((B + 1 + 16) * 4, 16);
+  const int fixed = g.xch_bytes + g.merge_bytes + pre_bytes + 8 * 2 * 8 + 1024;
+  int s = (kSmemLimit - fixed) / g.stage_bytes;
+  if (s > 8) s = 8;
+  g.stages = s;
+  int off = g.stages * g.stage_bytes;
+  g.xch_off = off;
+  off += g.xch_bytes;
+  g.merge_off = off;
+  off += g.merge_bytes;
+  g.pre_off = off;
+  off += pre_bytes;
+  g.bar_off = off;
+  off += 2 * 8 * 8;
+  g.total = off + 1024;  // slack to align the dynamic base to 1 KB
+  return g;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false after ~kWaitCycles without completion.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Two signed int8 bytes of w (selected by sel, pre-biased by ^0x80808080)
+// as an exact fp16 pair: 0x64XX is 1024 + XX, minus 1152 gives XX - 128.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t wb, uint32_t sel) {
+  const uint32_t h = prmt(wb, 0x64646464u, sel);
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6480),
+                                                                                    __ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Byte offset of (channel chunk16 `ch16`, row) inside one K|V box region of
+// a stage: boxes of 128 channels (64 for D = 64) x [K rows | V rows].
+template <int D>
+__device__ __forceinline__ uint32_t box_off(int P, int kv, int key, int ch16) {
+  if constexpr (D == 64) {
+    const int row = kv * P + key;
+    return row * 64 + (((ch16 & 3) ^ ((row >> 1) & 3)) << 4);
+  } else {
+    const int box = ch16 >> 3;
+    const int row = kv * P + key;
+    return box * (2 * P * 128) + row * 128 + (((ch16 & 7) ^ (row & 7)) << 4);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+// Issues the CTA's page loads in order. Only warp 0, lane 0 calls it.
+struct Issuer {
+  int64_t x;
+  Segment seg;
+  int pi;
+  bool have;
+  int next;   // sequence number of the next page to issue
+  int total;  // pages of this CTA
+};
+
+template <int D>
+__device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensorMap* tmap, const Issuer& is,
+                                           uint32_t dst, uint32_t fb) {
+  const int P = p.P;
+  const int kv_bytes = 2 * P * D;
+  const int sc_bytes = P * (D / kGroup) * 4;
+  const int page = __ldg(p.bt + (int64_t)is.seg.b * p.max_pages + is.pi);
+  if (page < 0 || page >= p.num_pages) {
+    flag(p.status, NK_DEVFLAG_BAD_PAGE);
+    mbar_arrive(fb);  // release the consumers; the stage keeps stale data
+    return;
+  }
+  mbar_arrive_expect_tx(fb, kv_bytes + 2 * sc_bytes);
+  const int z = page * p.Hkv + is.seg.h;
+  if constexpr (D == 64) {
+    tma_load_4d(dst, tmap, fb, 0, 0, 0, z);
+  } else {
+#pragma unroll
+    for (int bx = 0; bx < D / 128; ++bx) tma_load_4d(dst + bx * 2 * P * 128, tmap, fb, bx * 128, 0, 0, z);
+  }
+  const uint8_t* chunk = p.pool + (int64_t)z * p.lay.chunk;
+  bulk_load(dst + kv_bytes, chunk + p.lay.ks, sc_bytes, fb);
+  bulk_load(dst + kv_bytes + sc_bytes, chunk + p.lay.vs, sc_bytes, fb);
+}
+
+// Issue pages while their stage is free: without blocking, and blocking
+// (bounded) up to and including page sequence number `must_through`.
+template <int D>
+__device__ __forceinline__ void pump(const DecodeParams& p, const CUtensorMap* tmap, Issuer& is,
+                                     const SplitShape& sh, const int* pre, int64_t x_end, int must_through,
+                                     uint32_t stage0, int stage_bytes, int S, uint64_t* full_bar,
+                                     uint64_t* empty_bar, volatile int* abort_flag) {
+  while (is.next < is.total) {
+    const bool must = is.next <= must_through;
+    const int s = is.next % S;
+    const uint32_t par = ((is.next / S) & 1) ^ 1;
+    const uint32_t eb = smem_u32(&empty_bar[s]);
+    if (*abort_flag) return;
+    if (must) {
+      if (!mbar_wait(eb, par)) {
+        flag(p.status, NK_DEVFLAG_TIMEOUT);
+        *abort_flag = 1;
+        return;
+      }
+    } else if (!mbar_try_wait(eb, par)) {
+      return;
+    }
+    while (!is.have || is.pi >= is.seg.page_end) {
+      if (!next_segment(sh, pre, is.x, x_end, is.seg)) return;  // cannot happen while next < total
+      is.pi = is.seg.page_begin;
+      is.have = true;
+    }
+    issue_page<D>(p, tmap, is, stage0 + s * stage_bytes, smem_u32(&full_bar[s]));
+    ++is.pi;
+    ++is.next;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int D, int NT, int CS>
+__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                 const DecodeParams p) {
+  constexpr int NTEAMS = kConsumerWarps / CS;
+  constexpr int DW = D / CS;        // channels per warp
+  constexpr int NCH = DW / 16;      // 16-channel chunks per warp
+  constexpr int GW = DW / kGroup;   // groups per warp
+  constexpr int G_ALL = D / kGroup;
+  constexpr int MROWS = NT * 8;
+  static_assert(DW % kGroup == 0, "a warp owns whole 64-channel groups");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Geometry geo = geometry(D, NT, CS, p.P, p.B);
+  const int S = geo.stages;
+  int* pre = reinterpret_cast<int*>(smem + geo.pre_off);
+  int* warp_tot = pre + (p.B + 1);
+  volatile int* abort_flag = pre + (p.B + 1) + 8;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + geo.bar_off);
+  uint64_t* empty_bar = full_bar + 8;
+  float* xch = reinterpret_cast<float*>(smem + geo.xch_off);
+  float* mo = reinterpret_cast<float*>(smem + geo.merge_off);
+  float* tm_m = mo + MROWS * (D + 4);
+  float* tm_l = tm_m + NTEAMS * MROWS;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = p.P, BPP = P / 16;
+  const SplitShape sh = p.shape();
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), BPP * CS);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  flag_bad_ctx(p);
+  block_page_prefix(sh, p.ctx, pre, warp_tot);  // ends with __syncthreads
+
+  const int64_t W = (int64_t)pre[p.B] * p.Hkv;
+  if (W == 0) return;
+  const int64_t x_begin = cta_begin(W, p.n_ctas, blockIdx.x);
+  const int64_t x_end = cta_begin(W, p.n_ctas, blockIdx.x + 1);
+  const uint32_t stage0 = smem_u32(smem);
+  const bool issuer = (tid == 0);
+  Issuer is;
+  is.x = x_begin;
+  is.have = false;
+  is.pi = 0;
+  is.next = 0;
+  is.total = (int)(x_end - x_begin);
+  if (issuer)
+    pump<D>(p, &tmap, is, sh, pre, x_end, -1, stage0, geo.stage_bytes, S, full_bar, empty_bar, abort_flag);
+
+  const int team = warp / CS, wit = warp % CS;  // team, warp-in-team
+  const int g = lane >> 2, t4 = lane & 3;
+  const int ch0 = wit * DW;                     // first channel of this warp
+  const int grp0 = ch0 / kGroup;
+  const int G = p.G, T = p.T, M = G * T;
+  const uint32_t bias = 0x80808080u;
+  // ldmatrix lane geometry: matrix mi = lane / 8, row-in-matrix = lane % 8
+  const int lm_key = ((lane >> 3) & 1) * 8 + (lane & 7);
+  const int lm_chunk = lane >> 4;
+
+  uint32_t bq[NT][NCH][2];
+  float o[NCH][NT][4];
+  float m_run[NT][2], l_run[NT][2];
+  int row_limit_t[NT][2];  // column index t of each held row (or -1 for padding rows)
+
+  int64_t x = x_begin;
+  Segment seg;
+  int page_seq = 0, block_seq = 0;
+  while (next_segment(sh, pre, x, x_end, seg)) {
+    const int L = p.ctx[seg.b];
+    // ---- Q fragments (fp16) of this warp's channels, all rows
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = nt * 8 + g;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        uint32_t w0 = 0, w1 = 0;
+        if (r < M) {
+          const int t = r / G, hg = r % G;
+          const uint16_t* qp =
+              p.q + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch0 + c * 16 + t4 * 4;
+          const uint2 raw = *reinterpret_cast<const uint2*>(qp);
+          const float f0 = bf16_lo(raw.x), f1 = bf16_hi(raw.x), f2 = bf16_lo(raw.y), f3 = bf16_hi(raw.y);
+          if (fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))) > 65504.f)
+            flag(p.status, NK_DEVFLAG_RANGE);
+          w0 = pack_f16(f0, f1);
+          w1 = pack_f16(f2, f3);
+        }
+        bq[nt][c][0] = w0;
+        bq[nt][c][1] = w1;
+      }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r2 = nt * 8 + 2 * t4 + e;
+        row_limit_t[nt][e] = r2 < M ? r2 / G : T - 1;
+        m_run[nt][e] = -INFINITY;
+        l_run[nt][e] = 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[c][nt][k] = 0.f;
+    }
+
+    for (int pi = seg.page_begin; pi < seg.page_end; ++pi, ++page_seq) {
+      const int s = page_seq % S;
+      const uint32_t par = (page_seq / S) & 1;
+      const uint32_t st = stage0 + s * geo.stage_bytes;
+      const float* ks_s = reinterpret_cast<const float*>(smem + s * geo.stage_bytes + 2 * P * D);
+      const float* vs_s = ks_s + P * G_ALL;
+      for (int kb = 0; kb < BPP; ++kb, ++block_seq) {
+        if (block_seq % NTEAMS != team) continue;
+        if (issuer)
+          pump<D>(p, &tmap, is, sh, pre, x_end, page_seq, stage0, geo.stage_bytes, S, full_bar, empty_bar,
+                  abort_flag);
+        __syncwarp();
+        if (!*abort_flag && !mbar_wait(smem_u32(&full_bar[s]), par)) {
+          if (lane == 0) flag(p.status, NK_DEVFLAG_TIMEOUT);
+          *abort_flag = 1;
+        }
+        const int key0 = kb * 16;
+        const int pos0 = pi * P + key0;  // sequence position of the block's key 0
+        if (pos0 >= L) {                 // the block lies past ctx_len: nothing to attend
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+          continue;
+        }
+
+        // ---- QK: per-group fp32 partial dot products, scaled per key
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sc[nt][k] = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < GW; ++gi) {
+          uint32_t kw[4][2];  // [chunk in group][keys 0-7 | 8-15]
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
+            ldsm_x4(st + box_off<D>(P, 0, key0 + lm_key, c16), kw[q2 * 2][0], kw[q2 * 2][1], kw[q2 * 2 + 1][0],
+                    kw[q2 * 2 + 1][1]);
+          }
+          float acc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[nt][k] = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const uint32_t lo = kw[cc][0] ^ bias, hi = kw[cc][1] ^ bias;
+            const uint32_t a0 = i8x2_to_f16x2(lo, 0x4140), a2 = i8x2_to_f16x2(lo, 0x4342);
+            const uint32_t a1 = i8x2_to_f16x2(hi, 0x4140), a3 = i8x2_to_f16x2(hi, 0x4342);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma16816(acc[nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
+          }
+          const float k0 = ks_s[(key0 + g) * G_ALL + grp0 + gi] * p.scale2;
+          const float k1 = ks_s[(key0 + g + 8) * G_ALL + grp0 + gi] * p.scale2;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][0] = fmaf(k0, acc[nt][0], sc[nt][0]);
+            sc[nt][1] = fmaf(k0, acc[nt][1], sc[nt][1]);
+            sc[nt][2] = fmaf(k1, acc[nt][2], sc[nt][2]);
+            sc[nt][3] = fmaf(k1, acc[nt][3], sc[nt][3]);
+          }
+        }
+
+        // ---- team exchange: every warp of the team sums the CS partials in warp order
+        if constexpr (CS > 1) {
+          const int buf = (block_seq / NTEAMS) & 1;
+          float* xb = xch + (((size_t)team * 2 + buf) * CS) * (NT * 4 * 32);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) xb[(wit * NT * 4 + nt * 4 + k) * 32 + lane] = sc[nt][k];
+          named_bar(2 + team, CS * 32);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float sum = 0.f;
+#pragma unroll
+              for (int w2 = 0; w2 < CS; ++w2) {
+                const float v = (w2 == wit) ? sc[nt][k] : xb[(w2 * NT * 4 + nt * 4 + k) * 32 + lane];
+                sum = (w2 == 0) ? v : sum + v;
+              }
+              sc[nt][k] = sum;
+            }
+        }
+
+        // ---- causal / context mask (only blocks that reach past L - T)
+        const bool need_mask = pos0 + 15 > L - T;
+        bool valid[2] = {true, true};
+        if (need_mask) {
+          valid[0] = pos0 + g < L;
+          valid[1] = pos0 + g + 8 < L;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int key = g + (k >> 1) * 8;
+              const int lim = L - T + row_limit_t[nt][k & 1];
+              if (pos0 + key > lim) sc[nt][k] = -INFINITY;
+            }
+        }
+
+        // ---- online softmax (base 2)
+        float mnew[NT][2];
+        bool grow = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float mb = fmaxf(sc[nt][e], sc[nt][e + 2]);
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+            mnew[nt][e] = fmaxf(m_run[nt][e], mb);
+            grow |= mnew[nt][e] > m_run[nt][e];
+          }
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float mu = mnew[nt][e] == -INFINITY ? 0.f : mnew[nt][e];
+              const float alpha = exp2f(m_run[nt][e] - mu);
+              l_run[nt][e] *= alpha;
+#pragma unroll
+              for (int c = 0; c < NCH; ++c) {
+                o[c][nt][e] *= alpha;
+                o[c][nt][e + 2] *= alpha;
+              }
+              m_run[nt][e] = mnew[nt][e];
+            }
+        }
+        float pr[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float mu = m_run[nt][k & 1] == -INFINITY ? 0.f : m_run[nt][k & 1];
+            pr[nt][k] = exp2f(sc[nt][k] - mu);
+          }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          l_run[nt][0] += pr[nt][0] + pr[nt][2];
+          l_run[nt][1] += pr[nt][1] + pr[nt][3];
+        }
+
+        // ---- PV with P' = p * Vs split into fp16 hi + lo
+#pragma unroll
+        for (int gi = 0; gi < GW; ++gi) {
+          float v0 = vs_s[(key0 + g) * G_ALL + grp0 + gi];
+          float v1 = vs_s[(key0 + g + 8) * G_ALL + grp0 + gi];
+          v0 = valid[0] ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
+          v1 = valid[1] ? v1 : 0.f;
+          uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
+            const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
+            bh[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h01));
+            bh[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h23));
+            bl[nt][0] = movmatrix_t(l01);
+            bl[nt][1] = movmatrix_t(l23);
+          }
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            uint32_t w0, w1, w2, w3;  // chunk 2q2: keys 0-7, 8-15; chunk 2q2+1: keys 0-7, 8-15
+            const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
+            ldsm_x4_t(st + box_off<D>(P, 1, key0 + lm_key, c16), w0, w1, w2, w3);
+            const uint32_t vw[2][2] = {{w0 ^ bias, w1 ^ bias}, {w2 ^ bias, w3 ^ bias}};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = gi * 4 + q2 * 2 + h;  // warp-local chunk
+              const uint32_t a0 = i8x2_to_f16x2(vw[h][0], 0x4240), a1 = i8x2_to_f16x2(vw[h][0], 0x4341);
+              const uint32_t a2 = i8x2_to_f16x2(vw[h][1], 0x4240), a3 = i8x2_to_f16x2(vw[h][1], 0x4341);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma16816(o[c][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                mma16816(o[c][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+      }
+    }
+
+    // ---- merge the teams of this segment and write the result
+    // every page of the segment must be issued before warp 0 waits for the others
+    if (issuer)
+      pump<D>(p, &tmap, is, sh, pre, x_end, page_seq - 1, stage0, geo.stage_bytes, S, full_bar, empty_bar,
+              abort_flag);
+    // row sums: reduce the per-lane partial l over the 8 lanes of a row
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = l_run[nt][e];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l_run[nt][e] = v;
+      }
+    __syncthreads();  // previous segment's readers of mo are done
+    if (wit == 0 && g == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = nt * 8 + 2 * t4 + e;
+          tm_m[team * MROWS + r] = m_run[nt][e];
+          tm_l[team * MROWS + r] = l_run[nt][e];
+        }
+    }
+    __syncthreads();
+    float fac[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int r = nt * 8 + 2 * t4 + e;
+        float mx = -INFINITY;
+        for (int tm = 0; tm < NTEAMS; ++tm) mx = fmaxf(mx, tm_m[tm * MROWS + r]);
+        fac[nt][e] = (m_run[nt][e] == -INFINITY) ? 0.f : exp2f(m_run[nt][e] - mx);
+      }
+    for (int tm = 0; tm < NTEAMS; ++tm) {
+      if (team == tm) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = nt * 8 + 2 * t4 + (k & 1);
+              const int ch = ch0 + c * 16 + 2 * g + (k >> 1);
+              float* dst = mo + r * (D + 4) + ch;
+              const float v = o[c][nt][k] * fac[nt][k & 1];
+              *dst = (tm == 0) ? v : *dst + v;
+            }
+      }
+      __syncthreads();
+    }
+    // normalize and store
+    const int ctid = tid;  // 0 .. 255
+    for (int i = ctid; i < M * D; i += kConsumerWarps * 32) {
+      const int r = i / D, ch = i % D;
+      float mx = -INFINITY, lsum = 0.f;
+      for (int tm = 0; tm < NTEAMS; ++tm) mx = fmaxf(mx, tm_m[tm * MROWS + r]);
+      if (mx != -INFINITY)
+        for (int tm = 0; tm < NTEAMS; ++tm) {
+          const float mt = tm_m[tm * MROWS + r];
+          if (mt != -INFINITY) lsum += tm_l[tm * MROWS + r] * exp2f(mt - mx);
+        }
+      const float val = lsum > 0.f ? mo[r * (D + 4) + ch] / lsum : 0.f;
+      if (!isfinite(val)) flag(p.status, NK_DEVFLAG_RANGE);
+      const int t = r / G, hg = r % G;
+      if (seg.whole) {
+        p.out[(((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch] = f32_to_bf16(val);
+      } else {
+        const int64_t slot = (int64_t)blockIdx.x + seg.u;
+        p.part_o[(slot * M + r) * D + ch] = val;
+        if (ch == 0) p.part_lse[slot * M + r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+}
+
+}  // namespace mma
+}  // namespace nk

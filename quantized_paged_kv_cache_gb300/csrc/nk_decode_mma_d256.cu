@@ -1,0 +1,32 @@
+// nk_decode_mma_d256.cu -- tensor-core decode instances for head_dim 256
+// (one translation unit per head_dim so they compile in parallel).
+#include "nk_decode_mma.cuh"
+
+namespace nk {
+namespace mma {
+
+template <int D, int NT, int CS>
+static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
+  const Geometry geo = geometry(D, NT, CS, p.P, p.B);
+  if (geo.stages < 2 || geo.total > kSmemLimit) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, NT, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       geo.total);
+  if (e != cudaSuccess) return e;
+  decode_mma_kernel<D, NT, CS><<<p.n_ctas, kThreads, geo.total, st>>>(map, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_d256(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st) {
+  switch (NT) {
+    case 1: return launch_t<256, 1, 1>(map, p, st);
+    case 2: return launch_t<256, 2, 2>(map, p, st);
+    case 3: return launch_t<256, 3, 2>(map, p, st);
+    case 4: return launch_t<256, 4, 4>(map, p, st);
+    case 5: return launch_t<256, 5, 4>(map, p, st);
+    case 6: return launch_t<256, 6, 4>(map, p, st);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+}  // namespace mma
+}  // namespace nk

@@ -1,0 +1,215 @@
+"""Seeded synthetic workloads (shapes, tables and bf16 inputs), shared by the
+tests, the benchmark and the CPU oracle's callers.
+
+This module holds no quantization or attention arithmetic: it only draws
+random inputs with the shapes and value structure of the workloads the NInfer
+README pages describe (Qwen-27B-class GQA with 24 q-heads over 4 kv-heads and
+head_dim 256 -- "NInfer-4090" README, "What this fork changes", the
+d256-h24-kv4 shape; 4K..262,144-token depths; concurrency C1..C8; MTP3 verify
+with T = 4 columns).
+
+Every random draw comes from a torch.Generator seeded from (config seed,
+purpose), so each piece is reproducible on its own. Values are N(0, 1) in fp32
+rounded to bf16 (round to nearest even), then shaped per config:
+  * c1_decode: 4 fixed K channels per kv-head scaled x8 (outliers that stress
+    the group scales);
+  * long_context: K and V rows each scaled by an independent U(0.5, 2) factor
+    per (token, kv-head) (per-token norm spread).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    P: int
+    ctx_lens: list[int]
+    seed: int
+    # tokens each sequence appends in one step (the step's kv_cache_append)
+    append_len: int
+    # per-config input structure
+    outlier_channels: int = 0
+    outlier_scale: float = 1.0
+    token_norm_range: tuple[float, float] | None = None
+    note: str = ""
+    # filled by tables()
+    num_pages: int = 0
+    max_pages: int = 0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def max_ctx(self) -> int:
+        return max(self.ctx_lens)
+
+    def pages_of(self, b: int) -> int:
+        return (self.ctx_lens[b] + self.P - 1) // self.P
+
+    # algorithmic bytes of one attention call: int8 K/V + fp32 group scales
+    # of every visible key, bf16 Q read and bf16 O written
+    def kv_bytes(self) -> int:
+        per_key_head = 2 * self.D + 2 * (self.D // 64) * 4
+        return sum(self.ctx_lens) * self.Hkv * per_key_head
+
+    def q_bytes(self) -> int:
+        return self.B * self.T * self.Hq * self.D * 2
+
+    def attn_bytes(self) -> int:
+        return self.kv_bytes() + 2 * self.q_bytes()
+
+    # algorithmic bytes of one append call: bf16 K and V read, int8 codes and
+    # fp32 scales written
+    def append_rows(self) -> int:
+        return self.B * self.append_len
+
+    def append_bytes(self) -> int:
+        n = self.append_rows() * self.Hkv
+        return n * (2 * self.D * 2 + 2 * self.D + 2 * (self.D // 64) * 4)
+
+
+def _gen(seed: int, tag: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1_000_003 + tag)
+    return g
+
+
+def make(name: str) -> Workload:
+    """The five workloads: tiny, c1_decode, c8_verify, long_context, mix."""
+    if name == "tiny":
+        w = Workload("tiny", B=1, T=1, Hq=2, Hkv=1, D=64, P=16, ctx_lens=[256], seed=0, append_len=1,
+                     note="1 seq, 1 kv-head, 2 q-heads, head_dim 64, ctx 256, page 16, T=1")
+    elif name == "c1_decode":
+        w = Workload("c1_decode", B=1, T=1, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[32768], seed=1, append_len=1,
+                     outlier_channels=4, outlier_scale=8.0,
+                     note="C1 decode: 24 q / 4 kv heads, head_dim 256, ctx 32,768, page 64, T=1, "
+                          "4 K outlier channels per head x8")
+    elif name == "c8_verify":
+        g = _gen(2, 0, "cpu")
+        lens = torch.randint(4096, 65536 + 1, (8,), generator=g).tolist()
+        w = Workload("c8_verify", B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=lens, seed=2, append_len=4,
+                     note="MTP3 verify C8: 8 seqs, T=4 causal, ctx ~ U[4,096, 65,536]")
+    elif name == "long_context":
+        w = Workload("long_context", B=1, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[262144], seed=3, append_len=4,
+                     token_norm_range=(0.5, 2.0),
+                     note="long context C1: ctx 262,144, T=4 causal, per-token norm x U(0.5, 2)")
+    elif name == "mix":
+        w = Workload("mix", B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[131072] * 8, seed=4, append_len=1024,
+                     note="append of a 1,024-token chunk into each of 8 seqs (positions 130,048..131,071), "
+                          "then C8 x T4 attention at ctx 131,072")
+    else:
+        raise KeyError(name)
+    return tables(w)
+
+
+CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix")
+
+
+def tables(w: Workload, num_pages: int | None = None) -> Workload:
+    """Block tables: every sequence's pages drawn from one random permutation of the pool."""
+    need = sum(w.pages_of(b) for b in range(w.B))
+    w.num_pages = num_pages if num_pages is not None else need
+    w.max_pages = max(w.pages_of(b) for b in range(w.B))
+    perm = torch.randperm(w.num_pages, generator=_gen(w.seed, 1, "cpu")).to(torch.int32)
+    bt = torch.full((w.B, w.max_pages), -1, dtype=torch.int32)
+    off = 0
+    for b in range(w.B):
+        n = w.pages_of(b)
+        bt[b, :n] = perm[off:off + n]
+        off += n
+    w.extra["block_table"] = bt
+    return w
+
+
+def custom(name="custom", *, B, T, Hq, Hkv, D, P, ctx_lens, seed, append_len=None, num_pages=None,
+           outlier_channels=0, outlier_scale=1.0, token_norm_range=None) -> Workload:
+    w = Workload(name, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, P=P, ctx_lens=list(ctx_lens), seed=seed,
+                 append_len=T if append_len is None else append_len, outlier_channels=outlier_channels,
+                 outlier_scale=outlier_scale, token_norm_range=token_norm_range)
+    return tables(w, num_pages)
+
+
+def block_table(w: Workload) -> torch.Tensor:
+    return w.extra["block_table"]
+
+
+def outlier_index(w: Workload) -> torch.Tensor:
+    """[Hkv][outlier_channels] K channel indices scaled by outlier_scale."""
+    if w.outlier_channels == 0:
+        return torch.zeros((w.Hkv, 0), dtype=torch.long)
+    g = _gen(w.seed, 2, "cpu")
+    return torch.stack([torch.randperm(w.D, generator=g)[: w.outlier_channels] for _ in range(w.Hkv)])
+
+
+def kv_rows(w: Workload, b: int, start: int, n: int, device="cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """bf16 K and V rows [n][Hkv][D] for positions start .. start+n-1 of sequence b.
+
+    Rows are drawn per (sequence, 4096-position block) so any sub-range is
+    reproducible independently of how the caller slices it."""
+    blk = 4096
+    ks, vs = [], []
+    first, last = start // blk, (start + n - 1) // blk if n > 0 else start // blk - 1
+    oi = outlier_index(w)
+    for k in range(first, last + 1):
+        g = _gen(w.seed, 1000 + b * 100_000 + k, device)
+        kk = torch.randn((blk, w.Hkv, w.D), generator=g, device=device, dtype=torch.float32)
+        vv = torch.randn((blk, w.Hkv, w.D), generator=g, device=device, dtype=torch.float32)
+        if w.outlier_channels:
+            for h in range(w.Hkv):
+                kk[:, h, oi[h].to(device)] *= w.outlier_scale
+        if w.token_norm_range is not None:
+            lo, hi = w.token_norm_range
+            uk = torch.rand((blk, w.Hkv, 1), generator=g, device=device) * (hi - lo) + lo
+            uv = torch.rand((blk, w.Hkv, 1), generator=g, device=device) * (hi - lo) + lo
+            kk *= uk
+            vv *= uv
+        a = max(start, k * blk) - k * blk
+        e = min(start + n, (k + 1) * blk) - k * blk
+        ks.append(kk[a:e].to(torch.bfloat16))
+        vs.append(vv[a:e].to(torch.bfloat16))
+    if not ks:
+        z = torch.empty((0, w.Hkv, w.D), dtype=torch.bfloat16, device=device)
+        return z, z.clone()
+    return torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+
+
+def queries(w: Workload, device="cpu") -> torch.Tensor:
+    """bf16 Q [B][T][Hq][D]."""
+    g = _gen(w.seed, 3, device)
+    return torch.randn((w.B, w.T, w.Hq, w.D), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+
+def history_and_step(w: Workload):
+    """(prior lengths, step start positions): the step appends the last
+    append_len tokens of every sequence; everything before is history."""
+    starts = [L - w.append_len for L in w.ctx_lens]
+    return starts, starts
+
+
+def append_batch(w: Workload, starts: list[int], lens: list[int], device="cpu"):
+    """Concatenated rows for an append call: (k, v, start_pos int32 [B], cu_new int32 [B+1])."""
+    ks, vs, cu = [], [], [0]
+    for b in range(w.B):
+        k, v = kv_rows(w, b, starts[b], lens[b], device)
+        ks.append(k)
+        vs.append(v)
+        cu.append(cu[-1] + lens[b])
+    k = torch.cat(ks).contiguous() if ks else torch.empty((0, w.Hkv, w.D), dtype=torch.bfloat16)
+    v = torch.cat(vs).contiguous() if vs else torch.empty((0, w.Hkv, w.D), dtype=torch.bfloat16)
+    return k, v, torch.tensor(starts, dtype=torch.int32), torch.tensor(cu, dtype=torch.int32)

@@ -1,0 +1,110 @@
+"""The C ABI library loads, exports what include/nk.h declares, and rejects
+host-checkable argument errors before touching the GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import quantized_paged_kv_cache_gb300 as nk
+from quantized_paged_kv_cache_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(nk_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_function():
+    L = nk.lib()
+    decl = declared_functions()
+    assert decl, "no declarations found"
+    missing = [n for n in sorted(decl) if not hasattr(L, n)]
+    assert not missing, missing
+    assert set(_lib.EXPORTS) == decl
+
+
+def test_version_and_status_strings():
+    assert nk.lib().nk_version() >= 100
+    for code in range(8):
+        s = nk.status_string(code)
+        assert s and s != "unknown status"
+    assert nk.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("P,D,H,N", [(16, 64, 1, 16), (64, 256, 4, 512), (32, 128, 8, 3), (256, 256, 2, 7)])
+def test_pool_size_agrees_with_the_oracle_layout(P, D, H, N):
+    assert nk.kv_chunk_bytes(P, D) == oracle.chunk_bytes(P, D)
+    assert nk.kv_pool_bytes(N, P, H, D) == oracle.pool_bytes(N, P, H, D)
+    assert nk.kv_chunk_bytes(P, D) % 16 == 0
+
+
+def test_chunk_bytes_rejects_bad_sizes():
+    assert nk.kv_chunk_bytes(64, 100) == 0
+    assert nk.kv_chunk_bytes(0, 256) == 0
+
+
+def test_workspace_bytes_formula():
+    # (num_ctas + B*Hkv) partial slots of T*G rows, D fp32 + 1 fp32 LSE each, 256-byte rounded
+    n = nk.decode_workspace_bytes(8, 4, 24, 4, 256, 152)
+    rows = (152 + 32) * 6 * 4
+    assert n == ((rows * 257 * 4 + 255) // 256) * 256
+
+
+FAKE = 1 << 20  # never dereferenced: every call below fails host validation first
+
+
+def pool(num_pages=16, P=16, H=1, D=64, base=FAKE):
+    return _lib.nk_kv_pool(base, num_pages, P, H, D)
+
+
+def decode(p, T=1, Hq=2, B=1, max_ctx=64, max_pages=4, q=FAKE, out=FAKE, ws=FAKE, wsb=1 << 30, scale=0.125):
+    L = nk.lib()
+    return L.nk_paged_decode_attn(ctypes.byref(p) if p is not None else None, q, FAKE, max_pages, FAKE, B, T, Hq,
+                                  scale, max_ctx, 0, ws, wsb, out, None, None)
+
+
+def test_decode_rejects_bad_arguments():
+    E = nk
+    assert decode(None) == 1                                   # NULL pool
+    assert decode(pool(base=0)) == 1                           # NULL base
+    assert decode(pool(P=24)) == 2                             # page size not a multiple of 16
+    assert decode(pool(D=96)) == 2                             # head_dim not 64/128/256
+    assert decode(pool(), T=0) == 2
+    assert decode(pool(), T=9) == 2                            # above NK_MAX_T
+    assert decode(pool(H=2), Hq=3) == 2                        # Hq not a multiple of Hkv
+    assert decode(pool(), max_ctx=65, max_pages=4) == 2        # max_ctx beyond the table
+    assert decode(pool(), scale=float("nan")) == 2
+    assert decode(pool(), q=FAKE + 2) == 2                     # misaligned Q
+    assert decode(pool(), q=0) == 1
+    assert decode(pool(), B=2000) == 3                         # beyond the batch limit
+    assert decode(pool(), B=0) == 0                            # nothing to do
+    assert E.lib().nk_paged_decode_attn_simt(ctypes.byref(pool()), FAKE, FAKE, 4, FAKE, 1, 1, 16, 0.1, 64, 0,
+                                             FAKE, 1 << 30, FAKE, None, None) == 3  # G > 8 on CUDA cores
+
+
+def test_append_rejects_bad_arguments():
+    L = nk.lib()
+    p = pool()
+    assert L.nk_kv_append(None, FAKE, 4, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 1
+    assert L.nk_kv_append(ctypes.byref(p), None, 4, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 1
+    assert L.nk_kv_append(ctypes.byref(p), FAKE, 0, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 2
+    assert L.nk_kv_append(ctypes.byref(p), FAKE, 4, FAKE, FAKE, 1, 1, FAKE + 8, FAKE, None, None) == 2
+    assert L.nk_kv_append(ctypes.byref(p), FAKE, 4, FAKE, FAKE, 1, 0, FAKE, FAKE, None, None) == 0
+    assert L.nk_kv_append(ctypes.byref(pool(num_pages=0)), FAKE, 4, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 2
+
+
+def test_combine_rejects_bad_arguments():
+    L = nk.lib()
+    assert L.nk_attn_combine(FAKE, FAKE, 2, 4, 96, FAKE, None) == 3
+    assert L.nk_attn_combine(None, FAKE, 2, 4, 64, FAKE, None) == 1
+    assert L.nk_attn_combine(FAKE, FAKE, -1, 4, 64, FAKE, None) == 2
+    assert L.nk_attn_combine(FAKE, FAKE, 2, 0, 64, FAKE, None) == 0

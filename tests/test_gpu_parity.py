@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA kernels against the fp64 oracle on the same seeded inputs.
+
+Append: int8 codes and fp32 scales bit-exact, over the whole pool.
+Attention: max-abs <= 4e-3 and relative L2 <= 1e-3 against the oracle's fp64
+output rounded to bf16, for the tensor-core kernel and the CUDA-core kernel.
+Shapes span several pages and CTAs with ragged tails (unaligned context
+lengths and append starts), T = 1..8 causal verify columns, GQA ratios and
+page sizes; plus the degenerate cases (ctx = T, one key, empty sequences).
+"""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_paged_kv_cache_gb300 as nk
+from quantized_paged_kv_cache_gb300 import workloads as wl
+
+from _cases import ABS_TOL, REL_L2_TOL, build, compare, gpu_pool_bytes, oracle_attention_full, run_decode
+
+pytestmark = pytest.mark.gpu
+IMPLS = ["mma", "simt"]
+
+
+def small(name, B, T, Hq, Hkv, D, P, lens, seed, num_pages=None, **kw):
+    return wl.custom(name, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, P=P, ctx_lens=lens, seed=seed, num_pages=num_pages, **kw)
+
+
+SHAPES = [
+    # name,           B, T, Hq, Hkv,  D,   P, lens
+    ("tiny",          1, 1, 2, 1, 64, 16, [256]),
+    ("t1_d256",       1, 1, 24, 4, 256, 64, [1000]),
+    ("t4_d256",       2, 4, 24, 4, 256, 64, [700, 4099]),
+    ("t2_d128",       3, 2, 16, 2, 128, 32, [33, 2, 515]),
+    ("t8_d64",        2, 8, 8, 1, 64, 16, [8, 300]),       # M = 64: CUDA cores only
+    ("t8_g6",         2, 8, 12, 2, 128, 16, [9, 700]),     # M = 48: largest tensor-core tile set
+    ("t3_g8",         2, 3, 32, 4, 128, 16, [77, 1234]),
+    ("t5_mix",        4, 5, 12, 4, 256, 16, [5, 64, 65, 3000]),
+    ("t1_b8",         8, 1, 24, 4, 256, 64, [64, 1, 128, 129, 4000, 63, 1000, 2]),
+    ("t4_p128",       2, 4, 24, 4, 256, 128, [255, 1025]),
+]
+
+
+@pytest.fixture(scope="module", params=SHAPES, ids=[s[0] for s in SHAPES])
+def case(request):
+    name, B, T, Hq, Hkv, D, P, lens = request.param
+    w = small(name, B, T, Hq, Hkv, D, P, lens, seed=zlib.crc32(name.encode()) % 1000, num_pages=sum((L + P - 1) // P for L in lens) + 5)
+    c = build(w, fill=0)
+    c.ref = oracle_attention_full(c)
+    return c
+
+
+def test_append_bit_exact(case):
+    assert np.array_equal(gpu_pool_bytes(case), case.opool)
+
+
+def unsupported(w, impl):
+    """The tensor-core kernel holds at most 48 query rows (G*T) per kv-head."""
+    return impl == "mma" and w.G * w.T > 48
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_matches_oracle(case, impl):
+    if unsupported(case.w, impl):
+        with pytest.raises(nk.NKError) as ei:
+            run_decode(case, impl)
+        assert ei.value.code == 3
+        return
+    out = run_decode(case, impl)
+    torch.cuda.synchronize()
+    compare(out, case.ref, f"{case.w.name}/{impl}")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_is_deterministic_and_cta_count_independent(case, impl):
+    if unsupported(case.w, impl):
+        pytest.skip("shape outside the tensor-core kernel (checked in test_decode_matches_oracle)")
+    a = run_decode(case, impl)
+    b = run_decode(case, impl)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b), "run-to-run results differ"
+    for n in (1, 3, 7, 200):
+        o = run_decode(case, impl, num_ctas=n)
+        torch.cuda.synchronize()
+        compare(o, case.ref, f"{case.w.name}/{impl}/ctas={n}")
+
+
+def test_append_ragged_starts_and_empty_sequences():
+    """Several sequences, unaligned starts, one sequence with no new rows."""
+    w = small("ragged", 4, 1, 8, 2, 128, 16, [50, 37, 90, 17], seed=5, num_pages=20)
+    bt = wl.block_table(w).cuda()
+    pool = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, fill=0)
+    opool = oracle.new_pool(w.num_pages, w.P, w.Hkv, w.D)
+    starts = [3, 0, 17, 16]
+    lens = [40, 0, 73, 1]
+    k, v, sp, cu = wl.append_batch(w, starts, lens, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nk.kv_append(pool, bt, sp.cuda(), cu.cuda(), k, v, status=status)
+    torch.cuda.synchronize()
+    assert oracle.kv_append(opool, w.num_pages, w.P, w.Hkv, w.D, wl.block_table(w), sp, cu, k.cpu(), v.cpu()) == 0
+    assert int(status.item()) == 0
+    assert np.array_equal(pool.storage.cpu().numpy(), opool)
+
+
+def _bits_to_bf16(x: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(x.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def test_append_special_values():
+    """Exact ties, zero groups, negative zeros, huge and tiny magnitudes, and
+    every finite bf16 bit pattern, quantized bit-exactly."""
+    D, H, P = 256, 2, 16
+    rng = np.random.default_rng(3)
+    rows = []
+    # exact ties: absmax 15.875 -> s = 0.125, values k*0.125 + 0.0625
+    g = np.zeros(64, np.float32)
+    g[0] = 15.875
+    g[1:40] = (np.arange(-19, 20) * 0.125 + 0.0625).astype(np.float32)
+    rows.append(g)
+    rows.append(np.zeros(64, np.float32))                    # a = 0
+    rows.append(-np.zeros(64, np.float32))                   # negative zeros
+    rows.append((rng.standard_normal(64) * 1e30).astype(np.float32))
+    rows.append((rng.standard_normal(64) * 1e-35).astype(np.float32))
+    rows.append(np.full(64, 3.0, np.float32))                # all equal
+    groups = [torch.from_numpy(r).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16) for r in rows]
+    # every finite bf16 pattern, in groups of 64 (absmax varies per group)
+    allb = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    fin = allb[np.isfinite(oracle.bits_to_double(allb))]
+    fin = fin[rng.permutation(fin.size)]
+    pad = (-fin.size) % 64
+    fin = np.concatenate([fin, np.zeros(pad, np.uint16)])
+    groups += list(fin.reshape(-1, 64))
+    n_groups = len(groups)
+    per_row = H * D // 64
+    n_rows = (n_groups + per_row - 1) // per_row
+    flat = np.concatenate(groups + [np.zeros(64, np.uint16)] * (n_rows * per_row - n_groups))
+    k = _bits_to_bf16(flat).reshape(n_rows, H, D)
+    v = _bits_to_bf16(np.roll(flat, 64)).reshape(n_rows, H, D)
+    pages = (n_rows + P - 1) // P
+    bt = torch.arange(pages, dtype=torch.int32).flip(0)[None].contiguous()
+    pool = nk.KVPool.empty(pages, P, H, D, fill=0xAB)
+    opool = oracle.new_pool(pages, P, H, D, fill=0xAB)
+    cu = torch.tensor([0, n_rows], dtype=torch.int32)
+    sp = torch.tensor([0], dtype=torch.int32)
+    nk.kv_append(pool, bt.cuda(), sp.cuda(), cu.cuda(), k.cuda(), v.cuda())
+    torch.cuda.synchronize()
+    assert oracle.kv_append(opool, pages, P, H, D, bt, sp, cu, k, v) == 0
+    got = pool.storage.cpu().numpy()
+    assert np.array_equal(got, opool)
+
+
+def test_append_flags_bad_pages_and_positions():
+    w = small("badpg", 1, 1, 2, 1, 64, 16, [40], seed=1, num_pages=4)
+    bt = wl.block_table(w).clone()
+    bt[0, 1] = 99                           # page outside the pool
+    pool = nk.KVPool.empty(w.num_pages, 16, 1, 64, fill=0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k, v, sp, cu = wl.append_batch(w, [0], [40], device="cuda")
+    nk.kv_append(pool, bt.cuda(), sp.cuda(), cu.cuda(), k, v, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & nk.NK_DEVFLAG_BAD_PAGE
+    # rows of the valid pages still landed where the oracle puts them
+    opool = oracle.new_pool(w.num_pages, 16, 1, 64)
+    assert oracle.kv_append(opool, w.num_pages, 16, 1, 64, bt, sp, cu, k.cpu(), v.cpu()) == 16
+    assert np.array_equal(pool.storage.cpu().numpy(), opool)
+    status.zero_()
+    k1, v1, _, cu1 = wl.append_batch(w, [0], [1], device="cuda")
+    nk.kv_append(pool, bt.cuda(), torch.tensor([3 * 16], dtype=torch.int32, device="cuda"), cu1.cuda(), k1, v1,
+                 status=status)        # position past the block table (max_pages = 3)
+    torch.cuda.synchronize()
+    assert int(status.item()) & nk.NK_DEVFLAG_BAD_POS
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_flags_bad_context(impl):
+    w = small("badctx", 2, 2, 4, 2, 64, 16, [40, 30], seed=2, num_pages=8)
+    c = build(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([1, 30], dtype=torch.int32, device="cuda")   # ctx < T for sequence 0
+    out = run_decode(c, impl, ctx=ctx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & nk.NK_DEVFLAG_BAD_CTX
+    ref = oracle.paged_attention(c.opool, w.num_pages, w.P, w.Hkv, w.D, c.bt_cpu, [40, 30], c.q_cpu, w.T, w.Hq,
+                                 w.sm_scale)
+    compare(out[1], ref[1], "valid sequence next to a bad one")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_ignores_garbage_past_context(impl):
+    """Slots past ctx_len hold 0xFF bytes (NaN scales, -1 codes); the output
+    must not see them."""
+    w = small("garbage", 3, 4, 24, 4, 256, 64, [70, 129, 5], seed=9, num_pages=9)
+    c = build(w, fill=0xFF)
+    assert np.array_equal(gpu_pool_bytes(c), c.opool)
+    ref = oracle_attention_full(c)
+    out = run_decode(c, impl)
+    torch.cuda.synchronize()
+    compare(out, ref, "garbage past ctx")
+
+
+@pytest.mark.parametrize("impl", IMPLS)
+def test_decode_page_permutation_bit_identical(impl):
+    w = small("perm", 2, 4, 24, 4, 256, 64, [300, 1000], seed=4, num_pages=30)
+    c = build(w)
+    a = run_decode(c, impl)
+    perm = torch.randperm(w.num_pages, generator=torch.Generator().manual_seed(1))
+    cb = nk.kv_chunk_bytes(w.P, w.D) * w.Hkv
+    moved = torch.empty_like(c.pool.storage).view(w.num_pages, cb)
+    moved[perm.cuda()] = c.pool.storage.view(w.num_pages, cb)
+    pool2 = nk.KVPool(moved.view(-1), w.num_pages, w.P, w.Hkv, w.D)
+    bt2 = torch.where(c.bt_cpu >= 0, perm[c.bt_cpu.clamp(min=0).long()].to(torch.int32), c.bt_cpu).cuda()
+    fn = nk.paged_decode_attn if impl == "mma" else nk.paged_decode_attn_simt
+    b = fn(pool2, c.q, bt2, c.ctx, w.sm_scale, w.max_ctx)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_combine_matches_oracle():
+    rng = np.random.default_rng(21)
+    for S, R, D in [(1, 5, 64), (4, 33, 256), (7, 8, 128), (16, 100, 256)]:
+        po = rng.standard_normal((S, R, D)).astype(np.float32)
+        pl = (rng.standard_normal((S, R)) * 5).astype(np.float32)
+        pl[rng.random((S, R)) < 0.2] = -np.inf
+        if S > 1:
+            pl[:, 0] = -np.inf                    # an all-empty row -> zeros
+        out = nk.attn_combine(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda())
+        torch.cuda.synchronize()
+        ref = oracle.combine(po, pl)
+        got = out.to(torch.float64).cpu().numpy()
+        exp = oracle.bits_to_double(oracle.round_bf16(ref))
+        # one bf16 ulp at most (fp32 accumulation vs fp64)
+        assert np.all(np.abs(got - exp) <= np.abs(exp) * 2.0 ** -7 + 1e-30)
+        assert np.linalg.norm(got - exp) <= 1e-3 * max(np.linalg.norm(exp), 1e-30)
