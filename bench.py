@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for a profiler: no load pre-roll, clock sampling, e2e or CPU baseline")
     return ap.parse_args()
 
 
@@ -191,8 +193,8 @@ def run_ours(args, w, rank, world, device):
         step(i)
     torch.cuda.synchronize()
     # keep the GPU loaded ~0.5 s so the clock samples cover the timed region
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    t_end = time.perf_counter() + 0.5
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 and not args.profile else None
+    t_end = time.perf_counter() + (0.0 if args.profile else 0.5)
     i = 0
     while time.perf_counter() < t_end:
         for _ in range(50):
@@ -228,7 +230,7 @@ def run_ours(args, w, rank, world, device):
     step_bytes = w.attn_bytes() + w.append_bytes()
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.profile:
         e2e = run_e2e(args, w, S, dec, replicas, step_bytes, world, device)
 
     return dict(ms=ms, attn_ms=attn_ms, clocks=clocks, step_bytes=step_bytes, replicas=replicas,
@@ -434,7 +436,7 @@ def main():
                      "kernel": "paged_decode split kernel + combine (one nk_paged_decode_attn call)",
                      "peak_source": f"{src} hbm_gbs", "bytes_per_launch": w.attn_bytes()},
     }
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and world == 1 and not args.profile:
         out["cpu_baseline"] = cpu_baseline(w)
     line = json.dumps(out)
     print(line, flush=True)

@@ -10,18 +10,26 @@
 
 namespace nk {
 
+// Merge S partials of one row. Partial s lives in slot slot0 + s; when
+// `skip_empty` is set, slots of CTAs whose item range is empty (possible when
+// there are more CTAs than page items) are left out: they were never written.
 template <int CPL>
 __device__ __forceinline__ void merge_row(const float* part_o, const float* part_lse, int64_t slot0,
                                           int64_t slot_stride_rows, int S, int64_t row, int D, int lane,
-                                          uint16_t* out_row) {
+                                          uint16_t* out_row, int64_t W = 0, int n_ctas = 0, int c0 = 0) {
+  auto skip = [&](int s) {
+    return W > 0 && cta_begin(W, n_ctas, c0 + s) == cta_begin(W, n_ctas, c0 + s + 1);
+  };
   float mx = -INFINITY;
-  for (int s = 0; s < S; ++s) mx = fmaxf(mx, part_lse[(slot0 + s) * slot_stride_rows + row]);
+  for (int s = 0; s < S; ++s)
+    if (!skip(s)) mx = fmaxf(mx, part_lse[(slot0 + s) * slot_stride_rows + row]);
   float acc[CPL];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) acc[j] = 0.f;
   float wsum = 0.f;
   if (mx != -INFINITY) {
     for (int s = 0; s < S; ++s) {
+      if (skip(s)) continue;
       const float ls = part_lse[(slot0 + s) * slot_stride_rows + row];
       if (ls == -INFINITY) continue;
       const float wgt = expf(ls - mx);
@@ -73,7 +81,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   if (c0 == c1) return;
   const int t = r / p.G, hg = r % p.G;
   uint16_t* orow = p.out + (((int64_t)b * p.T + t) * p.Hq + h * p.G + hg) * D;
-  merge_row<CPL>(p.part_o, p.part_lse, (int64_t)c0 + u, M, c1 - c0 + 1, r, D, lane, orow);
+  merge_row<CPL>(p.part_o, p.part_lse, (int64_t)c0 + u, M, c1 - c0 + 1, r, D, lane, orow, W, p.n_ctas, c0);
 }
 
 // Standalone combine: part_o [S][R][D], part_lse [S][R] -> out [R][D].

@@ -1,0 +1,75 @@
+"""Full-size parity on the five benchmark workloads, in the launch
+configuration bench.py times (default CTA count, the step's append as one
+batched call).
+
+Codes and scales are compared bit-exactly over the whole pool; the attention
+output is compared on sampled rows the oracle computes one by one (first and
+last verify column, first, last and a middle q-head, of every sequence)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_paged_kv_cache_gb300 as nk
+from quantized_paged_kv_cache_gb300 import workloads as wl
+
+from _cases import compare
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def build_like_bench(w):
+    """History appended per sequence in 16K-token chunks, then the step's
+    append of every sequence in one call (as bench.py does), on both sides."""
+    dev = "cuda"
+    bt_cpu = wl.block_table(w)
+    bt = bt_cpu.to(dev)
+    pool = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, device=dev, fill=0)
+    opool = oracle.new_pool(w.num_pages, w.P, w.Hkv, w.D)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    hist, _ = wl.history_and_step(w)
+    for b in range(w.B):
+        pos = 0
+        while pos < hist[b]:
+            n = min(16384, hist[b] - pos)
+            k, v = wl.kv_rows(w, b, pos, n, device=dev)
+            cu = torch.tensor([0, n], dtype=torch.int32)
+            nk.kv_append(pool, bt[b:b + 1].contiguous(), torch.tensor([pos], dtype=torch.int32, device=dev),
+                         cu.to(dev), k, v, status=status)
+            assert oracle.kv_append(opool, w.num_pages, w.P, w.Hkv, w.D, bt_cpu[b:b + 1], [pos], cu, k.cpu(),
+                                    v.cpu()) == 0
+            pos += n
+    starts, _ = wl.history_and_step(w)
+    k, v, sp, cu = wl.append_batch(w, starts, [w.append_len] * w.B, device=dev)
+    nk.kv_append(pool, bt, sp.to(dev), cu.to(dev), k, v, status=status)
+    assert oracle.kv_append(opool, w.num_pages, w.P, w.Hkv, w.D, bt_cpu, sp, cu, k.cpu(), v.cpu()) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return pool, opool, bt, bt_cpu
+
+
+@pytest.mark.parametrize("name", wl.CONFIGS)
+@pytest.mark.parametrize("impl", ["mma", "simt"])
+def test_full_size(name, impl):
+    if impl == "simt" and name in ("long_context", "mix"):
+        pytest.skip("CUDA-core kernel is checked on the three smaller workloads")
+    w = wl.make(name)
+    pool, opool, bt, bt_cpu = build_like_bench(w)
+    assert np.array_equal(pool.storage.cpu().numpy(), opool), "codes/scales differ from the oracle"
+    q = wl.queries(w, device="cuda")
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fn = nk.paged_decode_attn if impl == "mma" else nk.paged_decode_attn_simt
+    out = fn(pool, q, bt, ctx, w.sm_scale, w.max_ctx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = []
+    for b in range(w.B):
+        for t in sorted({0, w.T - 1}):
+            for i in sorted({0, w.Hq // 2 + 1, w.Hq - 1}):
+                rows.append((b, t, i))
+    q_cpu = q.cpu()
+    ref = np.stack([oracle.attention_row(opool, w.num_pages, w.P, w.Hkv, w.D, bt_cpu, w.ctx_lens, q_cpu, w.T, w.Hq,
+                                         w.sm_scale, b, t, i)[0] for (b, t, i) in rows])
+    got = torch.stack([out[b, t, i] for (b, t, i) in rows])
+    compare(got, ref, f"{name}/{impl}")
