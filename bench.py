@@ -179,8 +179,10 @@ def run_ours(args, w, rank, world, device):
     dec = nk.paged_decode_attn if args.kernel == "mma" else nk.paged_decode_attn_simt
     stream = torch.cuda.current_stream()
 
-    def step(i, ev_a=None, ev_b=None):
+    def step(i, ev_a=None, ev_b=None, ev_0=None):
         pool = S["pools"][i % replicas]
+        if ev_0 is not None:
+            ev_0.record(stream)
         nk.kv_append(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
         if ev_a is not None:
             ev_a.record(stream)
@@ -205,13 +207,14 @@ def run_ours(args, w, rank, world, device):
     K = args.steps
     evs_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     evs_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    evs_0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
     for j in range(K):
-        step(j, evs_a[j], evs_b[j])
+        step(j, evs_a[j], evs_b[j], evs_0[j])
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -219,6 +222,7 @@ def run_ours(args, w, rank, world, device):
     clocks = sampler.stop() if sampler else None
     total_ms = e0.elapsed_time(e1)
     attn_ms = [a.elapsed_time(b) for a, b in zip(evs_a, evs_b)]
+    append_ms = [z.elapsed_time(a) for z, a in zip(evs_0, evs_a)]
     if int(S["status"].item()) != 0:
         raise RuntimeError(f"device status {int(S['status'].item())} during the benchmark")
 
@@ -233,7 +237,7 @@ def run_ours(args, w, rank, world, device):
     if not args.no_e2e and not args.profile:
         e2e = run_e2e(args, w, S, dec, replicas, step_bytes, world, device)
 
-    return dict(ms=ms, attn_ms=attn_ms, clocks=clocks, step_bytes=step_bytes, replicas=replicas,
+    return dict(ms=ms, attn_ms=attn_ms, append_ms=append_ms, clocks=clocks, step_bytes=step_bytes, replicas=replicas,
                 pool_bytes=pool_bytes, e2e=e2e, nct=S["nct"])
 
 
@@ -416,6 +420,7 @@ def main():
     peaks, src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     attn_us = statistics.mean(r["attn_ms"]) * 1e3
+    append_us = statistics.mean(r["append_ms"]) * 1e3
     achieved = w.attn_bytes() / (attn_us * 1e-6) / 1e9
     traffic = ncu_traffic(w.name, args.kernel)
     us = r["ms"] * 1e3
@@ -428,6 +433,9 @@ def main():
         "vs_baseline": None, "dtype": "i8 KV, f16 MMA operands, f32 accumulate", "data": "synthetic",
         "config": config_dict(w, l2),
         "us_per_call": round(us, 3), "attn_us_per_call": round(attn_us, 3),
+        "append_us_per_call": round(append_us, 3),
+        "append_gbs": round(w.append_bytes() / (append_us * 1e-6) / 1e9, 2),
+        "attn_gbs": round(achieved, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
         "kernel": args.kernel, "num_ctas": r["nct"] or "default",
         "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": 3 * args.steps,

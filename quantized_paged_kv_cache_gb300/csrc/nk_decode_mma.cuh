@@ -10,14 +10,14 @@
 //
 // CTA layout (256 threads = 8 warps, two per SM sub-partition, so a thread
 // may hold up to 255 registers):
-//   * Loads: lane 0 of warp 0 walks the CTA's page items (sequence,
-//     kv-head, page) and, per page, issues TMA tile loads of the K and V code
-//     tiles (128-byte swizzled, [128 channels][P keys][K|V] boxes straight out
-//     of the pool by physical page id) plus 1-D bulk copies of the two scale
-//     arrays into a ring of shared-memory stages, signalled by mbarriers. It
-//     issues opportunistically before each of its own blocks (a stage whose
-//     readers are done is refilled at once) and blocks only when its own next
-//     page, or a page another warp needs before a segment ends, is missing.
+//   * Loads: per page, TMA tile loads of the K and V code tiles (128-byte
+//     swizzled, [128 channels][P keys][K|V] boxes straight out of the pool by
+//     physical page id) plus 1-D bulk copies of the two scale arrays land in
+//     one stage of a shared-memory ring and complete on its "full" mbarrier.
+//     Thread 0 fills the ring; afterwards the last warp to finish reading a
+//     stage (elected by a shared-memory counter, after arriving on the
+//     stage's "empty" mbarrier) immediately loads the page S ahead into it,
+//     so no thread ever blocks to issue a load.
 //   * Consumers: teams of CS warps. A team owns 16-key blocks of the stream
 //     (block j goes to team j % NTEAMS); its CS warps split the head_dim
 //     channels (DW = D/CS each, whole 64-channel groups), so each warp keeps
@@ -63,6 +63,7 @@ struct Geometry {
   int xch_off, xch_bytes;
   int merge_off, merge_bytes;
   int pre_off;
+  int pid_off;
   int bar_off;
   int total;
 };
@@ -79,8 +80,9 @@ __host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B
   g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
   const int mrows = NT * 8;
   g.merge_bytes = mrows * (D + 4) * 4 + 2 * nteams * mrows * 4;
-  const int pre_bytes = round_up((B + 1 + 16) * 4, 16);
-  const int fixed = g.xch_bytes + g.merge_bytes + pre_bytes + 8 * 2 * 8 + 1024;
+  const int pre_bytes = round_up((B + 1 + 24) * 4, 16);
+  const int pid_bytes = 1024 * 4;
+  const int fixed = g.xch_bytes + g.merge_bytes + pre_bytes + pid_bytes + 8 * 2 * 8 + 1024;
   int s = (kSmemLimit - fixed) / g.stage_bytes;
   if (s > 8) s = 8;
   g.stages = s;
@@ -91,6 +93,8 @@ __host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B
   off += g.merge_bytes;
   g.pre_off = off;
   off += pre_bytes;
+  g.pid_off = off;
+  off += pid_bytes;
   g.bar_off = off;
   off += 2 * 8 * 8;
   g.total = off + 1024;  // slack to align the dynamic base to 1 KB
@@ -165,13 +169,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 
 __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  // not volatile: a pure register operation, so the compiler may interleave
+  // independent MMAs and hide their latency
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -216,32 +222,41 @@ __device__ __forceinline__ uint32_t box_off(int P, int kv, int key, int ch16) {
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// page loads
 // ---------------------------------------------------------------------------
-// Issues the CTA's page loads in order. Only warp 0, lane 0 calls it.
-struct Issuer {
-  int64_t x;
-  Segment seg;
-  int pi;
-  bool have;
-  int next;   // sequence number of the next page to issue
-  int total;  // pages of this CTA
-};
+constexpr int kPidCache = 1024;  // page coordinates cached in shared memory per CTA
 
+// Coordinate z = page * Hkv + h of the CTA's page number q (-1 for a page id
+// outside the pool), from the cache or, past it, from the block table.
+__device__ __forceinline__ int page_coord(const DecodeParams& p, const SplitShape& sh, const int* pre, int64_t x_begin,
+                                          int q) {
+  const int64_t x = x_begin + q;
+  int lo = 0, hi = sh.B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)pre[mid] * sh.Hkv <= x) lo = mid; else hi = mid;
+  }
+  const int pages = pre[lo + 1] - pre[lo];
+  const int64_t off = x - (int64_t)pre[lo] * sh.Hkv;
+  const int h = (int)(off / pages), pi = (int)(off % pages);
+  const int page = __ldg(p.bt + (int64_t)lo * p.max_pages + pi);
+  return (page < 0 || page >= p.num_pages) ? -1 : page * p.Hkv + h;
+}
+
+// Load the CTA's page number q into its stage: TMA boxes of the K|V codes
+// plus bulk copies of the two scale arrays, all completing on full_bar.
 template <int D>
-__device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensorMap* tmap, const Issuer& is,
-                                           uint32_t dst, uint32_t fb) {
+__device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensorMap* tmap, int z, uint32_t dst,
+                                           uint32_t fb) {
   const int P = p.P;
   const int kv_bytes = 2 * P * D;
   const int sc_bytes = P * (D / kGroup) * 4;
-  const int page = __ldg(p.bt + (int64_t)is.seg.b * p.max_pages + is.pi);
-  if (page < 0 || page >= p.num_pages) {
+  if (z < 0) {
     flag(p.status, NK_DEVFLAG_BAD_PAGE);
     mbar_arrive(fb);  // release the consumers; the stage keeps stale data
     return;
   }
   mbar_arrive_expect_tx(fb, kv_bytes + 2 * sc_bytes);
-  const int z = page * p.Hkv + is.seg.h;
   if constexpr (D == 64) {
     tma_load_4d(dst, tmap, fb, 0, 0, 0, z);
   } else {
@@ -251,39 +266,6 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
   const uint8_t* chunk = p.pool + (int64_t)z * p.lay.chunk;
   bulk_load(dst + kv_bytes, chunk + p.lay.ks, sc_bytes, fb);
   bulk_load(dst + kv_bytes + sc_bytes, chunk + p.lay.vs, sc_bytes, fb);
-}
-
-// Issue pages while their stage is free: without blocking, and blocking
-// (bounded) up to and including page sequence number `must_through`.
-template <int D>
-__device__ __forceinline__ void pump(const DecodeParams& p, const CUtensorMap* tmap, Issuer& is,
-                                     const SplitShape& sh, const int* pre, int64_t x_end, int must_through,
-                                     uint32_t stage0, int stage_bytes, int S, uint64_t* full_bar,
-                                     uint64_t* empty_bar, volatile int* abort_flag) {
-  while (is.next < is.total) {
-    const bool must = is.next <= must_through;
-    const int s = is.next % S;
-    const uint32_t par = ((is.next / S) & 1) ^ 1;
-    const uint32_t eb = smem_u32(&empty_bar[s]);
-    if (*abort_flag) return;
-    if (must) {
-      if (!mbar_wait(eb, par)) {
-        flag(p.status, NK_DEVFLAG_TIMEOUT);
-        *abort_flag = 1;
-        return;
-      }
-    } else if (!mbar_try_wait(eb, par)) {
-      return;
-    }
-    while (!is.have || is.pi >= is.seg.page_end) {
-      if (!next_segment(sh, pre, is.x, x_end, is.seg)) return;  // cannot happen while next < total
-      is.pi = is.seg.page_begin;
-      is.have = true;
-    }
-    issue_page<D>(p, tmap, is, stage0 + s * stage_bytes, smem_u32(&full_bar[s]));
-    ++is.pi;
-    ++is.next;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -307,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   int* pre = reinterpret_cast<int*>(smem + geo.pre_off);
   int* warp_tot = pre + (p.B + 1);
   volatile int* abort_flag = pre + (p.B + 1) + 8;
+  int* cnt = pre + (p.B + 1) + 9;  // [8] consumer count per stage
+  int* pid = reinterpret_cast<int*>(smem + geo.pid_off);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + geo.bar_off);
   uint64_t* empty_bar = full_bar + 8;
   float* xch = reinterpret_cast<float*>(smem + geo.xch_off);
@@ -316,12 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int P = p.P, BPP = P / 16;
+  const int per_stage = BPP * CS;  // consumer-warp arrivals per page
   const SplitShape sh = p.shape();
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), BPP * CS);
+      mbar_init(smem_u32(&empty_bar[s]), per_stage);
+      cnt[s] = 0;
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -333,16 +319,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   if (W == 0) return;
   const int64_t x_begin = cta_begin(W, p.n_ctas, blockIdx.x);
   const int64_t x_end = cta_begin(W, p.n_ctas, blockIdx.x + 1);
+  const int total = (int)(x_end - x_begin);
   const uint32_t stage0 = smem_u32(smem);
-  const bool issuer = (tid == 0);
-  Issuer is;
-  is.x = x_begin;
-  is.have = false;
-  is.pi = 0;
-  is.next = 0;
-  is.total = (int)(x_end - x_begin);
-  if (issuer)
-    pump<D>(p, &tmap, is, sh, pre, x_end, -1, stage0, geo.stage_bytes, S, full_bar, empty_bar, abort_flag);
+  const int ncache = total < kPidCache ? total : kPidCache;
+  for (int q = tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  __syncthreads();
+  // prologue: fill the ring; later pages are issued by the last reader of a stage
+  if (tid == 0) {
+    const int n0 = total < S ? total : S;
+    for (int q = 0; q < n0; ++q)
+      issue_page<D>(p, &tmap, q < kPidCache ? pid[q] : page_coord(p, sh, pre, x_begin, q),
+                    stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+  }
 
   const int team = warp / CS, wit = warp % CS;  // team, warp-in-team
   const int g = lane >> 2, t4 = lane & 3;
@@ -357,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   uint32_t bq[NT][NCH][2];
   float o[NCH][NT][4];
   float m_run[NT][2], l_run[NT][2];
-  int row_limit_t[NT][2];  // column index t of each held row (or -1 for padding rows)
+  int row_t[NT][2];  // verify column of each held row (T - 1 for padding rows)
 
   int64_t x = x_begin;
   Segment seg;
@@ -388,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r2 = nt * 8 + 2 * t4 + e;
-        row_limit_t[nt][e] = r2 < M ? r2 / G : T - 1;
+        row_t[nt][e] = r2 < M ? r2 / G : T - 1;
         m_run[nt][e] = -INFINITY;
         l_run[nt][e] = 0.f;
       }
@@ -406,193 +394,207 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       const float* vs_s = ks_s + P * G_ALL;
       for (int kb = 0; kb < BPP; ++kb, ++block_seq) {
         if (block_seq % NTEAMS != team) continue;
-        if (issuer)
-          pump<D>(p, &tmap, is, sh, pre, x_end, page_seq, stage0, geo.stage_bytes, S, full_bar, empty_bar,
-                  abort_flag);
-        __syncwarp();
         if (!*abort_flag && !mbar_wait(smem_u32(&full_bar[s]), par)) {
           if (lane == 0) flag(p.status, NK_DEVFLAG_TIMEOUT);
           *abort_flag = 1;
         }
         const int key0 = kb * 16;
         const int pos0 = pi * P + key0;  // sequence position of the block's key 0
-        if (pos0 >= L) {                 // the block lies past ctx_len: nothing to attend
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
-          continue;
-        }
-
-        // ---- QK: per-group fp32 partial dot products, scaled per key
-        float sc[NT][4];
+        if (pos0 < L) {
+          // ---- QK: per-group fp32 partial dot products (GW*NT independent accumulators)
+          uint32_t kw[GW][4][2];  // [group][chunk][keys 0-7 | 8-15]
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+          for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) sc[nt][k] = 0.f;
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
+              ldsm_x4(st + box_off<D>(P, 0, key0 + lm_key, c16), kw[gi][q2 * 2][0], kw[gi][q2 * 2][1],
+                      kw[gi][q2 * 2 + 1][0], kw[gi][q2 * 2 + 1][1]);
+            }
+          float acc[GW][NT][4];
 #pragma unroll
-        for (int gi = 0; gi < GW; ++gi) {
-          uint32_t kw[4][2];  // [chunk in group][keys 0-7 | 8-15]
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
-            ldsm_x4(st + box_off<D>(P, 0, key0 + lm_key, c16), kw[q2 * 2][0], kw[q2 * 2][1], kw[q2 * 2 + 1][0],
-                    kw[q2 * 2 + 1][1]);
-          }
-          float acc[NT][4];
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[nt][k] = 0.f;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const uint32_t lo = kw[cc][0] ^ bias, hi = kw[cc][1] ^ bias;
-            const uint32_t a0 = i8x2_to_f16x2(lo, 0x4140), a2 = i8x2_to_f16x2(lo, 0x4342);
-            const uint32_t a1 = i8x2_to_f16x2(hi, 0x4140), a3 = i8x2_to_f16x2(hi, 0x4342);
+          for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-              mma16816(acc[nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
-          }
-          const float k0 = ks_s[(key0 + g) * G_ALL + grp0 + gi] * p.scale2;
-          const float k1 = ks_s[(key0 + g + 8) * G_ALL + grp0 + gi] * p.scale2;
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            sc[nt][0] = fmaf(k0, acc[nt][0], sc[nt][0]);
-            sc[nt][1] = fmaf(k0, acc[nt][1], sc[nt][1]);
-            sc[nt][2] = fmaf(k1, acc[nt][2], sc[nt][2]);
-            sc[nt][3] = fmaf(k1, acc[nt][3], sc[nt][3]);
+              for (int k = 0; k < 4; ++k) acc[gi][nt][k] = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+            for (int gi = 0; gi < GW; ++gi) {
+              const uint32_t lo = kw[gi][cc][0] ^ bias, hi = kw[gi][cc][1] ^ bias;
+              const uint32_t a0 = i8x2_to_f16x2(lo, 0x4140), a2 = i8x2_to_f16x2(lo, 0x4342);
+              const uint32_t a1 = i8x2_to_f16x2(hi, 0x4140), a3 = i8x2_to_f16x2(hi, 0x4342);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma16816(acc[gi][nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
+            }
+          float sc[NT][4];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sc[nt][k] = 0.f;
+#pragma unroll
+          for (int gi = 0; gi < GW; ++gi) {
+            const float k0 = ks_s[(key0 + g) * G_ALL + grp0 + gi] * p.scale2;
+            const float k1 = ks_s[(key0 + g + 8) * G_ALL + grp0 + gi] * p.scale2;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              sc[nt][0] = fmaf(k0, acc[gi][nt][0], sc[nt][0]);
+              sc[nt][1] = fmaf(k0, acc[gi][nt][1], sc[nt][1]);
+              sc[nt][2] = fmaf(k1, acc[gi][nt][2], sc[nt][2]);
+              sc[nt][3] = fmaf(k1, acc[gi][nt][3], sc[nt][3]);
+            }
           }
-        }
 
-        // ---- team exchange: every warp of the team sums the CS partials in warp order
-        if constexpr (CS > 1) {
-          const int buf = (block_seq / NTEAMS) & 1;
-          float* xb = xch + (((size_t)team * 2 + buf) * CS) * (NT * 4 * 32);
+          // ---- team exchange: every warp of the team sums the CS partials in warp order
+          if constexpr (CS > 1) {
+            const int buf = (block_seq / NTEAMS) & 1;
+            float* xb = xch + (((size_t)team * 2 + buf) * CS) * (NT * 4 * 32);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) xb[(wit * NT * 4 + nt * 4 + k) * 32 + lane] = sc[nt][k];
-          named_bar(2 + team, CS * 32);
+              for (int k = 0; k < 4; ++k) xb[(wit * NT * 4 + nt * 4 + k) * 32 + lane] = sc[nt][k];
+            named_bar(2 + team, CS * 32);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              float sum = 0.f;
+              for (int k = 0; k < 4; ++k) {
+                float sum = 0.f;
 #pragma unroll
-              for (int w2 = 0; w2 < CS; ++w2) {
-                const float v = (w2 == wit) ? sc[nt][k] : xb[(w2 * NT * 4 + nt * 4 + k) * 32 + lane];
-                sum = (w2 == 0) ? v : sum + v;
+                for (int w2 = 0; w2 < CS; ++w2) {
+                  const float v = (w2 == wit) ? sc[nt][k] : xb[(w2 * NT * 4 + nt * 4 + k) * 32 + lane];
+                  sum = (w2 == 0) ? v : sum + v;
+                }
+                sc[nt][k] = sum;
               }
-              sc[nt][k] = sum;
-            }
-        }
-
-        // ---- causal / context mask (only blocks that reach past L - T)
-        const bool need_mask = pos0 + 15 > L - T;
-        bool valid[2] = {true, true};
-        if (need_mask) {
-          valid[0] = pos0 + g < L;
-          valid[1] = pos0 + g + 8 < L;
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int key = g + (k >> 1) * 8;
-              const int lim = L - T + row_limit_t[nt][k & 1];
-              if (pos0 + key > lim) sc[nt][k] = -INFINITY;
-            }
-        }
-
-        // ---- online softmax (base 2)
-        float mnew[NT][2];
-        bool grow = false;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float mb = fmaxf(sc[nt][e], sc[nt][e + 2]);
-            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-            mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-            mnew[nt][e] = fmaxf(m_run[nt][e], mb);
-            grow |= mnew[nt][e] > m_run[nt][e];
           }
-        if (__any_sync(0xffffffffu, grow)) {
+
+          // ---- causal / context mask (only blocks that reach past L - T)
+          const bool need_mask = pos0 + 15 > L - T;
+          bool valid0 = true, valid1 = true;
+          if (need_mask) {
+            valid0 = pos0 + g < L;
+            valid1 = pos0 + g + 8 < L;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int key = g + (k >> 1) * 8;
+                if (pos0 + key > L - T + row_t[nt][k & 1]) sc[nt][k] = -INFINITY;
+              }
+          }
+
+          // ---- online softmax (base 2)
+          float mnew[NT][2];
+          bool grow = false;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const float mu = mnew[nt][e] == -INFINITY ? 0.f : mnew[nt][e];
-              const float alpha = exp2f(m_run[nt][e] - mu);
-              l_run[nt][e] *= alpha;
-#pragma unroll
-              for (int c = 0; c < NCH; ++c) {
-                o[c][nt][e] *= alpha;
-                o[c][nt][e + 2] *= alpha;
-              }
-              m_run[nt][e] = mnew[nt][e];
+              float mb = fmaxf(sc[nt][e], sc[nt][e + 2]);
+              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+              mnew[nt][e] = fmaxf(m_run[nt][e], mb);
+              grow |= mnew[nt][e] > m_run[nt][e];
             }
-        }
-        float pr[NT][4];
+          if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float mu = m_run[nt][k & 1] == -INFINITY ? 0.f : m_run[nt][k & 1];
-            pr[nt][k] = exp2f(sc[nt][k] - mu);
+              for (int e = 0; e < 2; ++e) {
+                const float mu = mnew[nt][e] == -INFINITY ? 0.f : mnew[nt][e];
+                const float alpha = exp2f(m_run[nt][e] - mu);
+                l_run[nt][e] *= alpha;
+#pragma unroll
+                for (int c = 0; c < NCH; ++c) {
+                  o[c][nt][e] *= alpha;
+                  o[c][nt][e + 2] *= alpha;
+                }
+                m_run[nt][e] = mnew[nt][e];
+              }
           }
+          float pr[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          l_run[nt][0] += pr[nt][0] + pr[nt][2];
-          l_run[nt][1] += pr[nt][1] + pr[nt][3];
-        }
-
-        // ---- PV with P' = p * Vs split into fp16 hi + lo
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int gi = 0; gi < GW; ++gi) {
-          float v0 = vs_s[(key0 + g) * G_ALL + grp0 + gi];
-          float v1 = vs_s[(key0 + g + 8) * G_ALL + grp0 + gi];
-          v0 = valid[0] ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
-          v1 = valid[1] ? v1 : 0.f;
-          uint32_t bh[NT][2], bl[NT][2];
+            for (int k = 0; k < 4; ++k) {
+              const float mu = m_run[nt][k & 1] == -INFINITY ? 0.f : m_run[nt][k & 1];
+              pr[nt][k] = exp2f(sc[nt][k] - mu);
+            }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
-            const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
-            bh[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h01));
-            bh[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h23));
-            bl[nt][0] = movmatrix_t(l01);
-            bl[nt][1] = movmatrix_t(l23);
+            l_run[nt][0] += pr[nt][0] + pr[nt][2];
+            l_run[nt][1] += pr[nt][1] + pr[nt][3];
           }
+
+          // ---- PV with P' = p * Vs split into fp16 hi + lo
 #pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            uint32_t w0, w1, w2, w3;  // chunk 2q2: keys 0-7, 8-15; chunk 2q2+1: keys 0-7, 8-15
-            const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
-            ldsm_x4_t(st + box_off<D>(P, 1, key0 + lm_key, c16), w0, w1, w2, w3);
-            const uint32_t vw[2][2] = {{w0 ^ bias, w1 ^ bias}, {w2 ^ bias, w3 ^ bias}};
+          for (int gi = 0; gi < GW; ++gi) {
+            uint32_t vw[4][2];  // [chunk][keys 0-7 | 8-15], transposed fragments
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int c = gi * 4 + q2 * 2 + h;  // warp-local chunk
-              const uint32_t a0 = i8x2_to_f16x2(vw[h][0], 0x4240), a1 = i8x2_to_f16x2(vw[h][0], 0x4341);
-              const uint32_t a2 = i8x2_to_f16x2(vw[h][1], 0x4240), a3 = i8x2_to_f16x2(vw[h][1], 0x4341);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                mma16816(o[c][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                mma16816(o[c][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
-              }
+            for (int q2 = 0; q2 < 2; ++q2) {
+              const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
+              ldsm_x4_t(st + box_off<D>(P, 1, key0 + lm_key, c16), vw[q2 * 2][0], vw[q2 * 2][1],
+                        vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
             }
+            float v0 = vs_s[(key0 + g) * G_ALL + grp0 + gi];
+            float v1 = vs_s[(key0 + g + 8) * G_ALL + grp0 + gi];
+            v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
+            v1 = valid1 ? v1 : 0.f;
+            uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
+              const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+              const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+              const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
+              bh[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h01));
+              bh[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h23));
+              bl[nt][0] = movmatrix_t(l01);
+              bl[nt][1] = movmatrix_t(l23);
+            }
+            uint32_t av[4][4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const uint32_t w0 = vw[cc][0] ^ bias, w1 = vw[cc][1] ^ bias;
+              av[cc][0] = i8x2_to_f16x2(w0, 0x4240);
+              av[cc][1] = i8x2_to_f16x2(w0, 0x4341);
+              av[cc][2] = i8x2_to_f16x2(w1, 0x4240);
+              av[cc][3] = i8x2_to_f16x2(w1, 0x4341);
+            }
+            // all hi products first, then all lo: 4*NT independent accumulators between dependent pairs
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bh[nt][0], bh[nt][1]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bl[nt][0], bl[nt][1]);
           }
         }
+        // ---- release the stage; its last reader loads the page S ahead into it
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&empty_bar[s]));
+          if (atomicAdd(&cnt[s], 1) == per_stage - 1) {
+            cnt[s] = 0;
+            // every reader arrived before its increment: the phase is complete
+            if (!mbar_wait(smem_u32(&empty_bar[s]), par)) flag(p.status, NK_DEVFLAG_TIMEOUT);
+            const int qn = page_seq + S;
+            if (qn < total)
+              issue_page<D>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
+                            smem_u32(&full_bar[s]));
+          }
+        }
       }
     }
 
     // ---- merge the teams of this segment and write the result
-    // every page of the segment must be issued before warp 0 waits for the others
-    if (issuer)
-      pump<D>(p, &tmap, is, sh, pre, x_end, page_seq - 1, stage0, geo.stage_bytes, S, full_bar, empty_bar,
-              abort_flag);
     // row sums: reduce the per-lane partial l over the 8 lanes of a row
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -644,8 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       __syncthreads();
     }
     // normalize and store
-    const int ctid = tid;  // 0 .. 255
-    for (int i = ctid; i < M * D; i += kConsumerWarps * 32) {
+    for (int i = tid; i < M * D; i += kThreads) {
       const int r = i / D, ch = i % D;
       float mx = -INFINITY, lsum = 0.f;
       for (int tm = 0; tm < NTEAMS; ++tm) mx = fmaxf(mx, tm_m[tm * MROWS + r]);

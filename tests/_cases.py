@@ -72,17 +72,28 @@ def oracle_rows(c, rows) -> np.ndarray:
     return out
 
 
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
 def compare(gpu_bf16: torch.Tensor, ref64: np.ndarray, what=""):
-    """Tolerance of the attention output: max-abs <= 4e-3 and relative L2 <= 1e-3
-    against the oracle's fp64 result rounded to bf16 (ties to even)."""
+    """Tolerance of the attention output against the oracle's fp64 result
+    rounded to bf16 (ties to even): relative L2 <= 1e-3, and every element
+    within 4e-3 -- or within one bf16 ulp of the reference where that ulp is
+    larger (|O| >= 1, reached only by short contexts), since a bf16 output
+    that differs from the rounded reference differs by at least one ulp."""
     ref = oracle.bits_to_double(oracle.round_bf16(ref64))
     g = gpu_bf16.to(torch.float64).cpu().numpy().reshape(ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
     err = np.abs(g - ref)
+    allow = np.maximum(ABS_TOL, bf16_ulp(ref))
     maxabs = float(err.max())
+    worst = float((err / allow).max())
     rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300))
     rel_exact = float(np.linalg.norm(g - ref64.reshape(ref.shape)) / max(np.linalg.norm(ref64), 1e-300))
-    assert maxabs <= ABS_TOL, f"{what}: max-abs {maxabs:.3e} > {ABS_TOL}"
+    assert worst <= 1.0, f"{what}: max-abs {maxabs:.3e} exceeds max(4e-3, 1 ulp) (ratio {worst:.2f})"
     assert rel <= REL_L2_TOL, f"{what}: rel-L2 {rel:.3e} > {REL_L2_TOL} (vs unrounded fp64: {rel_exact:.3e})"
     return maxabs, rel, rel_exact
 
