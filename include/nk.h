@@ -155,6 +155,32 @@ int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const i
                               int32_t* status_dev, void* stream);
 
 /*
+ * nk_paged_decode_attn_noalloc -- nk_paged_decode_attn for callers that
+ * cannot allocate device memory (the pages have no counterpart of this entry
+ * point). Some callers cannot call cudaMalloc or pass a scratch buffer: hosts
+ * that own a fixed device-memory budget and forbid allocation after start,
+ * or code that must not risk the device synchronization an allocation can
+ * bring. This variant keeps the split partials in a fixed array of
+ * NK_NOALLOC_MAX_WORKSPACE bytes inside the library's device memory (held on
+ * every GPU that loads the library, until the process exits) and calls no
+ * allocator. The caller still provides q, the pool, the tables, out and the
+ * optional status word; the arguments mean what they mean for
+ * nk_paged_decode_attn.
+ *   - The first call on a device looks up the array's device address once
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Returns NK_ERR_WORKSPACE when nk_decode_workspace_bytes() for this shape
+ *     and CTA count exceeds NK_NOALLOC_MAX_WORKSPACE.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (no part of it needs to start at zero). Calls whose kernels
+ *     overlap on the GPU race on it: serialize them (one stream, or events).
+ */
+#define NK_NOALLOC_MAX_WORKSPACE (8u << 20)
+int nk_paged_decode_attn_noalloc(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                                 int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                                 int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                                 void* out_dev, int32_t* status_dev, void* stream);
+
+/*
  * nk_attn_combine -- log-sum-exp merge of S partial results.
  *   part_o_dev    fp32 [S][R][D]: each partial normalized by its own softmax sum
  *   part_lse_dev  fp32 [S][R]: natural-log LSE of the partial's scaled scores,

@@ -22,7 +22,8 @@ MAX_T = 8
 
 __all__ = [
     "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_ctas",
-    "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "attn_combine", "status_string",
+    "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "paged_decode_attn_noalloc",
+    "attn_combine", "status_string",
 ]
 
 
@@ -136,6 +137,28 @@ def paged_decode_attn_simt(pool: KVPool, q, block_table, ctx_lens, sm_scale: flo
     """Same result from the fp32 CUDA-core kernel (nk_paged_decode_attn_simt)."""
     return _decode(lib().nk_paged_decode_attn_simt, "nk_paged_decode_attn_simt", pool, q, block_table, ctx_lens,
                    sm_scale, max_ctx, num_ctas, workspace, out, status, stream)
+
+
+NOALLOC_MAX_WORKSPACE = 8 << 20
+
+
+def paged_decode_attn_noalloc(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int,
+                              num_ctas: int = 0, out=None, status=None, stream=None):
+    """nk_paged_decode_attn_noalloc: the tensor-core decode with its split
+    partials in the library's own fixed device array, for callers that cannot
+    allocate device memory. Calls that overlap on the GPU race on that array."""
+    import torch
+
+    _need_cuda(q, block_table, ctx_lens, out, status)
+    B, T, Hq, D = (int(s) for s in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    ps = pool.c_struct()
+    rc = lib().nk_paged_decode_attn_noalloc(ctypes.byref(ps), _ptr(q), _ptr(block_table), int(block_table.shape[-1]),
+                                            _ptr(ctx_lens), B, T, Hq, float(sm_scale), int(max_ctx), int(num_ctas),
+                                            _ptr(out), _ptr(status), _stream(stream))
+    _check(rc, "nk_paged_decode_attn_noalloc")
+    return out
 
 
 def attn_combine(part_o, part_lse, out=None, stream=None):
