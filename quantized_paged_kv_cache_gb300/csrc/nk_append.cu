@@ -10,10 +10,11 @@
 // of one (row, kv-head) for both K and V (two 32-byte loads in flight per
 // tensor), four threads form a 64-channel group and reduce its absmax with two
 // shuffles. The per-element quotient is x * RN(1/s) with an exactness guard:
-// the product differs from x/s by less than 2^-16 (|x/s| <= 127.00001), so
-// unless it lies within 2^-14 of a half-integer its nearest integer equals
-// the nearest integer of the correctly rounded fp32 quotient; the rare
-// elements inside that window (and exact ties) take the IEEE division.
+// the product differs from x/s by less than 2^-16 (|x/s| <= 127.00001) and the
+// correctly rounded fp32 quotient differs from x/s by at most 2^-18, so unless
+// the product lies within 2^-14 of a half-integer both round to the same
+// integer; the rare elements inside that window (and exact ties) take the
+// IEEE division out of line.
 #include "nk_common.cuh"
 
 namespace nk {
@@ -32,6 +33,15 @@ struct AppendParams {
   int32_t* status;
 };
 
+// Exact IEEE path for one element: fp32 quotient, clamp, round half to even.
+// Kept out of line: it runs only for elements within 2^-14 of a rounding
+// boundary (or for groups with a tiny scale), so the common path stays short.
+__device__ __noinline__ uint32_t quantize_exact(float x, float s) {
+  float e = __fdiv_rn(x, s);
+  e = fminf(fmaxf(e, -127.f), 127.f);
+  return (uint32_t)__float2int_rn(e) & 0xffu;
+}
+
 // Quantize 16 values (already fp32) of one group slice; returns the scale and
 // writes 16 int8 codes packed into 4 words.
 __device__ __forceinline__ float quantize16(const float (&x)[16], uint32_t (&packed)[4]) {
@@ -44,25 +54,30 @@ __device__ __forceinline__ float quantize16(const float (&x)[16], uint32_t (&pac
   const float s = (a == 0.f) ? 1.f : __fdiv_rn(a, 127.f);
   const float y = __frcp_rn(s);
   const bool tiny = s < 7.888609052210118e-31f;  // 2^-100: keep RN(1/s) far from overflow
-  int q[16];
+  // |x * y - x / s| < 2^-16 here, so no clamp is needed on the fast path
+  // (|x / s| <= 127 * (1 + 2^-23)); t = r + 1.5 * 2^23 rounds r to an integer
+  // (ties to even) whose two's-complement low byte is the low byte of t's bits.
+  uint32_t tb[16];
+  uint32_t slow = tiny ? 0xffffu : 0u;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float r = __fmul_rn(x[i], y);
-    r = fminf(fmaxf(r, -127.f), 127.f);
-    const float t = __fadd_rn(r, 12582912.f);  // 1.5 * 2^23: rounds r to an integer, ties to even
-    const float ri = __fsub_rn(t, 12582912.f);
-    int qi = __float_as_int(t) - 0x4B400000;
-    if (tiny || fabsf(__fsub_rn(r, ri)) > 0.49993896484375f /* 0.5 - 2^-14 */) {
-      float e = __fdiv_rn(x[i], s);
-      e = fminf(fmaxf(e, -127.f), 127.f);
-      qi = __float2int_rn(e);
-    }
-    q[i] = qi;
+    const float r = __fmul_rn(x[i], y);
+    const float t = __fadd_rn(r, 12582912.f);
+    const float d = __fsub_rn(r, __fsub_rn(t, 12582912.f));
+    if (fabsf(d) > 0.49993896484375f /* 0.5 - 2^-14 */) slow |= 1u << i;
+    tb[i] = __float_as_uint(t);
+  }
+  if (slow) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((slow >> i) & 1u) tb[i] = quantize_exact(x[i], s);
   }
 #pragma unroll
-  for (int w = 0; w < 4; ++w)
-    packed[w] = (uint32_t)(q[4 * w] & 0xff) | ((uint32_t)(q[4 * w + 1] & 0xff) << 8) |
-                ((uint32_t)(q[4 * w + 2] & 0xff) << 16) | ((uint32_t)(q[4 * w + 3] & 0xff) << 24);
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t lo = __byte_perm(tb[4 * w], tb[4 * w + 1], 0x0040);
+    const uint32_t hi = __byte_perm(tb[4 * w + 2], tb[4 * w + 3], 0x0040);
+    packed[w] = __byte_perm(lo, hi, 0x5410);
+  }
   return s;
 }
 

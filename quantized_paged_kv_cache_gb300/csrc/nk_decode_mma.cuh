@@ -79,7 +79,7 @@ __host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B
   g.stage_bytes = round_up(kv_bytes + sc_bytes, 1024);
   g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
   const int mrows = NT * 8;
-  g.merge_bytes = mrows * (D + 4) * 4 + 2 * nteams * mrows * 4;
+  g.merge_bytes = mrows * (D + 4) * 4 + 3 * nteams * mrows * 4 + mrows * 4;
   const int pre_bytes = round_up((B + 1 + 24) * 4, 16);
   const int pid_bytes = 1024 * 4;
   const int fixed = g.xch_bytes + g.merge_bytes + pre_bytes + pid_bytes + 8 * 2 * 8 + 1024;
@@ -196,6 +196,13 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t wb, uint32_t sel) {
   const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6480),
                                                                                     __ushort_as_half(0x6480)));
   return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// 2^x on the SFU (relative error ~2^-22); ex2(-inf) = 0.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
@@ -321,16 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   const int64_t x_end = cta_begin(W, p.n_ctas, blockIdx.x + 1);
   const int total = (int)(x_end - x_begin);
   const uint32_t stage0 = smem_u32(smem);
-  const int ncache = total < kPidCache ? total : kPidCache;
-  for (int q = tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
-  __syncthreads();
-  // prologue: fill the ring; later pages are issued by the last reader of a stage
-  if (tid == 0) {
-    const int n0 = total < S ? total : S;
-    for (int q = 0; q < n0; ++q)
-      issue_page<D>(p, &tmap, q < kPidCache ? pid[q] : page_coord(p, sh, pre, x_begin, q),
-                    stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
-  }
 
   const int team = warp / CS, wit = warp % CS;  // team, warp-in-team
   const int g = lane >> 2, t4 = lane & 3;
@@ -338,41 +335,87 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   const int grp0 = ch0 / kGroup;
   const int G = p.G, T = p.T, M = G * T;
   const uint32_t bias = 0x80808080u;
-  // ldmatrix lane geometry: matrix mi = lane / 8, row-in-matrix = lane % 8
+  // ldmatrix lane geometry: matrix mi = lane / 8, row-in-matrix = lane % 8.
+  // Keys of a block start at a multiple of 16 and P is a multiple of 16, so
+  // the swizzle term depends on the lane only: the per-lane byte offsets of
+  // this warp's 16x16 sub-tiles are fixed for the whole kernel.
+  constexpr int RB = D == 64 ? 64 : 128;  // bytes per smem row of a box
   const int lm_key = ((lane >> 3) & 1) * 8 + (lane & 7);
   const int lm_chunk = lane >> 4;
+  uint32_t loff[GW][2];
+#pragma unroll
+  for (int gi = 0; gi < GW; ++gi)
+#pragma unroll
+    for (int q2 = 0; q2 < 2; ++q2) loff[gi][q2] = box_off<D>(P, 0, lm_key, (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk);
 
   uint32_t bq[NT][NCH][2];
   float o[NCH][NT][4];
   float m_run[NT][2], l_run[NT][2];
   int row_t[NT][2];  // verify column of each held row (T - 1 for padding rows)
 
-  int64_t x = x_begin;
-  Segment seg;
-  int page_seq = 0, block_seq = 0;
-  while (next_segment(sh, pre, x, x_end, seg)) {
-    const int L = p.ctx[seg.b];
-    // ---- Q fragments (fp16) of this warp's channels, all rows
+  // Q fragments of this warp's channels, all rows of a segment's unit:
+  // load_q fetches the raw bf16 pairs, convert_q turns them into fp16 pairs
+  // (exact for |q| in [2^-14, 65504]; larger values set NK_DEVFLAG_RANGE).
+  auto load_q = [&](const Segment& sg) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int r = nt * 8 + g;
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
-        uint32_t w0 = 0, w1 = 0;
+        uint2 raw = make_uint2(0u, 0u);
         if (r < M) {
           const int t = r / G, hg = r % G;
-          const uint16_t* qp =
-              p.q + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch0 + c * 16 + t4 * 4;
-          const uint2 raw = *reinterpret_cast<const uint2*>(qp);
-          const float f0 = bf16_lo(raw.x), f1 = bf16_hi(raw.x), f2 = bf16_lo(raw.y), f3 = bf16_hi(raw.y);
-          if (fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3))) > 65504.f)
-            flag(p.status, NK_DEVFLAG_RANGE);
-          w0 = pack_f16(f0, f1);
-          w1 = pack_f16(f2, f3);
+          raw = *reinterpret_cast<const uint2*>(p.q + (((int64_t)sg.b * T + t) * p.Hq + sg.h * G + hg) * D + ch0 +
+                                                c * 16 + t4 * 4);
         }
-        bq[nt][c][0] = w0;
-        bq[nt][c][1] = w1;
+        bq[nt][c][0] = raw.x;
+        bq[nt][c][1] = raw.y;
       }
+    }
+  };
+  auto convert_q = [&]() {
+    bool big = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float f0 = bf16_lo(bq[nt][c][h]), f1 = bf16_hi(bq[nt][c][h]);
+          big |= fmaxf(fabsf(f0), fabsf(f1)) > 65504.f;
+          bq[nt][c][h] = pack_f16(f0, f1);
+        }
+    if (big) flag(p.status, NK_DEVFLAG_RANGE);
+  };
+
+  // The first unit's Q loads go out first (converted at first use), so they
+  // are not queued behind the page prefetch; then warp 0 fetches the first S
+  // page coordinates and issues their loads, while the other threads fill
+  // the page-coordinate cache that the stage refills read.
+  int64_t x = x_begin;
+  Segment seg;
+  bool have = next_segment(sh, pre, x, x_end, seg);
+  if (have) load_q(seg);
+  if (warp == 0) {
+    const int n0 = total < S ? total : S;
+    if (lane < n0) pid[lane] = page_coord(p, sh, pre, x_begin, lane);
+    __syncwarp();
+    if (lane == 0)
+      for (int q = 0; q < n0; ++q) issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+  }
+  const int ncache = total < kPidCache ? total : kPidCache;
+  for (int q = S + tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  __syncthreads();
+
+  int page_seq = 0, block_seq = 0;
+  bool first_seg = true;
+  for (; have; have = next_segment(sh, pre, x, x_end, seg)) {
+    const int L = p.ctx[seg.b];
+    if (!first_seg) load_q(seg);
+    first_seg = false;
+    convert_q();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int r2 = nt * 8 + 2 * t4 + e;
@@ -403,14 +446,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         if (pos0 < L) {
           // ---- QK: per-group fp32 partial dot products (GW*NT independent accumulators)
           uint32_t kw[GW][4][2];  // [group][chunk][keys 0-7 | 8-15]
+          const uint32_t kbase = st + key0 * RB;
 #pragma unroll
           for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-              const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
-              ldsm_x4(st + box_off<D>(P, 0, key0 + lm_key, c16), kw[gi][q2 * 2][0], kw[gi][q2 * 2][1],
-                      kw[gi][q2 * 2 + 1][0], kw[gi][q2 * 2 + 1][1]);
-            }
+            for (int q2 = 0; q2 < 2; ++q2)
+              ldsm_x4(kbase + loff[gi][q2], kw[gi][q2 * 2][0], kw[gi][q2 * 2][1], kw[gi][q2 * 2 + 1][0],
+                      kw[gi][q2 * 2 + 1][1]);
           float acc[GW][NT][4];
 #pragma unroll
           for (int gi = 0; gi < GW; ++gi)
@@ -485,44 +527,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
               }
           }
 
-          // ---- online softmax (base 2)
-          float mnew[NT][2];
-          bool grow = false;
+          // ---- online softmax (base 2). The reference m_run is raised only when a
+          // score passes it by more than 8 (p would exceed 2^8); the softmax
+          // does not depend on the reference, so most blocks skip the row-max
+          // reduction and the accumulator rescale.
+          bool over = false;
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float mb = fmaxf(sc[nt][e], sc[nt][e + 2]);
-              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-              mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-              mnew[nt][e] = fmaxf(m_run[nt][e], mb);
-              grow |= mnew[nt][e] > m_run[nt][e];
-            }
-          if (__any_sync(0xffffffffu, grow)) {
+            for (int k = 0; k < 4; ++k) over |= sc[nt][k] > m_run[nt][k & 1] + 8.f;
+          if (__any_sync(0xffffffffu, over)) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const float mu = mnew[nt][e] == -INFINITY ? 0.f : mnew[nt][e];
-                const float alpha = exp2f(m_run[nt][e] - mu);
-                l_run[nt][e] *= alpha;
+                float mb = fmaxf(sc[nt][e], sc[nt][e + 2]);
+                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+                mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+                const float mnew = fmaxf(m_run[nt][e], mb);
+                if (mnew > m_run[nt][e]) {
+                  const float alpha = ex2(m_run[nt][e] - mnew);  // 0 while the row was empty
+                  l_run[nt][e] *= alpha;
 #pragma unroll
-                for (int c = 0; c < NCH; ++c) {
-                  o[c][nt][e] *= alpha;
-                  o[c][nt][e + 2] *= alpha;
+                  for (int c = 0; c < NCH; ++c) {
+                    o[c][nt][e] *= alpha;
+                    o[c][nt][e + 2] *= alpha;
+                  }
+                  m_run[nt][e] = mnew;
                 }
-                m_run[nt][e] = mnew[nt][e];
               }
           }
           float pr[NT][4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float mu = m_run[nt][k & 1] == -INFINITY ? 0.f : m_run[nt][k & 1];
-              pr[nt][k] = exp2f(sc[nt][k] - mu);
-            }
+          for (int nt = 0; nt < NT; ++nt) {
+            const float mu0 = m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
+            const float mu1 = m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
+            pr[nt][0] = ex2(sc[nt][0] - mu0);
+            pr[nt][1] = ex2(sc[nt][1] - mu1);
+            pr[nt][2] = ex2(sc[nt][2] - mu0);
+            pr[nt][3] = ex2(sc[nt][3] - mu1);
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             l_run[nt][0] += pr[nt][0] + pr[nt][2];
@@ -533,12 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
           for (int gi = 0; gi < GW; ++gi) {
             uint32_t vw[4][2];  // [chunk][keys 0-7 | 8-15], transposed fragments
+            const uint32_t vbase = st + (P + key0) * RB;
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2) {
-              const int c16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
-              ldsm_x4_t(st + box_off<D>(P, 1, key0 + lm_key, c16), vw[q2 * 2][0], vw[q2 * 2][1],
-                        vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
-            }
+            for (int q2 = 0; q2 < 2; ++q2)
+              ldsm_x4_t(vbase + loff[gi][q2], vw[q2 * 2][0], vw[q2 * 2][1], vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
             float v0 = vs_s[(key0 + g) * G_ALL + grp0 + gi];
             float v1 = vs_s[(key0 + g + 8) * G_ALL + grp0 + gi];
             v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
@@ -606,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         v += __shfl_xor_sync(0xffffffffu, v, 16);
         l_run[nt][e] = v;
       }
-    __syncthreads();  // previous segment's readers of mo are done
+    __syncthreads();  // all blocks of the segment read; previous merge buffers free
     if (wit == 0 && g == 0) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -617,53 +660,91 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
           tm_l[team * MROWS + r] = l_run[nt][e];
         }
     }
-    __syncthreads();
-    float fac[NT][2];
+    float* facs = tm_l + NTEAMS * MROWS;   // [NTEAMS][MROWS]: weight of a team's rows
+    float* row_lse = facs + NTEAMS * MROWS;
+    // After the CTA's last segment the stage ring is idle (every issued page
+    // has been consumed), so each team can park its accumulator there and one
+    // pass merges them; otherwise the teams add into mo one after another.
+    constexpr int kSlot = MROWS * (D + 4);
+    const bool parked = (x >= x_end) && (size_t)NTEAMS * kSlot * 4 <= (size_t)S * geo.stage_bytes;
+    float* acc_buf = parked ? reinterpret_cast<float*>(smem) + team * kSlot : mo;
+    if (parked) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int c = 0; c < NCH; ++c)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int r = nt * 8 + 2 * t4 + e;
-        float mx = -INFINITY;
-        for (int tm = 0; tm < NTEAMS; ++tm) mx = fmaxf(mx, tm_m[tm * MROWS + r]);
-        fac[nt][e] = (m_run[nt][e] == -INFINITY) ? 0.f : exp2f(m_run[nt][e] - mx);
-      }
-    for (int tm = 0; tm < NTEAMS; ++tm) {
-      if (team == tm) {
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int r = nt * 8 + 2 * t4 + (k & 1);
-              const int ch = ch0 + c * 16 + 2 * g + (k >> 1);
-              float* dst = mo + r * (D + 4) + ch;
-              const float v = o[c][nt][k] * fac[nt][k & 1];
-              *dst = (tm == 0) ? v : *dst + v;
-            }
-      }
-      __syncthreads();
+          for (int k = 0; k < 4; ++k)
+            acc_buf[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)] = o[c][nt][k];
     }
-    // normalize and store
-    for (int i = tid; i < M * D; i += kThreads) {
-      const int r = i / D, ch = i % D;
+    __syncthreads();
+    if (tid < MROWS) {
+      const int r = tid;
       float mx = -INFINITY, lsum = 0.f;
       for (int tm = 0; tm < NTEAMS; ++tm) mx = fmaxf(mx, tm_m[tm * MROWS + r]);
       if (mx != -INFINITY)
         for (int tm = 0; tm < NTEAMS; ++tm) {
           const float mt = tm_m[tm * MROWS + r];
-          if (mt != -INFINITY) lsum += tm_l[tm * MROWS + r] * exp2f(mt - mx);
+          if (mt != -INFINITY) lsum += tm_l[tm * MROWS + r] * ex2(mt - mx);
         }
-      const float val = lsum > 0.f ? mo[r * (D + 4) + ch] / lsum : 0.f;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      for (int tm = 0; tm < NTEAMS; ++tm) {
+        const float mt = tm_m[tm * MROWS + r];
+        facs[tm * MROWS + r] = (mt == -INFINITY) ? 0.f : ex2(mt - mx) * inv;
+      }
+      row_lse[r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+    }
+    __syncthreads();
+    if (!parked) {
+      // team tm adds its weighted accumulator into mo, one 16-channel chunk at
+      // a time with all of the chunk's loads issued before its stores
+      for (int tm = 0; tm < NTEAMS; ++tm) {
+        if (team == tm) {
+          float f[NT][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) f[nt][e] = facs[team * MROWS + nt * 8 + 2 * t4 + e];
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            float prev[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                prev[nt][k] = (tm == 0) ? 0.f
+                                        : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)] =
+                    fmaf(o[c][nt][k], f[nt][k & 1], prev[nt][k]);
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // normalize (weights already include 1/sum) and store
+    const int64_t slot = (int64_t)blockIdx.x + seg.u;
+    const float* park = reinterpret_cast<const float*>(smem);
+    for (int i = tid; i < M * D; i += kThreads) {
+      const int r = i / D, ch = i % D;
+      float val;
+      if (parked) {
+        val = 0.f;
+#pragma unroll
+        for (int tm = 0; tm < NTEAMS; ++tm) val = fmaf(park[tm * kSlot + r * (D + 4) + ch], facs[tm * MROWS + r], val);
+      } else {
+        val = mo[r * (D + 4) + ch];
+      }
       if (!isfinite(val)) flag(p.status, NK_DEVFLAG_RANGE);
-      const int t = r / G, hg = r % G;
       if (seg.whole) {
+        const int t = r / G, hg = r % G;
         p.out[(((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch] = f32_to_bf16(val);
       } else {
-        const int64_t slot = (int64_t)blockIdx.x + seg.u;
         p.part_o[(slot * M + r) * D + ch] = val;
-        if (ch == 0) p.part_lse[slot * M + r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+        if (ch == 0) p.part_lse[slot * M + r] = row_lse[r];
       }
     }
   }

@@ -21,22 +21,31 @@ namespace nk {
 constexpr int kSimtWarps = 8;
 constexpr int kSimtMaxG = 8;
 
+// Raw code bytes of one lane for one key (CPL int8 values), loaded ahead of use.
 template <int CPL>
-__device__ __forceinline__ void load_codes(const int8_t* src, float (&c)[CPL]) {
+struct Raw {
+  uint32_t w[CPL >= 4 ? CPL / 4 : 1];
+};
+
+template <int CPL>
+__device__ __forceinline__ Raw<CPL> load_raw(const uint8_t* src) {
+  Raw<CPL> r;
   if constexpr (CPL == 8) {
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(src));
-    const uint32_t ws[2] = {w.x, w.y};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = (float)(int8_t)(ws[i / 4] >> (8 * (i % 4)));
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+    r.w[0] = v.x;
+    r.w[1] = v.y;
   } else if constexpr (CPL == 4) {
-    const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(src));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = (float)(int8_t)(w >> (8 * i));
+    r.w[0] = __ldg(reinterpret_cast<const unsigned int*>(src));
   } else {
-    const uint16_t w = __ldg(reinterpret_cast<const unsigned short*>(src));
-#pragma unroll
-    for (int i = 0; i < 2; ++i) c[i] = (float)(int8_t)(w >> (8 * i));
+    r.w[0] = __ldg(reinterpret_cast<const unsigned short*>(src));
   }
+  return r;
+}
+
+template <int CPL>
+__device__ __forceinline__ void widen(const Raw<CPL>& r, float (&c)[CPL]) {
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) c[i] = (float)(int8_t)(r.w[i / 4] >> (8 * (i % 4)));
 }
 
 template <int CPL>
@@ -90,41 +99,71 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(const DecodeParams p) 
         }
         const uint8_t* chunk = p.pool + ((int64_t)page * p.Hkv + seg.h) * p.lay.chunk;
         const int kend = min(p.P, last - pi * p.P + 1);
-        for (int k = 0; k < kend; ++k) {
-          float kc[CPL], vc[CPL];
-          load_codes<CPL>(reinterpret_cast<const int8_t*>(chunk + (int64_t)k * D + lane * CPL), kc);
-          load_codes<CPL>(reinterpret_cast<const int8_t*>(chunk + p.lay.vc + (int64_t)k * D + lane * CPL), vc);
-          const int grp = (lane * CPL) / kGroup;
-          const float ks = __ldg(reinterpret_cast<const float*>(chunk + p.lay.ks) + k * g + grp);
-          const float vs = __ldg(reinterpret_cast<const float*>(chunk + p.lay.vs) + k * g + grp);
-          float s[kSimtMaxG];
+        // keys in groups of four, the next group's loads issued before the current group's math
+        constexpr int KB = 4;
+        const int grp = (lane * CPL) / kGroup;
+        const float* ksp = reinterpret_cast<const float*>(chunk + p.lay.ks);
+        const float* vsp = reinterpret_cast<const float*>(chunk + p.lay.vs);
+        Raw<CPL> nkr[KB], nvr[KB];
+        float nks[KB], nvs[KB];
+        auto load_group = [&](int k0) {
 #pragma unroll
-          for (int hg = 0; hg < kSimtMaxG; ++hg) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) acc = fmaf(qf[hg][j], kc[j], acc);
-            s[hg] = acc * ks;
+          for (int j = 0; j < KB; ++j) {
+            const int k = min(k0 + j, kend - 1);  // clamped: a repeated key is never used
+            nkr[j] = load_raw<CPL>(chunk + (int64_t)k * D + lane * CPL);
+            nvr[j] = load_raw<CPL>(chunk + p.lay.vc + (int64_t)k * D + lane * CPL);
+            nks[j] = __ldg(ksp + k * g + grp);
+            nvs[j] = __ldg(vsp + k * g + grp);
           }
+        };
+        load_group(0);
+        for (int k0 = 0; k0 < kend; k0 += KB) {
+          Raw<CPL> ckr[KB], cvr[KB];
+          float cks[KB], cvs[KB];
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
+          for (int j = 0; j < KB; ++j) {
+            ckr[j] = nkr[j];
+            cvr[j] = nvr[j];
+            cks[j] = nks[j];
+            cvs[j] = nvs[j];
+          }
+          if (k0 + KB < kend) load_group(k0 + KB);
 #pragma unroll
-            for (int hg = 0; hg < kSimtMaxG; ++hg) s[hg] += __shfl_xor_sync(0xffffffffu, s[hg], off);
+          for (int j = 0; j < KB; ++j) {
+            if (k0 + j >= kend) break;
+            float kc[CPL], vc[CPL];
+            widen<CPL>(ckr[j], kc);
+            widen<CPL>(cvr[j], vc);
+            const float ks = cks[j], vs = cvs[j];
+            float s[kSimtMaxG];
 #pragma unroll
-          for (int hg = 0; hg < kSimtMaxG; ++hg) {
-            if (hg >= G) break;
-            const float sc = s[hg] * p.scale2;
-            if (sc > m[hg]) {
-              const float alpha = exp2f(m[hg] - sc);
-              l[hg] *= alpha;
+            for (int hg = 0; hg < kSimtMaxG; ++hg) {
+              float acc = 0.f;
 #pragma unroll
-              for (int j = 0; j < CPL; ++j) o[hg][j] *= alpha;
-              m[hg] = sc;
+              for (int jj = 0; jj < CPL; ++jj) acc = fmaf(qf[hg][jj], kc[jj], acc);
+              s[hg] = acc * ks;
             }
-            const float pw = exp2f(sc - m[hg]);
-            l[hg] += pw;
-            const float pv = pw * vs;
 #pragma unroll
-            for (int j = 0; j < CPL; ++j) o[hg][j] = fmaf(pv, vc[j], o[hg][j]);
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+              for (int hg = 0; hg < kSimtMaxG; ++hg) s[hg] += __shfl_xor_sync(0xffffffffu, s[hg], off);
+#pragma unroll
+            for (int hg = 0; hg < kSimtMaxG; ++hg) {
+              if (hg >= G) break;
+              const float sc = s[hg] * p.scale2;
+              if (sc > m[hg]) {
+                const float alpha = exp2f(m[hg] - sc);
+                l[hg] *= alpha;
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) o[hg][jj] *= alpha;
+                m[hg] = sc;
+              }
+              const float pw = exp2f(sc - m[hg]);
+              l[hg] += pw;
+              const float pv = pw * vs;
+#pragma unroll
+              for (int jj = 0; jj < CPL; ++jj) o[hg][jj] = fmaf(pv, vc[jj], o[hg][jj]);
+            }
           }
         }
       }

@@ -5,6 +5,9 @@ batched call).
 Codes and scales are compared bit-exactly over the whole pool; the attention
 output is compared on sampled rows the oracle computes one by one (first and
 last verify column, first, last and a middle q-head, of every sequence)."""
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -72,4 +75,10 @@ def test_full_size(name, impl):
     ref = np.stack([oracle.attention_row(opool, w.num_pages, w.P, w.Hkv, w.D, bt_cpu, w.ctx_lens, q_cpu, w.T, w.Hq,
                                          w.sm_scale, b, t, i)[0] for (b, t, i) in rows])
     got = torch.stack([out[b, t, i] for (b, t, i) in rows])
-    compare(got, ref, f"{name}/{impl}")
+    maxabs, rel, rel_exact = compare(got, ref, f"{name}/{impl}")
+    log = os.environ.get("NK_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps({"workload": name, "kernel": impl, "rows": len(rows), "max_abs": maxabs,
+                                "rel_l2_vs_bf16_oracle": rel, "rel_l2_vs_fp64_oracle": rel_exact,
+                                "codes_scales": "bit-exact", "pool_bytes": int(pool.storage.numel())}) + "\n")
