@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   for (int q = S + tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
   __syncthreads();
 
-  int page_seq = 0, block_seq = 0;
+  int page_seq = 0;   // CTA page number of the current segment's first page
+  int jn = team;       // next block of this team
   bool first_seg = true;
   for (; have; have = next_segment(sh, pre, x, x_end, seg)) {
     const int L = p.ctx[seg.b];
@@ -429,14 +430,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         for (int k = 0; k < 4; ++k) o[c][nt][k] = 0.f;
     }
 
-    for (int pi = seg.page_begin; pi < seg.page_end; ++pi, ++page_seq) {
-      const int s = page_seq % S;
-      const uint32_t par = (page_seq / S) & 1;
+    // this team's blocks of the segment: CTA-wide block numbers jn = team,
+    // team + NTEAMS, ... (4 blocks of 16 keys per 64-key page)
+    const int seg_first = page_seq, seg_pages = seg.page_end - seg.page_begin;
+    for (; jn < (seg_first + seg_pages) * BPP; jn += NTEAMS) {
+      const int q = jn / BPP, kb = jn - q * BPP;  // CTA page number, block in page
+      const int pi = seg.page_begin + (q - seg_first);
+      const int s = q % S;
+      const uint32_t par = (q / S) & 1;
       const uint32_t st = stage0 + s * geo.stage_bytes;
       const float* ks_s = reinterpret_cast<const float*>(smem + s * geo.stage_bytes + 2 * P * D);
       const float* vs_s = ks_s + P * G_ALL;
-      for (int kb = 0; kb < BPP; ++kb, ++block_seq) {
-        if (block_seq % NTEAMS != team) continue;
+      {
         if (!*abort_flag && !mbar_wait(smem_u32(&full_bar[s]), par)) {
           if (lane == 0) flag(p.status, NK_DEVFLAG_TIMEOUT);
           *abort_flag = 1;
@@ -491,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
           // ---- team exchange: every warp of the team sums the CS partials in warp order
           if constexpr (CS > 1) {
-            const int buf = (block_seq / NTEAMS) & 1;
+            const int buf = (jn / NTEAMS) & 1;
             float* xb = xch + (((size_t)team * 2 + buf) * CS) * (NT * 4 * 32);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             cnt[s] = 0;
             // every reader arrived before its increment: the phase is complete
             if (!mbar_wait(smem_u32(&empty_bar[s]), par)) flag(p.status, NK_DEVFLAG_TIMEOUT);
-            const int qn = page_seq + S;
+            const int qn = q + S;
             if (qn < total)
               issue_page<D>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
                             smem_u32(&full_bar[s]));
@@ -636,6 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         }
       }
     }
+
+    page_seq += seg_pages;
 
     // ---- merge the teams of this segment and write the result
     // row sums: reduce the per-lane partial l over the 8 lanes of a row
