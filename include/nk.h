@@ -109,7 +109,8 @@ size_t nk_kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_hea
  *   k_dev, v_dev     bf16 [total_new][Hkv][D].
  * Writes codes and scales of every (row, kv-head) into the pool. Rows whose
  * position or page id is out of range are skipped and flagged. Two new rows
- * that map to the same slot race (undefined which one wins).
+ * that map to the same slot race (undefined which one wins). Returns
+ * NK_ERR_SHAPE when total_new * Hkv * D / 32 reaches 2^31.
  */
 int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
                  const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,

@@ -6,7 +6,7 @@
 #include "nk_decode.cuh"
 
 namespace nk {
-cudaError_t launch_kv_append(const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
+cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
                              const int32_t* cu_new, int B, int total_new, const void* k, const void* v,
                              int32_t* status, cudaStream_t stream);
 }
@@ -134,8 +134,9 @@ int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t
   if (B == 0 || total_new == 0) return NK_OK;
   if (!block_table_dev || !start_pos_dev || !cu_new_dev || !k_dev || !v_dev) return NK_ERR_NULL;
   if (!aligned(k_dev, 16) || !aligned(v_dev, 16)) return NK_ERR_SHAPE;
-  if ((int64_t)total_new * pool->num_kv_heads * (pool->head_dim / 16) > ((int64_t)1 << 40)) return NK_ERR_SHAPE;
-  const cudaError_t e = launch_kv_append(*pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B,
+  // items of one 64-channel group of K or V of one (row, kv-head), numbered in 32 bits
+  if ((int64_t)total_new * pool->num_kv_heads * 2 * (pool->head_dim / 64) >= ((int64_t)1 << 31)) return NK_ERR_SHAPE;
+  const cudaError_t e = launch_kv_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B,
                                          total_new, k_dev, v_dev, status_dev,
                                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;

@@ -6,16 +6,16 @@
 // INT8 group-64 storage ("NInfer" README, capability list). Rule per group:
 //   a = max|x|, s = fp32(a / 127) (1 if a = 0), q = clamp(rne(fp32(x / s)), +-127).
 //
-// Bandwidth-bound streaming scatter: each thread owns 16 consecutive channels
-// of one (row, kv-head) for both K and V (two 32-byte loads in flight per
-// tensor), four threads form a 64-channel group and reduce its absmax with two
-// shuffles. The per-element quotient is x * RN(1/s) with an exactness guard:
-// the product differs from x/s by less than 2^-16 (|x/s| <= 127.00001) and the
-// correctly rounded fp32 quotient differs from x/s by at most 2^-18, so unless
-// the product lies within 2^-14 of a half-integer both round to the same
-// integer; the rare elements inside that window (and exact ties) take the
-// IEEE division out of line.
+// Bandwidth-bound streaming scatter: a persistent grid streams chunks of
+// consecutive K and V rows into shared memory with bulk asynchronous copies,
+// quantizes one 64-channel group per thread and stores the codes with
+// coalesced writes. The
+// group's scale and its reciprocal come from a per-block table indexed by the
+// bf16 mantissa of the absmax, and the quotient x / s is formed exactly from
+// y = RN(1/s) by one fma refinement, so every element takes the same short
+// path without a division.
 #include "nk_common.cuh"
+#include "nk_ptx.cuh"
 
 namespace nk {
 
@@ -31,130 +31,256 @@ struct AppendParams {
   const uint4* k;
   const uint4* v;
   int32_t* status;
+  int p_shift, hkv_shift;  // log2 of P and Hkv when they are powers of two, else -1
 };
 
-// Exact IEEE path for one element: fp32 quotient, clamp, round half to even.
-// Kept out of line: it runs only for elements within 2^-14 of a rounding
-// boundary (or for groups with a tiny scale), so the common path stays short.
+// Per-block table of the group scale and its reciprocal by bf16 mantissa:
+// for a = (1 + m/128) * 2^E, s = fp32(a / 127) = fp32((1 + m/128) / 127) * 2^E
+// and RN(1/s) = RN(1/s_m) * 2^-E exactly, since scaling by a power of two
+// commutes with rounding while every value stays a normal number. The table
+// holds the bit patterns of s_m and RN(1/s_m); a group applies its exponent
+// E by integer addition on those patterns.
+struct ScaleEntry {
+  uint32_t s_bits, y_bits;
+};
+constexpr int kMinFastExp = 40;  // biased exponent of a: below it (s < 2^-93) every element divides
+
+// IEEE path for one element: fp32 quotient, clamp, round half to even. Kept
+// out of line: only groups of magnitude below 2^-87 take it.
 __device__ __noinline__ uint32_t quantize_exact(float x, float s) {
   float e = __fdiv_rn(x, s);
   e = fminf(fmaxf(e, -127.f), 127.f);
   return (uint32_t)__float2int_rn(e) & 0xffu;
 }
 
-// Quantize 16 values (already fp32) of one group slice; returns the scale and
-// writes 16 int8 codes packed into 4 words.
-__device__ __forceinline__ float quantize16(const float (&x)[16], uint32_t (&packed)[4]) {
-  float a = 0.f;
+// Quantize one 64-channel group held as 32 raw bf16 pairs; returns the
+// group's scale and writes the 64 int8 codes packed into 16 words.
+//
+// absmax: for finite values |x| orders like the bf16 bit pattern with the sign
+// cleared, so it is a 16-bit unsigned max over the pairs. Quotient: with
+// y = RN(1/s), q0 = RN(x * y) is within one ulp of x / s; the remainder
+// r = x - s * q0 is exact in one fma, and RN(q0 + r * y) is the correctly
+// rounded quotient (Markstein's theorem on division by fused multiply-add;
+// tests/quotient_check.c also replays these steps over every bf16 (group max,
+// element) pair of the exponents that matter). t = q + 1.5 * 2^23 then rounds
+// q to an integer (ties to even) whose two's-complement low byte is the low
+// byte of t's bits; |q| <= 127 needs no clamp.
+__device__ __forceinline__ float quantize64(const uint32_t (&w)[32], uint32_t (&packed)[16], const ScaleEntry* tab) {
+  uint32_t m2 = 0;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(x[i]));
-  // four consecutive lanes hold one 64-channel group
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-  const float s = (a == 0.f) ? 1.f : __fdiv_rn(a, 127.f);
-  const float y = __frcp_rn(s);
-  const bool tiny = s < 7.888609052210118e-31f;  // 2^-100: keep RN(1/s) far from overflow
-  // |x * y - x / s| < 2^-16 here, so no clamp is needed on the fast path
-  // (|x / s| <= 127 * (1 + 2^-23)); t = r + 1.5 * 2^23 rounds r to an integer
-  // (ties to even) whose two's-complement low byte is the low byte of t's bits.
-  uint32_t tb[16];
-  uint32_t slow = tiny ? 0xffffu : 0u;
+  for (int i = 0; i < 32; ++i) m2 = __vmaxu2(m2, w[i] & 0x7fff7fffu);
+  const uint32_t abits = max(m2 << 16, m2 & 0xffff0000u);  // fp32 bits of a
+  const int ea = (int)(abits >> 23);
+  if (abits != 0u && ea < kMinFastExp) {
+    const float s = __fdiv_rn(__uint_as_float(abits), 127.f);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float r = __fmul_rn(x[i], y);
-    const float t = __fadd_rn(r, 12582912.f);
-    const float d = __fsub_rn(r, __fsub_rn(t, 12582912.f));
-    if (fabsf(d) > 0.49993896484375f /* 0.5 - 2^-14 */) slow |= 1u << i;
-    tb[i] = __float_as_uint(t);
+    for (int k = 0; k < 16; ++k) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t wv = w[2 * k + (e >> 1)];
+        word |= quantize_exact((e & 1) ? bf16_hi(wv) : bf16_lo(wv), s) << (8 * e);
+      }
+      packed[k] = word;
+    }
+    return s;
   }
-  if (slow) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if ((slow >> i) & 1u) tb[i] = quantize_exact(x[i], s);
+  float s = 1.f, y = 1.f;  // a = 0: every code is 0
+  if (abits != 0u) {
+    const ScaleEntry t = tab[(abits >> 16) & 0x7fu];
+    const int sh = (ea - 127) << 23;
+    s = __uint_as_float(t.s_bits + sh);
+    y = __uint_as_float(t.y_bits - sh);
   }
+  const float ns = -s;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const uint32_t lo = __byte_perm(tb[4 * w], tb[4 * w + 1], 0x0040);
-    const uint32_t hi = __byte_perm(tb[4 * w + 2], tb[4 * w + 3], 0x0040);
-    packed[w] = __byte_perm(lo, hi, 0x5410);
+  for (int k = 0; k < 16; ++k) {
+    uint32_t tb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t wv = w[2 * k + (e >> 1)];
+      const float x = (e & 1) ? bf16_hi(wv) : bf16_lo(wv);
+      const float q0 = __fmul_rn(x, y);
+      const float r = __fmaf_rn(ns, q0, x);
+      const float q = __fmaf_rn(r, y, q0);
+      tb[e] = __float_as_uint(__fadd_rn(q, 12582912.f));
+    }
+    packed[k] = __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
   }
   return s;
 }
 
-__device__ __forceinline__ void unpack16(const uint4& lo, const uint4& hi, float (&x)[16]) {
-  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    x[2 * i] = bf16_lo(w[i]);
-    x[2 * i + 1] = bf16_hi(w[i]);
-  }
-}
+constexpr int kAppendThreads = 128;     // one 64-channel group per thread and chunk
+constexpr int kAppendStages = 3;
+constexpr int kAppendBlocksPerSM = 3;
+constexpr int kChunkBytes = 8192;       // bf16 bytes of K (and of V) per chunk
+constexpr int kDestEntries = 512;       // (row, head) destinations a block looks up at once
+constexpr int kAppendSmemSeqs = 256;    // sequences whose cu_new/start_pos a block stages in shared memory
 
-__global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
-  const int tpr = p.D / 16;  // threads per (row, head)
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t idx = tid / tpr;  // (row, head) index
-  const int part = (int)(tid % tpr);
-  const bool live = idx < (int64_t)p.total_new * p.Hkv;
-  const int j = live ? (int)(idx / p.Hkv) : 0;
-  const int h = live ? (int)(idx % p.Hkv) : 0;
+struct __align__(128) AppendSmem {
+  uint8_t stage[kAppendStages][2 * kChunkBytes];  // K rows | V rows of one chunk, bf16
+  uint8_t codes[2][kChunkBytes];                  // [K|V][row][D] int8 of a chunk, double-buffered
+  int2 dest[kDestEntries];                        // per (chunk of a batch, row): (page * Hkv + head or -1, slot)
+  uint64_t full[kAppendStages];
+  ScaleEntry tab[128];
+  int cu[kAppendSmemSeqs + 1];
+  int start[kAppendSmemSeqs];
+};
 
-  uint4 klo = make_uint4(0, 0, 0, 0), khi = klo, vlo = klo, vhi = klo;
-  if (live) {
-    const int64_t base = (idx * p.D + part * 16) / 8;  // in uint4 units
-    klo = __ldg(p.k + base);
-    khi = __ldg(p.k + base + 1);
-    vlo = __ldg(p.v + base);
-    vhi = __ldg(p.v + base + 1);
-  }
+// Persistent grid, a whole number of blocks per SM. The (row, kv-head) pairs
+// are cut into chunks of R = 8 KB / (2 D) consecutive pairs; block b takes
+// chunks b, b + grid, ... Thread 0 streams the K rows and the V rows of a
+// chunk into a stage of a 3-deep shared-memory ring with two bulk copies
+// (cp.async.bulk, completing on the stage's mbarrier). The destinations of
+// up to kDestEntries / R of the block's chunks (binary search over cu_new,
+// block-table entry) are looked up together, one pair per thread, so their
+// global loads overlap. Per chunk, thread t quantizes group t (K groups, then
+// V groups), reading its 128 bytes in a lane-rotated order so the eight lanes
+// of a quarter-warp hit distinct banks, and puts its 64 codes into a
+// [K|V][row][D] buffer; after one block barrier the stage is refilled and the
+// block stores the codes with coalesced 16-byte writes, one row of one tensor
+// being D contiguous bytes of its page.
+template <int D>
+__global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_kernel(const AppendParams p) {
+  constexpr int GPR = D / kGroup;           // groups per (row, head)
+  constexpr int R = kChunkBytes / (2 * D);  // (row, head) pairs per chunk
+  constexpr int CB = kDestEntries / R;      // chunks per destination batch
+  static_assert(R * GPR == kAppendThreads / 2, "one group per thread");
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  AppendSmem& sm = *reinterpret_cast<AppendSmem*>(smem_raw);
+  const int t = threadIdx.x, lane = t & 31;
+  const bool staged = p.B <= kAppendSmemSeqs;
+  const uint32_t npairs = (uint32_t)p.total_new * (uint32_t)p.Hkv;
+  const uint32_t nchunks = (npairs + R - 1) / R;
+  const uint32_t grid = gridDim.x;
+  if (blockIdx.x >= nchunks) return;
+  const uint32_t my_chunks = (nchunks - blockIdx.x + grid - 1) / grid;
 
-  // destination: sequence b owns rows cu_new[b] .. cu_new[b+1]-1
-  bool ok = live;
-  int64_t dst = 0;
-  int slot = 0;
-  if (live) {
+  auto rows_of = [&](uint32_t c) { return (int)min((uint32_t)R, npairs - c * R); };
+  auto issue = [&](uint32_t k) {  // chunk number k of this block into its stage
+    if (k >= my_chunks) return;
+    const uint32_t c = blockIdx.x + k * grid;
+    const int st = (int)(k % kAppendStages);
+    const uint32_t bytes = (uint32_t)rows_of(c) * D * 2;
+    const uint32_t fb = smem_u32(&sm.full[st]);
+    mbar_arrive_expect_tx(fb, 2 * bytes);
+    const size_t off = (size_t)c * kChunkBytes;
+    bulk_load(smem_u32(sm.stage[st]), reinterpret_cast<const uint8_t*>(p.k) + off, bytes, fb);
+    bulk_load(smem_u32(sm.stage[st]) + kChunkBytes, reinterpret_cast<const uint8_t*>(p.v) + off, bytes, fb);
+  };
+  // destination of pair number `pair`: (page * Hkv + head, slot), or -1 after
+  // flagging a position or page id out of range
+  auto lookup = [&](uint32_t pair) {
+    const uint32_t j = p.hkv_shift >= 0 ? pair >> p.hkv_shift : pair / (uint32_t)p.Hkv;
+    const int h = (int)(pair - j * (uint32_t)p.Hkv);
     int lo = 0, hi = p.B;  // find b with cu_new[b] <= j < cu_new[b+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (__ldg(p.cu_new + mid) <= j) lo = mid; else hi = mid;
+      const int c = staged ? sm.cu[mid] : __ldg(p.cu_new + mid);
+      if (c <= (int)j) lo = mid; else hi = mid;
     }
-    const int b = lo;
-    const int64_t pos = (int64_t)__ldg(p.start_pos + b) + (j - __ldg(p.cu_new + b));
-    if (pos < 0 || pos >= (int64_t)p.max_pages * p.P) {
-      ok = false;
-      if (part == 0) flag(p.status, NK_DEVFLAG_BAD_POS);
-    } else {
-      const int page = __ldg(p.bt + (int64_t)b * p.max_pages + pos / p.P);
-      if (page < 0 || page >= p.num_pages) {
-        ok = false;
-        if (part == 0) flag(p.status, NK_DEVFLAG_BAD_PAGE);
-      } else {
-        slot = (int)(pos % p.P);
-        dst = ((int64_t)page * p.Hkv + h) * p.lay.chunk;
-      }
+    const int c0 = staged ? sm.cu[lo] : __ldg(p.cu_new + lo);
+    const int st0 = staged ? sm.start[lo] : __ldg(p.start_pos + lo);
+    const int64_t pos64 = (int64_t)st0 + ((int)j - c0);
+    if (pos64 < 0 || pos64 >= (int64_t)p.max_pages * p.P || pos64 > 0x7fffffff) {
+      flag(p.status, NK_DEVFLAG_BAD_POS);
+      return make_int2(-1, 0);
     }
-  }
+    const int pos = (int)pos64;
+    const uint32_t pi = p.p_shift >= 0 ? (uint32_t)pos >> p.p_shift : (uint32_t)pos / (uint32_t)p.P;
+    const int page = __ldg(p.bt + (size_t)lo * p.max_pages + pi);
+    if (page < 0 || page >= p.num_pages) {
+      flag(p.status, NK_DEVFLAG_BAD_PAGE);
+      return make_int2(-1, 0);
+    }
+    const int slot = p.p_shift >= 0 ? (pos & (p.P - 1)) : (int)((uint32_t)pos % (uint32_t)p.P);
+    return make_int2(page * p.Hkv + h, slot);
+  };
+  // destinations of the block's chunks k0 .. k0 + CB - 1 (the loads of one
+  // thread's entries are independent, so they are all in flight together)
+  auto lookup_batch = [&](uint32_t k0) {
+#pragma unroll 4
+    for (int e = t; e < kDestEntries; e += kAppendThreads) {
+      const uint32_t k = k0 + e / R;
+      const uint32_t pair = (blockIdx.x + k * grid) * R + e % R;
+      sm.dest[e] = (k < my_chunks && pair < npairs) ? lookup(pair) : make_int2(-1, 0);
+    }
+  };
 
-  const int g = p.D / kGroup;
-  float x[16];
-  uint32_t packed[4];
-  unpack16(klo, khi, x);
-  float s = quantize16(x, packed);
-  if (ok) {
-    *reinterpret_cast<uint4*>(p.pool + dst + (int64_t)slot * p.D + part * 16) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    if ((part & 3) == 0) *reinterpret_cast<float*>(p.pool + dst + p.lay.ks + ((int64_t)slot * g + part / 4) * 4) = s;
+  if (t == 0) {
+    for (int st = 0; st < kAppendStages; ++st) mbar_init(smem_u32(&sm.full[st]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int k = 0; k < kAppendStages; ++k) issue(k);
   }
-  unpack16(vlo, vhi, x);
-  s = quantize16(x, packed);
-  if (ok) {
-    *reinterpret_cast<uint4*>(p.pool + dst + p.lay.vc + (int64_t)slot * p.D + part * 16) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    if ((part & 3) == 0) *reinterpret_cast<float*>(p.pool + dst + p.lay.vs + ((int64_t)slot * g + part / 4) * 4) = s;
+  if (staged) {
+    for (int i = t; i <= p.B; i += kAppendThreads) sm.cu[i] = __ldg(p.cu_new + i);
+    for (int i = t; i < p.B; i += kAppendThreads) sm.start[i] = __ldg(p.start_pos + i);
+  }
+  {
+    const float s_m = __fdiv_rn(1.f + (float)t * 0.0078125f, 127.f);  // t < 128
+    sm.tab[t] = ScaleEntry{__float_as_uint(s_m), __float_as_uint(__frcp_rn(s_m))};
+  }
+  __syncthreads();
+
+  // this thread's group in a chunk: tensor, pair row, group in the row
+  const int isv = t / (R * GPR), gk = t % (R * GPR), row = gk / GPR, grp = gk % GPR;
+  const int rot = lane & 7;  // 16-byte piece read first
+  for (uint32_t k = 0; k < my_chunks; ++k) {
+    if (k % CB == 0) {
+      if (k > 0) __syncthreads();  // the previous batch's entries are no longer read
+      lookup_batch(k);
+      __syncthreads();
+    }
+    const uint32_t c = blockIdx.x + k * grid;
+    const int st = (int)(k % kAppendStages);
+    const int rows = rows_of(c);
+    const int2* dest = sm.dest + (k % CB) * R;
+    if (!mbar_wait(smem_u32(&sm.full[st]), (k / kAppendStages) & 1)) {
+      flag(p.status, NK_DEVFLAG_TIMEOUT);
+      return;
+    }
+    // load the group (pieces in rotated order), quantize
+    uint32_t w[32];
+    const uint8_t* src = sm.stage[st] + isv * kChunkBytes + gk * 128;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int piece = (i + rot) & 7;
+      const uint4 v = *reinterpret_cast<const uint4*>(src + piece * 16);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    uint32_t packed[16];  // codes of the pieces in the same rotated order
+    const float s = quantize64(w, packed, sm.tab);
+    uint8_t* codes = sm.codes[k & 1];
+    uint8_t* cdst = codes + isv * (R * D) + row * D + grp * kGroup;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int piece = (i + rot) & 7;
+      *reinterpret_cast<uint2*>(cdst + piece * 8) = make_uint2(packed[2 * i], packed[2 * i + 1]);
+    }
+    const int2 d = dest[row];
+    if (row < rows && d.x >= 0)
+      *reinterpret_cast<float*>(p.pool + (int64_t)d.x * p.lay.chunk + (isv ? p.lay.vs : p.lay.ks) +
+                                (d.y * GPR + grp) * 4) = s;
+    __syncthreads();  // stage st fully read, codes of chunk k complete, codes of chunk k - 1 stored
+    if (t == 0) {
+      // generic-proxy reads of the stage are ordered before the bulk copy that refills it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(k + kAppendStages);
+    }
+    // coalesced stores: 16 bytes per thread and step, rows of D bytes
+#pragma unroll
+    for (int i = 0; i < kChunkBytes / (16 * kAppendThreads); ++i) {
+      const int o = (i * kAppendThreads + t) * 16;
+      const int tv = o / (R * D), rem = o % (R * D), r = rem / D, col = rem % D;
+      const int2 dd = dest[r];
+      if (r < rows && dd.x >= 0)
+        *reinterpret_cast<uint4*>(p.pool + (int64_t)dd.x * p.lay.chunk + (tv ? p.lay.vc : 0) + dd.y * D + col) =
+            *reinterpret_cast<const uint4*>(codes + o);
+    }
   }
 }
 
-cudaError_t launch_kv_append(const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
+cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
                              const int32_t* cu_new, int B, int total_new, const void* k, const void* v,
                              int32_t* status, cudaStream_t stream) {
   AppendParams p;
@@ -173,11 +299,33 @@ cudaError_t launch_kv_append(const nk_kv_pool& pool, const int32_t* bt, int max_
   p.k = reinterpret_cast<const uint4*>(k);
   p.v = reinterpret_cast<const uint4*>(v);
   p.status = status;
-  const int64_t threads = (int64_t)total_new * p.Hkv * (p.D / 16);
-  const int block = 256;
-  const int64_t grid = (threads + block - 1) / block;
-  if (grid == 0) return cudaSuccess;
-  kv_append_kernel<<<(unsigned)grid, block, 0, stream>>>(p);
+  auto log2_exact = [](int n) {
+    int sh = 0;
+    while ((1 << sh) < n) ++sh;
+    return (1 << sh) == n ? sh : -1;
+  };
+  p.p_shift = log2_exact(p.P);
+  p.hkv_shift = log2_exact(p.Hkv);
+  const int64_t pairs = (int64_t)total_new * p.Hkv;
+  if (pairs * 2 * (p.D / kGroup) >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit numbering
+  if (pairs == 0) return cudaSuccess;
+  if (sms < 1) sms = 1;
+  const int64_t rows_per_chunk = kChunkBytes / (2 * p.D);
+  const int64_t nchunks = (pairs + rows_per_chunk - 1) / rows_per_chunk;
+  const int64_t grid = nchunks < (int64_t)sms * kAppendBlocksPerSM ? nchunks : (int64_t)sms * kAppendBlocksPerSM;
+  const int smem = (int)sizeof(AppendSmem);
+  cudaError_t e;
+  if (p.D == 256) {
+    e = cudaFuncSetAttribute(kv_append_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) kv_append_kernel<256><<<(unsigned)grid, kAppendThreads, smem, stream>>>(p);
+  } else if (p.D == 128) {
+    e = cudaFuncSetAttribute(kv_append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) kv_append_kernel<128><<<(unsigned)grid, kAppendThreads, smem, stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(kv_append_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) kv_append_kernel<64><<<(unsigned)grid, kAppendThreads, smem, stream>>>(p);
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
