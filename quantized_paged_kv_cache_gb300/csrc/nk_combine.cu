@@ -5,106 +5,104 @@
 //   O = sum_s exp(LSE_s - M) O_s / sum_s exp(LSE_s - M),  M = max_s LSE_s,
 // with empty partials (LSE = -inf) weighted 0.
 //
-// One warp per (row, 128-channel slice). The lanes first read the S LSE values
-// in parallel (max and weights by warp shuffles, weights kept in shared
-// memory), then walk the partials with four independent vector loads in
-// flight per lane, so the merge is bound by L2/HBM bandwidth rather than by
-// one dependent load per partial.
+// One 256-thread block per output row. Thread t owns 4 channels (a float4)
+// and every PL = 256 / (D / 4)-th partial: it issues the loads of up to 8 of
+// its partials (LSE and row slice) before using any, merges them online
+// (running max, rescaled sum), and the PL partial-lanes of a channel group are
+// merged through shared memory. A row of S partials thus costs about
+// S / (8 PL) dependent memory round trips instead of S / 4.
 #include "nk_decode.cuh"
 
 namespace nk {
 
-constexpr int kCombWarps = 8;
-constexpr int kWtsPerWarp = 512;  // weights kept in shared memory; more partials recompute theirs
+constexpr int kCombThreads = 256;
+constexpr int kCombUnroll = 8;
 
-// lse_of(s): LSE of partial s (-inf to skip it); row_of(s): its fp32 row slice.
-template <int CPL, class LseFn, class RowFn>
-__device__ __forceinline__ void merge_slice(int S, LseFn lse_of, RowFn row_of, int lane, float* wts,
-                                            uint16_t* out_slice) {
-  float mx = -INFINITY;
-  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_of(s));
+// lse_of(s): LSE of partial s (-inf: skip it); row_of(s): its fp32 row.
+template <int D, class LseFn, class RowFn>
+__device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uint16_t* out_row) {
+  constexpr int CH = D / 4;               // float4 channel groups
+  constexpr int PL = kCombThreads / CH;   // partial-lanes
+  __shared__ float sm_m[PL][CH], sm_l[PL][CH];
+  __shared__ float4 sm_o[PL][CH];
+  const int t = threadIdx.x, pl = t / CH, ch = t % CH;
+  float m = -INFINITY, l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = pl; s0 < S; s0 += PL * kCombUnroll) {
+    float ls[kCombUnroll];
+    float4 v[kCombUnroll];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float wsum = 0.f;
-  if (mx != -INFINITY) {
-    for (int s = lane; s < S; s += 32) {
-      const float ls = lse_of(s);
-      const float w = (ls == -INFINITY) ? 0.f : expf(ls - mx);
-      if (s < kWtsPerWarp) wts[s] = w;
-      wsum += w;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-  __syncwarp();
-  float acc[CPL];
-#pragma unroll
-  for (int j = 0; j < CPL; ++j) acc[j] = 0.f;
-  if (mx != -INFINITY) {
-    auto weight = [&](int s) {
-      if (s < kWtsPerWarp) return wts[s];
-      const float ls = lse_of(s);
-      return ls == -INFINITY ? 0.f : expf(ls - mx);
-    };
-    int s = 0;
-    for (; s + 4 <= S; s += 4) {
-      float w[4];
-      float v[4][CPL];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        w[u] = weight(s + u);
-        const float* src = row_of(s + u) + lane * CPL;
-        if constexpr (CPL == 4) {
-          const float4 f = (w[u] != 0.f) ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
-          v[u][0] = f.x;
-          v[u][1] = f.y;
-          v[u][2] = f.z;
-          v[u][3] = f.w;
-        } else {
-          const float2 f = (w[u] != 0.f) ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
-          v[u][0] = f.x;
-          v[u][1] = f.y;
-        }
+    for (int u = 0; u < kCombUnroll; ++u) {
+      const int s = s0 + u * PL;
+      ls[u] = -INFINITY;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s < S) {
+        ls[u] = lse_of(s);
+        v[u] = *reinterpret_cast<const float4*>(row_of(s) + ch * 4);  // read even if skipped: never used then
       }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) acc[j] = fmaf(w[u], v[u][j], acc[j]);
     }
-    for (; s < S; ++s) {
-      const float w = weight(s);
-      if (w == 0.f) continue;
-      const float* src = row_of(s) + lane * CPL;
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) acc[j] = fmaf(w, src[j], acc[j]);
+    for (int u = 0; u < kCombUnroll; ++u) {
+      if (ls[u] == -INFINITY) continue;
+      if (ls[u] > m) {
+        const float a = expf(m - ls[u]);  // 0 while nothing was merged
+        l *= a;
+        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+        m = ls[u];
+      }
+      const float w = expf(ls[u] - m);
+      l += w;
+      acc.x = fmaf(w, v[u].x, acc.x);
+      acc.y = fmaf(w, v[u].y, acc.y);
+      acc.z = fmaf(w, v[u].z, acc.z);
+      acc.w = fmaf(w, v[u].w, acc.w);
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  sm_m[pl][ch] = m;
+  sm_l[pl][ch] = l;
+  sm_o[pl][ch] = acc;
+  __syncthreads();
+  if (pl == 0) {
+    float mx = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < CPL; j += 2) {
-    const uint32_t lo = f32_to_bf16(acc[j] * inv), hi = f32_to_bf16(acc[j + 1] * inv);
-    *reinterpret_cast<uint32_t*>(out_slice + lane * CPL + j) = lo | (hi << 16);
+    for (int q = 0; q < PL; ++q) mx = fmaxf(mx, sm_m[q][ch]);
+    float lsum = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int q = 0; q < PL; ++q) {
+        const float mq = sm_m[q][ch];
+        if (mq == -INFINITY) continue;
+        const float a = expf(mq - mx);
+        const float4 oq = sm_o[q][ch];
+        lsum = fmaf(a, sm_l[q][ch], lsum);
+        o.x = fmaf(a, oq.x, o.x);
+        o.y = fmaf(a, oq.y, o.y);
+        o.z = fmaf(a, oq.z, o.z);
+        o.w = fmaf(a, oq.w, o.w);
+      }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const uint32_t w0 = f32_to_bf16(o.x * inv) | (f32_to_bf16(o.y * inv) << 16);
+    const uint32_t w1 = f32_to_bf16(o.z * inv) | (f32_to_bf16(o.w * inv) << 16);
+    *reinterpret_cast<uint2*>(out_row + ch * 4) = make_uint2(w0, w1);
   }
 }
 
 // Combine for the decode kernels: units whose pages sit in one CTA were
 // written directly by that CTA; the others merge the partial slots c + u of
 // the CTAs c their pages span (CTAs with an empty range wrote nothing).
-template <int CPL>
-__global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const DecodeParams p) {
+// Block = one (unit, row).
+template <int D>
+__global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const DecodeParams p) {
   __shared__ int pre[kMaxBatch + 1];
   __shared__ int warp_tot[8];
-  __shared__ float wts_all[kCombWarps][kWtsPerWarp];
   const SplitShape sh = p.shape();
   block_page_prefix(sh, p.ctx, pre, warp_tot);
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
-  const int M = p.G * p.T, D = p.D;
-  const int slices = D / (CPL * 32);
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int64_t gw = (int64_t)blockIdx.x * kCombWarps + wib;
-  if (gw >= (int64_t)p.B * p.Hkv * M * slices || W == 0) return;
-  const int slice = (int)(gw % slices);
-  const int64_t ur = gw / slices;
+  const int M = p.G * p.T;
+  const int64_t ur = blockIdx.x;
+  if (ur >= (int64_t)p.B * p.Hkv * M || W == 0) return;
   const int u = (int)(ur / M), r = (int)(ur % M);
   const int b = u / p.Hkv, h = u % p.Hkv;
   const int pages = pre[b + 1] - pre[b];
@@ -119,48 +117,37 @@ __global__ void __launch_bounds__(kCombWarps * 32) decode_combine_kernel(const D
     if (cta_begin(W, n, c) == cta_begin(W, n, c + 1)) return -INFINITY;
     return p.part_lse[((int64_t)c + u) * M + r];
   };
-  auto row_of = [&](int s) { return p.part_o + (((int64_t)c0 + s + u) * M + r) * D + slice * CPL * 32; };
+  auto row_of = [&](int s) { return p.part_o + (((int64_t)c0 + s + u) * M + r) * D; };
   const int t = r / p.G, hg = r % p.G;
-  uint16_t* orow = p.out + (((int64_t)b * p.T + t) * p.Hq + h * p.G + hg) * D + slice * CPL * 32;
-  merge_slice<CPL>(c1 - c0 + 1, lse_of, row_of, lane, wts_all[wib], orow);
+  merge_row<D>(c1 - c0 + 1, lse_of, row_of, p.out + (((int64_t)b * p.T + t) * p.Hq + h * p.G + hg) * D);
 }
 
-// Standalone combine: part_o [S][R][D], part_lse [S][R] -> out [R][D].
-template <int CPL>
-__global__ void __launch_bounds__(kCombWarps * 32) attn_combine_kernel(const float* part_o, const float* part_lse,
-                                                                     int S, int R, int D, uint16_t* out) {
-  __shared__ float wts_all[kCombWarps][kWtsPerWarp];
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const int slices = D / (CPL * 32);
-  const int64_t gw = (int64_t)blockIdx.x * kCombWarps + wib;
-  if (gw >= (int64_t)R * slices) return;
-  const int slice = (int)(gw % slices);
-  const int64_t row = gw / slices;
+// Standalone combine: part_o [S][R][D], part_lse [S][R] -> out [R][D]; block = row.
+template <int D>
+__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const float* part_o, const float* part_lse, int S,
+                                                                  int R, uint16_t* out) {
+  const int64_t row = blockIdx.x;
+  if (row >= R) return;
   auto lse_of = [&](int s) { return part_lse[(int64_t)s * R + row]; };
-  auto row_of = [&](int s) { return part_o + ((int64_t)s * R + row) * D + slice * CPL * 32; };
-  merge_slice<CPL>(S, lse_of, row_of, lane, wts_all[wib], out + row * D + slice * CPL * 32);
+  auto row_of = [&](int s) { return part_o + ((int64_t)s * R + row) * D; };
+  merge_row<D>(S, lse_of, row_of, out + row * D);
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
-  const int cpl = p.D >= 128 ? 4 : 2;
-  const int64_t warps = (int64_t)p.B * p.Hkv * p.G * p.T * (p.D / (cpl * 32));
-  const int64_t grid = (warps + kCombWarps - 1) / kCombWarps;
+  const int64_t grid = (int64_t)p.B * p.Hkv * p.G * p.T;
   if (grid == 0) return cudaSuccess;
-  if (cpl == 4) decode_combine_kernel<4><<<(unsigned)grid, kCombWarps * 32, 0, stream>>>(p);
-  else decode_combine_kernel<2><<<(unsigned)grid, kCombWarps * 32, 0, stream>>>(p);
+  if (p.D == 256) decode_combine_kernel<256><<<(unsigned)grid, kCombThreads, 0, stream>>>(p);
+  else if (p.D == 128) decode_combine_kernel<128><<<(unsigned)grid, kCombThreads, 0, stream>>>(p);
+  else decode_combine_kernel<64><<<(unsigned)grid, kCombThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_combine(const float* part_o, const float* part_lse, int S, int R, int D, uint16_t* out,
                                 cudaStream_t stream) {
-  const int cpl = D >= 128 ? 4 : 2;
-  const int64_t warps = (int64_t)R * (D / (cpl * 32));
-  const int64_t grid = (warps + kCombWarps - 1) / kCombWarps;
-  if (grid == 0) return cudaSuccess;
-  if (cpl == 4)
-    attn_combine_kernel<4><<<(unsigned)grid, kCombWarps * 32, 0, stream>>>(part_o, part_lse, S, R, D, out);
-  else
-    attn_combine_kernel<2><<<(unsigned)grid, kCombWarps * 32, 0, stream>>>(part_o, part_lse, S, R, D, out);
+  if (R == 0) return cudaSuccess;
+  if (D == 256) attn_combine_kernel<256><<<(unsigned)R, kCombThreads, 0, stream>>>(part_o, part_lse, S, R, out);
+  else if (D == 128) attn_combine_kernel<128><<<(unsigned)R, kCombThreads, 0, stream>>>(part_o, part_lse, S, R, out);
+  else attn_combine_kernel<64><<<(unsigned)R, kCombThreads, 0, stream>>>(part_o, part_lse, S, R, out);
   return cudaGetLastError();
 }
 

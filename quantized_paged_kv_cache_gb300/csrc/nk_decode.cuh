@@ -36,6 +36,8 @@ __device__ __forceinline__ void flag_bad_ctx(const DecodeParams& p) {
 
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
+bool decode_tc_supported(int D, int T, int G, int P);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_attn_combine(const float* part_o, const float* part_lse, int S, int R, int D, uint16_t* out,
                                 cudaStream_t stream);

@@ -1,0 +1,655 @@
+// nk_decode_tc.cu -- split-KV paged attention over the INT8 group-64 cache
+// with QK^T on the 5th-generation tensor cores (tcgen05, accumulators in
+// tensor memory) and PV on mma.sync, for head_dim 256, 64-key pages and up to
+// 32 query rows per kv-head (G * T).
+//
+// Attention re-reads the whole cache every step ("NInfer-3090" README,
+// "Choosing a KV format"); decode and MTP-verify rounds attend T = draft+1
+// columns per sequence ("Decode after the small-T kernels"). The int8 codes
+// enter both products exactly (as fp16); the group scales are applied to fp32
+// partial sums (K) and folded into the probabilities (V).
+//
+// CTA = 12 warps, one per SM, same stream-K split over (sequence, kv-head,
+// page) items as the mma.sync kernel, same TMA page ring (one stage = the
+// K|V code tiles and both scale arrays of one page; the last reader of a
+// stage loads the page S ahead into it).
+//
+// Score warps 0-3 (one per tensor-memory lane quadrant), per 64-key page:
+//   * Convert: thread (quadrant w, lane l) takes key k = 32 (w & 1) + l and
+//     channel half c = w >> 1, widens its 128 codes to fp16 and stores them
+//     into tensor-memory row 64 c + k: the page becomes a 128-row A operand
+//     whose rows 0-63 hold channels 0-127 of the keys and rows 64-127
+//     channels 128-255.
+//   * QK: one thread issues 8 tcgen05.mma (M = 128, N = 2W, K = 16) into two
+//     accumulators: A = groups 0|2, B = groups 1|3. The B operand stacks the
+//     query rows twice, once with the channels of the first half and once
+//     with those of the second (W rows each, zero padded), so lanes 0-63 of
+//     columns [0, W) and lanes 64-127 of columns [W, 2W) are the per-group
+//     dot products; the other quarter-blocks are unused.
+//   * Scores: each thread loads its lane's two accumulator rows, applies its
+//     key's two group scales (times sm_scale log2 e) and swaps half of its
+//     rows with the thread holding the other channel half of the same key,
+//     so quadrants 0-1 finish rows with (n mod 8) < 4 and quadrants 2-3 the
+//     rest.
+//   * Online softmax in base 2 with a lazy reference per row (raised only
+//     when a score passes it by more than 8, agreed by the two warps of a
+//     row half), P' = p * Vs[key][group] split into fp16 hi + lo, written to
+//     a double-buffered shared-memory tile [group][hi|lo][8-row tile][key].
+// PV warps 4-11: warp 4 + i owns channels [32 i, 32 i + 32) (group i / 2) for
+//   all rows; per page it rescales its accumulators if a reference moved,
+//   then O^T[ch][row] += V^T[ch][key] P'^T[key][row] with mma.sync m16n8k16
+//   (swap-AB), V^T fragments from ldmatrix.trans on the TMA tile, P'
+//   fragments from ldmatrix.trans on the score warps' tile (hi and lo: two
+//   MMAs).
+// The score warps run one page ahead: the conversion and MMAs of page j + 1
+// are issued before the scores of page j are read (two tensor-memory
+// buffers). At the end of a segment the row sums are reduced and the PV warps
+// write bf16 rows (whole unit) or fp32 partials with their LSE.
+// Every mbarrier wait is bounded; a timeout sets NK_DEVFLAG_TIMEOUT.
+#include "nk_decode_mma.cuh"
+
+namespace nk {
+namespace mma {
+cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map);
+}
+
+namespace tc {
+
+using namespace mma;
+
+constexpr int kD = 256, kP = 64;
+constexpr int kConvWarps = 4, kScoreWarps = 4, kPvWarps = 8;
+constexpr int kWarps = kConvWarps + kScoreWarps + kPvWarps;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTmemCols = 512;
+constexpr int kStageBytes = 2 * kP * kD + 2 * kP * (kD / kGroup) * 4;  // 34816, a multiple of 1024
+constexpr int kPidCache = 512;
+constexpr int kColA = 0;      // tensor-memory columns of the two K buffers (64 each)
+constexpr int kColAcc = 128;  // the two accumulator buffers (4W each)
+
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);  // fp16 A/B, K-major, fp32 D
+}
+
+// K-major, 128-byte-swizzled shared-memory operand: rows of 128 bytes, 8-row
+// atoms 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3fff) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+         ((uint64_t)2 << 61);
+}
+
+struct Layout {
+  int stages;
+  int off_qt, off_pbuf, off_hdr, off_xs, off_red, off_pre, off_pid, off_bar, off_tmem;
+  int total;
+};
+
+__host__ __device__ inline Layout layout(int W, int NT) {
+  Layout L;
+  int off = 0;
+  const int qt = 2 * (2 * W) * 128;
+  const int pbuf = 2 * NT * 8192;
+  const int hdr = 512;
+  const int xs = 2 * 2 * 64 * NT * 4 * 4;
+  const int red = (2 * 4 * 32 + 2 * 32) * 4 + 4 * 4 + 32 * 4 + 64;
+  const int pre = round_up((kMaxBatch + 1 + 16 + 8 + 4) * 4, 16);
+  const int pid = kPidCache * 4;
+  const int bar = 32 * 8;
+  const int fixed = qt + pbuf + hdr + xs + red + pre + pid + bar + 16;
+  int s = (kSmemLimit - 1024 - fixed) / kStageBytes;
+  if (s > 8) s = 8;
+  L.stages = s;
+  off = s * kStageBytes;
+  L.off_qt = off; off += qt;
+  L.off_pbuf = off; off += pbuf;
+  L.off_hdr = off; off += hdr;
+  L.off_xs = off; off += xs;
+  L.off_red = off; off += red;
+  L.off_pre = off; off += pre;
+  L.off_pid = off; off += pid;
+  L.off_bar = off; off += bar;
+  L.off_tmem = off; off += 16;
+  L.total = off + 1024;
+  return L;
+}
+
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// W: padded query rows per channel half of the QK operand (16 or 32);
+// NT: 8-row tiles of the PV product (ceil(G*T / 8) <= W / 8).
+template <int W, int NT>
+__global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                const DecodeParams p) {
+  constexpr int NR = NT * 4;  // rows a score thread finishes (half of each 8-row tile)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Layout LY = layout(W, NT);
+  const int S = LY.stages;
+  int* pre = reinterpret_cast<int*>(smem + LY.off_pre);
+  int* warp_tot = pre + (kMaxBatch + 1);
+  int* cnt = warp_tot + 16;  // [8]
+  volatile int* abort_flag = cnt + 8;
+  int* pid = reinterpret_cast<int*>(smem + LY.off_pid);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + LY.off_bar);
+  uint64_t* empty_bar = full_bar + 8;
+  uint64_t* qk_bar = empty_bar + 8;       // [2] QK MMAs of a page done
+  uint64_t* accfree_bar = qk_bar + 2;     // [2] score warps done reading an accumulator buffer
+  uint64_t* pfull_bar = accfree_bar + 2;  // [2]
+  uint64_t* pempty_bar = pfull_bar + 2;   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY.off_tmem);
+  float* red_l = reinterpret_cast<float*>(smem + LY.off_red);  // [4 score warps][32]
+  float* red_m = red_l + 4 * 32;                               // [4][32]
+  float* lrow = red_m + 4 * 32;                                // [32]
+  float* mrow = lrow + 32;                                     // [32]
+  int* sflag = reinterpret_cast<int*>(mrow + 32);              // [4]
+  int* row_t = sflag + 4;                                      // [32]: query column of row n (T for padding)
+  float* xs = reinterpret_cast<float*>(smem + LY.off_xs);      // [2 pages][2 sides][64 keys][NR]
+  const uint32_t qt0 = smem_u32(smem + LY.off_qt);             // two Q tiles of 2W x 128 bytes
+  uint8_t* pbuf = smem + LY.off_pbuf;                          // [2][4 g][2 h][NT][64][16 B]
+  float* hdr = reinterpret_cast<float*>(smem + LY.off_hdr);    // [2][alpha 32 | side flags 2 | pad]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int role = warp < kConvWarps ? 0 : (warp < kConvWarps + kScoreWarps ? 1 : 2);  // convert | score | PV
+  const int quad = warp & 3;  // tensor-memory lane quadrant this warp may access
+  const SplitShape sh = p.shape();
+  const int G = p.G, T = p.T, M = G * T;
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kWarps);
+      cnt[s] = 0;
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&qk_bar[i]), 1);
+      mbar_init(smem_u32(&accfree_bar[i]), kScoreWarps);
+      mbar_init(smem_u32(&pfull_bar[i]), kScoreWarps);
+      mbar_init(smem_u32(&pempty_bar[i]), kPvWarps);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid < 32) row_t[tid] = tid < M ? tid / G : T;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  flag_bad_ctx(p);
+  block_page_prefix(sh, p.ctx, pre, warp_tot);  // ends with __syncthreads
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int64_t Witems = (int64_t)pre[p.B] * p.Hkv;
+  const int64_t x_begin = Witems == 0 ? 0 : cta_begin(Witems, p.n_ctas, blockIdx.x);
+  const int64_t x_end = Witems == 0 ? 0 : cta_begin(Witems, p.n_ctas, blockIdx.x + 1);
+  const int total = (int)(x_end - x_begin);
+  const uint32_t stage0 = smem_u32(smem);
+
+  if (warp == 0 && total > 0) {
+    const int n0 = total < S ? total : S;
+    if (lane < n0) pid[lane] = page_coord(p, sh, pre, x_begin, lane);
+    __syncwarp();
+    if (lane == 0)
+      for (int q = 0; q < n0; ++q) issue_page<kD>(p, &tmap, pid[q], stage0 + q * kStageBytes, smem_u32(&full_bar[q]));
+  }
+  const int ncache = total < kPidCache ? total : kPidCache;
+  for (int q = S + tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  __syncthreads();
+
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+    if (*abort_flag) return;
+    if (!mbar_wait(smem_u32(bar), parity)) {
+      if (lane == 0) flag(p.status, NK_DEVFLAG_TIMEOUT);
+      *abort_flag = 1;
+    }
+  };
+  // A warp is done with CTA page q's stage; the last of all warps loads page q + S into it.
+  auto release_stage = [&](int q) {
+    __syncwarp();
+    if (lane == 0) {
+      const int s = q % S;
+      mbar_arrive(smem_u32(&empty_bar[s]));
+      if (atomicAdd(&cnt[s], 1) == kWarps - 1) {
+        cnt[s] = 0;
+        if (!mbar_wait(smem_u32(&empty_bar[s]), (q / S) & 1)) flag(p.status, NK_DEVFLAG_TIMEOUT);
+        const int qn = q + S;
+        if (qn < total)
+          issue_page<kD>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn),
+                         stage0 + s * kStageBytes, smem_u32(&full_bar[s]));
+      }
+    }
+  };
+
+  int64_t x = x_begin;
+  Segment seg;
+  int q0 = 0;  // CTA page number of the segment's first page
+  if (role == 0) {
+    // ======================= convert warps: K codes -> tensor memory, QK MMAs
+    const int half = quad >> 1, key = 32 * (quad & 1) + lane;
+    while (next_segment(sh, pre, x, x_end, seg)) {
+      const int npages = seg.page_end - seg.page_begin;
+      // the previous segment's MMAs still read the Q tiles: wait for the last one
+      if (q0 > 0) wait_bar(&qk_bar[(q0 - 1) & 1], ((q0 - 1) >> 1) & 1);
+      // Q tile tb, row r: query row r % W, channels 128 (r / W) + 64 tb + [0, 64)
+      bool big = false;
+      for (int i = tid; i < 2 * 2 * W * 8; i += kConvWarps * 32) {
+        const int c = i & 7, r = (i >> 3) % (2 * W), tb = i / (2 * W * 8);
+        const int n = r % W, ch = 128 * (r / W) + 64 * tb + 8 * c;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n < M) {
+          const int t = n / G, hg = n % G;
+          const uint4 raw =
+              *reinterpret_cast<const uint4*>(p.q + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * kD + ch);
+          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t hw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float f0 = bf16_lo(rw[j]), f1 = bf16_hi(rw[j]);
+            big |= fmaxf(fabsf(f0), fabsf(f1)) > 65504.f;
+            hw[j] = pack_f16(f0, f1);
+          }
+          v = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+        *reinterpret_cast<uint4*>(smem + LY.off_qt + tb * (2 * W * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+      }
+      if (big) flag(p.status, NK_DEVFLAG_RANGE);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q writes -> tensor-core reads
+      named_bar(1, kConvWarps * 32);
+      for (int j = 0; j < npages; ++j) {
+        const int q = q0 + j;
+        const int s = q % S;
+        wait_bar(&full_bar[s], (q / S) & 1);
+        wait_bar(&qk_bar[q & 1], ((q >> 1) & 1) ^ 1);  // MMAs of page q - 2 (same K buffer) done
+        const uint8_t* st = smem + s * kStageBytes;
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + kColA + (q & 1) * 64;
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          uint32_t r[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c = hc * 4 + c4;
+            // box `half` (channels 128 half ..), K row `key`, 16-byte chunk c, 128-byte swizzle
+            const uint4 w4 =
+                *reinterpret_cast<const uint4*>(st + half * (2 * kP * 128) + key * 128 + ((c ^ (key & 7)) << 4));
+            const uint32_t w[4] = {w4.x ^ 0x80808080u, w4.y ^ 0x80808080u, w4.z ^ 0x80808080u, w4.w ^ 0x80808080u};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              r[c4 * 8 + 2 * i] = i8x2_to_f16x2(w[i], 0x4140);
+              r[c4 * 8 + 2 * i + 1] = i8x2_to_f16x2(w[i], 0x4342);
+            }
+          }
+          tmem_st_x32(taddr + hc * 32, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar(1, kConvWarps * 32);
+        if (tid == 0) {
+          wait_bar(&accfree_bar[q & 1], ((q >> 1) & 1) ^ 1);  // scores of page q - 2 read
+          tc_fence_after();
+          constexpr uint32_t idesc = idesc_f16_f32(128, 2 * W);
+          const uint32_t acc = tmem + kColAcc + (q & 1) * (4 * W);
+#pragma unroll
+          for (int tb = 0; tb < 2; ++tb)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_tmem_a(acc + tb * (2 * W), tmem + kColA + (q & 1) * 64 + tb * 32 + ks * 8,
+                         sdesc_sw128(qt0 + tb * (2 * W * 128) + ks * 32), idesc, ks > 0);
+          mma_commit(smem_u32(&qk_bar[q & 1]));
+        }
+        release_stage(q);
+      }
+      q0 += npages;
+    }
+    // all MMAs done before the tensor memory is released
+    if (q0 > 0) wait_bar(&qk_bar[(q0 - 1) & 1], ((q0 - 1) >> 1) & 1);
+  } else if (role == 1) {
+    // ======================= score warps: scores, softmax, P'
+    const int half = quad >> 1, key = 32 * (quad & 1) + lane;
+    float m_ref[NR], l_part[NR];
+    while (next_segment(sh, pre, x, x_end, seg)) {
+      const int L = p.ctx[seg.b];
+      const int npages = seg.page_end - seg.page_begin;
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        m_ref[i] = -INFINITY;
+        l_part[i] = 0.f;
+      }
+      for (int j = 0; j < npages; ++j) {
+        const int q = q0 + j;
+        const int s = q % S;
+        wait_bar(&full_bar[s], (q / S) & 1);  // scale arrays of the page visible
+        wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
+        tc_fence_after();
+        const uint8_t* st = smem + s * kStageBytes;
+        const float* ks_s = reinterpret_cast<const float*>(st + 2 * kP * kD);
+        const float* vs_s = ks_s + kP * (kD / kGroup);
+        const float ka = ks_s[key * 4 + 2 * half] * p.scale2, kb = ks_s[key * 4 + 2 * half + 1] * p.scale2;
+        // ---- this lane's accumulator rows (groups 2 half, 2 half + 1), 16 query rows at a time;
+        // half of the rows go to the thread holding the other channel half of the key
+        float* xq = xs + (q & 1) * (2 * 64 * NR);  // by page parity: a side rewrites it only two pages later
+        float* mine = xq + (half * 64 + key) * NR;
+        float sc[NR];
+        {
+          const uint32_t base = tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + (q & 1) * (4 * W) + half * W;
+#pragma unroll
+          for (int c = 0; c < NT * 8; c += 16) {
+            float ta[16], tb[16];
+            tmem_ld_x16(base + c, ta);
+            tmem_ld_x16(base + 2 * W + c, tb);
+            tmem_wait_ld();
+#pragma unroll
+            for (int nt2 = 0; nt2 < 2; ++nt2) {
+              const int nt = c / 8 + nt2;
+              if (nt >= NT) break;
+              float keep[4], send[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float lo = fmaf(kb, tb[nt2 * 8 + i], ka * ta[nt2 * 8 + i]);
+                const float hi = fmaf(kb, tb[nt2 * 8 + 4 + i], ka * ta[nt2 * 8 + 4 + i]);
+                keep[i] = half ? hi : lo;
+                send[i] = half ? lo : hi;
+                sc[nt * 4 + i] = keep[i];
+              }
+              *reinterpret_cast<float4*>(mine + nt * 4) = make_float4(send[0], send[1], send[2], send[3]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&accfree_bar[q & 1]));
+        named_bar(2, kScoreWarps * 32);
+        {
+          const float* theirs = xq + ((1 - half) * 64 + key) * NR;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float4 rcv = *reinterpret_cast<const float4*>(theirs + nt * 4);
+            sc[nt * 4 + 0] += rcv.x;
+            sc[nt * 4 + 1] += rcv.y;
+            sc[nt * 4 + 2] += rcv.z;
+            sc[nt * 4 + 3] += rcv.w;
+          }
+        }
+        // ---- causal / context mask
+        const int pos = (seg.page_begin + j) * kP + key;
+        const bool key_valid = pos < L;
+        const int lim = pos - (L - T);  // visible to column t when lim <= t
+#pragma unroll
+        for (int i = 0; i < NR; ++i)
+          if (lim > row_t[8 * (i >> 2) + 4 * half + (i & 3)]) sc[i] = -INFINITY;  // padding rows: row_t = T
+        // ---- lazy reference: raised when a score passes it by more than 8
+        bool over = false;
+#pragma unroll
+        for (int i = 0; i < NR; ++i) over |= sc[i] > m_ref[i] + 8.f;
+        const unsigned vote = __ballot_sync(0xffffffffu, over);
+        if (lane == 0) sflag[quad] = vote != 0;
+        named_bar(3 + half, 64);
+        const bool raise = sflag[2 * half] | sflag[2 * half + 1];
+        float al[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) al[i] = 1.f;
+        if (raise) {
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            float mb = sc[i];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+            if (lane == 0) red_m[quad * 32 + i] = mb;
+          }
+          named_bar(3 + half, 64);
+#pragma unroll
+          for (int i = 0; i < NR; ++i) {
+            const float mb = fmaxf(red_m[(2 * half) * 32 + i], red_m[(2 * half + 1) * 32 + i]);
+            const float mnew = fmaxf(m_ref[i], mb);
+            if (mnew > m_ref[i]) {
+              al[i] = ex2(m_ref[i] - mnew);  // 0 while the row was empty
+              l_part[i] *= al[i];
+              m_ref[i] = mnew;
+            }
+          }
+        }
+        // ---- probabilities, row sums, P' = p Vs split into fp16 hi + lo
+        float pr[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          const float mu = m_ref[i] == -INFINITY ? 0.f : m_ref[i];
+          pr[i] = ex2(sc[i] - mu);
+          l_part[i] += pr[i];
+        }
+        wait_bar(&pempty_bar[q & 1], ((q >> 1) & 1) ^ 1);
+        float* alpha = hdr + (q & 1) * 40;  // [32 alpha | side flags]
+        if ((quad & 1) == 0 && lane == 0) {
+          // the PV warps rescale their accumulators by alpha before adding this page
+#pragma unroll
+          for (int i = 0; i < NR; ++i) alpha[8 * (i >> 2) + 4 * half + (i & 3)] = al[i];
+          reinterpret_cast<int*>(alpha + 32)[half] = raise ? 1 : 0;
+        }
+        uint8_t* pb = pbuf + (q & 1) * (NT * 8192);
+#pragma unroll
+        for (int gq = 0; gq < 4; ++gq) {
+          const float vs = key_valid ? vs_s[key * 4 + gq] : 0.f;  // slots past ctx_len may hold NaN scales
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float q0v = pr[nt * 4 + 0] * vs, q1v = pr[nt * 4 + 1] * vs;
+            const float q2v = pr[nt * 4 + 2] * vs, q3v = pr[nt * 4 + 3] * vs;
+            const __half2 h01 = __floats2half2_rn(q0v, q1v), h23 = __floats2half2_rn(q2v, q3v);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const uint32_t l01 = pack_f16(q0v - f01.x, q1v - f01.y), l23 = pack_f16(q2v - f23.x, q3v - f23.y);
+            uint8_t* dst = pb + (((gq * 2 + 0) * NT + nt) * 64 + key) * 16 + half * 8;
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+            *reinterpret_cast<uint2*>(dst + NT * 64 * 16) = make_uint2(l01, l23);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&pfull_bar[q & 1]));
+        release_stage(q);
+      }
+      q0 += npages;
+      // ---- row sums of the segment: reduce l over the 64 keys of each side
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        float v = l_part[i];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == 0) red_l[quad * 32 + i] = v;
+      }
+      named_bar(5, (kScoreWarps + kPvWarps) * 32);
+      if ((quad & 1) == 0 && lane == 0) {
+        // m_ref is identical across the two warps of a side
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          const int n = 8 * (i >> 2) + 4 * half + (i & 3);
+          lrow[n] = red_l[quad * 32 + i] + red_l[(quad + 1) * 32 + i];
+          mrow[n] = m_ref[i];
+        }
+      }
+      named_bar(5, (kScoreWarps + kPvWarps) * 32);
+      named_bar(5, (kScoreWarps + kPvWarps) * 32);  // the PV warps have read lrow / mrow
+    }
+  } else {
+    // ======================= PV warps
+    const int pw = warp - kConvWarps - kScoreWarps;
+    const int g_lane = lane >> 2, t4 = lane & 3;
+    const int gq = pw >> 1;  // channel group of this warp
+    const int lm_key = ((lane >> 3) & 1) * 8 + (lane & 7);
+    const uint32_t loff = box_off<kD>(kP, 0, lm_key, 2 * pw + (lane >> 4));
+    float o[2][NT][4];
+    while (next_segment(sh, pre, x, x_end, seg)) {
+      const int npages = seg.page_end - seg.page_begin;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[cc][nt][k] = 0.f;
+      for (int j = 0; j < npages; ++j) {
+        const int q = q0 + j;
+        const int s = q % S;
+        wait_bar(&full_bar[s], (q / S) & 1);
+        wait_bar(&pfull_bar[q & 1], (q >> 1) & 1);
+        const float* alpha = hdr + (q & 1) * 40;
+        const int* sf = reinterpret_cast<const int*>(alpha + 32);
+        if (sf[0] | sf[1]) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float al = alpha[8 * nt + 2 * t4 + e];
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc) {
+                o[cc][nt][e] *= al;
+                o[cc][nt][e + 2] *= al;
+              }
+            }
+        }
+        const uint32_t st = stage0 + s * kStageBytes;
+        const uint32_t pb = smem_u32(pbuf + (q & 1) * (NT * 8192));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t vw[2][2];
+          ldsm_x4_t(st + (kP + kk * 16) * 128 + loff, vw[0][0], vw[0][1], vw[1][0], vw[1][1]);
+          uint32_t av[2][4];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint32_t w0 = vw[cc][0] ^ 0x80808080u, w1 = vw[cc][1] ^ 0x80808080u;
+            av[cc][0] = i8x2_to_f16x2(w0, 0x4240);
+            av[cc][1] = i8x2_to_f16x2(w0, 0x4341);
+            av[cc][2] = i8x2_to_f16x2(w1, 0x4240);
+            av[cc][3] = i8x2_to_f16x2(w1, 0x4341);
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            // matrices: (hi, keys 0-7), (hi, keys 8-15), (lo, keys 0-7), (lo, keys 8-15)
+            const int mi = lane >> 3;
+            const uint32_t addr =
+                pb + (((gq * 2 + (mi >> 1)) * NT + nt) * 64 + kk * 16 + (mi & 1) * 8 + (lane & 7)) * 16;
+            uint32_t bh0, bh1, bl0, bl1;
+            ldsm_x4_t(addr, bh0, bh1, bl0, bl1);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) mma16816(o[cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bh0, bh1);
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) mma16816(o[cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bl0, bl1);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&pempty_bar[q & 1]));
+        release_stage(q);
+      }
+      q0 += npages;
+      // ---- segment result: wait for the row statistics, then write the rows
+      named_bar(5, (kScoreWarps + kPvWarps) * 32);
+      named_bar(5, (kScoreWarps + kPvWarps) * 32);
+      const int64_t slot = (int64_t)blockIdx.x + seg.u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int n = 8 * nt + 2 * t4 + e;
+          if (n >= M) continue;
+          const float lsum = lrow[n];
+          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int ch = 32 * pw + 16 * cc + 2 * g_lane;
+            const float v0 = o[cc][nt][e] * inv, v1 = o[cc][nt][e + 2] * inv;
+            if (!isfinite(v0) || !isfinite(v1)) flag(p.status, NK_DEVFLAG_RANGE);
+            if (seg.whole) {
+              const int t = n / G, hg = n % G;
+              *reinterpret_cast<uint32_t*>(p.out + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * kD + ch) =
+                  (uint32_t)f32_to_bf16(v0) | ((uint32_t)f32_to_bf16(v1) << 16);
+            } else {
+              *reinterpret_cast<float2*>(p.part_o + (slot * M + n) * kD + ch) = make_float2(v0, v1);
+            }
+          }
+          if (!seg.whole && pw == 0 && g_lane == 0) {
+            const float mx = mrow[n];
+            p.part_lse[slot * M + n] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+          }
+        }
+      named_bar(5, (kScoreWarps + kPvWarps) * 32);
+    }
+  }
+
+  // release tensor memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+template <int W, int NT>
+static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
+  const Layout LY = layout(W, NT);
+  if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<W, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY.total);
+  if (e != cudaSuccess) return e;
+  decode_tc_kernel<W, NT><<<p.n_ctas, kThreads, LY.total, st>>>(map, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+bool decode_tc_supported(int D, int T, int G, int P) {
+  const int M = G * T;
+  return D == tc::kD && P == tc::kP && M >= 1 && M <= 32;
+}
+
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
+  CUtensorMap map;
+  cudaError_t e = mma::make_pool_map(p, &map);
+  if (e != cudaSuccess) return e;
+  const int M = p.G * p.T, NT = (M + 7) / 8;
+  switch (NT) {
+    case 1: return tc::launch_t<16, 1>(map, p, stream);
+    case 2: return tc::launch_t<16, 2>(map, p, stream);
+    case 3: return tc::launch_t<32, 3>(map, p, stream);
+    case 4: return tc::launch_t<32, 4>(map, p, stream);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+}  // namespace nk
