@@ -411,13 +411,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             sc[nt * 4 + 3] += rcv.w;
           }
         }
-        // ---- causal / context mask
+        // ---- causal / context mask: only pages that reach past L - T (padding rows
+        // hold zero queries and are never written out, so they need no mask)
         const int pos = (seg.page_begin + j) * kP + key;
         const bool key_valid = pos < L;
-        const int lim = pos - (L - T);  // visible to column t when lim <= t
+        if ((seg.page_begin + j + 1) * kP > L - T) {
+          const int lim = pos - (L - T);  // visible to column t when lim <= t
 #pragma unroll
-        for (int i = 0; i < NR; ++i)
-          if (lim > row_t[8 * (i >> 2) + 4 * half + (i & 3)]) sc[i] = -INFINITY;  // padding rows: row_t = T
+          for (int i = 0; i < NR; ++i)
+            if (lim > row_t[8 * (i >> 2) + 4 * half + (i & 3)]) sc[i] = -INFINITY;
+        }
         // ---- lazy reference: raised when a score passes it by more than 8
         bool over = false;
 #pragma unroll
