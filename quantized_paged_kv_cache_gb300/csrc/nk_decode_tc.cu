@@ -245,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       *abort_flag = 1;
     }
   };
-  // A warp is done with CTA page q's stage; the last of all warps loads page q + S into it.
-  auto release_stage = [&](int q) {
+  // A warp is done with CTA page q's stage s (phase ph); the last of all warps
+  // loads page q + S into it.
+  auto release_stage = [&](int q, int s, uint32_t ph) {
     __syncwarp();
     if (lane == 0) {
-      const int s = q % S;
       mbar_arrive(smem_u32(&empty_bar[s]));
       if (atomicAdd(&cnt[s], 1) == kWarps - 1) {
         cnt[s] = 0;
-        if (!mbar_wait(smem_u32(&empty_bar[s]), (q / S) & 1)) flag(p.status, NK_DEVFLAG_TIMEOUT);
+        if (!mbar_wait(smem_u32(&empty_bar[s]), ph)) flag(p.status, NK_DEVFLAG_TIMEOUT);
         const int qn = q + S;
         if (qn < total)
           issue_page<kD>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn),
@@ -265,6 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   int64_t x = x_begin;
   Segment seg;
   int q0 = 0;  // CTA page number of the segment's first page
+  // stage and phase of the current page, advanced page by page (no division by S)
+  int s = 0;
+  uint32_t ph = 0;
+  auto next_stage = [&]() {
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  };
   if (role == 0) {
     // ======================= convert warps: K codes -> tensor memory, QK MMAs
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
@@ -299,8 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       named_bar(1, kConvWarps * 32);
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
-        const int s = q % S;
-        wait_bar(&full_bar[s], (q / S) & 1);
+        wait_bar(&full_bar[s], ph);
         wait_bar(&qk_bar[q & 1], ((q >> 1) & 1) ^ 1);  // MMAs of page q - 2 (same K buffer) done
         const uint8_t* st = smem + s * kStageBytes;
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + kColA + (q & 1) * 64;
@@ -338,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
                          sdesc_sw128(qt0 + tb * (2 * W * 128) + ks * 32), idesc, ks > 0);
           mma_commit(smem_u32(&qk_bar[q & 1]));
         }
-        release_stage(q);
+        release_stage(q, s, ph);
+        next_stage();
       }
       q0 += npages;
     }
@@ -358,8 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       }
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
-        const int s = q % S;
-        wait_bar(&full_bar[s], (q / S) & 1);  // scale arrays of the page visible
+        wait_bar(&full_bar[s], ph);  // scale arrays of the page visible
         wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
         tc_fence_after();
         const uint8_t* st = smem + s * kStageBytes;
@@ -487,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&pfull_bar[q & 1]));
-        release_stage(q);
+        release_stage(q, s, ph);
+        next_stage();
       }
       q0 += npages;
       // ---- row sums of the segment: reduce l over the 64 keys of each side
@@ -529,8 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           for (int k = 0; k < 4; ++k) o[cc][nt][k] = 0.f;
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
-        const int s = q % S;
-        wait_bar(&full_bar[s], (q / S) & 1);
+        wait_bar(&full_bar[s], ph);
         wait_bar(&pfull_bar[q & 1], (q >> 1) & 1);
         const float* alpha = hdr + (q & 1) * 40;
         const int* sf = reinterpret_cast<const int*>(alpha + 32);
@@ -578,7 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&pempty_bar[q & 1]));
-        release_stage(q);
+        release_stage(q, s, ph);
+        next_stage();
       }
       q0 += npages;
       // ---- segment result: wait for the row statistics, then write the rows
