@@ -104,7 +104,7 @@ int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32
   p.out = reinterpret_cast<uint16_t*>(out);
   p.status = status;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and <= 32
+  // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and 9 to 32
   // rows per kv-head; the mma.sync kernel for the other shapes
   cudaError_t e = simt ? launch_decode_simt(p, st)
                        : (decode_tc_supported(D, T, G, P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));

@@ -1,6 +1,6 @@
 // nk_decode_tc.cu -- split-KV paged attention over the INT8 group-64 cache
 // with QK^T on the 5th-generation tensor cores (tcgen05, accumulators in
-// tensor memory) and PV on mma.sync, for head_dim 256, 64-key pages and up to
+// tensor memory) and PV on mma.sync, for head_dim 256, 64-key pages and 9 to
 // 32 query rows per kv-head (G * T).
 //
 // Attention re-reads the whole cache every step ("NInfer-3090" README,
@@ -645,9 +645,12 @@ static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaS
 
 }  // namespace tc
 
+// At G * T <= 8 (one 8-row tile, e.g. plain decode at G = 6) the QK product is
+// small and the mma.sync kernel's shorter per-page chain is faster (C1 32K:
+// 34.7 us against 37.3 us for split + combine), so this kernel takes 9 to 32 rows.
 bool decode_tc_supported(int D, int T, int G, int P) {
   const int M = G * T;
-  return D == tc::kD && P == tc::kP && M >= 1 && M <= 32;
+  return D == tc::kD && P == tc::kP && M > 8 && M <= 32;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
@@ -656,7 +659,6 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int M = p.G * p.T, NT = (M + 7) / 8;
   switch (NT) {
-    case 1: return tc::launch_t<16, 1>(map, p, stream);
     case 2: return tc::launch_t<16, 2>(map, p, stream);
     case 3: return tc::launch_t<32, 3>(map, p, stream);
     case 4: return tc::launch_t<32, 4>(map, p, stream);
