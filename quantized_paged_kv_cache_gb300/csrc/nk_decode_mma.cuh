@@ -365,6 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   for (int q = S + tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
   __syncthreads();
 
+  const int bpp_sh = (BPP & (BPP - 1)) == 0 ? __ffs(BPP) - 1 : -1;  // blocks per page, as a shift
+  int q_cur = 0, s_cur = 0;  // last page whose stage was located, and that stage
+  uint32_t par_cur = 0;
   int page_seq = 0;   // CTA page number of the current segment's first page
   int jn = team;       // next block of this team
   bool first_seg = true;
@@ -392,10 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     // team + NTEAMS, ... (4 blocks of 16 keys per 64-key page)
     const int seg_first = page_seq, seg_pages = seg.page_end - seg.page_begin;
     for (; jn < (seg_first + seg_pages) * BPP; jn += NTEAMS) {
-      const int q = jn / BPP, kb = jn - q * BPP;  // CTA page number, block in page
+      const int q = bpp_sh >= 0 ? jn >> bpp_sh : jn / BPP;  // CTA page number
+      const int kb = jn - q * BPP;                           // block in page
       const int pi = seg.page_begin + (q - seg_first);
-      const int s = q % S;
-      const uint32_t par = (q / S) & 1;
+      while (q_cur < q) {  // stage and phase of page q, advanced without a division
+        ++q_cur;
+        if (++s_cur == S) {
+          s_cur = 0;
+          par_cur ^= 1u;
+        }
+      }
+      const int s = s_cur;
+      const uint32_t par = par_cur;
       const uint32_t st = stage0 + s * geo.stage_bytes;
       const float* ks_s = reinterpret_cast<const float*>(smem + s * geo.stage_bytes + 2 * P * D);
       const float* vs_s = ks_s + P * G_ALL;
