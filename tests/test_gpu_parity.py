@@ -39,6 +39,11 @@ SHAPES = [
     ("t5_mix",        4, 5, 12, 4, 256, 16, [5, 64, 65, 3000]),
     ("t1_b8",         8, 1, 24, 4, 256, 64, [64, 1, 128, 129, 4000, 63, 1000, 2]),
     ("t4_p128",       2, 4, 24, 4, 256, 128, [255, 1025]),
+    # the tcgen05 kernel's instances (D = 256, P = 64, 9 <= G*T <= 32)
+    ("t2_tc",         3, 2, 24, 4, 256, 64, [100, 2, 700]),     # M = 12: two 8-row tiles
+    ("t3_tc",         2, 3, 24, 4, 256, 64, [3, 1500]),         # M = 18: three tiles, rows padded to 32
+    ("t4_g8_tc",      2, 4, 32, 4, 256, 64, [65, 900]),         # M = 32: four tiles
+    ("t5_g2_tc",      5, 5, 8, 4, 256, 64, [5, 64, 65, 128, 2000]),  # M = 10, many short units
 ]
 
 
