@@ -6,12 +6,13 @@
 // INT8 group-64 storage ("NInfer" README, capability list). Rule per group:
 //   a = max|x|, s = fp32(a / 127) (1 if a = 0), q = clamp(rne(fp32(x / s)), +-127).
 //
-// Bandwidth-bound streaming scatter: a persistent grid streams chunks of
-// consecutive K and V rows into shared memory with bulk asynchronous copies,
-// quantizes one 64-channel group per thread and stores the codes with
-// coalesced writes. The
-// group's scale and its reciprocal come from a per-block table indexed by the
-// bf16 mantissa of the absmax, and the quotient x / s is formed exactly from
+// Two kernels. Small appends (decode and verify steps, up to 4,096 groups):
+// one thread per group, loading directly. Larger ones: a bandwidth-bound
+// streaming scatter, a persistent grid that streams chunks of consecutive K
+// and V rows into shared memory with bulk asynchronous copies, quantizes one
+// 64-channel group per thread and stores the codes with coalesced writes;
+// there the group's scale and its reciprocal come from a per-block table
+// indexed by the bf16 mantissa of the absmax. Both form x / s exactly from
 // y = RN(1/s) by one fma refinement, so every element takes the same short
 // path without a division.
 #include "nk_common.cuh"
@@ -65,6 +66,9 @@ __device__ __noinline__ uint32_t quantize_exact(float x, float s) {
 // element) pair of the exponents that matter). t = q + 1.5 * 2^23 then rounds
 // q to an integer (ties to even) whose two's-complement low byte is the low
 // byte of t's bits; |q| <= 127 needs no clamp.
+// kTable: s and RN(1/s) from the block's table; otherwise by IEEE division
+// (the same values: the table holds them for every mantissa).
+template <bool kTable>
 __device__ __forceinline__ float quantize64(const uint32_t (&w)[32], uint32_t (&packed)[16], const ScaleEntry* tab) {
   uint32_t m2 = 0;
 #pragma unroll
@@ -87,10 +91,15 @@ __device__ __forceinline__ float quantize64(const uint32_t (&w)[32], uint32_t (&
   }
   float s = 1.f, y = 1.f;  // a = 0: every code is 0
   if (abits != 0u) {
-    const ScaleEntry t = tab[(abits >> 16) & 0x7fu];
-    const int sh = (ea - 127) << 23;
-    s = __uint_as_float(t.s_bits + sh);
-    y = __uint_as_float(t.y_bits - sh);
+    if constexpr (kTable) {
+      const ScaleEntry t = tab[(abits >> 16) & 0x7fu];
+      const int sh = (ea - 127) << 23;
+      s = __uint_as_float(t.s_bits + sh);
+      y = __uint_as_float(t.y_bits - sh);
+    } else {
+      s = __fdiv_rn(__uint_as_float(abits), 127.f);
+      y = __frcp_rn(s);
+    }
   }
   const float ns = -s;
 #pragma unroll
@@ -249,7 +258,7 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
       w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
     uint32_t packed[16];  // codes of the pieces in the same rotated order
-    const float s = quantize64(w, packed, sm.tab);
+    const float s = quantize64<true>(w, packed, sm.tab);
     uint8_t* codes = sm.codes[k & 1];
     uint8_t* cdst = codes + isv * (R * D) + row * D + grp * kGroup;
 #pragma unroll
@@ -278,6 +287,87 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
             *reinterpret_cast<const uint4*>(codes + o);
     }
   }
+}
+
+constexpr int kSmallThreads = 128;
+constexpr int64_t kSmallMaxGroups = 4096;  // appends up to this many groups take the direct kernel
+
+// Small appends (decode and verify steps: a few rows per sequence): one thread
+// per 64-channel group of K or V of one (row, kv-head), nothing staged. The
+// group's eight 16-byte loads go out first and the destination lookup
+// (binary search over cu_new, block-table entry) runs while they are in
+// flight; s = fp32(a / 127) and RN(1/s) come from IEEE division; the codes
+// from the same exact quotient as the streaming kernel.
+template <int D>
+__global__ void __launch_bounds__(kSmallThreads) kv_append_small_kernel(const AppendParams p) {
+  constexpr int GPR = D / kGroup;
+  const uint32_t gid = blockIdx.x * kSmallThreads + threadIdx.x;
+  const uint32_t ngroups = (uint32_t)p.total_new * (uint32_t)p.Hkv * 2u * GPR;
+  const bool live = gid < ngroups;
+  const int lane = threadIdx.x & 31;
+  // up to 32 sequences: lane l holds cu_new[l] and start_pos[l], and the
+  // search below reads them by shuffle instead of by dependent global loads
+  const bool in_regs = p.B <= 32;
+  int cu_l = 0, st_l = 0;
+  if (in_regs) {
+    cu_l = lane <= p.B ? __ldg(p.cu_new + lane) : 0x7fffffff;
+    st_l = lane < p.B ? __ldg(p.start_pos + lane) : 0;
+  }
+  const uint32_t g = live ? gid : 0u;
+  const uint32_t pair = g / (2 * GPR), isv = (g / GPR) & 1u, grp = g % GPR;
+  uint32_t w[32];
+  {
+    const uint4* src = (isv ? p.v : p.k) + (size_t)pair * (D / 8) + grp * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 a = __ldg(src + i);
+      w[4 * i] = a.x; w[4 * i + 1] = a.y; w[4 * i + 2] = a.z; w[4 * i + 3] = a.w;
+    }
+  }
+  const bool flagger = isv == 0 && grp == 0;  // one thread per pair reports bad positions and pages
+  const uint32_t j = p.hkv_shift >= 0 ? pair >> p.hkv_shift : pair / (uint32_t)p.Hkv;
+  const int h = (int)(pair - j * (uint32_t)p.Hkv);
+  int lo = 0, hi = p.B;  // find b with cu_new[b] <= j < cu_new[b+1]
+  int c0, st0;
+  if (in_regs) {
+    for (int it = 0; it < 6; ++it) {  // ceil(log2(32)) + 1 rounds, the same count in every lane
+      const int mid = (lo + hi) >> 1;
+      const int c = __shfl_sync(0xffffffffu, cu_l, mid & 31);
+      if (hi - lo > 1) {
+        if (c <= (int)j) lo = mid; else hi = mid;
+      }
+    }
+    c0 = __shfl_sync(0xffffffffu, cu_l, lo & 31);
+    st0 = __shfl_sync(0xffffffffu, st_l, lo & 31);
+  } else {
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.cu_new + mid) <= (int)j) lo = mid; else hi = mid;
+    }
+    c0 = __ldg(p.cu_new + lo);
+    st0 = __ldg(p.start_pos + lo);
+  }
+  if (!live) return;
+  const int64_t pos64 = (int64_t)st0 + ((int)j - c0);
+  uint32_t packed[16];
+  const float s = quantize64<false>(w, packed, nullptr);
+  if (pos64 < 0 || pos64 >= (int64_t)p.max_pages * p.P || pos64 > 0x7fffffff) {
+    if (flagger) flag(p.status, NK_DEVFLAG_BAD_POS);
+    return;
+  }
+  const int pos = (int)pos64;
+  const uint32_t pi = p.p_shift >= 0 ? (uint32_t)pos >> p.p_shift : (uint32_t)pos / (uint32_t)p.P;
+  const int page = __ldg(p.bt + (size_t)lo * p.max_pages + pi);
+  if (page < 0 || page >= p.num_pages) {
+    if (flagger) flag(p.status, NK_DEVFLAG_BAD_PAGE);
+    return;
+  }
+  const int slot = p.p_shift >= 0 ? (pos & (p.P - 1)) : (int)((uint32_t)pos % (uint32_t)p.P);
+  uint8_t* chunk = p.pool + ((int64_t)page * p.Hkv + h) * p.lay.chunk;
+  uint4* dst = reinterpret_cast<uint4*>(chunk + (isv ? p.lay.vc : 0) + slot * D + grp * kGroup);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  *reinterpret_cast<float*>(chunk + (isv ? p.lay.vs : p.lay.ks) + (slot * GPR + grp) * 4) = s;
 }
 
 cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
@@ -309,6 +399,14 @@ cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt,
   const int64_t pairs = (int64_t)total_new * p.Hkv;
   if (pairs * 2 * (p.D / kGroup) >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit numbering
   if (pairs == 0) return cudaSuccess;
+  const int64_t groups = pairs * 2 * (p.D / kGroup);
+  if (groups <= kSmallMaxGroups) {
+    const unsigned g = (unsigned)((groups + kSmallThreads - 1) / kSmallThreads);
+    if (p.D == 256) kv_append_small_kernel<256><<<g, kSmallThreads, 0, stream>>>(p);
+    else if (p.D == 128) kv_append_small_kernel<128><<<g, kSmallThreads, 0, stream>>>(p);
+    else kv_append_small_kernel<64><<<g, kSmallThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   if (sms < 1) sms = 1;
   const int64_t rows_per_chunk = kChunkBytes / (2 * p.D);
   const int64_t nchunks = (pairs + rows_per_chunk - 1) / rows_per_chunk;

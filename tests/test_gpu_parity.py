@@ -112,9 +112,12 @@ def _bits_to_bf16(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(x.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
 
 
-def test_append_special_values():
+@pytest.mark.parametrize("copies", [1, 3])
+def test_append_special_values(copies):
     """Exact ties, zero groups, negative zeros, huge and tiny magnitudes, and
-    every finite bf16 bit pattern, quantized bit-exactly."""
+    every finite bf16 bit pattern, quantized bit-exactly. One copy (about
+    2,000 groups) takes the small-append kernel, three copies the streaming
+    kernel."""
     D, H, P = 256, 2, 16
     rng = np.random.default_rng(3)
     rows = []
@@ -136,6 +139,7 @@ def test_append_special_values():
     pad = (-fin.size) % 64
     fin = np.concatenate([fin, np.zeros(pad, np.uint16)])
     groups += list(fin.reshape(-1, 64))
+    groups = groups * copies
     n_groups = len(groups)
     per_row = H * D // 64
     n_rows = (n_groups + per_row - 1) // per_row
