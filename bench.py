@@ -61,10 +61,12 @@ def measured_peaks():
 
 
 def source_hash() -> str:
+    """Hash of the decode split kernels' sources and the headers they include
+    (the kernels whose ncu traffic profiles/ncu_traffic.json records)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_paged_kv_cache_gb300", "csrc")
     for fn in sorted(os.listdir(d)):
-        if fn.endswith((".cu", ".cuh")):
+        if fn.startswith("nk_decode") or fn in ("nk_common.cuh", "nk_ptx.cuh"):
             with open(os.path.join(d, fn), "rb") as f:
                 h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
