@@ -482,14 +482,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const float vs = key_valid ? vs_s[key * 4 + gq] : 0.f;  // slots past ctx_len may hold NaN scales
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const float q0v = pr[nt * 4 + 0] * vs, q1v = pr[nt * 4 + 1] * vs;
-            const float q2v = pr[nt * 4 + 2] * vs, q3v = pr[nt * 4 + 3] * vs;
-            const __half2 h01 = __floats2half2_rn(q0v, q1v), h23 = __floats2half2_rn(q2v, q3v);
-            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-            const uint32_t l01 = pack_f16(q0v - f01.x, q1v - f01.y), l23 = pack_f16(q2v - f23.x, q3v - f23.y);
+            // hi = the value cut to 11 significant bits (exact in fp16 for
+            // normal magnitudes), lo = the exact remainder rounded to fp16
+            float v[4], hv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              v[i] = pr[nt * 4 + i] * vs;
+              hv[i] = __uint_as_float(__float_as_uint(v[i]) & 0xffffe000u);
+            }
+            const uint32_t h01 = pack_f16(hv[0], hv[1]), h23 = pack_f16(hv[2], hv[3]);
+            const uint32_t l01 = pack_f16(v[0] - hv[0], v[1] - hv[1]), l23 = pack_f16(v[2] - hv[2], v[3] - hv[3]);
             uint8_t* dst = pb + (((gq * 2 + 0) * NT + nt) * 64 + key) * 16 + half * 8;
-            *reinterpret_cast<uint2*>(dst) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+            *reinterpret_cast<uint2*>(dst) = make_uint2(h01, h23);
             *reinterpret_cast<uint2*>(dst + NT * 64 * 16) = make_uint2(l01, l23);
           }
         }
