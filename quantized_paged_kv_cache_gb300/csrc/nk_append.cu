@@ -151,6 +151,8 @@ struct __align__(128) AppendSmem {
 // being D contiguous bytes of its page.
 template <int D>
 __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_kernel(const AppendParams p) {
+  chain_wait();
+  chain_release();
   constexpr int GPR = D / kGroup;           // groups per (row, head)
   constexpr int R = kChunkBytes / (2 * D);  // (row, head) pairs per chunk
   constexpr int CB = kDestEntries / R;      // chunks per destination batch
@@ -300,6 +302,8 @@ constexpr int64_t kSmallMaxGroups = 4096;  // appends up to this many groups tak
 // from the same exact quotient as the streaming kernel.
 template <int D>
 __global__ void __launch_bounds__(kSmallThreads) kv_append_small_kernel(const AppendParams p) {
+  chain_wait();
+  chain_release();
   constexpr int GPR = D / kGroup;
   const uint32_t gid = blockIdx.x * kSmallThreads + threadIdx.x;
   const uint32_t ngroups = (uint32_t)p.total_new * (uint32_t)p.Hkv * 2u * GPR;
@@ -402,10 +406,9 @@ cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt,
   const int64_t groups = pairs * 2 * (p.D / kGroup);
   if (groups <= kSmallMaxGroups) {
     const unsigned g = (unsigned)((groups + kSmallThreads - 1) / kSmallThreads);
-    if (p.D == 256) kv_append_small_kernel<256><<<g, kSmallThreads, 0, stream>>>(p);
-    else if (p.D == 128) kv_append_small_kernel<128><<<g, kSmallThreads, 0, stream>>>(p);
-    else kv_append_small_kernel<64><<<g, kSmallThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (p.D == 256) return launch_chained(kv_append_small_kernel<256>, dim3(g), dim3(kSmallThreads), 0, stream, p);
+    if (p.D == 128) return launch_chained(kv_append_small_kernel<128>, dim3(g), dim3(kSmallThreads), 0, stream, p);
+    return launch_chained(kv_append_small_kernel<64>, dim3(g), dim3(kSmallThreads), 0, stream, p);
   }
   if (sms < 1) sms = 1;
   const int64_t rows_per_chunk = kChunkBytes / (2 * p.D);
@@ -415,16 +418,18 @@ cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt,
   cudaError_t e;
   if (p.D == 256) {
     e = cudaFuncSetAttribute(kv_append_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) kv_append_kernel<256><<<(unsigned)grid, kAppendThreads, smem, stream>>>(p);
+    if (e == cudaSuccess)
+      e = launch_chained(kv_append_kernel<256>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
   } else if (p.D == 128) {
     e = cudaFuncSetAttribute(kv_append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) kv_append_kernel<128><<<(unsigned)grid, kAppendThreads, smem, stream>>>(p);
+    if (e == cudaSuccess)
+      e = launch_chained(kv_append_kernel<128>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
   } else {
     e = cudaFuncSetAttribute(kv_append_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess) kv_append_kernel<64><<<(unsigned)grid, kAppendThreads, smem, stream>>>(p);
+    if (e == cudaSuccess)
+      e = launch_chained(kv_append_kernel<64>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
   }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace nk

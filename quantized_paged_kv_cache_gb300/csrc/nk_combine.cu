@@ -95,6 +95,8 @@ __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uin
 // Block = one (unit, row).
 template <int D>
 __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const DecodeParams p) {
+  chain_wait();
+  chain_release();
   __shared__ int pre[kMaxBatch + 1];
   __shared__ int warp_tot[8];
   const SplitShape sh = p.shape();
@@ -126,6 +128,8 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
 template <int D>
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const float* part_o, const float* part_lse, int S,
                                                                   int R, uint16_t* out) {
+  chain_wait();
+  chain_release();
   const int64_t row = blockIdx.x;
   if (row >= R) return;
   auto lse_of = [&](int s) { return part_lse[(int64_t)s * R + row]; };
@@ -136,19 +140,19 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const float*
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
   const int64_t grid = (int64_t)p.B * p.Hkv * p.G * p.T;
   if (grid == 0) return cudaSuccess;
-  if (p.D == 256) decode_combine_kernel<256><<<(unsigned)grid, kCombThreads, 0, stream>>>(p);
-  else if (p.D == 128) decode_combine_kernel<128><<<(unsigned)grid, kCombThreads, 0, stream>>>(p);
-  else decode_combine_kernel<64><<<(unsigned)grid, kCombThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const dim3 g((unsigned)grid), b(kCombThreads);
+  if (p.D == 256) return launch_chained(decode_combine_kernel<256>, g, b, 0, stream, p);
+  if (p.D == 128) return launch_chained(decode_combine_kernel<128>, g, b, 0, stream, p);
+  return launch_chained(decode_combine_kernel<64>, g, b, 0, stream, p);
 }
 
 cudaError_t launch_attn_combine(const float* part_o, const float* part_lse, int S, int R, int D, uint16_t* out,
                                 cudaStream_t stream) {
   if (R == 0) return cudaSuccess;
-  if (D == 256) attn_combine_kernel<256><<<(unsigned)R, kCombThreads, 0, stream>>>(part_o, part_lse, S, R, out);
-  else if (D == 128) attn_combine_kernel<128><<<(unsigned)R, kCombThreads, 0, stream>>>(part_o, part_lse, S, R, out);
-  else attn_combine_kernel<64><<<(unsigned)R, kCombThreads, 0, stream>>>(part_o, part_lse, S, R, out);
-  return cudaGetLastError();
+  const dim3 g((unsigned)R), b(kCombThreads);
+  if (D == 256) return launch_chained(attn_combine_kernel<256>, g, b, 0, stream, part_o, part_lse, S, R, out);
+  if (D == 128) return launch_chained(attn_combine_kernel<128>, g, b, 0, stream, part_o, part_lse, S, R, out);
+  return launch_chained(attn_combine_kernel<64>, g, b, 0, stream, part_o, part_lse, S, R, out);
 }
 
 }  // namespace nk

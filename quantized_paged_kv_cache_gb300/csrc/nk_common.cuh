@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "nk.h"
 
 namespace nk {
@@ -30,6 +32,34 @@ struct ChunkLayout {
     return c;
   }
 };
+
+// Programmatic dependent launch. Every kernel of the library is launched
+// with programmatic stream serialization (launch_chained), so it may become
+// resident while the previous kernel on the stream is still running. Each one
+// therefore calls chain_wait() before its first global-memory access (read or
+// write): griddepcontrol.wait returns once every prerequisite grid has
+// completed and its memory operations are visible. Because every kernel waits
+// in every CTA, a kernel cannot complete before its predecessor, so the order
+// of the stream is kept transitively. chain_release() lets the next kernel's
+// CTAs start launching (they only wait, holding no data, until this grid ends).
+__device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void chain_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                  Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ void flag(int32_t* status, uint32_t bits) {
   if (status) atomicOr(reinterpret_cast<unsigned int*>(status), bits);

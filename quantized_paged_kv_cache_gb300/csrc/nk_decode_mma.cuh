@@ -239,6 +239,8 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
 template <int D, int NT, int CS>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                  const DecodeParams p) {
+  chain_wait();
+  chain_release();
   constexpr int NTEAMS = kConsumerWarps / CS;
   constexpr int DW = D / CS;        // channels per warp
   constexpr int NCH = DW / 16;      // 16-channel chunks per warp

@@ -12,8 +12,7 @@ static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaS
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, NT, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        geo.total);
   if (e != cudaSuccess) return e;
-  decode_mma_kernel<D, NT, CS><<<p.n_ctas, kThreads, geo.total, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_chained(decode_mma_kernel<D, NT, CS>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
 }
 
 cudaError_t launch_d64(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st) {

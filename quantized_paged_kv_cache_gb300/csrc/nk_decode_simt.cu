@@ -50,6 +50,8 @@ __device__ __forceinline__ void widen(const Raw<CPL>& r, float (&c)[CPL]) {
 
 template <int CPL>
 __global__ void __launch_bounds__(256) decode_simt_kernel(const DecodeParams p) {
+  chain_wait();
+  chain_release();
   extern __shared__ float smem[];
   __shared__ int pre[kMaxBatch + 1];
   __shared__ int warp_tot[8];
@@ -224,8 +226,7 @@ template <int CPL>
 static cudaError_t launch_simt_t(const DecodeParams& p, size_t smem, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_simt_kernel<CPL><<<p.n_ctas, 256, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(decode_simt_kernel<CPL>, dim3(p.n_ctas), dim3(256), smem, stream, p);
 }
 
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream) {

@@ -159,6 +159,8 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 template <int W, int NT>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const DecodeParams p) {
+  chain_wait();
+  chain_release();
   constexpr int NR = NT * 4;  // rows a score thread finishes (half of each 8-row tile)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -643,8 +645,7 @@ static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaS
   if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<W, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY.total);
   if (e != cudaSuccess) return e;
-  decode_tc_kernel<W, NT><<<p.n_ctas, kThreads, LY.total, st>>>(map, p);
-  return cudaGetLastError();
+  return launch_chained(decode_tc_kernel<W, NT>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
 }
 
 }  // namespace tc
