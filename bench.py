@@ -181,17 +181,13 @@ def run_ours(args, w, rank, world, device):
     dec = nk.paged_decode_attn if args.kernel == "mma" else nk.paged_decode_attn_simt
     stream = torch.cuda.current_stream()
 
-    def step(i, ev_a=None, ev_b=None, ev_0=None):
+    def step(i, what="step"):
         pool = S["pools"][i % replicas]
-        if ev_0 is not None:
-            ev_0.record(stream)
-        nk.kv_append(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
-        if ev_a is not None:
-            ev_a.record(stream)
-        dec(pool, S["q"], S["bt"], S["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
-            out=S["out"], status=S["status"], stream=stream)
-        if ev_b is not None:
-            ev_b.record(stream)
+        if what != "attn":
+            nk.kv_append(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
+        if what != "append":
+            dec(pool, S["q"], S["bt"], S["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
+                out=S["out"], status=S["status"], stream=stream)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -210,29 +206,32 @@ def run_ours(args, w, rank, world, device):
         torch.cuda.synchronize()
 
     K = args.steps
-    evs_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    evs_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    evs_0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    # The timed steps are enqueued behind a spin kernel that outlasts their
-    # host-side enqueue, so Python/launch overhead never leaves the GPU idle
-    # between steps: e0..e1 is back-to-back GPU time (the e2e figure keeps the
-    # host side in).
-    torch.cuda._sleep(int(min(K * host_per_step * 1.5 + 2e-3, 2.0) * 2.2e9))
-    e0.record(stream)
-    for j in range(K):
-        step(j, evs_a[j], evs_b[j], evs_0[j])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+
+    def timed(what):
+        # K back-to-back calls (what: "step" = append + attention, the
+        # headline; "attn" or "append" alone, for the per-call breakdown),
+        # enqueued behind a spin kernel that outlasts their host-side enqueue,
+        # so Python/launch overhead never leaves the GPU idle between them:
+        # e0..e1 is GPU time. No event is recorded between kernels (an event
+        # between two kernels of the stream adds a gap to every call).
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(min(K * host_per_step * 1.5 + 2e-3, 2.0) * 2.2e9))
+        e0.record(stream)
+        for j in range(K):
+            step(j, what)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        return e0.elapsed_time(e1)
+
+    total_ms = timed("step")
+    attn_ms = timed("attn") / K
+    append_ms = timed("append") / K
     clocks = sampler.stop() if sampler else None
-    total_ms = e0.elapsed_time(e1)
-    attn_ms = [a.elapsed_time(b) for a, b in zip(evs_a, evs_b)]
-    append_ms = [z.elapsed_time(a) for z, a in zip(evs_0, evs_a)]
     if int(S["status"].item()) != 0:
         raise RuntimeError(f"device status {int(S['status'].item())} during the benchmark")
 
@@ -429,8 +428,8 @@ def main():
         return 0
     peaks, src = measured_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    attn_us = statistics.mean(r["attn_ms"]) * 1e3
-    append_us = statistics.mean(r["append_ms"]) * 1e3
+    attn_us = r["attn_ms"] * 1e3
+    append_us = r["append_ms"] * 1e3
     achieved = w.attn_bytes() / (attn_us * 1e-6) / 1e9
     traffic = ncu_traffic(w.name, args.kernel)
     us = r["ms"] * 1e3
@@ -444,6 +443,8 @@ def main():
         "config": config_dict(w, l2),
         "us_per_call": round(us, 3), "attn_us_per_call": round(attn_us, 3),
         "append_us_per_call": round(append_us, 3),
+        "breakdown": "value/ms_per_step: K back-to-back steps (append + attention); attn/append us and the roofline: "
+                     "K back-to-back calls of that API alone, same inputs and pool rotation",
         "append_gbs": round(w.append_bytes() / (append_us * 1e-6) / 1e9, 2),
         "attn_gbs": round(achieved, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),

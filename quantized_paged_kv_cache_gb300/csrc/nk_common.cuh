@@ -104,10 +104,12 @@ namespace nk {
 constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shared memory)
 
 // Block-wide exclusive prefix of per-sequence page counts:
-// pre[b] = sum_{b' < b} pages(b'), pre[B] = total. Needs blockDim.x == 256 and
-// B <= kMaxBatch; every thread of the block must call it.
+// pre[b] = sum_{b' < b} pages(b'), pre[B] = total. Needs blockDim.x >= 256 and
+// B <= kMaxBatch; every thread of the block must call it. With `lens`, the
+// context lengths are also kept in shared memory (lens[b] = ctx_lens[b]), so
+// the kernel reads no length from global memory after its page loads start.
 __device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int32_t* ctx_lens, int* pre,
-                                                  int* warp_tot) {
+                                                  int* warp_tot, int* lens = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int v[4];
   int sum = 0;
@@ -115,6 +117,7 @@ __device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int
   for (int i = 0; i < 4; ++i) {
     const int b = tid * 4 + i;
     v[i] = (b < s.B) ? unit_pages(s, ctx_lens, b) : 0;
+    if (lens && b < s.B) lens[b] = ctx_lens[b];
     sum += v[i];
   }
   int incl = sum;

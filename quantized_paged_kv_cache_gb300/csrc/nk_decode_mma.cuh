@@ -80,7 +80,7 @@ __host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B
   g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
   const int mrows = NT * 8;
   g.merge_bytes = mrows * (D + 4) * 4 + 3 * nteams * mrows * 4 + mrows * 4;
-  const int pre_bytes = round_up((B + 1 + 24) * 4, 16);
+  const int pre_bytes = round_up((2 * B + 25) * 4, 16);  // pre[B+1], warp_tot, flags, lens[B]
   const int pid_bytes = 1024 * 4;
   const int fixed = g.xch_bytes + g.merge_bytes + pre_bytes + pid_bytes + 8 * 2 * 8 + 1024;
   int s = (kSmemLimit - fixed) / g.stage_bytes;
@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   int* warp_tot = pre + (p.B + 1);
   volatile int* abort_flag = pre + (p.B + 1) + 8;
   int* cnt = pre + (p.B + 1) + 9;  // [8] consumer count per stage
+  int* lens = pre + (p.B + 1) + 24;  // [B] context lengths
   int* pid = reinterpret_cast<int*>(smem + geo.pid_off);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + geo.bar_off);
   uint64_t* empty_bar = full_bar + 8;
@@ -280,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   flag_bad_ctx(p);
-  block_page_prefix(sh, p.ctx, pre, warp_tot);  // ends with __syncthreads
+  block_page_prefix(sh, p.ctx, pre, warp_tot, lens);  // ends with __syncthreads
 
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
   if (W == 0) return;
@@ -348,34 +349,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     if (big) flag(p.status, NK_DEVFLAG_RANGE);
   };
 
-  // The first unit's Q loads go out first (converted at first use), so they
-  // are not queued behind the page prefetch; then warp 0 fetches the first S
-  // page coordinates and issues their loads, while the other threads fill
-  // the page-coordinate cache that the stage refills read.
+  // Every global read of the prologue -- the first unit's Q (converted at
+  // first use) and the page coordinates of the CTA's pages up to the cache
+  // size -- goes out before the first page load: a load this SM issues after
+  // its page loads returns only behind their data (several microseconds).
   int64_t x = x_begin;
   Segment seg;
   bool have = next_segment(sh, pre, x, x_end, seg);
   if (have) load_q(seg);
-  if (warp == 0) {
-    const int n0 = total < S ? total : S;
-    if (lane < n0) pid[lane] = page_coord(p, sh, pre, x_begin, lane);
-    __syncwarp();
-    if (lane == 0)
-      for (int q = 0; q < n0; ++q) issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
-  }
   const int ncache = total < kPidCache ? total : kPidCache;
-  for (int q = S + tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  for (int q = tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
   __syncthreads();
+  if (tid == 0) {
+    const int n0 = total < S ? total : S;
+    for (int q = 0; q < n0; ++q) issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+  }
 
   const int bpp_sh = (BPP & (BPP - 1)) == 0 ? __ffs(BPP) - 1 : -1;  // blocks per page, as a shift
   int q_cur = 0, s_cur = 0;  // last page whose stage was located, and that stage
   uint32_t par_cur = 0;
   int page_seq = 0;   // CTA page number of the current segment's first page
   int jn = team;       // next block of this team
+  // With up to two row tiles the next unit's Q fragments are loaded before
+  // the merge of the current one (their latency overlaps it); with more,
+  // keeping them live through the merge would spill, so they load here.
+  constexpr bool kEarlyQ = NT <= 2;
   bool first_seg = true;
-  for (; have; have = next_segment(sh, pre, x, x_end, seg)) {
-    const int L = p.ctx[seg.b];
-    if (!first_seg) load_q(seg);
+  while (have) {
+    const int L = lens[seg.b];
+    if (!kEarlyQ && !first_seg) load_q(seg);
     first_seg = false;
     convert_q();
 #pragma unroll
@@ -615,6 +617,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
     page_seq += seg_pages;
 
+    // the next segment, located before the merge when its Q loads go out now
+    const bool last_seg = x >= x_end;
+    Segment nseg = seg;
+    int64_t nx = x;
+    bool nhave = false;
+    if constexpr (kEarlyQ) {
+      nhave = next_segment(sh, pre, nx, x_end, nseg);
+      if (nhave) load_q(nseg);
+    }
+
     // ---- merge the teams of this segment and write the result
     // row sums: reduce the per-lane partial l over the 8 lanes of a row
 #pragma unroll
@@ -644,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     // has been consumed), so each team can park its accumulator there and one
     // pass merges them; otherwise the teams add into mo one after another.
     constexpr int kSlot = MROWS * (D + 4);
-    const bool parked = (x >= x_end) && (size_t)NTEAMS * kSlot * 4 <= (size_t)S * geo.stage_bytes;
+    const bool parked = last_seg && (size_t)NTEAMS * kSlot * 4 <= (size_t)S * geo.stage_bytes;
     float* acc_buf = parked ? reinterpret_cast<float*>(smem) + team * kSlot : mo;
     if (parked) {
 #pragma unroll
@@ -724,6 +736,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         p.part_o[(slot * M + r) * D + ch] = val;
         if (ch == 0) p.part_lse[slot * M + r] = row_lse[r];
       }
+    }
+    if constexpr (kEarlyQ) {
+      seg = nseg;
+      x = nx;
+      have = nhave;
+    } else {
+      have = next_segment(sh, pre, x, x_end, seg);
     }
   }
 }
