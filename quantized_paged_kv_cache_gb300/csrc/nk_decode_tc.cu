@@ -66,6 +66,7 @@ constexpr int kStageBytes = 2 * kP * kD + 2 * kP * (kD / kGroup) * 4;  // 34816,
 constexpr int kPidCache = 512;
 constexpr int kColA = 0;      // tensor-memory columns of the two K buffers (64 each)
 constexpr int kColAcc = 128;  // the two accumulator buffers (4W each)
+constexpr int kQAhead = 4;    // pages before a segment's end at which the next unit's Q is prefetched
 
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);  // fp16 A/B, K-major, fp32 D
@@ -92,7 +93,7 @@ __host__ __device__ inline Layout layout(int W, int NT) {
   const int hdr = 512;
   const int xs = 2 * 2 * 64 * NT * 4 * 4;
   const int red = (2 * 4 * 32 + 2 * 32) * 4 + 4 * 4 + 32 * 4 + 64;
-  const int pre = round_up((kMaxBatch + 1 + 16 + 8 + 4) * 4, 16);
+  const int pre = round_up((2 * kMaxBatch + 1 + 16 + 8 + 4) * 4, 16);  // pre, warp_tot, cnt, flag, lens
   const int pid = kPidCache * 4;
   const int bar = 32 * 8;
   const int fixed = qt + pbuf + hdr + xs + red + pre + pid + bar + 16;
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   int* warp_tot = pre + (kMaxBatch + 1);
   int* cnt = warp_tot + 16;  // [8]
   volatile int* abort_flag = cnt + 8;
+  int* lens = cnt + 12;  // [kMaxBatch] context lengths
   int* pid = reinterpret_cast<int*>(smem + LY.off_pid);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + LY.off_bar);
   uint64_t* empty_bar = full_bar + 8;
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tc_fence_before();
   }
   flag_bad_ctx(p);
-  block_page_prefix(sh, p.ctx, pre, warp_tot);  // ends with __syncthreads
+  block_page_prefix(sh, p.ctx, pre, warp_tot, lens);  // ends with __syncthreads
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -229,16 +231,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const int total = (int)(x_end - x_begin);
   const uint32_t stage0 = smem_u32(smem);
 
-  if (warp == 0 && total > 0) {
-    const int n0 = total < S ? total : S;
-    if (lane < n0) pid[lane] = page_coord(p, sh, pre, x_begin, lane);
-    __syncwarp();
-    if (lane == 0)
-      for (int q = 0; q < n0; ++q) issue_page<kD>(p, &tmap, pid[q], stage0 + q * kStageBytes, smem_u32(&full_bar[q]));
-  }
+  // Q rows of a unit are pulled into L1 ahead of use: a load this SM issues
+  // while its page loads are in flight returns only behind their data
+  // (several microseconds), so the convert warps touch a unit's Q lines
+  // (M rows of 512 bytes, 128-byte lines) a few pages before they need them.
+  auto prefetch_q = [&](const Segment& sg) {
+    const int i = tid;  // convert-warp thread: line i & 3 of row i >> 2
+    if (i < 4 * M) {
+      const int n = i >> 2, t = n / G, hg = n % G;
+      const uint16_t* a = p.q + (((int64_t)sg.b * T + t) * p.Hq + sg.h * G + hg) * kD + (i & 3) * 64;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+    }
+  };
+  // Every global read of the prologue (page coordinates up to the cache
+  // size, the first unit's Q lines) goes out before the first page load.
   const int ncache = total < kPidCache ? total : kPidCache;
-  for (int q = S + tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  for (int q = tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  if (role == 0 && total > 0) {
+    int64_t x0 = x_begin;
+    Segment s0;
+    if (next_segment(sh, pre, x0, x_end, s0)) prefetch_q(s0);
+  }
   __syncthreads();
+  if (tid == 0) {
+    const int n0 = total < S ? total : S;
+    for (int q = 0; q < n0; ++q) issue_page<kD>(p, &tmap, pid[q], stage0 + q * kStageBytes, smem_u32(&full_bar[q]));
+  }
 
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
     if (*abort_flag) return;
@@ -308,8 +326,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (big) flag(p.status, NK_DEVFLAG_RANGE);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q writes -> tensor-core reads
       named_bar(1, kConvWarps * 32);
+      // the next unit's Q lines, kQAhead pages before this segment ends
+      int64_t xn = x;
+      Segment sn;
+      const bool has_next = next_segment(sh, pre, xn, x_end, sn);
+      const int j_pf = npages > kQAhead ? npages - kQAhead : 0;
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
+        if (j == j_pf && has_next) prefetch_q(sn);
         wait_bar(&full_bar[s], ph);
         wait_bar(&qk_bar[q & 1], ((q >> 1) & 1) ^ 1);  // MMAs of page q - 2 (same K buffer) done
         const uint8_t* st = smem + s * kStageBytes;
@@ -360,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
     float m_ref[NR], l_part[NR];
     while (next_segment(sh, pre, x, x_end, seg)) {
-      const int L = p.ctx[seg.b];
+      const int L = lens[seg.b];
       const int npages = seg.page_end - seg.page_begin;
 #pragma unroll
       for (int i = 0; i < NR; ++i) {
