@@ -5,12 +5,13 @@
 //   O = sum_s exp(LSE_s - M) O_s / sum_s exp(LSE_s - M),  M = max_s LSE_s,
 // with empty partials (LSE = -inf) weighted 0.
 //
-// One 256-thread block per output row. Thread t owns 4 channels (a float4)
-// and every PL = 256 / (D / 4)-th partial: it issues the loads of up to 8 of
-// its partials (LSE and row slice) before using any, merges them online
-// (running max, rescaled sum), and the PL partial-lanes of a channel group are
-// merged through shared memory. A row of S partials thus costs about
-// S / (8 PL) dependent memory round trips instead of S / 4.
+// One 256-thread block per output row, or per 64-channel slice of a row when
+// there are few rows. Thread t owns 4 channels (a float4) and every
+// PL = 256 / (C / 4)-th partial (C = channels per block): it issues the loads
+// of up to 8 of its partials (LSE and row slice) before using any, merges
+// them online (running max, rescaled sum), and the PL partial-lanes of a
+// channel group are merged through shared memory. A row of S partials thus
+// costs about S / (8 PL) dependent memory round trips instead of S / 4.
 #include "nk_decode.cuh"
 
 namespace nk {
@@ -18,7 +19,8 @@ namespace nk {
 constexpr int kCombThreads = 256;
 constexpr int kCombUnroll = 8;
 
-// lse_of(s): LSE of partial s (-inf: skip it); row_of(s): its fp32 row.
+// lse_of(s): LSE of partial s (-inf: skip it); row_of(s): its fp32 row slice
+// of D channels (the block's channels).
 template <int D, class LseFn, class RowFn>
 __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uint16_t* out_row) {
   constexpr int CH = D / 4;               // float4 channel groups
@@ -92,9 +94,10 @@ __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uin
 // Combine for the decode kernels: units whose pages sit in one CTA were
 // written directly by that CTA; the others merge the partial slots c + u of
 // the CTAs c their pages span (CTAs with an empty range wrote nothing).
-// Block = one (unit, row).
-template <int D>
+// Block = one (unit, row) and a slice of C channels.
+template <int D, int C>
 __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const DecodeParams p) {
+  static_assert(D % C == 0, "whole slices");
   chain_wait();
   chain_release();
   __shared__ int pre[kMaxBatch + 1];
@@ -103,7 +106,8 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
   block_page_prefix(sh, p.ctx, pre, warp_tot);
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
   const int M = p.G * p.T;
-  const int64_t ur = blockIdx.x;
+  const int64_t ur = blockIdx.x / (D / C);
+  const int c_off = (int)(blockIdx.x % (D / C)) * C;
   if (ur >= (int64_t)p.B * p.Hkv * M || W == 0) return;
   const int u = (int)(ur / M), r = (int)(ur % M);
   const int b = u / p.Hkv, h = u % p.Hkv;
@@ -119,9 +123,9 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
     if (cta_begin(W, n, c) == cta_begin(W, n, c + 1)) return -INFINITY;
     return p.part_lse[((int64_t)c + u) * M + r];
   };
-  auto row_of = [&](int s) { return p.part_o + (((int64_t)c0 + s + u) * M + r) * D; };
+  auto row_of = [&](int s) { return p.part_o + (((int64_t)c0 + s + u) * M + r) * D + c_off; };
   const int t = r / p.G, hg = r % p.G;
-  merge_row<D>(c1 - c0 + 1, lse_of, row_of, p.out + (((int64_t)b * p.T + t) * p.Hq + h * p.G + hg) * D);
+  merge_row<C>(c1 - c0 + 1, lse_of, row_of, p.out + (((int64_t)b * p.T + t) * p.Hq + h * p.G + hg) * D + c_off);
 }
 
 // Standalone combine: part_o [S][R][D], part_lse [S][R] -> out [R][D]; block = row.
@@ -137,13 +141,24 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(const float*
   merge_row<D>(S, lse_of, row_of, out + row * D);
 }
 
+// Rows are split into 64-channel slices when there are fewer rows than
+// kSliceRows: more blocks in flight, fewer partials per thread.
+constexpr int kSliceRows = 256;
+
+template <int D>
+static cudaError_t launch_combine_d(const DecodeParams& p, int64_t rows, cudaStream_t stream) {
+  const dim3 b(kCombThreads);
+  if (D > 64 && rows < kSliceRows)
+    return launch_chained(decode_combine_kernel<D, 64>, dim3((unsigned)(rows * (D / 64))), b, 0, stream, p);
+  return launch_chained(decode_combine_kernel<D, D>, dim3((unsigned)rows), b, 0, stream, p);
+}
+
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream) {
-  const int64_t grid = (int64_t)p.B * p.Hkv * p.G * p.T;
-  if (grid == 0) return cudaSuccess;
-  const dim3 g((unsigned)grid), b(kCombThreads);
-  if (p.D == 256) return launch_chained(decode_combine_kernel<256>, g, b, 0, stream, p);
-  if (p.D == 128) return launch_chained(decode_combine_kernel<128>, g, b, 0, stream, p);
-  return launch_chained(decode_combine_kernel<64>, g, b, 0, stream, p);
+  const int64_t rows = (int64_t)p.B * p.Hkv * p.G * p.T;
+  if (rows == 0) return cudaSuccess;
+  if (p.D == 256) return launch_combine_d<256>(p, rows, stream);
+  if (p.D == 128) return launch_combine_d<128>(p, rows, stream);
+  return launch_combine_d<64>(p, rows, stream);
 }
 
 cudaError_t launch_attn_combine(const float* part_o, const float* part_lse, int S, int R, int D, uint16_t* out,
