@@ -85,8 +85,8 @@ __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uin
       }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    const uint32_t w0 = f32_to_bf16(o.x * inv) | (f32_to_bf16(o.y * inv) << 16);
-    const uint32_t w1 = f32_to_bf16(o.z * inv) | (f32_to_bf16(o.w * inv) << 16);
+    const uint32_t w0 = f32_to_bf16(o.x * inv) | ((uint32_t)f32_to_bf16(o.y * inv) << 16);
+    const uint32_t w1 = f32_to_bf16(o.z * inv) | ((uint32_t)f32_to_bf16(o.w * inv) << 16);
     *reinterpret_cast<uint2*>(out_row + ch * 4) = make_uint2(w0, w1);
   }
 }
@@ -98,12 +98,17 @@ __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uin
 template <int D, int C>
 __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const DecodeParams p) {
   static_assert(D % C == 0, "whole slices");
-  chain_wait();
-  chain_release();
   __shared__ int pre[kMaxBatch + 1];
   __shared__ int warp_tot[8];
   const SplitShape sh = p.shape();
-  block_page_prefix(sh, p.ctx, pre, warp_tot);
+  // The page prefix runs before the wait for the split kernel: this kernel
+  // only ever follows the split kernel of the same call, which releases it
+  // after its own chain_wait returned, so every kernel that could have
+  // written the context lengths has completed; the split kernel only reads
+  // them. They are read at L2 (the point of coherence), not through L1.
+  block_page_prefix<true>(sh, p.ctx, pre, warp_tot);
+  chain_wait();
+  chain_release();
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
   const int M = p.G * p.T;
   const int64_t ur = blockIdx.x / (D / C);

@@ -37,7 +37,8 @@ struct ChunkLayout {
 // with programmatic stream serialization (launch_chained), so it may become
 // resident while the previous kernel on the stream is still running. Each one
 // therefore calls chain_wait() before its first global-memory access (read or
-// write): griddepcontrol.wait returns once every prerequisite grid has
+// write) -- the decode combine kernel reads the context lengths before it,
+// for the reason given there: griddepcontrol.wait returns once every prerequisite grid has
 // completed and its memory operations are visible. Because every kernel waits
 // in every CTA, a kernel cannot complete before its predecessor, so the order
 // of the stream is kept transitively. chain_release() lets the next kernel's
@@ -84,8 +85,8 @@ struct SplitShape {
   int B, Hkv, P, T, max_ctx, max_pages;
 };
 
-__device__ __forceinline__ int unit_pages(const SplitShape& s, const int32_t* ctx_lens, int b) {
-  const int L = ctx_lens[b];
+// Pages of a sequence of context length L (0 for an invalid length).
+__device__ __forceinline__ int pages_of_len(const SplitShape& s, int L) {
   if (L < s.T || L > s.max_ctx || (int64_t)L > (int64_t)s.max_pages * s.P) return 0;
   return (L + s.P - 1) / s.P;
 }
@@ -108,6 +109,8 @@ constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shar
 // B <= kMaxBatch; every thread of the block must call it. With `lens`, the
 // context lengths are also kept in shared memory (lens[b] = ctx_lens[b]), so
 // the kernel reads no length from global memory after its page loads start.
+// kL2Only reads the lengths at L2 (ld.global.cg), bypassing this SM's L1.
+template <bool kL2Only = false>
 __device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int32_t* ctx_lens, int* pre,
                                                   int* warp_tot, int* lens = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -116,8 +119,10 @@ __device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int b = tid * 4 + i;
-    v[i] = (b < s.B) ? unit_pages(s, ctx_lens, b) : 0;
-    if (lens && b < s.B) lens[b] = ctx_lens[b];
+    int L = 0;
+    if (b < s.B) L = kL2Only ? __ldcg(ctx_lens + b) : ctx_lens[b];
+    v[i] = (b < s.B) ? pages_of_len(s, L) : 0;
+    if (lens && b < s.B) lens[b] = L;
     sum += v[i];
   }
   int incl = sum;

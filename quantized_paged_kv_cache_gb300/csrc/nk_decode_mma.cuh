@@ -239,6 +239,9 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
 template <int D, int NT, int CS>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                  const DecodeParams p) {
+  // the tensor map is a launch parameter (no earlier kernel writes it): its
+  // descriptor fetch can start before the wait for the previous kernel
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
   chain_wait();
   chain_release();
   constexpr int NTEAMS = kConsumerWarps / CS;
@@ -334,6 +337,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       }
     }
   };
+  // The first unit's Q rows, staged once per CTA in the (then idle) merge
+  // buffer: one 16-byte load per thread instead of every warp loading all
+  // rows; rows are padded by 16 bytes so the fragment reads hit distinct banks.
+  constexpr int kQRow = D * 2 + 16;  // bytes per staged row
+  static_assert(MROWS * kQRow <= MROWS * (D + 4) * 4, "staged Q fits the merge buffer");
+  uint8_t* qstage = reinterpret_cast<uint8_t*>(mo);
+  constexpr int QPT = (MROWS * (D / 8) + kThreads - 1) / kThreads;  // 16-byte pieces per thread
+  uint4 qv[QPT];
+  auto fetch_q = [&](const Segment& sg) {  // global -> registers (no wait)
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int i = tid + k * kThreads, r = i / (D / 8), c8 = i % (D / 8);
+      qv[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < M) {
+        const int t = r / G, hg = r % G;
+        qv[k] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)sg.b * T + t) * p.Hq + sg.h * G + hg) * D + c8 * 8);
+      }
+    }
+  };
+  auto stage_q = [&]() {  // registers -> shared memory
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int i = tid + k * kThreads, r = i / (D / 8), c8 = i % (D / 8);
+      if (r < M) *reinterpret_cast<uint4*>(qstage + r * kQRow + c8 * 16) = qv[k];
+    }
+  };
+  auto load_q_staged = [&]() {  // after a barrier that follows stage_q
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = nt * 8 + g;
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        uint2 raw = make_uint2(0u, 0u);
+        if (r < M) raw = *reinterpret_cast<const uint2*>(qstage + r * kQRow + (ch0 + c * 16 + t4 * 4) * 2);
+        bq[nt][c][0] = raw.x;
+        bq[nt][c][1] = raw.y;
+      }
+    }
+  };
   auto convert_q = [&]() {
     bool big = false;
 #pragma unroll
@@ -356,11 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   int64_t x = x_begin;
   Segment seg;
   bool have = next_segment(sh, pre, x, x_end, seg);
-  if (have) load_q(seg);
+  if (have) fetch_q(seg);
   const int ncache = total < kPidCache ? total : kPidCache;
   for (int q = tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
+  if (have) stage_q();
   __syncthreads();
-  if (tid == 0) {
+  // The first S pages, issued in order by one thread (the copy unit then
+  // completes page 0 first). Each issue waits until the unit accepts the
+  // copy, so the issuer is the last warp, whose first block is in page 1.
+  if (tid == kThreads - 32) {
     const int n0 = total < S ? total : S;
     for (int q = 0; q < n0; ++q) issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
   }
@@ -377,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   bool first_seg = true;
   while (have) {
     const int L = lens[seg.b];
-    if (!kEarlyQ && !first_seg) load_q(seg);
+    if (first_seg) load_q_staged();  // staged in the prologue, before its barrier
+    else if (!kEarlyQ) load_q(seg);
     first_seg = false;
     convert_q();
 #pragma unroll
@@ -659,30 +706,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     const bool parked = last_seg && (size_t)NTEAMS * kSlot * 4 <= (size_t)S * geo.stage_bytes;
     float* acc_buf = parked ? reinterpret_cast<float*>(smem) + team * kSlot : mo;
     if (parked) {
+      // fragment elements k and k + 2 are adjacent channels of one row
 #pragma unroll
       for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            acc_buf[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)] = o[c][nt][k];
+          for (int e = 0; e < 2; ++e)
+            *reinterpret_cast<float2*>(acc_buf + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16 + 2 * g) =
+                make_float2(o[c][nt][e], o[c][nt][e + 2]);
     }
     __syncthreads();
-    if (tid < MROWS) {
-      const int r = tid;
-      float mx = -INFINITY, lsum = 0.f;
-      for (int tm = 0; tm < NTEAMS; ++tm) mx = fmaxf(mx, tm_m[tm * MROWS + r]);
-      if (mx != -INFINITY)
-        for (int tm = 0; tm < NTEAMS; ++tm) {
-          const float mt = tm_m[tm * MROWS + r];
-          if (mt != -INFINITY) lsum += tm_l[tm * MROWS + r] * ex2(mt - mx);
+    // team weights of each row: NTEAMS consecutive lanes per row, reduced by shuffles
+    for (int base = 0; base < MROWS * NTEAMS; base += kThreads) {
+      if (base + warp * 32 < MROWS * NTEAMS) {  // warp-uniform
+        const int j = base + tid;
+        const bool act = j < MROWS * NTEAMS;
+        const int r = act ? j / NTEAMS : 0, tm = j % NTEAMS;
+        const float mt = act ? tm_m[tm * MROWS + r] : -INFINITY;
+        float mx = mt;
+#pragma unroll
+        for (int o2 = 1; o2 < NTEAMS; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+        const float wgt = (mt == -INFINITY) ? 0.f : ex2(mt - mx);
+        float lsum = act ? wgt * tm_l[tm * MROWS + r] : 0.f;
+#pragma unroll
+        for (int o2 = 1; o2 < NTEAMS; o2 <<= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o2);
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        if (act) {
+          facs[tm * MROWS + r] = wgt * inv;
+          if (tm == 0) row_lse[r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
         }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      for (int tm = 0; tm < NTEAMS; ++tm) {
-        const float mt = tm_m[tm * MROWS + r];
-        facs[tm * MROWS + r] = (mt == -INFINITY) ? 0.f : ex2(mt - mx) * inv;
       }
-      row_lse[r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
     }
     __syncthreads();
     if (!parked) {
@@ -715,25 +769,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         __syncthreads();
       }
     }
-    // normalize (weights already include 1/sum) and store
+    // normalize (weights already include 1/sum) and store, 4 channels a thread
     const int64_t slot = (int64_t)blockIdx.x + seg.u;
     const float* park = reinterpret_cast<const float*>(smem);
-    for (int i = tid; i < M * D; i += kThreads) {
-      const int r = i / D, ch = i % D;
-      float val;
+    for (int i = tid; i < M * (D / 4); i += kThreads) {
+      const int r = i / (D / 4), ch = (i % (D / 4)) * 4;
+      float4 val;
       if (parked) {
-        val = 0.f;
+        val = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int tm = 0; tm < NTEAMS; ++tm) val = fmaf(park[tm * kSlot + r * (D + 4) + ch], facs[tm * MROWS + r], val);
+        for (int tm = 0; tm < NTEAMS; ++tm) {
+          const float f = facs[tm * MROWS + r];
+          const float4 v = *reinterpret_cast<const float4*>(park + tm * kSlot + r * (D + 4) + ch);
+          val.x = fmaf(v.x, f, val.x);
+          val.y = fmaf(v.y, f, val.y);
+          val.z = fmaf(v.z, f, val.z);
+          val.w = fmaf(v.w, f, val.w);
+        }
       } else {
-        val = mo[r * (D + 4) + ch];
+        val = *reinterpret_cast<const float4*>(mo + r * (D + 4) + ch);
       }
-      if (!isfinite(val)) flag(p.status, NK_DEVFLAG_RANGE);
+      if (!(isfinite(val.x) && isfinite(val.y) && isfinite(val.z) && isfinite(val.w))) flag(p.status, NK_DEVFLAG_RANGE);
       if (seg.whole) {
         const int t = r / G, hg = r % G;
-        p.out[(((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch] = f32_to_bf16(val);
+        const uint32_t w0 = f32_to_bf16(val.x) | ((uint32_t)f32_to_bf16(val.y) << 16);
+        const uint32_t w1 = f32_to_bf16(val.z) | ((uint32_t)f32_to_bf16(val.w) << 16);
+        *reinterpret_cast<uint2*>(p.out + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch) = make_uint2(w0, w1);
       } else {
-        p.part_o[(slot * M + r) * D + ch] = val;
+        *reinterpret_cast<float4*>(p.part_o + (slot * M + r) * D + ch) = val;
         if (ch == 0) p.part_lse[slot * M + r] = row_lse[r];
       }
     }

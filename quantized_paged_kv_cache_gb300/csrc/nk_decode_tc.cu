@@ -160,6 +160,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 template <int W, int NT>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const DecodeParams p) {
+  // the tensor map is a launch parameter: its descriptor fetch can start
+  // before the wait for the previous kernel
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
   chain_wait();
   chain_release();
   constexpr int NR = NT * 4;  // rows a score thread finishes (half of each 8-row tile)
