@@ -10,8 +10,9 @@
 // PL = 256 / (C / 4)-th partial (C = channels per block): it issues the loads
 // of up to 8 of its partials (LSE and row slice) before using any, merges
 // them online (running max, rescaled sum), and the PL partial-lanes of a
-// channel group are merged through shared memory. A row of S partials thus
-// costs about S / (8 PL) dependent memory round trips instead of S / 4.
+// channel group are merged by shuffles within a warp, then through shared
+// memory. A row of S partials thus costs about S / (8 PL) dependent memory
+// round trips instead of S / 4.
 #include "nk_decode.cuh"
 
 namespace nk {
@@ -25,8 +26,10 @@ template <int D, class LseFn, class RowFn>
 __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uint16_t* out_row) {
   constexpr int CH = D / 4;               // float4 channel groups
   constexpr int PL = kCombThreads / CH;   // partial-lanes
-  __shared__ float sm_m[PL][CH], sm_l[PL][CH];
-  __shared__ float4 sm_o[PL][CH];
+  constexpr int LPW = CH < 32 ? 32 / CH : 1;  // partial-lanes of one channel group within a warp
+  constexpr int PW = PL / LPW;            // partial-lanes left after the in-warp merge
+  __shared__ float sm_m[PW][CH], sm_l[PW][CH];
+  __shared__ float4 sm_o[PW][CH];
   const int t = threadIdx.x, pl = t / CH, ch = t % CH;
   float m = -INFINITY, l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -60,19 +63,39 @@ __device__ __forceinline__ void merge_row(int S, LseFn lse_of, RowFn row_of, uin
       acc.w = fmaf(w, v[u].w, acc.w);
     }
   }
-  sm_m[pl][ch] = m;
-  sm_l[pl][ch] = l;
-  sm_o[pl][ch] = acc;
+  // the partial-lanes of a channel group that share a warp merge by shuffles
+#pragma unroll
+  for (int off = CH; off < 32; off <<= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m, off), lo = __shfl_xor_sync(0xffffffffu, l, off);
+    float4 ao;
+    ao.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+    ao.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+    ao.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+    ao.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+    const float mx = fmaxf(m, mo);
+    const float a = m == -INFINITY ? 0.f : expf(m - mx), b = mo == -INFINITY ? 0.f : expf(mo - mx);
+    l = l * a + lo * b;
+    acc.x = fmaf(acc.x, a, ao.x * b);
+    acc.y = fmaf(acc.y, a, ao.y * b);
+    acc.z = fmaf(acc.z, a, ao.z * b);
+    acc.w = fmaf(acc.w, a, ao.w * b);
+    m = mx;
+  }
+  if (pl % LPW == 0) {
+    sm_m[pl / LPW][ch] = m;
+    sm_l[pl / LPW][ch] = l;
+    sm_o[pl / LPW][ch] = acc;
+  }
   __syncthreads();
   if (pl == 0) {
     float mx = -INFINITY;
 #pragma unroll
-    for (int q = 0; q < PL; ++q) mx = fmaxf(mx, sm_m[q][ch]);
+    for (int q = 0; q < PW; ++q) mx = fmaxf(mx, sm_m[q][ch]);
     float lsum = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     if (mx != -INFINITY) {
 #pragma unroll
-      for (int q = 0; q < PL; ++q) {
+      for (int q = 0; q < PW; ++q) {
         const float mq = sm_m[q][ch];
         if (mq == -INFINITY) continue;
         const float a = expf(mq - mx);
@@ -125,7 +148,8 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
   const int n = p.n_ctas;
   auto lse_of = [&](int s) {
     const int c = c0 + s;
-    if (cta_begin(W, n, c) == cta_begin(W, n, c + 1)) return -INFINITY;
+    // a CTA can own no item only when there are fewer items than CTAs
+    if (W < n && cta_begin(W, n, c) == cta_begin(W, n, c + 1)) return -INFINITY;
     return p.part_lse[((int64_t)c + u) * M + r];
   };
   auto row_of = [&](int s) { return p.part_o + (((int64_t)c0 + s + u) * M + r) * D + c_off; };
