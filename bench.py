@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -60,15 +61,24 @@ def measured_peaks():
         return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank lines (a comment edit does not
+    change the kernel the counters were taken on)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def source_hash() -> str:
-    """Hash of the decode split kernels' sources and the headers they include
-    (the kernels whose ncu traffic profiles/ncu_traffic.json records)."""
+    """Hash of the code of the decode split kernels' sources and the headers
+    they include (the kernels whose ncu traffic profiles/ncu_traffic.json
+    records), comments excluded."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_paged_kv_cache_gb300", "csrc")
     for fn in sorted(os.listdir(d)):
         if fn.startswith("nk_decode") or fn in ("nk_common.cuh", "nk_ptx.cuh"):
-            with open(os.path.join(d, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+            with open(os.path.join(d, fn), encoding="utf-8") as f:
+                h.update(fn.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,42 +9,41 @@
 // enter both products exactly (as fp16); the group scales are applied to fp32
 // partial sums (K) and folded into the probabilities (V).
 //
-// CTA = 12 warps, one per SM, same stream-K split over (sequence, kv-head,
-// page) items as the mma.sync kernel, same TMA page ring (one stage = the
-// K|V code tiles and both scale arrays of one page; the last reader of a
-// stage loads the page S ahead into it).
+// CTA = 16 warps in three roles, one CTA per SM, same stream-K split over
+// (sequence, kv-head, page) items as the mma.sync kernel, same TMA page ring
+// (one stage = the K|V code tiles and both scale arrays of one page; the last
+// of the 16 warps to release a stage loads the page S ahead into it).
 //
-// Score warps 0-3 (one per tensor-memory lane quadrant), per 64-key page:
-//   * Convert: thread (quadrant w, lane l) takes key k = 32 (w & 1) + l and
-//     channel half c = w >> 1, widens its 128 codes to fp16 and stores them
-//     into tensor-memory row 64 c + k: the page becomes a 128-row A operand
-//     whose rows 0-63 hold channels 0-127 of the keys and rows 64-127
-//     channels 128-255.
+// Convert warps 0-3 (one per tensor-memory lane quadrant), per 64-key page:
+//   * thread (quadrant w, lane l) takes key k = 32 (w & 1) + l and channel
+//     half c = w >> 1, widens its 128 codes to fp16 and stores them into
+//     tensor-memory row 64 c + k: the page becomes a 128-row A operand whose
+//     rows 0-63 hold channels 0-127 of the keys and rows 64-127 channels
+//     128-255 (two tensor-memory buffers, so page j + 1 converts while the
+//     scores of page j are read);
 //   * QK: one thread issues 8 tcgen05.mma (M = 128, N = 2W, K = 16) into two
 //     accumulators: A = groups 0|2, B = groups 1|3. The B operand stacks the
 //     query rows twice, once with the channels of the first half and once
 //     with those of the second (W rows each, zero padded), so lanes 0-63 of
 //     columns [0, W) and lanes 64-127 of columns [W, 2W) are the per-group
 //     dot products; the other quarter-blocks are unused.
-//   * Scores: each thread loads its lane's two accumulator rows, applies its
-//     key's two group scales (times sm_scale log2 e) and swaps half of its
-//     rows with the thread holding the other channel half of the same key,
-//     so quadrants 0-1 finish rows with (n mod 8) < 4 and quadrants 2-3 the
-//     rest.
-//   * Online softmax in base 2 with a lazy reference per row (raised only
+// Score warps 4-7 (same key / channel-half mapping by quadrant):
+//   * each thread loads its lane's two accumulator rows, applies its key's
+//     two group scales (times sm_scale log2 e) and swaps half of its rows
+//     with the thread holding the other channel half of the same key, so
+//     quadrants 0-1 finish rows with (n mod 8) < 4 and quadrants 2-3 the rest;
+//   * online softmax in base 2 with a lazy reference per row (raised only
 //     when a score passes it by more than 8, agreed by the two warps of a
 //     row half), P' = p * Vs[key][group] split into fp16 hi + lo, written to
 //     a double-buffered shared-memory tile [group][hi|lo][8-row tile][key].
-// PV warps 4-11: warp 4 + i owns channels [32 i, 32 i + 32) (group i / 2) for
+// PV warps 8-15: warp 8 + i owns channels [32 i, 32 i + 32) (group i / 2) for
 //   all rows; per page it rescales its accumulators if a reference moved,
 //   then O^T[ch][row] += V^T[ch][key] P'^T[key][row] with mma.sync m16n8k16
 //   (swap-AB), V^T fragments from ldmatrix.trans on the TMA tile, P'
 //   fragments from ldmatrix.trans on the score warps' tile (hi and lo: two
 //   MMAs).
-// The score warps run one page ahead: the conversion and MMAs of page j + 1
-// are issued before the scores of page j are read (two tensor-memory
-// buffers). At the end of a segment the row sums are reduced and the PV warps
-// write bf16 rows (whole unit) or fp32 partials with their LSE.
+// At the end of a segment the row sums are reduced and the PV warps write
+// bf16 rows (whole unit) or fp32 partials with their LSE.
 // Every mbarrier wait is bounded; a timeout sets NK_DEVFLAG_TIMEOUT.
 #include "nk_decode_mma.cuh"
 
