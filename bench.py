@@ -268,22 +268,38 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
 
     import quantized_paged_kv_cache_gb300 as nk
 
-    h = {name: S[name].cpu().pin_memory() for name in ("k", "v", "q", "sp", "cu", "ctx")}
-    dev = {name: torch.empty_like(S[name]) for name in h}
+    # The step's inputs (new K/V rows, Q, positions, lengths) sit back to back
+    # in one pinned host buffer and go over in one copy into one device
+    # buffer whose views are passed to the API.
+    names = ("k", "v", "q", "sp", "cu", "ctx")
+    offs, off = {}, 0
+    for name in names:
+        offs[name] = off
+        off += (S[name].numel() * S[name].element_size() + 255) // 256 * 256
+    h_buf = torch.empty(off, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(off, dtype=torch.uint8, device=device)
+
+    def view(buf, name):
+        t = S[name]
+        n = t.numel() * t.element_size()
+        return buf[offs[name]:offs[name] + n].view(t.dtype).view(t.shape)
+
+    for name in names:
+        view(h_buf, name).copy_(S[name].cpu())
+    dev = {name: view(d_buf, name) for name in names}
     out_h = torch.empty(S["out"].shape, dtype=S["out"].dtype).pin_memory()
     stream = torch.cuda.current_stream()
-    bi = sum(t.numel() * t.element_size() for t in h.values())
+    bi = h_buf.numel()  # the one host->device copy of a step (inputs + alignment padding)
     bo = out_h.numel() * out_h.element_size()
 
     def step(i):
-        for name in h:
-            dev[name].copy_(h[name], non_blocking=True)
+        d_buf.copy_(h_buf, non_blocking=True)
         pool = S["pools"][i % replicas]
         nk.kv_append(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], status=S["status"], stream=stream)
         dec(pool, dev["q"], S["bt"], dev["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
             out=S["out"], status=S["status"], stream=stream)
         out_h.copy_(S["out"], non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        stream.synchronize()
 
     for i in range(max(args.warmup, 3)):
         step(i)
