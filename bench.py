@@ -193,6 +193,10 @@ def run_ours(args, w, rank, world, device):
 
     def step(i, what="step"):
         pool = S["pools"][i % replicas]
+        if what == "step" and args.kernel == "mma":  # append + attention in one call
+            nk.decode_step(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], S["q"], S["ctx"], w.sm_scale, w.max_ctx,
+                           num_ctas=S["nct"], workspace=S["ws"], out=S["out"], status=S["status"], stream=stream)
+            return
         if what != "attn":
             nk.kv_append(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
         if what != "append":
@@ -295,9 +299,14 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
     def step(i):
         d_buf.copy_(h_buf, non_blocking=True)
         pool = S["pools"][i % replicas]
-        nk.kv_append(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], status=S["status"], stream=stream)
-        dec(pool, dev["q"], S["bt"], dev["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
-            out=S["out"], status=S["status"], stream=stream)
+        if args.kernel == "mma":
+            nk.decode_step(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], dev["q"], dev["ctx"], w.sm_scale,
+                           w.max_ctx, num_ctas=S["nct"], workspace=S["ws"], out=S["out"], status=S["status"],
+                           stream=stream)
+        else:
+            nk.kv_append(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], status=S["status"], stream=stream)
+            dec(pool, dev["q"], S["bt"], dev["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
+                out=S["out"], status=S["status"], stream=stream)
         out_h.copy_(S["out"], non_blocking=True)
         stream.synchronize()
 
@@ -469,8 +478,9 @@ def main():
         "config": config_dict(w, l2),
         "us_per_call": round(us, 3), "attn_us_per_call": round(attn_us, 3),
         "append_us_per_call": round(append_us, 3),
-        "breakdown": "value/ms_per_step: K back-to-back steps (append + attention); attn/append us and the roofline: "
-                     "K back-to-back calls of that API alone, same inputs and pool rotation",
+        "breakdown": "value/ms_per_step: K back-to-back steps (nk_decode_step: append + attention); attn/append us "
+                     "and the roofline: K back-to-back calls of nk_paged_decode_attn / nk_kv_append alone, same "
+                     "inputs and pool rotation",
         "append_gbs": round(w.append_bytes() / (append_us * 1e-6) / 1e9, 2),
         "attn_gbs": round(achieved, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),

@@ -147,6 +147,23 @@ int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_
                          void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
                          void* stream);
 
+/*
+ * nk_decode_step -- one decode (or verify) step: nk_kv_append of the step's
+ * new rows followed by nk_paged_decode_attn, on `stream`, with the arguments
+ * of those two calls (the block table is shared; B sequences in both). All
+ * arguments of both are checked before anything is launched; the result is
+ * bit-identical to the two calls in sequence. The attention's split kernel
+ * reads the context lengths, block-table entries and Q while the append is
+ * still running (the append writes only pool pages) and waits for it before
+ * its first page load. The pages define the append and the attention; this
+ * pairing of them has no counterpart there.
+ */
+int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                   const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t total_new, const void* k_dev,
+                   const void* v_dev, const void* q_dev, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                   int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                   size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream);
+
 /* Same contract and result, computed by the fp32 CUDA-core kernel that the
  * tensor-core path is measured against. */
 int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,

@@ -23,7 +23,7 @@ MAX_T = 8
 __all__ = [
     "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_ctas",
     "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "paged_decode_attn_noalloc",
-    "attn_combine", "status_string",
+    "attn_combine", "status_string", "decode_step",
 ]
 
 
@@ -137,6 +137,32 @@ def paged_decode_attn_simt(pool: KVPool, q, block_table, ctx_lens, sm_scale: flo
     """Same result from the fp32 CUDA-core kernel (nk_paged_decode_attn_simt)."""
     return _decode(lib().nk_paged_decode_attn_simt, "nk_paged_decode_attn_simt", pool, q, block_table, ctx_lens,
                    sm_scale, max_ctx, num_ctas, workspace, out, status, stream)
+
+
+def decode_step(pool: KVPool, block_table, start_pos, cu_new, k, v, q, ctx_lens, sm_scale: float, max_ctx: int,
+                num_ctas: int = 0, workspace=None, out=None, status=None, stream=None):
+    """kv_append of the step's rows, then paged_decode_attn, in one call
+    (nk_decode_step); returns out bf16 [B][T][Hq][D]."""
+    import torch
+
+    _need_cuda(block_table, start_pos, cu_new, k, v, q, ctx_lens, workspace, out, status)
+    B, T, Hq, D = (int(s) for s in q.shape)
+    if int(start_pos.numel()) != B:
+        raise ValueError("start_pos must hold one position per sequence of q")
+    total = int(k.shape[0]) if k.dim() > 0 else 0
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = decode_workspace_bytes(B, T, Hq, pool.num_kv_heads, D, num_ctas)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    ps = pool.c_struct()
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib().nk_decode_step(ctypes.byref(ps), _ptr(block_table), int(block_table.shape[-1]), _ptr(start_pos),
+                              _ptr(cu_new), total, _ptr(k), _ptr(v), _ptr(q), _ptr(ctx_lens), B, T, Hq,
+                              float(sm_scale), int(max_ctx), int(num_ctas), _ptr(workspace), wbytes, _ptr(out),
+                              _ptr(status), _stream(stream))
+    _check(rc, "nk_decode_step")
+    return out
 
 
 NOALLOC_MAX_WORKSPACE = 8 << 20

@@ -44,6 +44,7 @@ EXPORTS = (
     "nk_paged_decode_attn",
     "nk_paged_decode_attn_simt",
     "nk_paged_decode_attn_noalloc",
+    "nk_decode_step",
     "nk_attn_combine",
     "nk_status_string",
     "nk_version",
@@ -73,6 +74,9 @@ def lib() -> ctypes.CDLL:
             L.nk_paged_decode_attn_simt.argtypes, L.nk_paged_decode_attn_simt.restype = dec, ctypes.c_int
             L.nk_paged_decode_attn_noalloc.argtypes = [pool_p, P, P, I32, P, I32, I32, I32, F, I32, I32, P, P, P]
             L.nk_paged_decode_attn_noalloc.restype = ctypes.c_int
+            L.nk_decode_step.argtypes = [pool_p, P, I32, P, P, I32, P, P, P, P, I32, I32, I32, F, I32, I32, P, Z, P,
+                                         P, P]
+            L.nk_decode_step.restype = ctypes.c_int
             L.nk_attn_combine.argtypes = [P, P, I32, I32, I32, P, P]
             L.nk_attn_combine.restype = ctypes.c_int
             L.nk_status_string.argtypes, L.nk_status_string.restype = [ctypes.c_int], ctypes.c_char_p

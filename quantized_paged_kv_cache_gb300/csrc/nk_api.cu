@@ -53,9 +53,12 @@ int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per
   return (int32_t)n;
 }
 
-int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
-                 int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
-                 void* workspace, size_t workspace_bytes, void* out, int32_t* status, void* stream, bool simt) {
+// Checks the decode arguments and fills `p`; *empty = nothing to launch.
+int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
+                   int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                   void* workspace, size_t workspace_bytes, void* out, int32_t* status, bool simt, DecodeParams* pp,
+                   bool* empty) {
+  *empty = true;
   int err = NK_OK;
   if (!pool_ok(pool, &err)) return err;
   if (B < 0 || T < 1 || T > NK_MAX_T || Hq < 1) return NK_ERR_SHAPE;
@@ -79,7 +82,7 @@ int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32
   if (need > 0 && (!workspace || workspace_bytes < need)) return NK_ERR_WORKSPACE;
   if (workspace && !aligned(workspace, 16)) return NK_ERR_WORKSPACE;
 
-  DecodeParams p;
+  DecodeParams& p = *pp;
   p.pool = reinterpret_cast<const uint8_t*>(pool->base_dev);
   p.num_pages = pool->num_pages;
   p.P = P;
@@ -103,14 +106,46 @@ int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32
   p.part_lse = p.part_o + slots * G * T * D;
   p.out = reinterpret_cast<uint16_t*>(out);
   p.status = status;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  p.early = 0;
+  *empty = false;
+  return NK_OK;
+}
+
+int launch_decode(const DecodeParams& p, bool simt, cudaStream_t st) {
   // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and 9 to 32
   // rows per kv-head; the mma.sync kernel for the other shapes
   cudaError_t e = simt ? launch_decode_simt(p, st)
-                       : (decode_tc_supported(D, T, G, P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
+                       : (decode_tc_supported(p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
   if (e != cudaSuccess) return NK_ERR_CUDA;
   e = launch_decode_combine(p, st);
   if (e != cudaSuccess) return NK_ERR_CUDA;
+  return NK_OK;
+}
+
+int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
+                 int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                 void* workspace, size_t workspace_bytes, void* out, int32_t* status, void* stream, bool simt) {
+  DecodeParams p;
+  bool empty = true;
+  const int err = prepare_decode(pool, q, bt, max_pages, ctx, B, T, Hq, sm_scale, max_ctx, num_ctas, workspace,
+                                 workspace_bytes, out, status, simt, &p, &empty);
+  if (err != NK_OK || empty) return err;
+  return launch_decode(p, simt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Checks the append arguments; *empty = nothing to launch.
+int check_append(const nk_kv_pool* pool, const int32_t* bt, int32_t max_pages, const int32_t* start_pos,
+                 const int32_t* cu_new, int32_t B, int32_t total_new, const void* k, const void* v, bool* empty) {
+  *empty = true;
+  int err = NK_OK;
+  if (!pool_ok(pool, &err)) return err;
+  if (B < 0 || total_new < 0 || max_pages < 1) return NK_ERR_SHAPE;
+  if (B == 0 || total_new == 0) return NK_OK;
+  if (!bt || !start_pos || !cu_new || !k || !v) return NK_ERR_NULL;
+  if (!aligned(k, 16) || !aligned(v, 16)) return NK_ERR_SHAPE;
+  // items of one 64-channel group of K or V of one (row, kv-head), numbered in 32 bits
+  if ((int64_t)total_new * pool->num_kv_heads * 2 * (pool->head_dim / 64) >= ((int64_t)1 << 31)) return NK_ERR_SHAPE;
+  *empty = false;
   return NK_OK;
 }
 
@@ -131,18 +166,40 @@ size_t nk_kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_hea
 int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
                  const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
                  const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream) {
-  int err = NK_OK;
-  if (!pool_ok(pool, &err)) return err;
-  if (B < 0 || total_new < 0 || max_pages_per_seq < 1) return NK_ERR_SHAPE;
-  if (B == 0 || total_new == 0) return NK_OK;
-  if (!block_table_dev || !start_pos_dev || !cu_new_dev || !k_dev || !v_dev) return NK_ERR_NULL;
-  if (!aligned(k_dev, 16) || !aligned(v_dev, 16)) return NK_ERR_SHAPE;
-  // items of one 64-channel group of K or V of one (row, kv-head), numbered in 32 bits
-  if ((int64_t)total_new * pool->num_kv_heads * 2 * (pool->head_dim / 64) >= ((int64_t)1 << 31)) return NK_ERR_SHAPE;
-  const cudaError_t e = launch_kv_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B,
-                                         total_new, k_dev, v_dev, status_dev,
+  bool empty = true;
+  const int err = check_append(pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B, total_new,
+                               k_dev, v_dev, &empty);
+  if (err != NK_OK || empty) return err;
+  const cudaError_t e = launch_kv_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev,
+                                         cu_new_dev, B, total_new, k_dev, v_dev, status_dev,
                                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;
+}
+
+int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                   const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t total_new, const void* k_dev,
+                   const void* v_dev, const void* q_dev, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                   int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                   size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream) {
+  bool no_append = true, no_decode = true;
+  int err = check_append(pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B, total_new, k_dev,
+                         v_dev, &no_append);
+  if (err != NK_OK) return err;
+  DecodeParams p;
+  err = prepare_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
+                       max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, false, &p, &no_decode);
+  if (err != NK_OK) return err;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!no_append) {
+    const cudaError_t e = launch_kv_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev,
+                                           cu_new_dev, B, total_new, k_dev, v_dev, status_dev, st);
+    if (e != cudaSuccess) return NK_ERR_CUDA;
+  }
+  if (no_decode) return NK_OK;
+  // the decode's predecessor is this append, which writes only pool pages:
+  // its prologue (lengths, block-table entries, Q) may overlap the append
+  p.early = no_append ? 0 : 1;
+  return launch_decode(p, false, st);
 }
 
 int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {

@@ -125,10 +125,12 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
   __shared__ int warp_tot[8];
   const SplitShape sh = p.shape();
   // The page prefix runs before the wait for the split kernel: this kernel
-  // only ever follows the split kernel of the same call, which releases it
-  // after its own chain_wait returned, so every kernel that could have
-  // written the context lengths has completed; the split kernel only reads
-  // them. They are read at L2 (the point of coherence), not through L1.
+  // only ever follows the split kernel of the same call, which could start
+  // only once its own predecessor had passed its wait (that predecessor is
+  // the caller's previous kernel, or this call's append, which writes only
+  // pool pages), so every kernel that could have written the context
+  // lengths has completed; the split kernel only reads them. They are read
+  // at L2 (the point of coherence), not through L1.
   block_page_prefix<true>(sh, p.ctx, pre, warp_tot);
   chain_wait();
   chain_release();

@@ -22,6 +22,13 @@ struct DecodeParams {
   float* part_lse;        // [n_ctas + B*Hkv][T*G]
   uint16_t* out;          // bf16 [B][T][Hq][D]
   int32_t* status;
+  // 1: the previous kernel on the stream is this call's own append, which
+  // writes only pool pages, so the split kernel reads the context lengths,
+  // block-table entries and Q before waiting for it (it waits before its
+  // first page load). Written before that append was launched, those inputs
+  // are visible: the append itself waited for every earlier kernel before
+  // this kernel could start.
+  int early;
   __host__ __device__ SplitShape shape() const { return SplitShape{B, Hkv, P, T, max_ctx, max_pages}; }
 };
 

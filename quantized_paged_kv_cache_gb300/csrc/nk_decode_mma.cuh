@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   // the tensor map is a launch parameter (no earlier kernel writes it): its
   // descriptor fetch can start before the wait for the previous kernel
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-  chain_wait();
+  if (!p.early) chain_wait();  // (early: waits below, before the first page load)
   chain_release();
   constexpr int NTEAMS = kConsumerWarps / CS;
   constexpr int DW = D / CS;        // channels per warp
@@ -287,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   block_page_prefix(sh, p.ctx, pre, warp_tot, lens);  // ends with __syncthreads
 
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
-  if (W == 0) return;
+  if (W == 0) {
+    if (p.early) chain_wait();  // every CTA waits: the grid must not complete before its predecessor
+    return;
+  }
   const int64_t x_begin = cta_begin(W, p.n_ctas, blockIdx.x);
   const int64_t x_end = cta_begin(W, p.n_ctas, blockIdx.x + 1);
   const int total = (int)(x_end - x_begin);
@@ -403,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   for (int q = tid; q < ncache; q += kThreads) pid[q] = page_coord(p, sh, pre, x_begin, q);
   if (have) stage_q();
   __syncthreads();
+  if (p.early) chain_wait();  // the pages may hold the preceding append's rows
   // The first S pages, issued in order by one thread (the copy unit then
   // completes page 0 first). Each issue waits until the unit accepts the
   // copy, so the issuer is the last warp, whose first block is in page 1.

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   // the tensor map is a launch parameter: its descriptor fetch can start
   // before the wait for the previous kernel
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
-  chain_wait();
+  if (!p.early) chain_wait();  // (early: waits below, before the first page load)
   chain_release();
   constexpr int NR = NT * 4;  // rows a score thread finishes (half of each 8-row tile)
   extern __shared__ uint8_t smem_raw[];
@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     if (next_segment(sh, pre, x0, x_end, s0)) prefetch_q(s0);
   }
   __syncthreads();
+  if (p.early) chain_wait();  // the pages may hold the preceding append's rows
   if (tid == 0) {
     const int n0 = total < S ? total : S;
     for (int q = 0; q < n0; ++q) issue_page<kD>(p, &tmap, pid[q], stage0 + q * kStageBytes, smem_u32(&full_bar[q]));

@@ -102,6 +102,27 @@ def test_append_rejects_bad_arguments():
     assert L.nk_kv_append(ctypes.byref(pool(num_pages=0)), FAKE, 4, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 2
 
 
+def test_decode_step_checks_both_calls_before_launching():
+    """nk_decode_step returns the first argument error of the append or the
+    attention before launching anything (no GPU is touched here)."""
+    L = nk.lib()
+    p = pool()
+
+    def step(pp=p, bt=FAKE, sp=FAKE, cu=FAKE, total=1, k=FAKE, v=FAKE, q=FAKE, ctx=FAKE, B=1, T=1, Hq=4,
+             scale=0.1, max_ctx=64, max_pages=4):
+        return L.nk_decode_step(ctypes.byref(pp) if pp is not None else None, bt, max_pages, sp, cu, total, k, v, q,
+                                ctx, B, T, Hq, scale, max_ctx, 0, FAKE, 1 << 30, FAKE, None, None)
+
+    assert step(pp=None) == 1                 # NULL pool
+    assert step(sp=None) == 1                 # append: NULL start positions
+    assert step(k=FAKE + 8) == 2              # append: misaligned K
+    assert step(q=0) == 1                     # attention: NULL Q
+    assert step(T=0) == 2                     # attention: T < 1
+    assert step(scale=float("inf")) == 2      # attention: non-finite scale
+    assert step(pp=pool(H=2), Hq=3) == 2      # attention: Hq not a multiple of Hkv
+    assert step(B=0, total=0) == 0            # nothing to do
+
+
 def test_combine_rejects_bad_arguments():
     L = nk.lib()
     assert L.nk_attn_combine(FAKE, FAKE, 2, 4, 96, FAKE, None) == 3

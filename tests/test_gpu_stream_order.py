@@ -7,7 +7,9 @@ before its first global-memory access. These tests enqueue chains of dependent
 calls with no host synchronization in between -- append then decode, step
 after step, on one shared workspace (the next split kernel overwrites the
 partials the previous combine reads) -- eagerly and as a captured CUDA graph,
-and compare every step's output with the oracle run step by step.
+and compare every step's output with the oracle run step by step. The same
+chains run through nk_decode_step, whose split kernel reads its lengths,
+block-table entries and Q while the step's append still runs.
 """
 import numpy as np
 import pytest
@@ -73,9 +75,14 @@ def device_inputs(c):
     return ins
 
 
-def enqueue(c, ins, ws, outs, status, stream):
+def enqueue(c, ins, ws, outs, status, stream, fused=False):
+    """Append + attention per step: two calls, or one nk_decode_step (fused)."""
     w = c.w_final
     for i, a in enumerate(ins):
+        if fused:
+            nk.decode_step(c.pool, c.bt_full, a["sp"], a["cu"], a["k"], a["v"], a["q"], a["ctx"], w.sm_scale,
+                           a["max_ctx"], workspace=ws, out=outs[i], status=status, stream=stream)
+            continue
         nk.kv_append(c.pool, c.bt_full, a["sp"], a["cu"], a["k"], a["v"], status=status, stream=stream)
         nk.paged_decode_attn(c.pool, a["q"], c.bt_full, a["ctx"], w.sm_scale, a["max_ctx"], workspace=ws,
                              out=outs[i], status=status, stream=stream)
@@ -87,8 +94,9 @@ def workspace(c):
 
 
 # T = 1 runs the mma.sync kernel, T = 2 (12 rows per kv-head) the tcgen05 kernel
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "decode_step"])
 @pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700])], ids=["t1", "t2"])
-def test_chained_steps_match_oracle(T, lens):
+def test_chained_steps_match_oracle(T, lens, fused):
     c = chain_case(T, lens, seed=40 + T)
     refs = oracle_steps(c)
     ins = device_inputs(c)
@@ -96,14 +104,37 @@ def test_chained_steps_match_oracle(T, lens):
     outs = [torch.empty_like(a["q"]) for a in ins]
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
-    enqueue(c, ins, ws, outs, status, torch.cuda.current_stream())
+    enqueue(c, ins, ws, outs, status, torch.cuda.current_stream(), fused=fused)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     for i in range(STEPS):
         compare(outs[i], refs[i], f"step {i}")
 
 
-def test_graph_replay_matches_eager():
+@pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700]), (4, [5, 640])], ids=["t1", "t2", "t4"])
+def test_decode_step_equals_two_calls(T, lens):
+    """nk_decode_step leaves the same pool bytes and the same outputs, bit for
+    bit, as nk_kv_append followed by nk_paged_decode_attn."""
+    c = chain_case(T, lens, seed=90 + T)
+    ins = device_inputs(c)
+    ws = workspace(c)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist = c.pool.storage.clone()
+    res = {}
+    for fused in (False, True):
+        c.pool.storage.copy_(hist)
+        outs = [torch.empty_like(a["q"]) for a in ins]
+        enqueue(c, ins, ws, outs, status, torch.cuda.current_stream(), fused=fused)
+        torch.cuda.synchronize()
+        res[fused] = (c.pool.storage.clone(), outs)
+    assert int(status.item()) == 0
+    assert torch.equal(res[False][0], res[True][0]), "pool bytes differ"
+    for i in range(STEPS):
+        assert torch.equal(res[False][1][i], res[True][1][i]), f"step {i} output differs"
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "decode_step"])
+def test_graph_replay_matches_eager(fused):
     """The same chain captured once into a CUDA graph: a replay on a pool reset
     to the history gives bit-identical outputs and pool bytes to the eager run."""
     c = chain_case(1, [100, 900], seed=77)
@@ -112,7 +143,7 @@ def test_graph_replay_matches_eager():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     hist = c.pool.storage.clone()
     eager = [torch.empty_like(a["q"]) for a in ins]
-    enqueue(c, ins, ws, eager, status, torch.cuda.current_stream())
+    enqueue(c, ins, ws, eager, status, torch.cuda.current_stream(), fused=fused)
     torch.cuda.synchronize()
     pool_eager = c.pool.storage.clone()
 
@@ -123,7 +154,7 @@ def test_graph_replay_matches_eager():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
-            enqueue(c, ins, ws, outs, status, s)
+            enqueue(c, ins, ws, outs, status, s, fused=fused)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     for rep in range(2):
