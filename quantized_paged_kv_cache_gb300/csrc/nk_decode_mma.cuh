@@ -420,17 +420,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   uint32_t par_cur = 0;
   int page_seq = 0;   // CTA page number of the current segment's first page
   int jn = team;       // next block of this team
-  // With up to two row tiles the next unit's Q fragments are loaded before
-  // the merge of the current one (their latency overlaps it); with more,
-  // keeping them live through the merge would spill, so they load here.
+  // With up to two row tiles the next unit's Q rows are fetched (one or two
+  // 16-byte pieces per thread) at the start of the current segment -- a
+  // load issued at its end would return behind the pages in flight -- and
+  // staged through the merge buffer after the merge; with more tiles the
+  // registers are not there, and Q loads at the segment start.
   constexpr bool kEarlyQ = NT <= 2;
-  bool first_seg = true;
+  bool staged = true;  // the current unit's Q sits in the merge buffer
   while (have) {
     const int L = lens[seg.b];
-    if (first_seg) load_q_staged();  // staged in the prologue, before its barrier
-    else if (!kEarlyQ) load_q(seg);
-    first_seg = false;
+    if (staged) load_q_staged();
+    else load_q(seg);
     convert_q();
+    if constexpr (kEarlyQ) {
+      int64_t xn = x;
+      Segment sn;
+      if (next_segment(sh, pre, xn, x_end, sn)) fetch_q(sn);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
@@ -668,15 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
     page_seq += seg_pages;
 
-    // the next segment, located before the merge when its Q loads go out now
     const bool last_seg = x >= x_end;
-    Segment nseg = seg;
-    int64_t nx = x;
-    bool nhave = false;
-    if constexpr (kEarlyQ) {
-      nhave = next_segment(sh, pre, nx, x_end, nseg);
-      if (nhave) load_q(nseg);
-    }
 
     // ---- merge the teams of this segment and write the result
     // row sums: reduce the per-lane partial l over the 8 lanes of a row
@@ -744,33 +742,56 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     }
     __syncthreads();
     if (!parked) {
-      // team tm adds its weighted accumulator into mo, one 16-channel chunk at
-      // a time with all of the chunk's loads issued before its stores
-      for (int tm = 0; tm < NTEAMS; ++tm) {
-        if (team == tm) {
-          float f[NT][2];
+      // The teams add their weighted accumulators into mo in NTEAMS rounds.
+      float f[NT][2];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) f[nt][e] = facs[team * MROWS + nt * 8 + 2 * t4 + e];
+        for (int e = 0; e < 2; ++e) f[nt][e] = facs[team * MROWS + nt * 8 + 2 * t4 + e];
+      if constexpr (NT <= 2) {
+        // In round rd team tm takes its 16-channel chunks c with
+        // c = tm + rd (mod NTEAMS): the teams of a round touch disjoint
+        // chunks, and every chunk gets one team per round (fixed order).
+        for (int rd = 0; rd < NTEAMS; ++rd) {
 #pragma unroll
           for (int c = 0; c < NCH; ++c) {
-            float prev[NT][4];
+            if (((c - team - rd) & (NTEAMS - 1)) != 0) continue;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                prev[nt][k] = (tm == 0) ? 0.f
-                                        : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)] =
-                    fmaf(o[c][nt][k], f[nt][k & 1], prev[nt][k]);
+              for (int e = 0; e < 2; ++e) {
+                // fragment elements e and e + 2 are adjacent channels of one row
+                float2* dst = reinterpret_cast<float2*>(mo + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16 + 2 * g);
+                const float2 prev = rd == 0 ? make_float2(0.f, 0.f) : *dst;
+                *dst = make_float2(fmaf(o[c][nt][e], f[nt][e], prev.x), fmaf(o[c][nt][e + 2], f[nt][e], prev.y));
+              }
           }
+          __syncthreads();
         }
-        __syncthreads();
+      } else {
+        // more row tiles: team tm adds all its chunks in round tm (fewer
+        // registers), all of a chunk's loads issued before its stores
+        for (int tm = 0; tm < NTEAMS; ++tm) {
+          if (team == tm) {
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+              float prev[NT][4];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  prev[nt][k] =
+                      (tm == 0) ? 0.f : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)] =
+                      fmaf(o[c][nt][k], f[nt][k & 1], prev[nt][k]);
+            }
+          }
+          __syncthreads();
+        }
       }
     }
     // normalize (weights already include 1/sum) and store, 4 channels a thread
@@ -804,12 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         if (ch == 0) p.part_lse[slot * M + r] = row_lse[r];
       }
     }
-    if constexpr (kEarlyQ) {
-      seg = nseg;
-      x = nx;
-      have = nhave;
-    } else {
-      have = next_segment(sh, pre, x, x_end, seg);
+    have = next_segment(sh, pre, x, x_end, seg);
+    staged = kEarlyQ && have;
+    if (staged) {
+      __syncthreads();  // the merge buffer has been read
+      stage_q();
+      __syncthreads();
     }
   }
 }

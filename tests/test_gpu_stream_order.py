@@ -75,17 +75,17 @@ def device_inputs(c):
     return ins
 
 
-def enqueue(c, ins, ws, outs, status, stream, fused=False):
+def enqueue(c, ins, ws, outs, status, stream, fused=False, num_ctas=0):
     """Append + attention per step: two calls, or one nk_decode_step (fused)."""
     w = c.w_final
     for i, a in enumerate(ins):
         if fused:
             nk.decode_step(c.pool, c.bt_full, a["sp"], a["cu"], a["k"], a["v"], a["q"], a["ctx"], w.sm_scale,
-                           a["max_ctx"], workspace=ws, out=outs[i], status=status, stream=stream)
+                           a["max_ctx"], num_ctas=num_ctas, workspace=ws, out=outs[i], status=status, stream=stream)
             continue
         nk.kv_append(c.pool, c.bt_full, a["sp"], a["cu"], a["k"], a["v"], status=status, stream=stream)
-        nk.paged_decode_attn(c.pool, a["q"], c.bt_full, a["ctx"], w.sm_scale, a["max_ctx"], workspace=ws,
-                             out=outs[i], status=status, stream=stream)
+        nk.paged_decode_attn(c.pool, a["q"], c.bt_full, a["ctx"], w.sm_scale, a["max_ctx"], num_ctas=num_ctas,
+                             workspace=ws, out=outs[i], status=status, stream=stream)
 
 
 def workspace(c):
@@ -114,8 +114,10 @@ def test_chained_steps_match_oracle(T, lens, fused):
 @pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700]), (4, [5, 640])], ids=["t1", "t2", "t4"])
 def test_decode_step_equals_two_calls(T, lens):
     """nk_decode_step leaves the same pool bytes and the same outputs, bit for
-    bit, as nk_kv_append followed by nk_paged_decode_attn."""
+    bit, as nk_kv_append followed by nk_paged_decode_attn (same CTA count)."""
     c = chain_case(T, lens, seed=90 + T)
+    w = c.w_final
+    n = nk.decode_default_ctas(w.B, w.Hkv, max(a for a in w.ctx_lens), w.P)
     ins = device_inputs(c)
     ws = workspace(c)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -124,7 +126,7 @@ def test_decode_step_equals_two_calls(T, lens):
     for fused in (False, True):
         c.pool.storage.copy_(hist)
         outs = [torch.empty_like(a["q"]) for a in ins]
-        enqueue(c, ins, ws, outs, status, torch.cuda.current_stream(), fused=fused)
+        enqueue(c, ins, ws, outs, status, torch.cuda.current_stream(), fused=fused, num_ctas=n)
         torch.cuda.synchronize()
         res[fused] = (c.pool.storage.clone(), outs)
     assert int(status.item()) == 0
