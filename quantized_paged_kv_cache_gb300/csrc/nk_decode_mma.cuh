@@ -14,10 +14,13 @@
 //     swizzled, [128 channels][P keys][K|V] boxes straight out of the pool by
 //     physical page id) plus 1-D bulk copies of the two scale arrays land in
 //     one stage of a shared-memory ring and complete on its "full" mbarrier.
-//     Thread 0 fills the ring; afterwards the last warp to finish reading a
+//     The prologue does every global read first (context lengths into
+//     shared memory, the page-coordinate cache, the first unit's Q staged
+//     once per CTA), since a load issued behind this SM's page loads returns
+//     only after their data; then one thread of the last warp issues the
+//     first S pages in order. Afterwards the last warp to finish reading a
 //     stage (elected by a shared-memory counter, after arriving on the
-//     stage's "empty" mbarrier) immediately loads the page S ahead into it,
-//     so no thread ever blocks to issue a load.
+//     stage's "empty" mbarrier) immediately loads the page S ahead into it.
 //   * Consumers: teams of CS warps. A team owns 16-key blocks of the stream
 //     (block j goes to team j % NTEAMS); its CS warps split the head_dim
 //     channels (DW = D/CS each, whole 64-channel groups), so each warp keeps
@@ -32,15 +35,18 @@
 //       team exchange of the partial scores (CS > 1) through shared memory,
 //            summed in a fixed order so every warp of the team holds identical
 //            scores.
-//       online softmax in base 2 (running max and sum per row; the
-//            accumulator is rescaled only when a row's max grows).
+//       online softmax in base 2 with a lazy reference per row (raised, and
+//            the accumulator rescaled, only when a score passes it by more
+//            than 8).
 //       PV   O^T[ch][row] += V^T[ch][key] P'^T[key][row] with
 //            P' = p * Vs[key][group] split into fp16 hi + lo parts (two MMAs)
 //            so the product keeps ~22 bits; V^T fragments come from
 //            ldmatrix.trans, P'^T fragments from movmatrix of the score tile.
 //     At the end of a segment (the CTA's share of one (sequence, kv-head))
-//     the teams merge through shared memory in a fixed order and the CTA
-//     writes the bf16 output (whole unit) or an fp32 partial plus LSE.
+//     the teams merge through shared memory in a fixed order (parked in the
+//     idle ring after the CTA's last segment) and the CTA writes the bf16
+//     output (whole unit) or an fp32 partial plus LSE; the next unit's Q was
+//     fetched when the segment started.
 // Every wait on an mbarrier is bounded; a timeout sets NK_DEVFLAG_TIMEOUT.
 #pragma once
 
