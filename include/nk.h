@@ -17,6 +17,15 @@
  *                         covers draft+1 token columns per sequence).
  *   nk_attn_combine       the log-sum-exp merge of split partial results, on
  *                         its own.
+ * and two conveniences the pages have no counterpart for: nk_decode_step (a
+ * step's append and attention in one call) and nk_paged_decode_attn_noalloc
+ * (the attention with library-owned scratch).
+ *
+ * Every kernel is launched with programmatic stream serialization: it may
+ * become resident while the previous kernel of the stream is still running,
+ * and waits for it before touching memory that kernel could have written, so
+ * the order of the stream is kept (calls can also be captured in a CUDA
+ * graph).
  *
  * Conventions for every entry point
  *   - Pointers named *_dev are device pointers; everything else is host.
