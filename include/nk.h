@@ -90,7 +90,7 @@ typedef enum {
 
 /* Limits of this build. */
 #define NK_GROUP 64      /* channels per quantization group */
-#define NK_MAX_T 8       /* query tokens per sequence (decode + MTP verify) */
+#define NK_MAX_T 16      /* query tokens per sequence (decode + MTP verify) */
 #define NK_MAX_HEAD_DIM 256
 
 /* A KV pool: `base_dev` points at num_pages * num_kv_heads chunks laid out

@@ -18,7 +18,7 @@ NK_DEVFLAG_BAD_POS = 0x2
 NK_DEVFLAG_BAD_CTX = 0x4
 NK_DEVFLAG_TIMEOUT = 0x8
 GROUP = 64
-MAX_T = 8
+MAX_T = 16
 
 __all__ = [
     "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_ctas",

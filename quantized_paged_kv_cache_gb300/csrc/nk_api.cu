@@ -53,6 +53,19 @@ int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per
   return (int32_t)n;
 }
 
+// Query columns per launch. A verify whose G*T rows exceed what one kernel
+// holds runs as column chunks over the same pages (each chunk masks its own
+// columns; the pages are read once per chunk): on the tcgen05 shapes (head
+// dim 256, 64-key pages) chunks of at most 24 rows, where that kernel is
+// fastest; on the mma.sync shapes at most 48 rows; on CUDA cores 8 columns.
+int chunk_cols(bool simt, int D, int T, int G, int P) {
+  if (simt) return T < 8 ? T : 8;
+  if (decode_tc_supported(D, T, G, P) || (G * T <= 48 && !(D == 256 && P == 64))) return T;
+  const int rows = (D == 256 && P == 64) ? 24 : 48;
+  const int c = rows / G;
+  return c < 1 ? 1 : (c < T ? c : T);
+}
+
 // Checks the decode arguments and fills `p`; *empty = nothing to launch.
 int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
                    int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
@@ -71,10 +84,11 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   if (max_pages < 1 || max_ctx < T || (int64_t)max_ctx > (int64_t)max_pages * P) return NK_ERR_SHAPE;
   if (!isfinite(sm_scale)) return NK_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(out, 16)) return NK_ERR_SHAPE;
+  const int Tc = chunk_cols(simt, D, T, G, P);
   if (simt) {
     if (G > 8) return NK_ERR_UNSUPPORTED;
   } else {
-    if (!decode_mma_supported(D, T, G, P)) return NK_ERR_UNSUPPORTED;
+    if (!decode_tc_supported(D, Tc, G, P) && !decode_mma_supported(D, Tc, G, P)) return NK_ERR_UNSUPPORTED;
   }
   const int per_sm = simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G);
   const int32_t n = num_ctas > 0 ? num_ctas : default_ctas(B, Hkv, max_ctx, P, per_sm);
@@ -106,19 +120,33 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   p.part_lse = p.part_o + slots * G * T * D;
   p.out = reinterpret_cast<uint16_t*>(out);
   p.status = status;
+  p.qT = T;
+  p.trim = 0;
   p.early = 0;
   *empty = false;
   return NK_OK;
 }
 
-int launch_decode(const DecodeParams& p, bool simt, cudaStream_t st) {
-  // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and 9 to 32
-  // rows per kv-head; the mma.sync kernel for the other shapes
-  cudaError_t e = simt ? launch_decode_simt(p, st)
-                       : (decode_tc_supported(p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
-  if (e != cudaSuccess) return NK_ERR_CUDA;
-  e = launch_decode_combine(p, st);
-  if (e != cudaSuccess) return NK_ERR_CUDA;
+int launch_decode(const DecodeParams& p0, bool simt, cudaStream_t st) {
+  const int Tc = chunk_cols(simt, p0.D, p0.T, p0.G, p0.P);
+  const int64_t slots = (int64_t)p0.n_ctas + (int64_t)p0.B * p0.Hkv;
+  for (int t0 = 0; t0 < p0.T; t0 += Tc) {
+    DecodeParams p = p0;
+    p.T = Tc < p0.T - t0 ? Tc : p0.T - t0;
+    p.qT = p0.T;
+    p.trim = p0.T - t0 - p.T;  // columns after this chunk
+    p.q = p0.q + (int64_t)t0 * p0.Hq * p0.D;
+    p.out = p0.out + (int64_t)t0 * p0.Hq * p0.D;
+    p.part_lse = p.part_o + slots * p.G * p.T * p.D;
+    if (t0 > 0) p.early = 0;  // the predecessor is the previous chunk's combine
+    // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and 9 to
+    // 32 rows per kv-head; the mma.sync kernel for the other shapes
+    cudaError_t e = simt ? launch_decode_simt(p, st)
+                         : (decode_tc_supported(p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
+    if (e != cudaSuccess) return NK_ERR_CUDA;
+    e = launch_decode_combine(p, st);
+    if (e != cudaSuccess) return NK_ERR_CUDA;
+  }
   return NK_OK;
 }
 

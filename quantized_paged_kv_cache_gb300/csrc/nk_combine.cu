@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
   // pool pages), so every kernel that could have written the context
   // lengths has completed; the split kernel only reads them. They are read
   // at L2 (the point of coherence), not through L1.
-  block_page_prefix<true>(sh, p.ctx, pre, warp_tot);
+  block_page_prefix<true>(sh, p.ctx, p.trim, pre, warp_tot);
   chain_wait();
   chain_release();
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const Deco
   };
   auto row_of = [&](int s) { return p.part_o + (((int64_t)c0 + s + u) * M + r) * D + c_off; };
   const int t = r / p.G, hg = r % p.G;
-  merge_row<C>(c1 - c0 + 1, lse_of, row_of, p.out + (((int64_t)b * p.T + t) * p.Hq + h * p.G + hg) * D + c_off);
+  merge_row<C>(c1 - c0 + 1, lse_of, row_of, p.out + (((int64_t)b * p.qT + t) * p.Hq + h * p.G + hg) * D + c_off);
 }
 
 // Standalone combine: part_o [S][R][D], part_lse [S][R] -> out [R][D]; block = row.

@@ -111,7 +111,7 @@ constexpr int kMaxBatch = 1024;  // sequences per call (prefix sums live in shar
 // the kernel reads no length from global memory after its page loads start.
 // kL2Only reads the lengths at L2 (ld.global.cg), bypassing this SM's L1.
 template <bool kL2Only = false>
-__device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int32_t* ctx_lens, int* pre,
+__device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int32_t* ctx_lens, int trim, int* pre,
                                                   int* warp_tot, int* lens = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   int v[4];
@@ -120,7 +120,7 @@ __device__ __forceinline__ void block_page_prefix(const SplitShape& s, const int
   for (int i = 0; i < 4; ++i) {
     const int b = tid * 4 + i;
     int L = 0;
-    if (b < s.B) L = kL2Only ? __ldcg(ctx_lens + b) : ctx_lens[b];
+    if (b < s.B) L = (kL2Only ? __ldcg(ctx_lens + b) : ctx_lens[b]) - trim;
     v[i] = (b < s.B) ? pages_of_len(s, L) : 0;
     if (lens && b < s.B) lens[b] = L;
     sum += v[i];

@@ -9,18 +9,23 @@ struct DecodeParams {
   const uint8_t* pool;
   int num_pages, P, Hkv, D;
   ChunkLayout lay;
-  const uint16_t* q;      // bf16 [B][T][Hq][D]
+  const uint16_t* q;      // bf16 [B][qT][Hq][D], already offset to this call's first column
   const int32_t* bt;      // [B][max_pages]
   int max_pages;
   const int32_t* ctx;     // [B]
   int B, T, Hq, G;
+  // Column chunks of a wide verify: this launch covers T of the qT columns
+  // of q / out, and every context length is read as ctx[b] - trim (the
+  // columns after the chunk are left out, so the chunk's last column sees
+  // keys up to its own causal limit).
+  int qT, trim;
   float sm_scale;
   float scale2;           // sm_scale * log2(e)
   int max_ctx;
   int n_ctas;
   float* part_o;          // [n_ctas + B*Hkv][T*G][D]
   float* part_lse;        // [n_ctas + B*Hkv][T*G]
-  uint16_t* out;          // bf16 [B][T][Hq][D]
+  uint16_t* out;          // bf16 [B][qT][Hq][D], offset like q
   int32_t* status;
   // 1: the previous kernel on the stream is this call's own append, which
   // writes only pool pages, so the split kernel reads the context lengths,
@@ -36,7 +41,7 @@ struct DecodeParams {
 __device__ __forceinline__ void flag_bad_ctx(const DecodeParams& p) {
   if (blockIdx.x != 0) return;
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const int L = p.ctx[b];
+    const int L = p.ctx[b] - p.trim;
     if (L < p.T || L > p.max_ctx || (int64_t)L > (int64_t)p.max_pages * p.P) flag(p.status, NK_DEVFLAG_BAD_CTX);
   }
 }

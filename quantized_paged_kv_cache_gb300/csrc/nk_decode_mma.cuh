@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   flag_bad_ctx(p);
-  block_page_prefix(sh, p.ctx, pre, warp_tot, lens);  // ends with __syncthreads
+  block_page_prefix(sh, p.ctx, p.trim, pre, warp_tot, lens);  // ends with __syncthreads
 
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
   if (W == 0) {
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         uint2 raw = make_uint2(0u, 0u);
         if (r < M) {
           const int t = r / G, hg = r % G;
-          raw = *reinterpret_cast<const uint2*>(p.q + (((int64_t)sg.b * T + t) * p.Hq + sg.h * G + hg) * D + ch0 +
+          raw = *reinterpret_cast<const uint2*>(p.q + (((int64_t)sg.b * p.qT + t) * p.Hq + sg.h * G + hg) * D + ch0 +
                                                 c * 16 + t4 * 4);
         }
         bq[nt][c][0] = raw.x;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       qv[k] = make_uint4(0u, 0u, 0u, 0u);
       if (r < M) {
         const int t = r / G, hg = r % G;
-        qv[k] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)sg.b * T + t) * p.Hq + sg.h * G + hg) * D + c8 * 8);
+        qv[k] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)sg.b * p.qT + t) * p.Hq + sg.h * G + hg) * D + c8 * 8);
       }
     }
   };
@@ -825,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         const int t = r / G, hg = r % G;
         const uint32_t w0 = f32_to_bf16(val.x) | ((uint32_t)f32_to_bf16(val.y) << 16);
         const uint32_t w1 = f32_to_bf16(val.z) | ((uint32_t)f32_to_bf16(val.w) << 16);
-        *reinterpret_cast<uint2*>(p.out + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + ch) = make_uint2(w0, w1);
+        *reinterpret_cast<uint2*>(p.out + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * D + ch) = make_uint2(w0, w1);
       } else {
         *reinterpret_cast<float4*>(p.part_o + (slot * M + r) * D + ch) = val;
         if (ch == 0) p.part_lse[slot * M + r] = row_lse[r];

@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(const DecodeParams p) 
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const SplitShape sh = p.shape();
   flag_bad_ctx(p);
-  block_page_prefix(sh, p.ctx, pre, warp_tot);
+  block_page_prefix(sh, p.ctx, p.trim, pre, warp_tot);
   const int64_t W = (int64_t)pre[p.B] * p.Hkv;
   if (W == 0) return;
   int64_t x = cta_begin(W, p.n_ctas, blockIdx.x);
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(const DecodeParams p) 
 
   Segment seg;
   while (next_segment(sh, pre, x, x_end, seg)) {
-    const int L = p.ctx[seg.b];
+    const int L = p.ctx[seg.b] - p.trim;
     const int last = L - T + t;  // last key visible to column t
     float qf[kSimtMaxG][CPL], o[kSimtMaxG][CPL], m[kSimtMaxG], l[kSimtMaxG];
 #pragma unroll
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(const DecodeParams p) 
 #pragma unroll
       for (int j = 0; j < CPL; ++j) { o[hg][j] = 0.f; qf[hg][j] = 0.f; }
       if (hg < G) {
-        const uint16_t* qr = p.q + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * D + lane * CPL;
+        const uint16_t* qr = p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * D + lane * CPL;
 #pragma unroll
         for (int j = 0; j < CPL; ++j) qf[hg][j] = __uint_as_float((uint32_t)__ldg(qr + j) << 16);
       }
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(const DecodeParams p) 
       }
       const float val = lsum > 0.f ? acc / lsum : 0.f;
       if (seg.whole) {
-        p.out[(((int64_t)seg.b * T + tt) * p.Hq + seg.h * G + hg) * D + c] = f32_to_bf16(val);
+        p.out[(((int64_t)seg.b * p.qT + tt) * p.Hq + seg.h * G + hg) * D + c] = f32_to_bf16(val);
       } else {
         p.part_o[((int64_t)seg_slot * M + r) * D + c] = val;
         if (c == 0) p.part_lse[(int64_t)seg_slot * M + r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;

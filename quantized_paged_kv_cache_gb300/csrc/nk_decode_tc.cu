@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tc_fence_before();
   }
   flag_bad_ctx(p);
-  block_page_prefix(sh, p.ctx, pre, warp_tot, lens);  // ends with __syncthreads
+  block_page_prefix(sh, p.ctx, p.trim, pre, warp_tot, lens);  // ends with __syncthreads
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int i = tid;  // convert-warp thread: line i & 3 of row i >> 2
     if (i < 4 * M) {
       const int n = i >> 2, t = n / G, hg = n % G;
-      const uint16_t* a = p.q + (((int64_t)sg.b * T + t) * p.Hq + sg.h * G + hg) * kD + (i & 3) * 64;
+      const uint16_t* a = p.q + (((int64_t)sg.b * p.qT + t) * p.Hq + sg.h * G + hg) * kD + (i & 3) * 64;
       asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
     }
   };
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (n < M) {
           const int t = n / G, hg = n % G;
           const uint4 raw =
-              *reinterpret_cast<const uint4*>(p.q + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * kD + ch);
+              *reinterpret_cast<const uint4*>(p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * kD + ch);
           const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t hw[4];
 #pragma unroll
@@ -642,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             if (!isfinite(v0) || !isfinite(v1)) flag(p.status, NK_DEVFLAG_RANGE);
             if (seg.whole) {
               const int t = n / G, hg = n % G;
-              *reinterpret_cast<uint32_t*>(p.out + (((int64_t)seg.b * T + t) * p.Hq + seg.h * G + hg) * kD + ch) =
+              *reinterpret_cast<uint32_t*>(p.out + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * kD + ch) =
                   (uint32_t)f32_to_bf16(v0) | ((uint32_t)f32_to_bf16(v1) << 16);
             } else {
               *reinterpret_cast<float2*>(p.part_o + (slot * M + n) * kD + ch) = make_float2(v0, v1);

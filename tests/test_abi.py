@@ -79,7 +79,7 @@ def test_decode_rejects_bad_arguments():
     assert decode(pool(P=24)) == 2                             # page size not a multiple of 16
     assert decode(pool(D=96)) == 2                             # head_dim not 64/128/256
     assert decode(pool(), T=0) == 2
-    assert decode(pool(), T=9) == 2                            # above NK_MAX_T
+    assert decode(pool(), T=17) == 2                           # above NK_MAX_T
     assert decode(pool(H=2), Hq=3) == 2                        # Hq not a multiple of Hkv
     assert decode(pool(), max_ctx=65, max_pages=4) == 2        # max_ctx beyond the table
     assert decode(pool(), scale=float("nan")) == 2

@@ -33,7 +33,7 @@ SHAPES = [
     ("t1_d256",       1, 1, 24, 4, 256, 64, [1000]),
     ("t4_d256",       2, 4, 24, 4, 256, 64, [700, 4099]),
     ("t2_d128",       3, 2, 16, 2, 128, 32, [33, 2, 515]),
-    ("t8_d64",        2, 8, 8, 1, 64, 16, [8, 300]),       # M = 64: CUDA cores only
+    ("t8_d64",        2, 8, 8, 1, 64, 16, [8, 300]),       # M = 64: mma.sync in chunks of 6 columns
     ("t8_g6",         2, 8, 12, 2, 128, 16, [9, 700]),     # M = 48: largest tensor-core tile set
     ("t3_g8",         2, 3, 32, 4, 128, 16, [77, 1234]),
     ("t5_mix",        4, 5, 12, 4, 256, 16, [5, 64, 65, 3000]),
@@ -44,6 +44,12 @@ SHAPES = [
     ("t3_tc",         2, 3, 24, 4, 256, 64, [3, 1500]),         # M = 18: three tiles, rows padded to 32
     ("t4_g8_tc",      2, 4, 32, 4, 256, 64, [65, 900]),         # M = 32: four tiles
     ("t5_g2_tc",      5, 5, 8, 4, 256, 64, [5, 64, 65, 128, 2000]),  # M = 10, many short units
+    # wide verifies: column chunks of 4 (tcgen05, 24 rows) or of 48 // G
+    # columns (mma.sync); 8 on CUDA cores
+    ("t8_chunks",     2, 8, 24, 4, 256, 64, [300, 2500]),     # M = 48: two chunks of 4
+    ("t12_chunks",    2, 12, 24, 4, 256, 64, [12, 1500]),     # ctx = T; three chunks
+    ("t16_g2_tc",     3, 16, 8, 4, 256, 64, [16, 700, 2000]), # M = 32: one tcgen05 launch
+    ("t16_d128",      2, 16, 16, 2, 128, 32, [40, 900]),      # G = 8, M = 128: chunks of 6
 ]
 
 
@@ -61,8 +67,9 @@ def test_append_bit_exact(case):
 
 
 def unsupported(w, impl):
-    """The tensor-core kernel holds at most 48 query rows (G*T) per kv-head."""
-    return impl == "mma" and w.G * w.T > 48
+    """The tensor-core kernels hold at most 48 query rows per kv-head in one
+    launch, so a column chunk needs G <= 48; the CUDA-core kernel G <= 8."""
+    return (impl == "mma" and w.G > 48) or (impl == "simt" and w.G > 8)
 
 
 @pytest.mark.parametrize("impl", IMPLS)
