@@ -149,6 +149,12 @@ size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int3
  *                  scratch, contents on entry do not matter
  *   out_dev        bf16 [B][T][Hq][D]
  * Runs the split kernel (tensor-core path) and then the combine on `stream`.
+ * T is 1 .. NK_MAX_T. When the G*T query rows of a kv-head do not fit one
+ * split kernel -- more than 32 rows at head_dim 256 with 64-key pages, more
+ * than 48 otherwise -- the columns run as consecutive chunks (at most 24
+ * and 48 rows respectively), each a split kernel and a combine over the same
+ * pages with its own causal limits. The workspace size for T covers every
+ * chunk.
  */
 int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
