@@ -180,6 +180,22 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
                 ws=ws, out=out, nct=nct, kernel=kernel)
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: with one replica per rank, the job's time."""
+    if world <= 1:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(step_bytes: int, ms: float, world: int) -> float:
+    """Whole-job throughput: every rank moves step_bytes per step."""
+    return step_bytes * world / (ms * 1e-3) / 1e9
+
+
 def run_ours(args, w, rank, world, device):
     import torch
 
@@ -249,11 +265,7 @@ def run_ours(args, w, rank, world, device):
     if int(S["status"].item()) != 0:
         raise RuntimeError(f"device status {int(S['status'].item())} during the benchmark")
 
-    ms = total_ms / K
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(total_ms / K, world, device)
     step_bytes = w.attn_bytes() + w.append_bytes()
 
     e2e = None
@@ -318,12 +330,8 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
     t0 = time.perf_counter()
     for j in range(K):
         step(j)
-    el = (time.perf_counter() - t0) * 1e3 / K
-    if world > 1:
-        t = torch.tensor([el], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        el = float(t.item())
-    return {"value": round(step_bytes * world / (el * 1e-3) / 1e9, 3), "unit": "GB/s",
+    el = max_over_ranks((time.perf_counter() - t0) * 1e3 / K, world, device)
+    return {"value": round(job_gbs(step_bytes, el, world), 3), "unit": "GB/s",
             "ms_per_step": round(el, 5), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "sync": "host waits for each step's output"}
 
@@ -468,7 +476,7 @@ def main():
     achieved = w.attn_bytes() / (attn_us * 1e-6) / 1e9
     traffic = ncu_traffic(w.name, args.kernel)
     us = r["ms"] * 1e3
-    gbs = r["step_bytes"] * world / (r["ms"] * 1e-3) / 1e9
+    gbs = job_gbs(r["step_bytes"], r["ms"], world)
     l2 = (f"rotating {r['replicas']} pool copies ({r['replicas'] * r['pool_bytes'] / 2**20:.0f} MiB) > 2x L2"
           if r["replicas"] > 1 else f"pool {r['pool_bytes'] / 2**20:.0f} MiB > 2x L2")
     out = {
