@@ -93,9 +93,10 @@ def workspace(c):
     return torch.empty(nk.decode_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D), dtype=torch.uint8, device="cuda")
 
 
-# T = 1 runs the mma.sync kernel, T = 2 (12 rows per kv-head) the tcgen05 kernel
+# T = 1 runs the mma.sync kernel, T = 2 (12 rows per kv-head) the tcgen05
+# kernel, T = 8 (48 rows) two tcgen05 column chunks
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "decode_step"])
-@pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700])], ids=["t1", "t2"])
+@pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700]), (8, [8, 600])], ids=["t1", "t2", "t8"])
 def test_chained_steps_match_oracle(T, lens, fused):
     c = chain_case(T, lens, seed=40 + T)
     refs = oracle_steps(c)
@@ -111,7 +112,8 @@ def test_chained_steps_match_oracle(T, lens, fused):
         compare(outs[i], refs[i], f"step {i}")
 
 
-@pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700]), (4, [5, 640])], ids=["t1", "t2", "t4"])
+@pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (2, [63, 1500, 700]), (4, [5, 640]), (8, [9, 400])],
+                         ids=["t1", "t2", "t4", "t8"])
 def test_decode_step_equals_two_calls(T, lens):
     """nk_decode_step leaves the same pool bytes and the same outputs, bit for
     bit, as nk_kv_append followed by nk_paged_decode_attn (same CTA count)."""
