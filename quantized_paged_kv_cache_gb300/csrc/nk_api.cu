@@ -47,6 +47,9 @@ int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per
   // at most two CTAs per SM: the default workspace size assumes that bound
   const int k = per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm);
   int64_t n = (int64_t)(sms > 0 ? sms : 148) * k;
+  // one sequence: a multiple of Hkv CTAs, so that no CTA's range spans two
+  // kv-heads (a second segment costs a merge, a partial write and a Q load)
+  if (B == 1 && Hkv > 1 && n >= Hkv) n = n / Hkv * Hkv;
   const int64_t w = max_items(B, Hkv, max_ctx, P);
   if (w < n) n = w;
   if (n < 1) n = 1;
