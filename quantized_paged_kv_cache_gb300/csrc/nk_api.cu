@@ -60,13 +60,18 @@ int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per
 // holds runs as column chunks over the same pages (each chunk masks its own
 // columns; the pages are read once per chunk): on the tcgen05 shapes (head
 // dim 256, 64-key pages) chunks of at most 24 rows, where that kernel is
-// fastest; on the mma.sync shapes at most 48 rows; on CUDA cores 8 columns.
+// fastest; on the mma.sync shapes at most 48 rows, fewer where a larger
+// page leaves no room for them; on CUDA cores 8 columns.
 int chunk_cols(bool simt, int D, int T, int G, int P) {
   if (simt) return T < 8 ? T : 8;
-  if (decode_tc_supported(D, T, G, P) || (G * T <= 48 && !(D == 256 && P == 64))) return T;
-  const int rows = (D == 256 && P == 64) ? 24 : 48;
-  const int c = rows / G;
-  return c < 1 ? 1 : (c < T ? c : T);
+  if (decode_tc_supported(D, T, G, P)) return T;
+  const bool tc_shape = D == 256 && P == 64;  // the tcgen05 kernel's head dim and page size
+  if (!tc_shape && decode_mma_supported(D, T, G, P)) return T;
+  int c = (tc_shape ? 24 : 48) / G;
+  if (c < 1) c = 1;
+  if (c > T) c = T;
+  while (c > 1 && !decode_tc_supported(D, c, G, P) && !decode_mma_supported(D, c, G, P)) --c;
+  return c;
 }
 
 // Checks the decode arguments and fills `p`; *empty = nothing to launch.

@@ -50,6 +50,8 @@ SHAPES = [
     ("t12_chunks",    2, 12, 24, 4, 256, 64, [12, 1500]),     # ctx = T; three chunks
     ("t16_g2_tc",     3, 16, 8, 4, 256, 64, [16, 700, 2000]), # M = 32: one tcgen05 launch
     ("t16_d128",      2, 16, 16, 2, 128, 32, [40, 900]),      # G = 8, M = 128: chunks of 6
+    ("t16_p128",      1, 16, 24, 4, 256, 128, [3000]),        # mma.sync, 128-key pages: the largest chunk that fits
+    ("t16_g1_tc",     2, 16, 4, 4, 256, 64, [20, 900]),       # G = 1: 16 rows, one tcgen05 launch
 ]
 
 
@@ -200,6 +202,25 @@ def test_decode_flags_bad_context(impl):
     ref = oracle.paged_attention(c.opool, w.num_pages, w.P, w.Hkv, w.D, c.bt_cpu, [40, 30], c.q_cpu, w.T, w.Hq,
                                  w.sm_scale)
     compare(out[1], ref[1], "valid sequence next to a bad one")
+
+
+def test_decode_step_flags_bad_context_before_its_wait():
+    """nk_decode_step's split kernel checks the context lengths before it
+    waits for the step's append; a bad length is flagged, the other
+    sequence is still right, and the append's rows land bit-exactly."""
+    T = 2
+    w = small("badctx_step", 2, T, 24, 4, 256, 64, [300, 700], seed=8, num_pages=20)
+    c = build(w)
+    hist_lens = [L - T for L in w.ctx_lens]
+    # history is the whole context minus the step's T rows; re-append those rows through decode_step
+    k, v, sp, cu = wl.append_batch(w, hist_lens, [T, T], device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ctx = torch.tensor([1, w.ctx_lens[1]], dtype=torch.int32, device="cuda")  # ctx < T for sequence 0
+    out = nk.decode_step(c.pool, c.bt, sp.cuda(), cu.cuda(), k, v, c.q, ctx, w.sm_scale, w.max_ctx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & nk.NK_DEVFLAG_BAD_CTX
+    assert np.array_equal(gpu_pool_bytes(c), c.opool), "rows re-appended by decode_step differ"
+    compare(out[1], oracle_attention_full(c)[1], "valid sequence next to a bad one")
 
 
 @pytest.mark.parametrize("impl", IMPLS)
