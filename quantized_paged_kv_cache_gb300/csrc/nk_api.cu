@@ -3,6 +3,8 @@
 // synchronization; every launch goes on the caller's stream.
 #include <math.h>
 
+#include <atomic>
+
 #include "nk_decode.cuh"
 
 namespace nk {
@@ -29,12 +31,15 @@ bool pool_ok(const nk_kv_pool* pool, int* err) {
 }
 
 int sm_count() {
+  static std::atomic<int> cached[64];  // per device; 0 = not looked up yet
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) { (void)cudaGetLastError(); return 0; }
+  if (dev >= 0 && dev < 64 && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
+  if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 

@@ -417,15 +417,15 @@ cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt,
   const int smem = (int)sizeof(AppendSmem);
   cudaError_t e;
   if (p.D == 256) {
-    e = cudaFuncSetAttribute(kv_append_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<256>), smem);
     if (e == cudaSuccess)
       e = launch_chained(kv_append_kernel<256>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
   } else if (p.D == 128) {
-    e = cudaFuncSetAttribute(kv_append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<128>), smem);
     if (e == cudaSuccess)
       e = launch_chained(kv_append_kernel<128>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
   } else {
-    e = cudaFuncSetAttribute(kv_append_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<64>), smem);
     if (e == cudaSuccess)
       e = launch_chained(kv_append_kernel<64>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
   }

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
 #include <utility>
 
 #include "nk.h"
@@ -45,6 +46,32 @@ struct ChunkLayout {
 // CTAs start launching (they only wait, holding no data, until this grid ends).
 __device__ __forceinline__ void chain_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void chain_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Raises a kernel's dynamic shared-memory limit on the current device once
+// (the setting persists), instead of on every launch: the host side of a
+// decode step is on the critical path of a call that waits for its result.
+inline cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  struct Entry {
+    const void* kernel;
+    int device, bytes;
+  };
+  static std::mutex mu;
+  static Entry seen[256];
+  static int count = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < count; ++i)
+      if (seen[i].kernel == kernel && seen[i].device == dev && seen[i].bytes >= bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (count < 256) seen[count++] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
+}
 
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,

@@ -39,6 +39,22 @@ static EncodeTiledFn encode_fn() {
 // 4-D view of the pool's code bytes: [D channels][P keys][K|V][page*Hkv + h],
 // boxes of [min(D,128)][P][2][1] with the matching shared-memory swizzle.
 cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map) {
+  // the last few maps of this host thread, by pool geometry (encoding one is
+  // host work on the critical path of every call)
+  struct Cached {
+    const void* base;
+    int num_pages, P, Hkv, D;
+    CUtensorMap map;
+  };
+  thread_local Cached cache[8];
+  thread_local int used = 0, next = 0;
+  for (int i = 0; i < used; ++i) {
+    const Cached& c = cache[i];
+    if (c.base == p.pool && c.num_pages == p.num_pages && c.P == p.P && c.Hkv == p.Hkv && c.D == p.D) {
+      *map = c.map;
+      return cudaSuccess;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.P, 2, (cuuint64_t)p.num_pages * p.Hkv};
@@ -49,7 +65,12 @@ cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map) {
                         CU_TENSOR_MAP_INTERLEAVE_NONE,
                         p.D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  Cached& c = cache[next];
+  c = Cached{p.pool, p.num_pages, p.P, p.Hkv, p.D, *map};
+  next = (next + 1) % 8;
+  if (used < 8) ++used;
+  return cudaSuccess;
 }
 
 cudaError_t launch_d256(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st);

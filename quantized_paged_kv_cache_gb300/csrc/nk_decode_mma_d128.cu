@@ -9,8 +9,7 @@ template <int D, int NT, int CS>
 static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
   const Geometry geo = geometry(D, NT, CS, p.P, p.B);
   if (geo.stages < 2 || geo.total > kSmemLimit) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, NT, CS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       geo.total);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_mma_kernel<D, NT, CS>), geo.total);
   if (e != cudaSuccess) return e;
   return launch_chained(decode_mma_kernel<D, NT, CS>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
 }

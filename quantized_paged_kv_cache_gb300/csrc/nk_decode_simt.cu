@@ -224,7 +224,7 @@ int decode_simt_ctas_per_sm(int D, int G) {
 
 template <int CPL>
 static cudaError_t launch_simt_t(const DecodeParams& p, size_t smem, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(decode_simt_kernel<CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_simt_kernel<CPL>), (int)smem);
   if (e != cudaSuccess) return e;
   return launch_chained(decode_simt_kernel<CPL>, dim3(p.n_ctas), dim3(256), smem, stream, p);
 }

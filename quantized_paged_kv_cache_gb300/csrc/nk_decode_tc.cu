@@ -670,7 +670,7 @@ template <int W, int NT>
 static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
   const Layout LY = layout(W, NT);
   if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<W, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, LY.total);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT>), LY.total);
   if (e != cudaSuccess) return e;
   return launch_chained(decode_tc_kernel<W, NT>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
 }
