@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c1_decode",
-                    help="tiny | c1_decode | c8_verify | long_context | mix")
+                    help="tiny | c1_decode | c8_verify | long_context | mix | c8_decode")
     ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

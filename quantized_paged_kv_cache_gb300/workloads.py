@@ -91,7 +91,8 @@ def _gen(seed: int, tag: int, device) -> torch.Generator:
 
 
 def make(name: str) -> Workload:
-    """The five workloads: tiny, c1_decode, c8_verify, long_context, mix."""
+    """The workloads: tiny, c1_decode, c8_verify, long_context, mix, and
+    c8_decode (the C8 verify contexts at T = 1: plain decode of 8 sequences)."""
     if name == "tiny":
         w = Workload("tiny", B=1, T=1, Hq=2, Hkv=1, D=64, P=16, ctx_lens=[256], seed=0, append_len=1,
                      note="1 seq, 1 kv-head, 2 q-heads, head_dim 64, ctx 256, page 16, T=1")
@@ -100,11 +101,15 @@ def make(name: str) -> Workload:
                      outlier_channels=4, outlier_scale=8.0,
                      note="C1 decode: 24 q / 4 kv heads, head_dim 256, ctx 32,768, page 64, T=1, "
                           "4 K outlier channels per head x8")
-    elif name == "c8_verify":
+    elif name in ("c8_verify", "c8_decode"):
         g = _gen(2, 0, "cpu")
         lens = torch.randint(4096, 65536 + 1, (8,), generator=g).tolist()
-        w = Workload("c8_verify", B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=lens, seed=2, append_len=4,
-                     note="MTP3 verify C8: 8 seqs, T=4 causal, ctx ~ U[4,096, 65,536]")
+        if name == "c8_verify":
+            w = Workload("c8_verify", B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=lens, seed=2, append_len=4,
+                         note="MTP3 verify C8: 8 seqs, T=4 causal, ctx ~ U[4,096, 65,536]")
+        else:
+            w = Workload("c8_decode", B=8, T=1, Hq=24, Hkv=4, D=256, P=64, ctx_lens=lens, seed=2, append_len=1,
+                         note="plain decode C8: 8 seqs, T=1, the C8 verify contexts")
     elif name == "long_context":
         w = Workload("long_context", B=1, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[262144], seed=3, append_len=4,
                      token_norm_range=(0.5, 2.0),
@@ -118,7 +123,7 @@ def make(name: str) -> Workload:
     return tables(w)
 
 
-CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix")
+CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix", "c8_decode")
 
 
 def tables(w: Workload, num_pages: int | None = None) -> Workload:

@@ -1,4 +1,4 @@
-"""Full-size parity on the five benchmark workloads, in the launch
+"""Full-size parity on the benchmark workloads, in the launch
 configuration bench.py times (default CTA count, the step's append as one
 batched call).
 
