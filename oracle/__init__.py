@@ -39,29 +39,42 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of every exported function."""
+    P, I, D, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
+    L.oracle_bf16_to_double.argtypes, L.oracle_bf16_to_double.restype = [ctypes.c_uint16], D
+    L.oracle_double_to_bf16.argtypes, L.oracle_double_to_bf16.restype = [D], ctypes.c_uint16
+    L.oracle_round_bf16.argtypes, L.oracle_round_bf16.restype = [P, Z, P], None
+    L.oracle_quantize_group.argtypes, L.oracle_quantize_group.restype = [P, I, P], ctypes.c_float
+    L.oracle_chunk_bytes.argtypes, L.oracle_chunk_bytes.restype = [I, I], Z
+    L.oracle_pool_bytes.argtypes, L.oracle_pool_bytes.restype = [I, I, I, I], Z
+    L.oracle_kv_append.argtypes = [P, I, I, I, I, P, I, P, P, I, P, P]
+    L.oracle_kv_append.restype = I
+    L.oracle_attention_row.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, I, I, I, I, I, P, P]
+    L.oracle_attention_row.restype = I
+    L.oracle_paged_attention.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, P, P]
+    L.oracle_paged_attention.restype = I
+    L.oracle_combine.argtypes, L.oracle_combine.restype = [P, P, I, I, I, P], None
+    L.oracle_num_threads.argtypes, L.oracle_num_threads.restype = [], I
+    return L
+
+
 def lib() -> ctypes.CDLL:
     global _lib
     with _lock:
         if _lib is None:
             build()
-            L = ctypes.CDLL(_LIB)
-            P, I, D, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_size_t
-            L.oracle_bf16_to_double.argtypes, L.oracle_bf16_to_double.restype = [ctypes.c_uint16], D
-            L.oracle_double_to_bf16.argtypes, L.oracle_double_to_bf16.restype = [D], ctypes.c_uint16
-            L.oracle_round_bf16.argtypes, L.oracle_round_bf16.restype = [P, Z, P], None
-            L.oracle_quantize_group.argtypes, L.oracle_quantize_group.restype = [P, I, P], ctypes.c_float
-            L.oracle_chunk_bytes.argtypes, L.oracle_chunk_bytes.restype = [I, I], Z
-            L.oracle_pool_bytes.argtypes, L.oracle_pool_bytes.restype = [I, I, I, I], Z
-            L.oracle_kv_append.argtypes = [P, I, I, I, I, P, I, P, P, I, P, P]
-            L.oracle_kv_append.restype = I
-            L.oracle_attention_row.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, I, I, I, I, I, P, P]
-            L.oracle_attention_row.restype = I
-            L.oracle_paged_attention.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, P, P]
-            L.oracle_paged_attention.restype = I
-            L.oracle_combine.argtypes, L.oracle_combine.restype = [P, P, I, I, I, P], None
-            L.oracle_num_threads.argtypes, L.oracle_num_threads.restype = [], I
-            _lib = L
+            _lib = _bind(ctypes.CDLL(_LIB))
     return _lib
+
+
+def use_library(path: str) -> None:
+    """Make every wrapper below call the oracle compiled at `path` instead of
+    liboracle.so (the tests use this to run the pins against deliberately
+    altered copies of oracle.c)."""
+    global _lib
+    with _lock:
+        _lib = _bind(ctypes.CDLL(os.path.abspath(path)))
 
 
 def _ptr(a: np.ndarray):

@@ -40,7 +40,7 @@ def lossless_rows(rng, n, H, D, exp_range=(-3, 3)):
 class Case:
     """A paged cache filled through the oracle's own append."""
 
-    def __init__(self, rng, B, T, Hq, Hkv, D, P, lens, lossless=True, spare_pages=3, fill=0):
+    def __init__(self, rng, B, T, Hq, Hkv, D, P, lens, lossless=True, spare_pages=3, fill=0, k_exp=(-3, 3)):
         self.B, self.T, self.Hq, self.Hkv, self.D, self.P = B, T, Hq, Hkv, D, P
         self.lens = list(lens)
         need = [(L + P - 1) // P for L in lens]
@@ -56,7 +56,7 @@ class Case:
         self.k, self.v = [], []
         for b in range(B):
             if lossless:
-                k, v = lossless_rows(rng, lens[b], Hkv, D), lossless_rows(rng, lens[b], Hkv, D)
+                k, v = lossless_rows(rng, lens[b], Hkv, D, k_exp), lossless_rows(rng, lens[b], Hkv, D)
             else:
                 k = torch.from_numpy(rng.standard_normal((lens[b], Hkv, D))).to(torch.bfloat16)
                 v = torch.from_numpy(rng.standard_normal((lens[b], Hkv, D))).to(torch.bfloat16)
@@ -74,6 +74,21 @@ class Case:
         return oracle.paged_attention(self.pool, self.num_pages, self.P, self.Hkv, self.D, self.bt,
                                       np.array(self.lens, np.int32), self.q, self.T, self.Hq, self.scale, **kw)
 
+    def scores_max_weight(self):
+        """Median over rows of the largest softmax weight (unquantized inputs, torch fp64)."""
+        tops = []
+        for b in range(self.B):
+            L = self.lens[b]
+            G = self.Hq // self.Hkv
+            q = self.q[b].to(torch.float64)                                  # [T, Hq, D]
+            k = self.k[b].to(torch.float64).repeat_interleave(G, dim=1)     # [L, Hq, D]
+            z = torch.einsum("thd,lhd->thl", q, k) * self.scale
+            n = torch.arange(L)[None, None, :]
+            t = torch.arange(self.T)[:, None, None]
+            z = z.masked_fill(n > (L - self.T + t), float("-inf"))
+            tops.append(torch.softmax(z, dim=-1).amax(dim=-1).flatten())
+        return float(torch.cat(tops).median())
+
     def sdpa(self):
         """Dense causal GQA attention on the unquantized rows (torch, fp64)."""
         outs = []
@@ -90,6 +105,11 @@ class Case:
         return torch.stack(outs).numpy()
 
 
+# Key scales 2^-e: e in [-3, 3] gives keys up to +-1016 and near one-hot
+# softmax rows (a dominant key per row: index and selection errors show);
+# e in [5, 8] gives keys within +-4 and scores of order 1, so many keys weigh
+# in every row (normalization and weighting errors show).
+@pytest.mark.parametrize("k_exp", [(-3, 3), (5, 8)], ids=["peaked", "temperate"])
 @pytest.mark.parametrize("B,T,Hq,Hkv,D,P,lens", [
     (1, 1, 2, 1, 64, 16, [256]),
     (2, 1, 6, 2, 128, 16, [37, 130]),
@@ -97,9 +117,13 @@ class Case:
     (2, 8, 8, 4, 256, 16, [8, 45]),
     (1, 3, 24, 4, 256, 64, [200]),
 ])
-def test_lossless_equals_dense_sdpa(B, T, Hq, Hkv, D, P, lens):
+def test_lossless_equals_dense_sdpa(B, T, Hq, Hkv, D, P, lens, k_exp):
     rng = np.random.default_rng(B * 100 + T)
-    c = Case(rng, B, T, Hq, Hkv, D, P, lens)
+    c = Case(rng, B, T, Hq, Hkv, D, P, lens, k_exp=k_exp)
+    if k_exp[0] > 0:
+        # the softmax really is spread: the largest weight of a row is well below 1
+        s = c.scores_max_weight()
+        assert s < 0.5, s
     np.testing.assert_allclose(c.attention(), c.sdpa(), rtol=1e-12, atol=1e-12)
 
 

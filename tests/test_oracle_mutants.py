@@ -1,0 +1,155 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each mutant below is oracle.c with one plausible mistake planted in it: a
+dropped term, a wrong sign, rounding rule or bound, a wrong or transposed
+index (page, slot, group, head, query row), a swapped operand. Every mutant is
+compiled into a library of its own, and the oracle pins (the quantizer and
+attention test files) run against it in a child process; each mutant must be
+caught, i.e. make at least one pin fail, while the unaltered source, built the
+same way, passes all of them. The mistakes are planted in copies in a
+temporary directory: oracle.c itself is never changed.
+
+Mistakes that cannot change any result are not listed, with the reason:
+  * the clamp to [-127, 127]: fp32(x / s) with |x| <= absmax and
+    s = fp32(absmax / 127) is at most 127 (1 + 2^-24) < 127.5, so the clamp
+    never acts and no input can tell a different clamp apart;
+  * subtracting a different finite reference than the maximum in the softmax
+    or in the combine (the weights' ratios do not depend on it);
+  * skipping the empty partials in the combine (exp(-inf) = 0 already).
+"""
+import os
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PINS = ["tests/test_oracle_quantize.py", "tests/test_oracle_attention.py"]
+
+# (name, [(text in oracle.c, replacement), ...]); each text occurs exactly once.
+MUTANTS = [
+    # quantizer
+    ("scale divides by 128", [("(float)(a / 127.0)", "(float)(a / 128.0)")]),
+    ("zero group gets scale 1/2", [("(a == 0.0) ? 1.0f", "(a == 0.0) ? 0.5f")]),
+    ("absmax without the absolute value",
+     [("double v = fabs(oracle_bf16_to_double(x[i]));", "double v = oracle_bf16_to_double(x[i]);")]),
+    ("quotient not rounded to fp32",
+     [("float r = (float)(oracle_bf16_to_double(x[i]) / (double)s);",
+       "double r = oracle_bf16_to_double(x[i]) / (double)s;")]),
+    ("ties away from zero", [("double k = nearbyint((double)r);", "double k = round((double)r);")]),
+    ("truncation instead of rounding", [("double k = nearbyint((double)r);", "double k = trunc((double)r);")]),
+    # bf16 helpers
+    ("bf16 with 9 significant bits",
+     [("r = ldexp(nearbyint(ldexp(m, 8)), e - 8);", "r = ldexp(nearbyint(ldexp(m, 9)), e - 9);")]),
+    ("bf16 rounding truncates",
+     [("r = ldexp(nearbyint(ldexp(m, 8)), e - 8);", "r = ldexp(trunc(ldexp(m, 8)), e - 8);")]),
+    ("bf16 subnormal quantum 2^-132",
+     [("r = nearbyint(ldexp(x, 133)) * ldexp(1.0, -133);", "r = nearbyint(ldexp(x, 132)) * ldexp(1.0, -132);")]),
+    ("bf16 widening drops the sign",
+     [("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)(bits & 0x7fffu) << 16;")]),
+    # pool layout
+    ("K and V scale arrays swapped",
+     [("c.ks = (float*)(base + (size_t)P * D);",
+       "c.ks = (float*)(base + 2 * (size_t)P * D + (size_t)P * g * sizeof(float));"),
+      ("c.vs = (float*)(base + 2 * (size_t)P * D + (size_t)P * g * sizeof(float));",
+       "c.vs = (float*)(base + (size_t)P * D);")]),
+    ("chunk index misses the head stride",
+     [("((size_t)page * num_kv_heads + head)", "((size_t)page + head)")]),
+    # append
+    ("append slot off by one", [("int slot = (int)(pos % P);", "int slot = (int)((pos + 1) % P);")]),
+    ("append ignores the block table",
+     [("int page = block_table[(size_t)b * max_pages + pos / P];", "int page = (int)(pos / P);")]),
+    ("append assigns boundary rows to the wrong sequence",
+     [("while (b + 1 <= B && cu_new[b + 1] <= j) ++b;", "while (b + 1 < B && cu_new[b + 1] < j) ++b;")]),
+    ("append reads K rows head-major",
+     [("const uint16_t* krow = k + ((size_t)j * H + h) * D;",
+       "const uint16_t* krow = k + ((size_t)h * total + j) * D;")]),
+    ("append quantizes V from K",
+     [("oracle_quantize_group(vrow + gr * GROUP", "oracle_quantize_group(krow + gr * GROUP")]),
+    # attention
+    ("q-head i reads kv-head i mod Hkv", [("const int h = i / G;", "const int h = i % H;")]),
+    ("no causal mask among the T columns", [("const long last = L - T + t;", "const long last = L - 1;")]),
+    ("causal limit one key short", [("const long last = L - T + t;", "const long last = L - T + t - 1;")]),
+    ("query rows read head-major",
+     [("const uint16_t* qrow = q + (((size_t)b * T + t) * Hq + i) * D;",
+       "const uint16_t* qrow = q + (((size_t)b * Hq + i) * T + t) * D;")]),
+    ("softmax scale dropped", [("z[n - n0] = sm_scale * dot;", "z[n - n0] = dot;")]),
+    ("K pages read without the block table",
+     [("int page = block_table[(size_t)b * max_pages + n / P];\n    if (page < 0",
+       "int page = (int)(n / P);\n    if (page < 0")]),
+    ("K group scale indexed by channel mod groups",
+     [("(double)c.ks[(size_t)slot * g + ch / GROUP];", "(double)c.ks[(size_t)slot * g + ch % g];")]),
+    ("V dequantized with the K scales",
+     [("(double)c.vs[(size_t)slot * g + ch / GROUP]", "(double)c.ks[(size_t)slot * g + ch / GROUP]")]),
+    ("V channels of a pair transposed",
+     [("((double)c.vc[(size_t)slot * D + ch]", "((double)c.vc[(size_t)slot * D + (ch ^ 1)]")]),
+    ("softmax weights without the max shift but LSE with it",
+     [("double w = exp(z[n - n0] - m);", "double w = exp(z[n - n0]);")]),
+    ("softmax sum counts keys", [("l += w;", "l += 1.0;")]),
+    ("output not normalized", [("for (int ch = 0; ch < D; ++ch) o[ch] /= l;", "")]),
+    ("LSE without the max", [("*lse = m + log(l);", "*lse = log(l);")]),
+    # combine
+    ("combine weight with the wrong sign", [("double w = exp(ls - m);", "double w = exp(m - ls);")]),
+    ("combine not normalized", [("for (int c = 0; c < D; ++c) o[c] /= wsum;", "")]),
+    ("combine partials read row-major",
+     [("part_o[((size_t)s * R + r) * D + c]", "part_o[((size_t)r * S + s) * D + c]")]),
+]
+
+RUNNER = (
+    "import sys, oracle, pytest\n"
+    "oracle.use_library(sys.argv[1])\n"
+    "sys.exit(pytest.main(['-x', '-q', '-rf', '-p', 'no:cacheprovider', '-W', 'ignore'] + sys.argv[2:]))\n"
+)
+
+
+def _source() -> str:
+    with open(os.path.join(ROOT, "oracle", "oracle.c")) as f:
+        return f.read()
+
+
+def _mutate(src: str, edits) -> str:
+    for old, new in edits:
+        assert src.count(old) == 1, f"mutation anchor not unique or missing: {old!r}"
+        src = src.replace(old, new)
+    return src
+
+
+def _build_and_run(src: str, workdir: str, tag: str):
+    c_path = os.path.join(workdir, f"{tag}.c")
+    so_path = os.path.join(workdir, f"{tag}.so")
+    with open(c_path, "w") as f:
+        f.write(src)
+    inc = os.path.join(ROOT, "oracle")
+    subprocess.run(["gcc", *oracle.CFLAGS, "-I", inc, "-o", so_path, c_path, "-lm"], check=True,
+                   capture_output=True)
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-c", RUNNER, so_path, *PINS], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=300)
+    failed = [ln.split(" ")[1] for ln in r.stdout.splitlines() if ln.startswith("FAILED ")]
+    return r.returncode, failed, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def test_every_mutant_fails_a_pin(tmp_path):
+    src = _source()
+    jobs = [("unaltered", src)] + [(f"m{i:02d}", _mutate(src, edits)) for i, (_, edits) in enumerate(MUTANTS)]
+    with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
+        results = list(ex.map(lambda j: _build_and_run(j[1], str(tmp_path), j[0]), jobs))
+    rc0, failed0, log0 = results[0]
+    assert rc0 == 0, f"the unaltered oracle must pass every pin:\n{log0}"
+    survivors, crashed = [], []
+    for (name, _), (rc, failed, log) in zip(MUTANTS, results[1:]):
+        if rc == 0:
+            survivors.append(name)
+        elif rc != 1 or not failed:
+            crashed.append(f"{name}: exit {rc}\n{log}")
+    assert not crashed, "mutants must be caught by a failing pin, not by a crash:\n" + "\n".join(crashed)
+    assert not survivors, f"mutants no pin catches: {survivors}"
+
+
+@pytest.mark.parametrize("name,edits", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutation_anchors_exist(name, edits):
+    """Each planted mistake still applies to the current oracle.c."""
+    _mutate(_source(), edits)
