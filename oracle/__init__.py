@@ -56,6 +56,20 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_paged_attention.restype = I
     L.oracle_combine.argtypes, L.oracle_combine.restype = [P, P, I, I, I, P], None
     L.oracle_num_threads.argtypes, L.oracle_num_threads.restype = [], I
+    U16 = ctypes.c_uint16
+    L.oracle_double_to_f16.argtypes, L.oracle_double_to_f16.restype = [D], U16
+    L.oracle_f16_to_double.argtypes, L.oracle_f16_to_double.restype = [U16], D
+    L.oracle_rk_rotate64.argtypes, L.oracle_rk_rotate64.restype = [P, P], None
+    L.oracle_rk_quantize_k.argtypes, L.oracle_rk_quantize_k.restype = [P, P], U16
+    L.oracle_rk_quantize_v.argtypes, L.oracle_rk_quantize_v.restype = [P, P], U16
+    L.oracle_rk_chunk_bytes.argtypes, L.oracle_rk_chunk_bytes.restype = [I, I], Z
+    L.oracle_rk_pool_bytes.argtypes, L.oracle_rk_pool_bytes.restype = [I, I, I, I], Z
+    L.oracle_rk_append.argtypes = [P, I, I, I, I, P, I, P, P, I, P, P]
+    L.oracle_rk_append.restype = I
+    L.oracle_rk_attention_row.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, I, I, I, I, I, P, P]
+    L.oracle_rk_attention_row.restype = I
+    L.oracle_rk_paged_attention.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, P, P]
+    L.oracle_rk_paged_attention.restype = I
     return L
 
 
@@ -213,4 +227,112 @@ def chunk_view(pool: np.ndarray, num_pages, page_size, num_kv_heads, head_dim):
     ks = c[:, :, o1:o2].copy().view(np.float32).reshape(num_pages, num_kv_heads, P, g)
     vc = c[:, :, o2:o3].view(np.int8).reshape(num_pages, num_kv_heads, P, D)
     vs = c[:, :, o3:].copy().view(np.float32).reshape(num_pages, num_kv_heads, P, g)
+    return kc, ks, vc, vs
+
+
+# ---------------------------------------------------------------------------
+# rk8v4 (readings and layout in oracle.h)
+# ---------------------------------------------------------------------------
+
+def double_to_f16(x: float) -> int:
+    return int(lib().oracle_double_to_f16(float(x)))
+
+
+def f16_to_double(bits: int) -> float:
+    return float(lib().oracle_f16_to_double(int(bits)))
+
+
+def rk_rotate64(x_bits) -> np.ndarray:
+    """R x (fp32, the append's butterfly order) of one 64-channel bf16 group."""
+    x = _bits(x_bits).reshape(-1)
+    assert x.size == 64
+    y = np.empty(64, dtype=np.float32)
+    lib().oracle_rk_rotate64(_ptr(x), _ptr(y))
+    return y
+
+
+def rk_quantize_k(y) -> tuple[np.ndarray, int]:
+    """64 rotated fp32 values -> (int8 codes, fp16 scale bits)."""
+    y = np.ascontiguousarray(y, dtype=np.float32).reshape(-1)
+    assert y.size == 64
+    q = np.empty(64, dtype=np.int8)
+    sb = lib().oracle_rk_quantize_k(_ptr(y), _ptr(q))
+    return q, int(sb)
+
+
+def rk_quantize_v(x_bits) -> tuple[np.ndarray, int]:
+    """32 bf16 values -> (16 packed bytes, fp16 scale bits)."""
+    x = _bits(x_bits).reshape(-1)
+    assert x.size == 32
+    packed = np.empty(16, dtype=np.uint8)
+    sb = lib().oracle_rk_quantize_v(_ptr(x), _ptr(packed))
+    return packed, int(sb)
+
+
+def rk_chunk_bytes(page_size: int, head_dim: int) -> int:
+    return int(lib().oracle_rk_chunk_bytes(page_size, head_dim))
+
+
+def rk_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().oracle_rk_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def rk_new_pool(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int, fill: int = 0) -> np.ndarray:
+    return np.full(rk_pool_bytes(num_pages, page_size, num_kv_heads, head_dim), fill, dtype=np.uint8)
+
+
+def rk_append(pool: np.ndarray, num_pages, page_size, num_kv_heads, head_dim, block_table,
+              start_pos, cu_new, k, v) -> int:
+    bt = i32(block_table)
+    sp, cu = i32(start_pos), i32(cu_new)
+    kb, vb = _bits(k), _bits(v)
+    assert pool.dtype == np.uint8 and pool.size >= rk_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
+    B = sp.size
+    assert cu.size == B + 1 and kb.size == int(cu[-1]) * num_kv_heads * head_dim and vb.size == kb.size
+    max_pages = bt.shape[1] if bt.ndim == 2 else bt.size // max(B, 1)
+    return lib().oracle_rk_append(_ptr(pool), num_pages, page_size, num_kv_heads, head_dim, _ptr(bt),
+                                  max_pages, _ptr(sp), _ptr(cu), B, _ptr(kb), _ptr(vb))
+
+
+def rk_attention_row(pool, num_pages, page_size, num_kv_heads, head_dim, block_table, ctx_lens, q,
+                     T, num_q_heads, sm_scale, b, t, i, key_begin=0, key_end=0x7FFFFFFF):
+    bt, cl, qb = i32(block_table), i32(ctx_lens), _bits(q)
+    o = np.empty(head_dim, dtype=np.float64)
+    lse = np.empty(1, dtype=np.float64)
+    rc = lib().oracle_rk_attention_row(_ptr(pool), num_pages, page_size, num_kv_heads, head_dim, _ptr(bt),
+                                       bt.shape[1], _ptr(cl), cl.size, T, num_q_heads, _ptr(qb), float(sm_scale),
+                                       b, t, i, key_begin, key_end, _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_rk_attention_row: out-of-range data")
+    return o, float(lse[0])
+
+
+def rk_paged_attention(pool, num_pages, page_size, num_kv_heads, head_dim, block_table, ctx_lens, q,
+                       T, num_q_heads, sm_scale, want_lse=False):
+    """fp64 output [B][T][Hq][D] (and lse [B][T][Hq]) over an rk8v4 pool."""
+    bt, cl, qb = i32(block_table), i32(ctx_lens), _bits(q)
+    B = cl.size
+    out = np.empty((B, T, num_q_heads, head_dim), dtype=np.float64)
+    lse = np.empty((B, T, num_q_heads), dtype=np.float64)
+    rc = lib().oracle_rk_paged_attention(_ptr(pool), num_pages, page_size, num_kv_heads, head_dim, _ptr(bt),
+                                         bt.shape[1], _ptr(cl), B, T, num_q_heads, _ptr(qb), float(sm_scale),
+                                         _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_rk_paged_attention: {rc} rows with out-of-range data")
+    return (out, lse) if want_lse else out
+
+
+def rk_chunk_view(pool: np.ndarray, num_pages, page_size, num_kv_heads, head_dim):
+    """Split an rk8v4 pool into (Kc int8 [pages][heads][P][D], Ks fp16 bits [..][P][D/64],
+    Vc packed uint8 [..][P][D/2], Vs fp16 bits [..][P][D/32]) (layout from oracle.h)."""
+    P, D = page_size, head_dim
+    cb = rk_chunk_bytes(P, D)
+    c = pool[: num_pages * num_kv_heads * cb].reshape(num_pages, num_kv_heads, cb)
+    o1 = P * D
+    o2 = o1 + P * (D // 64) * 2
+    o3 = o2 + P * (D // 2)
+    kc = c[:, :, :o1].view(np.int8).reshape(num_pages, num_kv_heads, P, D)
+    ks = c[:, :, o1:o2].copy().view(np.uint16).reshape(num_pages, num_kv_heads, P, D // 64)
+    vc = c[:, :, o2:o3].reshape(num_pages, num_kv_heads, P, D // 2)
+    vs = c[:, :, o3:].copy().view(np.uint16).reshape(num_pages, num_kv_heads, P, D // 32)
     return kc, ks, vc, vs

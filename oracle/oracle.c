@@ -239,6 +239,261 @@ void oracle_combine(const float* part_o, const float* part_lse, int S, int R, in
   }
 }
 
+/* ===========================================================================
+ * rk8v4 ("NInfer-3090" README, "RotorQuant KV (rk8v4)"); readings in oracle.h.
+ * ======================================================================== */
+
+uint16_t oracle_double_to_f16(double x) {
+  /* fp16: 11 significant bits, normal exponents -14 .. 15, subnormal quantum 2^-24. */
+  ensure_round_to_nearest();
+  if (isnan(x)) return 0x7e00;
+  const uint16_t sign = signbit(x) ? 0x8000 : 0;
+  const double a = fabs(x);
+  if (a == 0.0) return sign;
+  int e;
+  frexp(a, &e); /* a = m * 2^e, 0.5 <= m < 1 */
+  double r;
+  if (e - 1 < -14) {
+    r = nearbyint(ldexp(a, 24)) * ldexp(1.0, -24);
+  } else {
+    r = ldexp(nearbyint(ldexp(a, 11 - e)), e - 11);
+  }
+  if (r > 65504.0) return sign | 0x7c00;
+  if (r < ldexp(1.0, -14)) return sign | (uint16_t)ldexp(r, 24); /* subnormal (or zero) */
+  int e2;
+  const double m2 = frexp(r, &e2); /* r = m2 * 2^e2 */
+  const uint16_t exp_field = (uint16_t)(e2 - 1 + 15);
+  const uint16_t mant = (uint16_t)ldexp(2.0 * m2 - 1.0, 10);
+  return sign | (uint16_t)(exp_field << 10) | mant;
+}
+
+double oracle_f16_to_double(uint16_t bits) {
+  const int e = (bits >> 10) & 0x1f, m = bits & 0x3ff;
+  double v;
+  if (e == 0) v = ldexp((double)m, -24);
+  else if (e == 31) v = m ? NAN : INFINITY;
+  else v = ldexp((double)(1024 + m), e - 25);
+  return (bits & 0x8000) ? -v : v;
+}
+
+void oracle_rk_rotate64(const uint16_t* x, float* y) {
+  float t[GROUP];
+  for (int i = 0; i < GROUP; ++i) t[i] = (float)oracle_bf16_to_double(x[i]);
+  /* butterflies over index bit 0, then 1, ..., 5; every add rounds to fp32 */
+  for (int h = 1; h < GROUP; h <<= 1)
+    for (int i = 0; i < GROUP; ++i)
+      if ((i & h) == 0) {
+        const float a = t[i], b = t[i + h];
+        t[i] = a + b;
+        t[i + h] = a - b;
+      }
+  for (int i = 0; i < GROUP; ++i) y[i] = t[i] * 0.125f;
+}
+
+/* fp16 scale bits for a group absmax a and code bound qmax: RN_fp16(a / qmax),
+ * 1 when that is 0, 65504 when it is past the fp16 range. */
+static uint16_t rk_scale_bits(double a, double qmax) {
+  uint16_t sb = oracle_double_to_f16(a / qmax);
+  if ((sb & 0x7fff) == 0) sb = 0x3c00;
+  else if ((sb & 0x7fff) == 0x7c00) sb = 0x7bff;
+  return sb;
+}
+
+uint16_t oracle_rk_quantize_k(const float* y, int8_t* q) {
+  ensure_round_to_nearest();
+  double a = 0.0;
+  for (int i = 0; i < GROUP; ++i) {
+    const double v = fabs((double)y[i]);
+    if (v > a) a = v;
+  }
+  const uint16_t sb = rk_scale_bits(a, 127.0);
+  const double s = oracle_f16_to_double(sb);
+  for (int i = 0; i < GROUP; ++i) {
+    const float r = (float)((double)y[i] / s); /* the fp32 quotient (53 >= 2*24 + 2) */
+    double k = nearbyint((double)r);
+    if (k > 127.0) k = 127.0;
+    if (k < -127.0) k = -127.0;
+    q[i] = (int8_t)k;
+  }
+  return sb;
+}
+
+#define VGROUP 32 /* value channels per scale */
+
+uint16_t oracle_rk_quantize_v(const uint16_t* x, uint8_t* packed) {
+  ensure_round_to_nearest();
+  double a = 0.0;
+  for (int i = 0; i < VGROUP; ++i) {
+    const double v = fabs(oracle_bf16_to_double(x[i]));
+    if (v > a) a = v;
+  }
+  const uint16_t sb = rk_scale_bits(a, 7.0);
+  const double s = oracle_f16_to_double(sb);
+  int q[VGROUP];
+  for (int i = 0; i < VGROUP; ++i) {
+    const float r = (float)(oracle_bf16_to_double(x[i]) / s);
+    double k = nearbyint((double)r);
+    if (k > 7.0) k = 7.0;
+    if (k < -7.0) k = -7.0;
+    q[i] = (int)k;
+  }
+  for (int j = 0; j < VGROUP / 2; ++j) packed[j] = (uint8_t)((q[2 * j] & 0xf) | ((q[2 * j + 1] & 0xf) << 4));
+  return sb;
+}
+
+size_t oracle_rk_chunk_bytes(int page_size, int head_dim) {
+  size_t P = (size_t)page_size, D = (size_t)head_dim;
+  return P * D + P * (D / GROUP) * 2 + P * (D / 2) + P * (D / VGROUP) * 2;
+}
+
+size_t oracle_rk_pool_bytes(int num_pages, int page_size, int num_kv_heads, int head_dim) {
+  return (size_t)num_pages * (size_t)num_kv_heads * oracle_rk_chunk_bytes(page_size, head_dim);
+}
+
+typedef struct {
+  int8_t* kc;   /* [P][D] */
+  uint16_t* ks; /* [P][D/64] fp16 bits */
+  uint8_t* vc;  /* [P][D/2] */
+  uint16_t* vs; /* [P][D/32] fp16 bits */
+} rk_chunk_ptrs;
+
+static rk_chunk_ptrs rk_chunk_at(const uint8_t* pool, int page, int head, int num_kv_heads, int P, int D) {
+  uint8_t* base = (uint8_t*)pool + ((size_t)page * num_kv_heads + head) * oracle_rk_chunk_bytes(P, D);
+  const size_t ks = (size_t)P * D, vc = ks + (size_t)P * (D / GROUP) * 2, vs = vc + (size_t)P * (D / 2);
+  rk_chunk_ptrs c;
+  c.kc = (int8_t*)base;
+  c.ks = (uint16_t*)(base + ks);
+  c.vc = base + vc;
+  c.vs = (uint16_t*)(base + vs);
+  return c;
+}
+
+int oracle_rk_append(uint8_t* pool, int num_pages, int page_size, int num_kv_heads, int head_dim,
+                     const int32_t* block_table, int max_pages, const int32_t* start_pos,
+                     const int32_t* cu_new, int B, const uint16_t* k, const uint16_t* v) {
+  const int P = page_size, D = head_dim, H = num_kv_heads;
+  const int total = cu_new[B];
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(+ : bad)
+  for (int j = 0; j < total; ++j) {
+    int b = 0;
+    while (b + 1 <= B && cu_new[b + 1] <= j) ++b;
+    long pos = (long)start_pos[b] + (j - cu_new[b]);
+    if (pos < 0 || pos >= (long)max_pages * P) { ++bad; continue; }
+    int page = block_table[(size_t)b * max_pages + pos / P];
+    if (page < 0 || page >= num_pages) { ++bad; continue; }
+    int slot = (int)(pos % P);
+    for (int h = 0; h < H; ++h) {
+      rk_chunk_ptrs c = rk_chunk_at(pool, page, h, H, P, D);
+      const uint16_t* krow = k + ((size_t)j * H + h) * D;
+      const uint16_t* vrow = v + ((size_t)j * H + h) * D;
+      for (int gr = 0; gr < D / GROUP; ++gr) {
+        float y[GROUP];
+        oracle_rk_rotate64(krow + gr * GROUP, y);
+        c.ks[(size_t)slot * (D / GROUP) + gr] = oracle_rk_quantize_k(y, c.kc + (size_t)slot * D + gr * GROUP);
+      }
+      for (int gr = 0; gr < D / VGROUP; ++gr)
+        c.vs[(size_t)slot * (D / VGROUP) + gr] =
+            oracle_rk_quantize_v(vrow + gr * VGROUP, c.vc + (size_t)slot * (D / 2) + gr * (VGROUP / 2));
+    }
+  }
+  return bad;
+}
+
+/* signed 4-bit code of channel ch from a packed value row */
+static int rk_nibble(const uint8_t* row, int ch) {
+  int n = (row[ch / 2] >> (4 * (ch & 1))) & 0xf;
+  return n >= 8 ? n - 16 : n;
+}
+
+int oracle_rk_attention_row(const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                            int head_dim, const int32_t* block_table, int max_pages,
+                            const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                            const uint16_t* q, double sm_scale, int b, int t, int i,
+                            int key_begin, int key_end, double* o, double* lse) {
+  const int P = page_size, D = head_dim, Hq = num_q_heads, H = num_kv_heads;
+  for (int c = 0; c < D; ++c) o[c] = 0.0;
+  *lse = -INFINITY;
+  if (b < 0 || b >= B || t < 0 || t >= T || i < 0 || i >= Hq || Hq % H != 0) return 1;
+  const int G = Hq / H;
+  const int h = i / G;
+  const long L = ctx_lens[b];
+  if (L < T || L > (long)max_pages * P) return 1;
+  const long last = L - T + t;
+  long n0 = key_begin < 0 ? 0 : key_begin;
+  long n1 = (long)key_end < last + 1 ? (long)key_end : last + 1;
+  if (n1 <= n0) return 0;
+
+  /* the query row in the rotated basis: (R q)_r = sum_j (-1)^popcount(r & j) q_j / 8 per group */
+  const uint16_t* qrow = q + (((size_t)b * T + t) * Hq + i) * D;
+  double* qr = (double*)malloc(sizeof(double) * (size_t)D);
+  double* z = (double*)malloc(sizeof(double) * (size_t)(n1 - n0));
+  if (!qr || !z) { free(qr); free(z); return 1; }
+  for (int g0 = 0; g0 < D; g0 += GROUP)
+    for (int r = 0; r < GROUP; ++r) {
+      double acc = 0.0;
+      for (int jj = 0; jj < GROUP; ++jj) {
+        const double x = oracle_bf16_to_double(qrow[g0 + jj]);
+        acc += (__builtin_popcount((unsigned)(r & jj)) & 1) ? -x : x;
+      }
+      qr[g0 + r] = acc / 8.0;
+    }
+  int err = 0;
+  for (long n = n0; n < n1; ++n) {
+    int page = block_table[(size_t)b * max_pages + n / P];
+    if (page < 0 || page >= num_pages) { err = 1; break; }
+    int slot = (int)(n % P);
+    rk_chunk_ptrs c = rk_chunk_at(pool, page, h, H, P, D);
+    double dot = 0.0;
+    for (int ch = 0; ch < D; ++ch) {
+      const double khat = (double)c.kc[(size_t)slot * D + ch] *
+                          oracle_f16_to_double(c.ks[(size_t)slot * (D / GROUP) + ch / GROUP]);
+      dot += qr[ch] * khat;
+    }
+    z[n - n0] = sm_scale * dot;
+  }
+  if (err) { free(qr); free(z); return 1; }
+  double m = -INFINITY;
+  for (long n = n0; n < n1; ++n) if (z[n - n0] > m) m = z[n - n0];
+  double l = 0.0;
+  for (long n = n0; n < n1; ++n) {
+    double w = exp(z[n - n0] - m);
+    int page = block_table[(size_t)b * max_pages + n / P];
+    int slot = (int)(n % P);
+    rk_chunk_ptrs c = rk_chunk_at(pool, page, h, H, P, D);
+    const uint8_t* vrow = c.vc + (size_t)slot * (D / 2);
+    for (int ch = 0; ch < D; ++ch)
+      o[ch] += w * ((double)rk_nibble(vrow, ch) * oracle_f16_to_double(c.vs[(size_t)slot * (D / VGROUP) + ch / VGROUP]));
+    l += w;
+  }
+  for (int ch = 0; ch < D; ++ch) o[ch] /= l;
+  *lse = m + log(l);
+  free(qr);
+  free(z);
+  return 0;
+}
+
+int oracle_rk_paged_attention(const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                              int head_dim, const int32_t* block_table, int max_pages,
+                              const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                              const uint16_t* q, double sm_scale, double* out, double* lse) {
+  const long rows = (long)B * T * num_q_heads;
+  const int D = head_dim;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+  for (long r = 0; r < rows; ++r) {
+    int i = (int)(r % num_q_heads);
+    int t = (int)((r / num_q_heads) % T);
+    int b = (int)(r / ((long)num_q_heads * T));
+    double row_lse;
+    bad += oracle_rk_attention_row(pool, num_pages, page_size, num_kv_heads, head_dim, block_table,
+                                   max_pages, ctx_lens, B, T, num_q_heads, q, sm_scale, b, t, i, 0,
+                                   0x7fffffff, out + (size_t)r * D, &row_lse);
+    if (lse) lse[r] = row_lse;
+  }
+  return bad;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

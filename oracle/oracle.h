@@ -29,6 +29,9 @@
  * Tensors given to the oracle are host arrays; bf16 values are passed as their
  * raw uint16 bit patterns.
  *
+ * The rk8v4 format (second section below) follows the same plan with its own
+ * layout and readings.
+ *
  * Parity status: every function here is pinned by tests in tests/test_oracle_*.py
  * against library routines, closed forms, invariants and hand-derived golden
  * cases (see the test files for which pin covers which function).
@@ -87,6 +90,62 @@ int oracle_paged_attention(const uint8_t* pool, int num_pages, int page_size, in
 /* Log-sum-exp merge of S partial results: part_o[S][R][D] (normalized, fp32),
  * part_lse[S][R] (fp32, -inf for an empty split). out[R][D] fp64. */
 void oracle_combine(const float* part_o, const float* part_lse, int S, int R, int D, double* out);
+
+/* ---------------------------------------------------------------------------
+ * rk8v4 ("NInfer-3090" README, "RotorQuant KV (rk8v4)"): keys rotated by the
+ * 64-point Hadamard transform and stored as INT8 group-64 codes; values not
+ * rotated, stored as signed 4-bit codes (15 levels), two per byte, one scale
+ * per 32 channels; every scale fp16 (the section's 26,112 bytes per token on
+ * the 27B model: 16 attention layers x 4 kv-heads x 408 bytes). Readings taken
+ * where the section is silent:
+ *   rotation R = H64 / 8 per 64-channel group (Sylvester order,
+ *     H[i][j] = (-1)^popcount(i & j); orthonormal and its own inverse), so
+ *     q . k = (R q) . (R k);
+ *   at append R k is evaluated in fp32 as butterflies (a + b, a - b) over
+ *     index bits 0, 1, ..., 5 in that order, rounding after every add, then
+ *     times 1/8 -- the precision in which the kernel takes the code decision;
+ *   key scale  s = RN_fp16(absmax(R k) / 127), value scale s = RN_fp16(absmax(v) / 7);
+ *     s = 1 when it rounds to 0 (absmax = 0 or below the fp16 range), and
+ *     s = 65504 when it rounds past the fp16 maximum;
+ *   codes q = clamp(round_half_even(fp32(x / s)), -127, 127) for keys and
+ *     [-7, 7] for values; byte j of a value group holds element 2j in its low
+ *     nibble and 2j + 1 in its high nibble (two's complement);
+ *   attention rotates each query row by R (fp64 here) and scores it against
+ *     the dequantized rotated keys; values are dequantized as q * s.
+ * Pool layout (one contiguous chunk per (page, kv-head)):
+ *   Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D/2] uint8 | Vs[P][D/32] fp16
+ * ------------------------------------------------------------------------- */
+
+/* Round a double to the nearest fp16, ties to even (overflow -> inf); the bits. */
+uint16_t oracle_double_to_f16(double x);
+/* Exact widening of an fp16 bit pattern. */
+double oracle_f16_to_double(uint16_t bits);
+/* R x of one 64-channel group of bf16 values, in the fp32 order above. */
+void oracle_rk_rotate64(const uint16_t* x, float* y);
+/* Key group: 64 rotated fp32 values -> 64 codes; returns the fp16 scale bits. */
+uint16_t oracle_rk_quantize_k(const float* y, int8_t* q);
+/* Value group: 32 bf16 values -> 16 packed bytes; returns the fp16 scale bits. */
+uint16_t oracle_rk_quantize_v(const uint16_t* x, uint8_t* packed);
+
+size_t oracle_rk_chunk_bytes(int page_size, int head_dim);
+size_t oracle_rk_pool_bytes(int num_pages, int page_size, int num_kv_heads, int head_dim);
+
+/* kv_cache_append into an rk8v4 pool; arguments and result as oracle_kv_append. */
+int oracle_rk_append(uint8_t* pool, int num_pages, int page_size, int num_kv_heads, int head_dim,
+                     const int32_t* block_table, int max_pages, const int32_t* start_pos,
+                     const int32_t* cu_new, int B, const uint16_t* k, const uint16_t* v);
+
+/* Attention over an rk8v4 pool; arguments and results as oracle_attention_row
+ * and oracle_paged_attention. */
+int oracle_rk_attention_row(const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                            int head_dim, const int32_t* block_table, int max_pages,
+                            const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                            const uint16_t* q, double sm_scale, int b, int t, int i,
+                            int key_begin, int key_end, double* o, double* lse);
+int oracle_rk_paged_attention(const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                              int head_dim, const int32_t* block_table, int max_pages,
+                              const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                              const uint16_t* q, double sm_scale, double* out, double* lse);
 
 /* Threads the oracle's parallel loops use. */
 int oracle_num_threads(void);

@@ -3,8 +3,8 @@
 Each mutant below is oracle.c with one plausible mistake planted in it: a
 dropped term, a wrong sign, rounding rule or bound, a wrong or transposed
 index (page, slot, group, head, query row), a swapped operand. Every mutant is
-compiled into a library of its own, and the oracle pins (the quantizer and
-attention test files) run against it in a child process; each mutant must be
+compiled into a library of its own, and the oracle pins (the quantizer,
+attention and rk8v4 test files) run against it in a child process; each mutant must be
 caught, i.e. make at least one pin fail, while the unaltered source, built the
 same way, passes all of them. The mistakes are planted in copies in a
 temporary directory: oracle.c itself is never changed.
@@ -13,6 +13,8 @@ Mistakes that cannot change any result are not listed, with the reason:
   * the clamp to [-127, 127]: fp32(x / s) with |x| <= absmax and
     s = fp32(absmax / 127) is at most 127 (1 + 2^-24) < 127.5, so the clamp
     never acts and no input can tell a different clamp apart;
+  * the rk8v4 value clamp to [-7, 7], for the same reason (fp32(x / s) with
+    s = RN_fp16(absmax / 7) is at most 7 (1 + 2^-11) < 7.5);
   * subtracting a different finite reference than the maximum in the softmax
     or in the combine (the weights' ratios do not depend on it);
   * skipping the empty partials in the combine (exp(-inf) = 0 already).
@@ -27,75 +29,118 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = ["tests/test_oracle_quantize.py", "tests/test_oracle_attention.py"]
+PINS = ["tests/test_oracle_quantize.py", "tests/test_oracle_attention.py", "tests/test_oracle_rk8v4.py"]
 
-# (name, [(text in oracle.c, replacement), ...]); each text occurs exactly once.
+# (name, section, [(text in oracle.c, replacement), ...]); each text occurs
+# exactly once in its section of oracle.c: "int8" (the INT8 group-64 format,
+# the combine and the shared helpers) or "rk8v4" (the part from its banner on).
 MUTANTS = [
     # quantizer
-    ("scale divides by 128", [("(float)(a / 127.0)", "(float)(a / 128.0)")]),
-    ("zero group gets scale 1/2", [("(a == 0.0) ? 1.0f", "(a == 0.0) ? 0.5f")]),
-    ("absmax without the absolute value",
+    ("scale divides by 128", "int8", [("(float)(a / 127.0)", "(float)(a / 128.0)")]),
+    ("zero group gets scale 1/2", "int8", [("(a == 0.0) ? 1.0f", "(a == 0.0) ? 0.5f")]),
+    ("absmax without the absolute value", "int8",
      [("double v = fabs(oracle_bf16_to_double(x[i]));", "double v = oracle_bf16_to_double(x[i]);")]),
-    ("quotient not rounded to fp32",
+    ("quotient not rounded to fp32", "int8",
      [("float r = (float)(oracle_bf16_to_double(x[i]) / (double)s);",
        "double r = oracle_bf16_to_double(x[i]) / (double)s;")]),
-    ("ties away from zero", [("double k = nearbyint((double)r);", "double k = round((double)r);")]),
-    ("truncation instead of rounding", [("double k = nearbyint((double)r);", "double k = trunc((double)r);")]),
+    ("ties away from zero", "int8", [("double k = nearbyint((double)r);", "double k = round((double)r);")]),
+    ("truncation instead of rounding", "int8", [("double k = nearbyint((double)r);", "double k = trunc((double)r);")]),
     # bf16 helpers
-    ("bf16 with 9 significant bits",
+    ("bf16 with 9 significant bits", "int8",
      [("r = ldexp(nearbyint(ldexp(m, 8)), e - 8);", "r = ldexp(nearbyint(ldexp(m, 9)), e - 9);")]),
-    ("bf16 rounding truncates",
+    ("bf16 rounding truncates", "int8",
      [("r = ldexp(nearbyint(ldexp(m, 8)), e - 8);", "r = ldexp(trunc(ldexp(m, 8)), e - 8);")]),
-    ("bf16 subnormal quantum 2^-132",
+    ("bf16 subnormal quantum 2^-132", "int8",
      [("r = nearbyint(ldexp(x, 133)) * ldexp(1.0, -133);", "r = nearbyint(ldexp(x, 132)) * ldexp(1.0, -132);")]),
-    ("bf16 widening drops the sign",
+    ("bf16 widening drops the sign", "int8",
      [("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)(bits & 0x7fffu) << 16;")]),
     # pool layout
-    ("K and V scale arrays swapped",
+    ("K and V scale arrays swapped", "int8",
      [("c.ks = (float*)(base + (size_t)P * D);",
        "c.ks = (float*)(base + 2 * (size_t)P * D + (size_t)P * g * sizeof(float));"),
       ("c.vs = (float*)(base + 2 * (size_t)P * D + (size_t)P * g * sizeof(float));",
        "c.vs = (float*)(base + (size_t)P * D);")]),
-    ("chunk index misses the head stride",
+    ("chunk index misses the head stride", "int8",
      [("((size_t)page * num_kv_heads + head)", "((size_t)page + head)")]),
     # append
-    ("append slot off by one", [("int slot = (int)(pos % P);", "int slot = (int)((pos + 1) % P);")]),
-    ("append ignores the block table",
+    ("append slot off by one", "int8", [("int slot = (int)(pos % P);", "int slot = (int)((pos + 1) % P);")]),
+    ("append ignores the block table", "int8",
      [("int page = block_table[(size_t)b * max_pages + pos / P];", "int page = (int)(pos / P);")]),
-    ("append assigns boundary rows to the wrong sequence",
+    ("append assigns boundary rows to the wrong sequence", "int8",
      [("while (b + 1 <= B && cu_new[b + 1] <= j) ++b;", "while (b + 1 < B && cu_new[b + 1] < j) ++b;")]),
-    ("append reads K rows head-major",
+    ("append reads K rows head-major", "int8",
      [("const uint16_t* krow = k + ((size_t)j * H + h) * D;",
        "const uint16_t* krow = k + ((size_t)h * total + j) * D;")]),
-    ("append quantizes V from K",
+    ("append quantizes V from K", "int8",
      [("oracle_quantize_group(vrow + gr * GROUP", "oracle_quantize_group(krow + gr * GROUP")]),
     # attention
-    ("q-head i reads kv-head i mod Hkv", [("const int h = i / G;", "const int h = i % H;")]),
-    ("no causal mask among the T columns", [("const long last = L - T + t;", "const long last = L - 1;")]),
-    ("causal limit one key short", [("const long last = L - T + t;", "const long last = L - T + t - 1;")]),
-    ("query rows read head-major",
+    ("q-head i reads kv-head i mod Hkv", "int8", [("const int h = i / G;", "const int h = i % H;")]),
+    ("no causal mask among the T columns", "int8", [("const long last = L - T + t;", "const long last = L - 1;")]),
+    ("causal limit one key short", "int8", [("const long last = L - T + t;", "const long last = L - T + t - 1;")]),
+    ("query rows read head-major", "int8",
      [("const uint16_t* qrow = q + (((size_t)b * T + t) * Hq + i) * D;",
        "const uint16_t* qrow = q + (((size_t)b * Hq + i) * T + t) * D;")]),
-    ("softmax scale dropped", [("z[n - n0] = sm_scale * dot;", "z[n - n0] = dot;")]),
-    ("K pages read without the block table",
+    ("softmax scale dropped", "int8", [("z[n - n0] = sm_scale * dot;", "z[n - n0] = dot;")]),
+    ("K pages read without the block table", "int8",
      [("int page = block_table[(size_t)b * max_pages + n / P];\n    if (page < 0",
        "int page = (int)(n / P);\n    if (page < 0")]),
-    ("K group scale indexed by channel mod groups",
+    ("K group scale indexed by channel mod groups", "int8",
      [("(double)c.ks[(size_t)slot * g + ch / GROUP];", "(double)c.ks[(size_t)slot * g + ch % g];")]),
-    ("V dequantized with the K scales",
+    ("V dequantized with the K scales", "int8",
      [("(double)c.vs[(size_t)slot * g + ch / GROUP]", "(double)c.ks[(size_t)slot * g + ch / GROUP]")]),
-    ("V channels of a pair transposed",
+    ("V channels of a pair transposed", "int8",
      [("((double)c.vc[(size_t)slot * D + ch]", "((double)c.vc[(size_t)slot * D + (ch ^ 1)]")]),
-    ("softmax weights without the max shift but LSE with it",
+    ("softmax weights without the max shift but LSE with it", "int8",
      [("double w = exp(z[n - n0] - m);", "double w = exp(z[n - n0]);")]),
-    ("softmax sum counts keys", [("l += w;", "l += 1.0;")]),
-    ("output not normalized", [("for (int ch = 0; ch < D; ++ch) o[ch] /= l;", "")]),
-    ("LSE without the max", [("*lse = m + log(l);", "*lse = log(l);")]),
+    ("softmax sum counts keys", "int8", [("l += w;", "l += 1.0;")]),
+    ("output not normalized", "int8", [("for (int ch = 0; ch < D; ++ch) o[ch] /= l;", "")]),
+    ("LSE without the max", "int8", [("*lse = m + log(l);", "*lse = log(l);")]),
     # combine
-    ("combine weight with the wrong sign", [("double w = exp(ls - m);", "double w = exp(m - ls);")]),
-    ("combine not normalized", [("for (int c = 0; c < D; ++c) o[c] /= wsum;", "")]),
-    ("combine partials read row-major",
+    ("combine weight with the wrong sign", "int8", [("double w = exp(ls - m);", "double w = exp(m - ls);")]),
+    ("combine not normalized", "int8", [("for (int c = 0; c < D; ++c) o[c] /= wsum;", "")]),
+    ("combine partials read row-major", "int8",
      [("part_o[((size_t)s * R + r) * D + c]", "part_o[((size_t)r * S + s) * D + c]")]),
+    # rk8v4: fp16 helpers, rotation, quantizers, layout, attention
+    ("fp16 with 10 significant bits", "rk8v4",
+     [("r = ldexp(nearbyint(ldexp(a, 11 - e)), e - 11);", "r = ldexp(nearbyint(ldexp(a, 10 - e)), e - 10);")]),
+    ("fp16 subnormal quantum 2^-23", "rk8v4",
+     [("r = nearbyint(ldexp(a, 24)) * ldexp(1.0, -24);", "r = nearbyint(ldexp(a, 23)) * ldexp(1.0, -23);")]),
+    ("rotation without the 1/8", "rk8v4", [("y[i] = t[i] * 0.125f;", "y[i] = t[i];")]),
+    ("rotation butterfly with the difference reversed", "rk8v4", [("t[i + h] = a - b;", "t[i + h] = b - a;")]),
+    ("keys stored unrotated", "rk8v4",
+     [("oracle_rk_rotate64(krow + gr * GROUP, y);",
+       "for (int ii = 0; ii < GROUP; ++ii) y[ii] = (float)oracle_bf16_to_double(krow[gr * GROUP + ii]);")]),
+    ("key scale divides by 128", "rk8v4", [("rk_scale_bits(a, 127.0)", "rk_scale_bits(a, 128.0)")]),
+    ("value scale divides by 8", "rk8v4", [("rk_scale_bits(a, 7.0)", "rk_scale_bits(a, 8.0)")]),
+    ("scale below the fp16 range kept tiny", "rk8v4", [("if ((sb & 0x7fff) == 0) sb = 0x3c00;", "if ((sb & 0x7fff) == 0) sb = 0x0001;")]),
+    ("scale past the fp16 range left infinite", "rk8v4", [("else if ((sb & 0x7fff) == 0x7c00) sb = 0x7bff;", "")]),
+    ("value nibbles in the other order", "rk8v4",
+     [("packed[j] = (uint8_t)((q[2 * j] & 0xf) | ((q[2 * j + 1] & 0xf) << 4));",
+       "packed[j] = (uint8_t)((q[2 * j + 1] & 0xf) | ((q[2 * j] & 0xf) << 4));")]),
+    ("value groups written 32 bytes apart", "rk8v4",
+     [("c.vc + (size_t)slot * (D / 2) + gr * (VGROUP / 2))", "c.vc + (size_t)slot * (D / 2) + gr * VGROUP)")]),
+    ("value nibbles read without sign extension", "rk8v4", [("return n >= 8 ? n - 16 : n;", "return n;")]),
+    ("query not rotated", "rk8v4", [("qr[g0 + r] = acc / 8.0;", "qr[g0 + r] = oracle_bf16_to_double(qrow[g0 + r]);")]),
+    ("query rotation sign from r | j", "rk8v4",
+     [("(__builtin_popcount((unsigned)(r & jj)) & 1) ? -x : x", "(__builtin_popcount((unsigned)(r | jj)) & 1) ? -x : x")]),
+    ("key scale indexed per 32 channels", "rk8v4",
+     [("oracle_f16_to_double(c.ks[(size_t)slot * (D / GROUP) + ch / GROUP])",
+       "oracle_f16_to_double(c.ks[(size_t)slot * (D / GROUP) + ch / VGROUP])")]),
+    ("value scale indexed per 64 channels", "rk8v4",
+     [("c.vs[(size_t)slot * (D / VGROUP) + ch / VGROUP]", "c.vs[(size_t)slot * (D / VGROUP) + ch / GROUP]")]),
+    # rk8v4: the same attention and append logic as the INT8 section, planted there too
+    ("rk8v4: q-head i reads kv-head i mod Hkv", "rk8v4", [("const int h = i / G;", "const int h = i % H;")]),
+    ("rk8v4: causal limit one key short", "rk8v4",
+     [("const long last = L - T + t;", "const long last = L - T + t - 1;")]),
+    ("rk8v4: append slot off by one", "rk8v4", [("int slot = (int)(pos % P);", "int slot = (int)((pos + 1) % P);")]),
+    ("rk8v4: append ignores the block table", "rk8v4",
+     [("int page = block_table[(size_t)b * max_pages + pos / P];", "int page = (int)(pos / P);")]),
+    ("rk8v4: K pages read without the block table", "rk8v4",
+     [("int page = block_table[(size_t)b * max_pages + n / P];\n    if (page < 0",
+       "int page = (int)(n / P);\n    if (page < 0")]),
+    ("rk8v4: softmax scale dropped", "rk8v4", [("z[n - n0] = sm_scale * dot;", "z[n - n0] = dot;")]),
+    ("rk8v4: output not normalized", "rk8v4", [("for (int ch = 0; ch < D; ++ch) o[ch] /= l;", "")]),
+    ("rk8v4: LSE without the max", "rk8v4", [("*lse = m + log(l);", "*lse = log(l);")]),
 ]
 
 RUNNER = (
@@ -110,11 +155,17 @@ def _source() -> str:
         return f.read()
 
 
-def _mutate(src: str, edits) -> str:
+RK_BANNER = "/* ===========================================================================\n * rk8v4"
+
+
+def _mutate(src: str, section: str, edits) -> str:
+    cut = src.index(RK_BANNER)
+    head, tail = src[:cut], src[cut:]
+    part = head if section == "int8" else tail
     for old, new in edits:
-        assert src.count(old) == 1, f"mutation anchor not unique or missing: {old!r}"
-        src = src.replace(old, new)
-    return src
+        assert part.count(old) == 1, f"mutation anchor not unique or missing in {section}: {old!r}"
+        part = part.replace(old, new)
+    return part + tail if section == "int8" else head + part
 
 
 def _build_and_run(src: str, workdir: str, tag: str):
@@ -134,13 +185,13 @@ def _build_and_run(src: str, workdir: str, tag: str):
 
 def test_every_mutant_fails_a_pin(tmp_path):
     src = _source()
-    jobs = [("unaltered", src)] + [(f"m{i:02d}", _mutate(src, edits)) for i, (_, edits) in enumerate(MUTANTS)]
+    jobs = [("unaltered", src)] + [(f"m{i:02d}", _mutate(src, sec, edits)) for i, (_, sec, edits) in enumerate(MUTANTS)]
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         results = list(ex.map(lambda j: _build_and_run(j[1], str(tmp_path), j[0]), jobs))
     rc0, failed0, log0 = results[0]
     assert rc0 == 0, f"the unaltered oracle must pass every pin:\n{log0}"
     survivors, crashed = [], []
-    for (name, _), (rc, failed, log) in zip(MUTANTS, results[1:]):
+    for (name, _, _), (rc, failed, log) in zip(MUTANTS, results[1:]):
         if rc == 0:
             survivors.append(name)
         elif rc != 1 or not failed:
@@ -149,7 +200,7 @@ def test_every_mutant_fails_a_pin(tmp_path):
     assert not survivors, f"mutants no pin catches: {survivors}"
 
 
-@pytest.mark.parametrize("name,edits", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_mutation_anchors_exist(name, edits):
+@pytest.mark.parametrize("name,section,edits", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutation_anchors_exist(name, section, edits):
     """Each planted mistake still applies to the current oracle.c."""
-    _mutate(_source(), edits)
+    _mutate(_source(), section, edits)
