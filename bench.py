@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c1_decode",
-                    help="tiny | c1_decode | c8_verify | long_context | mix | c8_decode")
+                    help="tiny | c1_decode | c8_verify | long_context | mix | c8_decode | c1_rk8v4")
     ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -155,17 +155,19 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
     bt = wl.block_table(w).to(device)
     ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    base = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, device=device, fill=0)
+    append = nk.rk8v4_append if w.fmt == "rk8v4" else nk.kv_append
+    base = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, device=device, fill=0, fmt=w.fmt)
     hist, _ = wl.history_and_step(w)
     for b in range(w.B):
         pos = 0
         while pos < hist[b]:
             n = min(16384, hist[b] - pos)
             k, v = wl.kv_rows(w, b, pos, n, device=device)
-            nk.kv_append(base, bt[b:b + 1].contiguous(), torch.tensor([pos], dtype=torch.int32, device=device),
-                         torch.tensor([0, n], dtype=torch.int32, device=device), k, v, status=status)
+            append(base, bt[b:b + 1].contiguous(), torch.tensor([pos], dtype=torch.int32, device=device),
+                   torch.tensor([0, n], dtype=torch.int32, device=device), k, v, status=status)
             pos += n
-    pools = [base] + [nk.KVPool(base.storage.clone(), w.num_pages, w.P, w.Hkv, w.D) for _ in range(replicas - 1)]
+    pools = [base] + [nk.KVPool(base.storage.clone(), w.num_pages, w.P, w.Hkv, w.D, w.fmt)
+                      for _ in range(replicas - 1)]
     starts, _ = wl.history_and_step(w)
     k, v, sp, cu = wl.append_batch(w, starts, [w.append_len] * w.B, device=device)
     q = wl.queries(w, device=device)
@@ -177,7 +179,7 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
     if int(status.item()) != 0:
         raise RuntimeError(f"history append flagged device status {int(status.item())}")
     return dict(bt=bt, ctx=ctx, status=status, pools=pools, k=k, v=v, sp=sp.to(device), cu=cu.to(device), q=q,
-                ws=ws, out=out, nct=nct, kernel=kernel)
+                ws=ws, out=out, nct=nct, kernel=kernel, append=append)
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -196,25 +198,41 @@ def job_gbs(step_bytes: int, ms: float, world: int) -> float:
     return step_bytes * world / (ms * 1e-3) / 1e9
 
 
+def attention_call(args, w):
+    """The attention entry point the run times: the tensor-core or CUDA-core
+    kernel of an INT8 pool, or the rk8v4 kernel of an rk8v4 pool."""
+    import quantized_paged_kv_cache_gb300 as nk
+
+    if w.fmt == "rk8v4":
+        return nk.rk8v4_decode_attn
+    return nk.paged_decode_attn if args.kernel == "mma" else nk.paged_decode_attn_simt
+
+
+def one_call_step(args, w) -> bool:
+    """Whether a step runs as one nk_decode_step call (INT8 pool, tensor-core kernels)."""
+    return w.fmt == "int8" and args.kernel == "mma"
+
+
 def run_ours(args, w, rank, world, device):
     import torch
 
     import quantized_paged_kv_cache_gb300 as nk
 
-    pool_bytes = nk.kv_pool_bytes(w.num_pages, w.P, w.Hkv, w.D)
+    sizer = nk.rk8v4_pool_bytes if w.fmt == "rk8v4" else nk.kv_pool_bytes
+    pool_bytes = sizer(w.num_pages, w.P, w.Hkv, w.D)
     replicas = 1 if pool_bytes >= 2 * L2_BYTES else int(-(-2 * L2_BYTES // pool_bytes)) + 1
     S = setup_gpu(w, device, replicas, args.num_ctas, args.kernel)
-    dec = nk.paged_decode_attn if args.kernel == "mma" else nk.paged_decode_attn_simt
+    dec = attention_call(args, w)
     stream = torch.cuda.current_stream()
 
     def step(i, what="step"):
         pool = S["pools"][i % replicas]
-        if what == "step" and args.kernel == "mma":  # append + attention in one call
+        if what == "step" and one_call_step(args, w):  # append + attention in one call
             nk.decode_step(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], S["q"], S["ctx"], w.sm_scale, w.max_ctx,
                            num_ctas=S["nct"], workspace=S["ws"], out=S["out"], status=S["status"], stream=stream)
             return
         if what != "attn":
-            nk.kv_append(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
+            S["append"](pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
         if what != "append":
             dec(pool, S["q"], S["bt"], S["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
                 out=S["out"], status=S["status"], stream=stream)
@@ -311,12 +329,12 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
     def step(i):
         d_buf.copy_(h_buf, non_blocking=True)
         pool = S["pools"][i % replicas]
-        if args.kernel == "mma":
+        if one_call_step(args, w):
             nk.decode_step(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], dev["q"], dev["ctx"], w.sm_scale,
                            w.max_ctx, num_ctas=S["nct"], workspace=S["ws"], out=S["out"], status=S["status"],
                            stream=stream)
         else:
-            nk.kv_append(pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], status=S["status"], stream=stream)
+            S["append"](pool, S["bt"], dev["sp"], dev["cu"], dev["k"], dev["v"], status=S["status"], stream=stream)
             dec(pool, dev["q"], S["bt"], dev["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
                 out=S["out"], status=S["status"], stream=stream)
         out_h.copy_(S["out"], non_blocking=True)
@@ -353,15 +371,19 @@ class OracleStep:
         from quantized_paged_kv_cache_gb300 import workloads as wl
 
         self.w, self.oracle, self.np = w, oracle, np
+        rk = w.fmt == "rk8v4"
+        self.append = oracle.rk_append if rk else oracle.kv_append
+        self.attention = oracle.rk_paged_attention if rk else oracle.paged_attention
+        self.attention_row = oracle.rk_attention_row if rk else oracle.attention_row
         self.bt = wl.block_table(w)
-        self.pool = oracle.new_pool(w.num_pages, w.P, w.Hkv, w.D)
+        self.pool = (oracle.rk_new_pool if rk else oracle.new_pool)(w.num_pages, w.P, w.Hkv, w.D)
         hist, _ = wl.history_and_step(w)
         for b in range(w.B):
             pos = 0
             while pos < hist[b]:
                 n = min(16384, hist[b] - pos)
                 k, v = wl.kv_rows(w, b, pos, n, device="cpu")
-                oracle.kv_append(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt[b:b + 1], [pos], [0, n], k, v)
+                self.append(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt[b:b + 1], [pos], [0, n], k, v)
                 pos += n
         starts, _ = wl.history_and_step(w)
         self.k, self.v, self.sp, self.cu = wl.append_batch(w, starts, [w.append_len] * w.B, device="cpu")
@@ -376,15 +398,15 @@ class OracleStep:
         del torch
 
     def __call__(self):
-        w, oracle = self.w, self.oracle
-        oracle.kv_append(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, self.sp, self.cu, self.k, self.v)
+        w = self.w
+        self.append(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, self.sp, self.cu, self.k, self.v)
         if self.frac_rows == 1.0:
-            oracle.paged_attention(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T, w.Hq,
-                                   w.sm_scale)
+            self.attention(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T, w.Hq,
+                           w.sm_scale)
         else:
             for (b, t, i) in self.rows:
-                oracle.attention_row(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T,
-                                     w.Hq, w.sm_scale, b, t, i)
+                self.attention_row(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T,
+                                   w.Hq, w.sm_scale, b, t, i)
 
     def sample_text(self):
         return (f"{len(self.rows)} of {self.w.B * self.w.T * self.w.Hq} query rows over their full contexts "
@@ -436,8 +458,8 @@ def run_reference(args, w):
 
 
 def config_dict(w, l2):
-    return {"workload": w.name, "B": w.B, "T": w.T, "q_heads": w.Hq, "kv_heads": w.Hkv, "head_dim": w.D,
-            "page_size": w.P, "ctx_lens": w.ctx_lens if w.B <= 8 else f"{w.B} seqs", "append_rows": w.append_rows(),
+    return {"workload": w.name, "kv_format": w.fmt, "B": w.B, "T": w.T, "q_heads": w.Hq, "kv_heads": w.Hkv,
+            "head_dim": w.D, "page_size": w.P, "ctx_lens": w.ctx_lens if w.B <= 8 else f"{w.B} seqs", "append_rows": w.append_rows(),
             "l2": l2}
 
 
@@ -482,21 +504,27 @@ def main():
     out = {
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms"], 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "i8 KV, f16 MMA operands, f32 accumulate", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": ("i8 K / i4 V KV (fp16 scales), f32 CUDA-core arithmetic" if w.fmt == "rk8v4"
+                  else "i8 KV, f16 MMA operands, f32 accumulate"),
+        "data": "synthetic",
         "config": config_dict(w, l2),
         "us_per_call": round(us, 3), "attn_us_per_call": round(attn_us, 3),
         "append_us_per_call": round(append_us, 3),
-        "breakdown": "value/ms_per_step: K back-to-back steps (nk_decode_step: append + attention); attn/append us "
-                     "and the roofline: K back-to-back calls of nk_paged_decode_attn / nk_kv_append alone, same "
-                     "inputs and pool rotation",
+        "breakdown": (("value/ms_per_step: K back-to-back steps (nk_decode_step: append + attention); attn/append "
+                       "us and the roofline: K back-to-back calls of nk_paged_decode_attn / nk_kv_append alone, same "
+                       "inputs and pool rotation") if one_call_step(args, w) else
+                      ("value/ms_per_step: K back-to-back steps (append call + attention call); attn/append us and "
+                       "the roofline: K back-to-back calls of each alone, same inputs and pool rotation")),
         "append_gbs": round(w.append_bytes() / (append_us * 1e-6) / 1e9, 2),
         "attn_gbs": round(achieved, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
-        "kernel": args.kernel, "num_ctas": r["nct"] or "default",
+        "kernel": "rk8v4" if w.fmt == "rk8v4" else args.kernel, "num_ctas": r["nct"] or "default",
         "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_decode split kernel + combine (one nk_paged_decode_attn call)",
+                     "kernel": ("rk8v4 split kernel + combine (one nk_rk8v4_decode_attn call)" if w.fmt == "rk8v4"
+                                else "paged_decode split kernel + combine (one nk_paged_decode_attn call)"),
                      "peak_source": f"{src} hbm_gbs", "bytes_per_launch": w.attn_bytes()},
     }
     if not args.no_cpu_baseline and world == 1 and not args.profile:

@@ -86,7 +86,9 @@ typedef enum {
 #define NK_DEVFLAG_BAD_CTX 0x4u     /* ctx_len < T, > max_ctx or > table capacity */
 #define NK_DEVFLAG_TIMEOUT 0x8u     /* a bounded wait on an async copy gave up */
 #define NK_DEVFLAG_RANGE 0x10u      /* a Q value or an output left the fp16 range of the
-                                       tensor-core path (|Q| > 65504, or p * Vs > 65504) */
+                                       tensor-core path (|Q| > 65504, or p * Vs > 65504);
+                                       rk8v4 append: a group scale saturated at the fp16
+                                       maximum, or a non-finite value */
 
 /* Limits of this build. */
 #define NK_GROUP 64      /* channels per quantization group */
@@ -186,6 +188,47 @@ int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const i
                               int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
                               void* workspace_dev, size_t workspace_bytes, void* out_dev,
                               int32_t* status_dev, void* stream);
+
+/*
+ * rk8v4 -- the "RotorQuant KV (rk8v4)" format of the "NInfer-3090" README:
+ * keys rotated by R = H64 / 8 (64-point Sylvester Hadamard per 64-channel
+ * group; R is orthonormal and its own inverse) and stored as INT8 group-64
+ * codes; values stored unrotated as signed 4-bit codes (15 levels, -7..7),
+ * two per byte, one scale per 32 channels; every scale fp16 (26,112 bytes
+ * per token on the page's 27B model). Chunk per (page, kv-head):
+ *   Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D/2] uint8 | Vs[P][D/32] fp16
+ * with channel 2j of a value row in the low nibble of byte j and 2j + 1 in
+ * the high one; pool = [num_pages][num_kv_heads][chunk]. The same nk_kv_pool
+ * struct describes an rk8v4 pool; its storage is sized with
+ * nk_rk8v4_pool_bytes and only the nk_rk8v4_* calls may touch it.
+ * Quantization (the readings where the page is silent):
+ *   keys:   y = R k in fp32, as butterflies (a + b, a - b) over the index
+ *           bits 0, 1, ..., 5 in that order (every add rounded), then x 1/8;
+ *           s = RN_fp16(max|y| / 127); q = clamp(rne(fp32(y / s)), -127, 127);
+ *   values: s = RN_fp16(max|v| / 7);    q = clamp(rne(fp32(v / s)), -7, 7);
+ *   a scale that rounds to 0 is stored as 1 (the codes are then 0); one past
+ *   the fp16 maximum is stored as 65504 and sets NK_DEVFLAG_RANGE.
+ */
+size_t nk_rk8v4_chunk_bytes(int32_t page_size, int32_t head_dim);
+size_t nk_rk8v4_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+
+/* kv_cache_append into an rk8v4 pool: arguments, checks, device flags,
+ * ordering and ownership exactly as nk_kv_append. */
+int nk_rk8v4_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                    const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                    const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream);
+
+/* Split-KV decode / verify attention over an rk8v4 pool: arguments, checks,
+ * workspace (nk_decode_workspace_bytes), causal mask, output and device
+ * flags exactly as nk_paged_decode_attn. Each query row is rotated by R
+ * inside the kernel and scored against the stored rotated keys
+ * (q . k = (R q) . (R k)); values are dequantized as code * scale. fp32
+ * CUDA-core kernel; G = Hq / Hkv <= 8; verifies wider than 8 columns run as
+ * column chunks. */
+int nk_rk8v4_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                         int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                         int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                         size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream);
 
 /*
  * nk_paged_decode_attn_noalloc -- nk_paged_decode_attn for callers that

@@ -23,7 +23,8 @@ MAX_T = 16
 __all__ = [
     "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_ctas",
     "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "paged_decode_attn_noalloc",
-    "attn_combine", "status_string", "decode_step",
+    "attn_combine", "status_string", "decode_step", "rk8v4_chunk_bytes", "rk8v4_pool_bytes", "rk8v4_append",
+    "rk8v4_decode_attn",
 ]
 
 
@@ -60,26 +61,47 @@ def kv_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: i
     return int(lib().nk_kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
 
 
+def rk8v4_chunk_bytes(page_size: int, head_dim: int) -> int:
+    return int(lib().nk_rk8v4_chunk_bytes(page_size, head_dim))
+
+
+def rk8v4_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().nk_rk8v4_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
 @dataclass
 class KVPool:
-    """A caller-owned pool: ``storage`` is a uint8 CUDA tensor of
-    ``kv_pool_bytes(...)`` bytes laid out as [page][kv-head][chunk]."""
+    """A caller-owned pool: ``storage`` is a uint8 CUDA tensor laid out as
+    [page][kv-head][chunk], in the INT8 group-64 format (``fmt="int8"``,
+    ``kv_pool_bytes(...)`` bytes) or the rk8v4 format (``fmt="rk8v4"``,
+    ``rk8v4_pool_bytes(...)`` bytes)."""
 
     storage: "object"
     num_pages: int
     page_size: int
     num_kv_heads: int
     head_dim: int
+    fmt: str = "int8"
 
     @classmethod
-    def empty(cls, num_pages, page_size, num_kv_heads, head_dim, device="cuda", fill: int | None = None):
+    def empty(cls, num_pages, page_size, num_kv_heads, head_dim, device="cuda", fill: int | None = None,
+              fmt: str = "int8"):
         import torch
 
-        n = kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
+        if fmt == "int8":
+            n = kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
+        elif fmt == "rk8v4":
+            n = rk8v4_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
+        else:
+            raise ValueError(f"unknown KV format {fmt!r}")
         st = torch.empty(n, dtype=torch.uint8, device=device)
         if fill is not None:
             st.fill_(fill)
-        return cls(st, num_pages, page_size, num_kv_heads, head_dim)
+        return cls(st, num_pages, page_size, num_kv_heads, head_dim, fmt)
+
+    def need(self, fmt: str) -> None:
+        if self.fmt != fmt:
+            raise ValueError(f"this call needs a {fmt} pool, not a {self.fmt} one")
 
     def c_struct(self) -> nk_kv_pool:
         _need_cuda(self.storage)
@@ -89,6 +111,7 @@ class KVPool:
 def kv_append(pool: KVPool, block_table, start_pos, cu_new, k, v, status=None, stream=None) -> None:
     """Quantize k/v rows (bf16 [total_new][Hkv][D]) into the pool (nk_kv_append)."""
     _need_cuda(block_table, start_pos, cu_new, k, v, status)
+    pool.need("int8")
     B = int(start_pos.numel())
     total = int(k.shape[0]) if k.dim() > 0 else 0
     ps = pool.c_struct()
@@ -106,10 +129,12 @@ def decode_workspace_bytes(B: int, T: int, num_q_heads: int, num_kv_heads: int, 
     return int(lib().nk_decode_workspace_bytes(B, T, num_q_heads, num_kv_heads, head_dim, num_ctas))
 
 
-def _decode(fn, name, pool, q, block_table, ctx_lens, sm_scale, max_ctx, num_ctas, workspace, out, status, stream):
+def _decode(fn, name, pool, q, block_table, ctx_lens, sm_scale, max_ctx, num_ctas, workspace, out, status, stream,
+            fmt="int8"):
     import torch
 
     _need_cuda(q, block_table, ctx_lens, workspace, out, status)
+    pool.need(fmt)
     B, T, Hq, D = (int(s) for s in q.shape)
     if out is None:
         out = torch.empty_like(q)
@@ -146,6 +171,7 @@ def decode_step(pool: KVPool, block_table, start_pos, cu_new, k, v, q, ctx_lens,
     import torch
 
     _need_cuda(block_table, start_pos, cu_new, k, v, q, ctx_lens, workspace, out, status)
+    pool.need("int8")
     B, T, Hq, D = (int(s) for s in q.shape)
     if int(start_pos.numel()) != B:
         raise ValueError("start_pos must hold one position per sequence of q")
@@ -176,6 +202,7 @@ def paged_decode_attn_noalloc(pool: KVPool, q, block_table, ctx_lens, sm_scale: 
     import torch
 
     _need_cuda(q, block_table, ctx_lens, out, status)
+    pool.need("int8")
     B, T, Hq, D = (int(s) for s in q.shape)
     if out is None:
         out = torch.empty_like(q)
@@ -185,6 +212,25 @@ def paged_decode_attn_noalloc(pool: KVPool, q, block_table, ctx_lens, sm_scale: 
                                             _ptr(out), _ptr(status), _stream(stream))
     _check(rc, "nk_paged_decode_attn_noalloc")
     return out
+
+
+def rk8v4_append(pool: KVPool, block_table, start_pos, cu_new, k, v, status=None, stream=None) -> None:
+    """Rotate, quantize and scatter k/v rows (bf16 [total_new][Hkv][D]) into an rk8v4 pool (nk_rk8v4_append)."""
+    _need_cuda(block_table, start_pos, cu_new, k, v, status)
+    pool.need("rk8v4")
+    B = int(start_pos.numel())
+    total = int(k.shape[0]) if k.dim() > 0 else 0
+    ps = pool.c_struct()
+    rc = lib().nk_rk8v4_append(ctypes.byref(ps), _ptr(block_table), int(block_table.shape[-1]), _ptr(start_pos),
+                               _ptr(cu_new), B, total, _ptr(k), _ptr(v), _ptr(status), _stream(stream))
+    _check(rc, "nk_rk8v4_append")
+
+
+def rk8v4_decode_attn(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int, num_ctas: int = 0,
+                      workspace=None, out=None, status=None, stream=None):
+    """Split-KV paged attention over an rk8v4 pool (nk_rk8v4_decode_attn); returns out bf16 [B][T][Hq][D]."""
+    return _decode(lib().nk_rk8v4_decode_attn, "nk_rk8v4_decode_attn", pool, q, block_table, ctx_lens, sm_scale,
+                   max_ctx, num_ctas, workspace, out, status, stream, fmt="rk8v4")
 
 
 def attn_combine(part_o, part_lse, out=None, stream=None):

@@ -46,6 +46,10 @@ EXPORTS = (
     "nk_paged_decode_attn_noalloc",
     "nk_decode_step",
     "nk_attn_combine",
+    "nk_rk8v4_chunk_bytes",
+    "nk_rk8v4_pool_bytes",
+    "nk_rk8v4_append",
+    "nk_rk8v4_decode_attn",
     "nk_status_string",
     "nk_version",
 )
@@ -77,6 +81,11 @@ def lib() -> ctypes.CDLL:
             L.nk_decode_step.argtypes = [pool_p, P, I32, P, P, I32, P, P, P, P, I32, I32, I32, F, I32, I32, P, Z, P,
                                          P, P]
             L.nk_decode_step.restype = ctypes.c_int
+            L.nk_rk8v4_chunk_bytes.argtypes, L.nk_rk8v4_chunk_bytes.restype = [I32, I32], Z
+            L.nk_rk8v4_pool_bytes.argtypes, L.nk_rk8v4_pool_bytes.restype = [I32, I32, I32, I32], Z
+            L.nk_rk8v4_append.argtypes = [pool_p, P, I32, P, P, I32, I32, P, P, P, P]
+            L.nk_rk8v4_append.restype = ctypes.c_int
+            L.nk_rk8v4_decode_attn.argtypes, L.nk_rk8v4_decode_attn.restype = dec, ctypes.c_int
             L.nk_attn_combine.argtypes = [P, P, I32, I32, I32, P, P]
             L.nk_attn_combine.restype = ctypes.c_int
             L.nk_status_string.argtypes, L.nk_status_string.restype = [ctypes.c_int], ctypes.c_char_p

@@ -6,6 +6,7 @@
 #include <atomic>
 
 #include "nk_decode.cuh"
+#include "nk_rk8v4.cuh"
 
 namespace nk {
 cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
@@ -79,11 +80,17 @@ int chunk_cols(bool simt, int D, int T, int G, int P) {
   return c;
 }
 
+// Which split kernel a decode call runs: the tensor-core kernels or the fp32
+// CUDA-core kernel on an INT8 group-64 pool, or the CUDA-core kernel of the
+// rk8v4 format on an rk8v4 pool.
+enum class Path { kTensor, kSimt, kRk8v4 };
+
 // Checks the decode arguments and fills `p`; *empty = nothing to launch.
 int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
                    int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
-                   void* workspace, size_t workspace_bytes, void* out, int32_t* status, bool simt, DecodeParams* pp,
+                   void* workspace, size_t workspace_bytes, void* out, int32_t* status, Path path, DecodeParams* pp,
                    bool* empty) {
+  const bool simt = path != Path::kTensor;
   *empty = true;
   int err = NK_OK;
   if (!pool_ok(pool, &err)) return err;
@@ -103,7 +110,8 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   } else {
     if (!decode_tc_supported(D, Tc, G, P) && !decode_mma_supported(D, Tc, G, P)) return NK_ERR_UNSUPPORTED;
   }
-  const int per_sm = simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G);
+  const int per_sm = path == Path::kRk8v4 ? decode_rk8v4_ctas_per_sm(D, G)
+                     : (simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G));
   const int32_t n = num_ctas > 0 ? num_ctas : default_ctas(B, Hkv, max_ctx, P, per_sm);
   const size_t need = nk_decode_workspace_bytes(B, T, Hq, Hkv, D, n);
   if (need > 0 && (!workspace || workspace_bytes < need)) return NK_ERR_WORKSPACE;
@@ -115,7 +123,7 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   p.P = P;
   p.Hkv = Hkv;
   p.D = D;
-  p.lay = ChunkLayout::make(P, D);
+  p.lay = path == Path::kRk8v4 ? rk8v4_layout(P, D) : ChunkLayout::make(P, D);
   p.q = reinterpret_cast<const uint16_t*>(q);
   p.bt = bt;
   p.max_pages = max_pages;
@@ -140,7 +148,8 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   return NK_OK;
 }
 
-int launch_decode(const DecodeParams& p0, bool simt, cudaStream_t st) {
+int launch_decode(const DecodeParams& p0, Path path, cudaStream_t st) {
+  const bool simt = path != Path::kTensor;
   const int Tc = chunk_cols(simt, p0.D, p0.T, p0.G, p0.P);
   const int64_t slots = (int64_t)p0.n_ctas + (int64_t)p0.B * p0.Hkv;
   for (int t0 = 0; t0 < p0.T; t0 += Tc) {
@@ -154,8 +163,9 @@ int launch_decode(const DecodeParams& p0, bool simt, cudaStream_t st) {
     if (t0 > 0) p.early = 0;  // the predecessor is the previous chunk's combine
     // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and 9 to
     // 32 rows per kv-head; the mma.sync kernel for the other shapes
-    cudaError_t e = simt ? launch_decode_simt(p, st)
-                         : (decode_tc_supported(p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
+    cudaError_t e = path == Path::kRk8v4 ? launch_decode_rk8v4(p, st)
+                    : path == Path::kSimt   ? launch_decode_simt(p, st)
+                    : (decode_tc_supported(p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
     if (e != cudaSuccess) return NK_ERR_CUDA;
     e = launch_decode_combine(p, st);
     if (e != cudaSuccess) return NK_ERR_CUDA;
@@ -165,13 +175,13 @@ int launch_decode(const DecodeParams& p0, bool simt, cudaStream_t st) {
 
 int paged_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
                  int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
-                 void* workspace, size_t workspace_bytes, void* out, int32_t* status, void* stream, bool simt) {
+                 void* workspace, size_t workspace_bytes, void* out, int32_t* status, void* stream, Path path) {
   DecodeParams p;
   bool empty = true;
   const int err = prepare_decode(pool, q, bt, max_pages, ctx, B, T, Hq, sm_scale, max_ctx, num_ctas, workspace,
-                                 workspace_bytes, out, status, simt, &p, &empty);
+                                 workspace_bytes, out, status, path, &p, &empty);
   if (err != NK_OK || empty) return err;
-  return launch_decode(p, simt, reinterpret_cast<cudaStream_t>(stream));
+  return launch_decode(p, path, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Checks the append arguments; *empty = nothing to launch.
@@ -228,7 +238,8 @@ int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32
   if (err != NK_OK) return err;
   DecodeParams p;
   err = prepare_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
-                       max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, false, &p, &no_decode);
+                       max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, Path::kTensor, &p,
+                       &no_decode);
   if (err != NK_OK) return err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (!no_append) {
@@ -240,7 +251,7 @@ int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32
   // the decode's predecessor is this append, which writes only pool pages:
   // its prologue (lengths, block-table entries, Q) may overlap the append
   p.early = no_append ? 0 : 1;
-  return launch_decode(p, false, st);
+  return launch_decode(p, Path::kTensor, st);
 }
 
 int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {
@@ -264,7 +275,7 @@ int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_
                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
                          size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream) {
   return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
-                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, false);
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kTensor);
 }
 
 int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
@@ -273,7 +284,38 @@ int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const i
                               void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
                               void* stream) {
   return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
-                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, true);
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kSimt);
+}
+
+size_t nk_rk8v4_chunk_bytes(int32_t page_size, int32_t head_dim) {
+  if (page_size < 1 || head_dim < kGroup || head_dim % kGroup != 0) return 0;
+  return (size_t)rk8v4_layout(page_size, head_dim).chunk;
+}
+
+size_t nk_rk8v4_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_pages < 0 || num_kv_heads < 1) return 0;
+  return (size_t)num_pages * (size_t)num_kv_heads * nk_rk8v4_chunk_bytes(page_size, head_dim);
+}
+
+int nk_rk8v4_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                    const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                    const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream) {
+  bool empty = true;
+  const int err = check_append(pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B, total_new,
+                               k_dev, v_dev, &empty);
+  if (err != NK_OK || empty) return err;
+  const cudaError_t e = launch_rk8v4_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev,
+                                            cu_new_dev, B, total_new, k_dev, v_dev, status_dev,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;
+}
+
+int nk_rk8v4_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                         int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                         int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                         size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream) {
+  return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kRk8v4);
 }
 
 int nk_attn_combine(const float* part_o_dev, const float* part_lse_dev, int32_t num_splits, int32_t rows,

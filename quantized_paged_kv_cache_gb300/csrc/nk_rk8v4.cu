@@ -1,0 +1,464 @@
+// nk_rk8v4.cu -- append and split-KV decode attention for the rk8v4 KV format
+// ("NInfer-3090" README, "RotorQuant KV (rk8v4)"): the keys of every
+// 64-channel group are rotated by R = H64 / 8 (Sylvester Hadamard, its own
+// inverse) and stored as INT8 codes, the values are stored unrotated as 4-bit
+// codes over 32-channel groups; all scales are fp16. Attention rotates each
+// query row by the same R, so q . k = (R q) . (R k) is scored against the
+// stored keys directly and no inverse rotation is needed.
+//
+// Quantization (both sides of the parity tests take these decisions in the
+// same precision):
+//   keys   y = R k in fp32: butterflies (a + b, a - b) over index bits 0..5 in
+//          that order, each add rounded, then times 1/8;
+//          s = RN_fp16(fp32(max|y| / 127)), q = clamp(rne(fp32(y / s)), +-127);
+//   values s = RN_fp16(fp32(max|v| / 7)),   q = clamp(rne(fp32(v / s)), +-7);
+//   a scale that rounds to 0 becomes 1 (its codes are then 0), one past the
+//   fp16 maximum saturates at 65504 (NK_DEVFLAG_RANGE).
+// fp32(a / c) rounded again to fp16 is the correctly rounded fp16 quotient
+// here: a / c (c = 127 or 7) is never an fp16 rounding midpoint and lies
+// more than half an fp32 ulp away from every one.
+//
+// The attention kernel runs on fp32 CUDA cores with the split and partial
+// layout of the INT8 decode kernels, so their log-sum-exp combine merges its
+// partials unchanged.
+#include <cuda_fp16.h>
+
+#include "nk_rk8v4.cuh"
+
+namespace nk {
+
+// fp16 scale bits of a group whose absmax is a, for codes up to qmax.
+__device__ __forceinline__ uint16_t rk_scale_bits(float a, float qmax, bool& range) {
+  uint16_t b = __half_as_ushort(__float2half_rn(__fdiv_rn(a, qmax)));
+  if ((b & 0x7fffu) == 0) {
+    b = 0x3c00u;
+  } else if ((b & 0x7fffu) >= 0x7c00u) {  // past the fp16 range (or not a number)
+    b = 0x7bffu;
+    range = true;
+  }
+  return b;
+}
+
+__device__ __forceinline__ uint32_t rk_code(float x, float s, int qmax) {
+  int q = __float2int_rn(__fdiv_rn(x, s));
+  q = q > qmax ? qmax : (q < -qmax ? -qmax : q);
+  return (uint32_t)q;
+}
+
+// One key group: 64 bf16 channels -> 64 int8 codes of R k and the fp16 scale.
+__device__ __forceinline__ void rk_key_group(const uint4* src, uint4* dst, uint16_t* scale, bool& range) {
+  float t[kGroup];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 w = __ldg(src + c);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      t[8 * c + 2 * i] = bf16_lo(ws[i]);
+      t[8 * c + 2 * i + 1] = bf16_hi(ws[i]);
+    }
+  }
+#pragma unroll
+  for (int h = 1; h < kGroup; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i)
+      if ((i & h) == 0) {
+        const float a = t[i], b = t[i + h];
+        t[i] = __fadd_rn(a, b);
+        t[i + h] = __fsub_rn(a, b);
+      }
+  float amax = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < kGroup; ++i) {
+    t[i] = __fmul_rn(t[i], 0.125f);
+    finite &= isfinite(t[i]);
+    amax = fmaxf(amax, fabsf(t[i]));
+  }
+  if (!finite) range = true;
+  const uint16_t sb = rk_scale_bits(amax, 127.f, range);
+  const float s = __half2float(__ushort_as_half(sb));
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 16 * c + 4 * j;
+      w[j] = (rk_code(t[e], s, 127) & 0xffu) | ((rk_code(t[e + 1], s, 127) & 0xffu) << 8) |
+             ((rk_code(t[e + 2], s, 127) & 0xffu) << 16) | ((rk_code(t[e + 3], s, 127) & 0xffu) << 24);
+    }
+    dst[c] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  *scale = sb;
+}
+
+// One value group: 32 bf16 channels -> 16 bytes of 4-bit codes and the fp16 scale.
+__device__ __forceinline__ void rk_value_group(const uint4* src, uint4* dst, uint16_t* scale, bool& range) {
+  uint32_t raw[16];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 w = __ldg(src + c);
+    raw[4 * c] = w.x;
+    raw[4 * c + 1] = w.y;
+    raw[4 * c + 2] = w.z;
+    raw[4 * c + 3] = w.w;
+  }
+  float amax = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float a = bf16_lo(raw[i]), b = bf16_hi(raw[i]);
+    finite &= isfinite(a) && isfinite(b);
+    amax = fmaxf(amax, fmaxf(fabsf(a), fabsf(b)));
+  }
+  if (!finite) range = true;
+  const uint16_t sb = rk_scale_bits(amax, 7.f, range);
+  const float s = __half2float(__ushort_as_half(sb));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {  // byte i: channel 2i (low nibble), 2i + 1 (high nibble)
+    const uint32_t byte = (rk_code(bf16_lo(raw[i]), s, 7) & 0xfu) | ((rk_code(bf16_hi(raw[i]), s, 7) & 0xfu) << 4);
+    w[i / 4] |= byte << (8 * (i % 4));
+  }
+  *dst = make_uint4(w[0], w[1], w[2], w[3]);
+  *scale = sb;
+}
+
+struct RkAppendParams {
+  uint8_t* pool;
+  int num_pages, P, Hkv, D;
+  ChunkLayout lay;
+  const int32_t* bt;
+  int max_pages;
+  const int32_t* start_pos;
+  const int32_t* cu_new;
+  int B, total_new;
+  const uint16_t* k;
+  const uint16_t* v;
+  int32_t* status;
+};
+
+// One thread per item; the items of a (row, kv-head) are its D/64 key groups
+// followed by its D/32 value groups.
+__global__ void __launch_bounds__(128) rk8v4_append_kernel(const RkAppendParams p) {
+  chain_wait();
+  chain_release();
+  const int kg = p.D / kGroup, vg = p.D / kRkVGroup, per = kg + vg;
+  const int64_t items = (int64_t)p.total_new * p.Hkv * per;
+  for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t rh = it / per;
+    const int r = (int)(it % per);
+    const int j = (int)(rh / p.Hkv), h = (int)(rh % p.Hkv);
+    // sequence b of row j: cu_new[b] <= j < cu_new[b + 1]
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.cu_new + mid) <= j) lo = mid; else hi = mid;
+    }
+    const int b = lo;
+    const int64_t pos = (int64_t)__ldg(p.start_pos + b) + (j - __ldg(p.cu_new + b));
+    if (pos < 0 || pos >= (int64_t)p.max_pages * p.P) {
+      flag(p.status, NK_DEVFLAG_BAD_POS);
+      continue;
+    }
+    const int page = __ldg(p.bt + (int64_t)b * p.max_pages + pos / p.P);
+    if (page < 0 || page >= p.num_pages) {
+      flag(p.status, NK_DEVFLAG_BAD_PAGE);
+      continue;
+    }
+    const int slot = (int)(pos % p.P);
+    uint8_t* chunk = p.pool + ((int64_t)page * p.Hkv + h) * p.lay.chunk;
+    const int64_t row = ((int64_t)j * p.Hkv + h) * p.D;
+    bool range = false;
+    if (r < kg) {
+      rk_key_group(reinterpret_cast<const uint4*>(p.k + row + r * kGroup),
+                   reinterpret_cast<uint4*>(chunk + (int64_t)slot * p.D + r * kGroup),
+                   reinterpret_cast<uint16_t*>(chunk + p.lay.ks) + slot * kg + r, range);
+    } else {
+      const int g = r - kg;
+      rk_value_group(reinterpret_cast<const uint4*>(p.v + row + g * kRkVGroup),
+                     reinterpret_cast<uint4*>(chunk + p.lay.vc + (int64_t)slot * (p.D / 2) + g * (kRkVGroup / 2)),
+                     reinterpret_cast<uint16_t*>(chunk + p.lay.vs) + slot * vg + g, range);
+    }
+    if (range) flag(p.status, NK_DEVFLAG_RANGE);
+  }
+}
+
+cudaError_t launch_rk8v4_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages,
+                                const int32_t* start_pos, const int32_t* cu_new, int B, int total_new, const void* k,
+                                const void* v, int32_t* status, cudaStream_t stream) {
+  RkAppendParams p;
+  p.pool = reinterpret_cast<uint8_t*>(pool.base_dev);
+  p.num_pages = pool.num_pages;
+  p.P = pool.page_size;
+  p.Hkv = pool.num_kv_heads;
+  p.D = pool.head_dim;
+  p.lay = rk8v4_layout(p.P, p.D);
+  p.bt = bt;
+  p.max_pages = max_pages;
+  p.start_pos = start_pos;
+  p.cu_new = cu_new;
+  p.B = B;
+  p.total_new = total_new;
+  p.k = reinterpret_cast<const uint16_t*>(k);
+  p.v = reinterpret_cast<const uint16_t*>(v);
+  p.status = status;
+  const int64_t items = (int64_t)total_new * p.Hkv * (p.D / kGroup + p.D / kRkVGroup);
+  int64_t blocks = (items + 127) / 128;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_chained(rk8v4_append_kernel, dim3((unsigned)blocks), dim3(128), 0, stream, p);
+}
+
+// ---------------------------------------------------------------------------
+// Decode attention. Same structure as the INT8 CUDA-core kernel: each CTA
+// walks its segments of (sequence, kv-head, page) items; warp w serves query
+// column t = w % T for pages sub, sub + nsub, ...; lane l owns channels
+// [l CPL, (l + 1) CPL). The query rows are rotated once per segment (the
+// butterflies of the channel bits a lane holds in registers, then those of the
+// lane bits by shuffles); per key a warp forms the G dot products with the
+// int8 codes, all-reduces them, applies the key's fp16 group scale and the
+// online softmax (base 2), and accumulates p * Vs * (4-bit code).
+// ---------------------------------------------------------------------------
+constexpr int kRkWarps = 8;
+constexpr int kRkMaxG = 8;
+
+template <int CPL>
+struct RkRaw {
+  uint32_t k[CPL >= 4 ? CPL / 4 : 1];  // CPL int8 key codes
+  uint32_t v;                          // CPL 4-bit value codes
+};
+
+template <int CPL>
+__device__ __forceinline__ RkRaw<CPL> rk_load(const uint8_t* kc, const uint8_t* vc) {
+  RkRaw<CPL> r;
+  if constexpr (CPL == 8) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(kc));
+    r.k[0] = w.x;
+    r.k[1] = w.y;
+    r.v = __ldg(reinterpret_cast<const unsigned int*>(vc));
+  } else if constexpr (CPL == 4) {
+    r.k[0] = __ldg(reinterpret_cast<const unsigned int*>(kc));
+    r.v = __ldg(reinterpret_cast<const unsigned short*>(vc));
+  } else {
+    r.k[0] = __ldg(reinterpret_cast<const unsigned short*>(kc));
+    r.v = __ldg(vc);
+  }
+  return r;
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(256) decode_rk8v4_kernel(const DecodeParams p) {
+  chain_wait();
+  chain_release();
+  extern __shared__ float smem[];
+  __shared__ int pre[kMaxBatch + 1];
+  __shared__ int warp_tot[8];
+  constexpr int D = CPL * 32;
+  constexpr int LPG = kGroup / CPL;  // lanes per 64-channel group
+  const int G = p.G, T = p.T, M = G * T;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const SplitShape sh = p.shape();
+  flag_bad_ctx(p);
+  block_page_prefix(sh, p.ctx, p.trim, pre, warp_tot);
+  const int64_t W = (int64_t)pre[p.B] * p.Hkv;
+  if (W == 0) return;
+  int64_t x = cta_begin(W, p.n_ctas, blockIdx.x);
+  const int64_t x_end = cta_begin(W, p.n_ctas, blockIdx.x + 1);
+
+  float* red_o = smem;                          // [8 warps][G][D]
+  float* red_m = smem + kRkWarps * G * D;       // [8][G]
+  float* red_l = red_m + kRkWarps * G;          // [8][G]
+  const int nsub = kRkWarps / T;
+  const bool active = w < nsub * T;
+  const int t = w % T, sub = w / T;
+  const int kgrp = (lane * CPL) / kGroup, vgrp = (lane * CPL) / kRkVGroup;
+
+  Segment seg;
+  while (next_segment(sh, pre, x, x_end, seg)) {
+    const int L = p.ctx[seg.b] - p.trim;
+    const int last = L - T + t;  // last key visible to column t
+    float qf[kRkMaxG][CPL], o[kRkMaxG][CPL], m[kRkMaxG], l[kRkMaxG];
+#pragma unroll
+    for (int hg = 0; hg < kRkMaxG; ++hg) {
+      m[hg] = -INFINITY;
+      l[hg] = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) { o[hg][j] = 0.f; qf[hg][j] = 0.f; }
+      if (hg < G) {
+        const uint16_t* qr = p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * D + lane * CPL;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) qf[hg][j] = __uint_as_float((uint32_t)__ldg(qr + j) << 16);
+      }
+      // R q: channel c of a group is j + CPL (lane mod LPG); its low bits are
+      // j (in registers), the high ones the lane's (by shuffles)
+#pragma unroll
+      for (int h = 1; h < CPL; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+          if ((j & h) == 0) {
+            const float a = qf[hg][j], b = qf[hg][j + h];
+            qf[hg][j] = a + b;
+            qf[hg][j + h] = a - b;
+          }
+#pragma unroll
+      for (int lb = 1; lb < LPG; lb <<= 1) {
+        const bool upper = (lane & lb) != 0;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const float other = __shfl_xor_sync(0xffffffffu, qf[hg][j], lb);
+          qf[hg][j] = upper ? other - qf[hg][j] : qf[hg][j] + other;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) qf[hg][j] *= 0.125f;
+    }
+    if (active) {
+      for (int pi = seg.page_begin + sub; pi < seg.page_end; pi += nsub) {
+        if (pi * p.P > last) break;
+        const int page = __ldg(p.bt + (int64_t)seg.b * p.max_pages + pi);
+        if (page < 0 || page >= p.num_pages) {
+          if (lane == 0) flag(p.status, NK_DEVFLAG_BAD_PAGE);
+          continue;
+        }
+        const uint8_t* chunk = p.pool + ((int64_t)page * p.Hkv + seg.h) * p.lay.chunk;
+        const int kend = min(p.P, last - pi * p.P + 1);
+        const __half* ksp = reinterpret_cast<const __half*>(chunk + p.lay.ks);
+        const __half* vsp = reinterpret_cast<const __half*>(chunk + p.lay.vs);
+        // keys in groups of four, the next group's loads issued before the current group's math
+        constexpr int KB = 4;
+        RkRaw<CPL> nr[KB];
+        __half nks[KB], nvs[KB];
+        auto load_group = [&](int k0) {
+#pragma unroll
+          for (int j = 0; j < KB; ++j) {
+            const int k = min(k0 + j, kend - 1);  // clamped: a repeated key is never used
+            nr[j] = rk_load<CPL>(chunk + (int64_t)k * D + lane * CPL, chunk + p.lay.vc + (int64_t)k * (D / 2) +
+                                                                          lane * (CPL / 2));
+            nks[j] = ksp[k * (D / kGroup) + kgrp];
+            nvs[j] = vsp[k * (D / kRkVGroup) + vgrp];
+          }
+        };
+        load_group(0);
+        for (int k0 = 0; k0 < kend; k0 += KB) {
+          RkRaw<CPL> cr[KB];
+          float cks[KB], cvs[KB];
+#pragma unroll
+          for (int j = 0; j < KB; ++j) {
+            cr[j] = nr[j];
+            cks[j] = __half2float(nks[j]);
+            cvs[j] = __half2float(nvs[j]);
+          }
+          if (k0 + KB < kend) load_group(k0 + KB);
+#pragma unroll
+          for (int j = 0; j < KB; ++j) {
+            if (k0 + j >= kend) break;
+            float kc[CPL], vc[CPL];
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+              kc[i] = (float)(int8_t)(cr[j].k[i / 4] >> (8 * (i % 4)));
+              vc[i] = (float)((int32_t)(cr[j].v << (28 - 4 * i)) >> 28);  // sign-extended nibble i
+            }
+            float s[kRkMaxG];
+#pragma unroll
+            for (int hg = 0; hg < kRkMaxG; ++hg) {
+              float acc = 0.f;
+#pragma unroll
+              for (int jj = 0; jj < CPL; ++jj) acc = fmaf(qf[hg][jj], kc[jj], acc);
+              s[hg] = acc * cks[j];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+              for (int hg = 0; hg < kRkMaxG; ++hg) s[hg] += __shfl_xor_sync(0xffffffffu, s[hg], off);
+#pragma unroll
+            for (int hg = 0; hg < kRkMaxG; ++hg) {
+              if (hg >= G) break;
+              const float sc = s[hg] * p.scale2;
+              if (sc > m[hg]) {
+                const float alpha = exp2f(m[hg] - sc);
+                l[hg] *= alpha;
+#pragma unroll
+                for (int jj = 0; jj < CPL; ++jj) o[hg][jj] *= alpha;
+                m[hg] = sc;
+              }
+              const float pw = exp2f(sc - m[hg]);
+              l[hg] += pw;
+              const float pv = pw * cvs[j];
+#pragma unroll
+              for (int jj = 0; jj < CPL; ++jj) o[hg][jj] = fmaf(pv, vc[jj], o[hg][jj]);
+            }
+          }
+        }
+      }
+    }
+    // merge the nsub warps of each column
+#pragma unroll
+    for (int hg = 0; hg < kRkMaxG; ++hg) {
+      if (hg >= G) break;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) red_o[(w * G + hg) * D + lane * CPL + j] = o[hg][j];
+      if (lane == 0) {
+        red_m[w * G + hg] = active ? m[hg] : -INFINITY;
+        red_l[w * G + hg] = active ? l[hg] : 0.f;
+      }
+    }
+    __syncthreads();
+    const int seg_slot = blockIdx.x + seg.u;
+    for (int i = tid; i < M * D; i += blockDim.x) {
+      const int r = i / D, c = i % D;
+      const int tt = r / G, hg = r % G;
+      float mx = -INFINITY;
+      for (int sb = 0; sb < nsub; ++sb) mx = fmaxf(mx, red_m[(sb * T + tt) * G + hg]);
+      float lsum = 0.f, acc = 0.f;
+      if (mx != -INFINITY) {
+        for (int sb = 0; sb < nsub; ++sb) {
+          const int ww = sb * T + tt;
+          const float mw = red_m[ww * G + hg];
+          if (mw == -INFINITY) continue;
+          const float sc = exp2f(mw - mx);
+          lsum += red_l[ww * G + hg] * sc;
+          acc += red_o[(ww * G + hg) * D + c] * sc;
+        }
+      }
+      const float val = lsum > 0.f ? acc / lsum : 0.f;
+      if (seg.whole) {
+        p.out[(((int64_t)seg.b * p.qT + tt) * p.Hq + seg.h * G + hg) * D + c] = f32_to_bf16(val);
+      } else {
+        p.part_o[((int64_t)seg_slot * M + r) * D + c] = val;
+        if (c == 0) p.part_lse[(int64_t)seg_slot * M + r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+static size_t rk_smem(int D, int G) { return (size_t)kRkWarps * G * (D + 2) * sizeof(float); }
+
+int decode_rk8v4_ctas_per_sm(int D, int G) {
+  int n = 0;
+  const size_t smem = rk_smem(D, G);
+  cudaError_t e;
+  if (D == 256) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_rk8v4_kernel<8>, 256, smem);
+  else if (D == 128) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_rk8v4_kernel<4>, 256, smem);
+  else e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_rk8v4_kernel<2>, 256, smem);
+  if (e != cudaSuccess) { (void)cudaGetLastError(); return 1; }
+  return n < 1 ? 1 : n;
+}
+
+template <int CPL>
+static cudaError_t launch_rk_t(const DecodeParams& p, size_t smem, cudaStream_t stream) {
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_rk8v4_kernel<CPL>), (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_chained(decode_rk8v4_kernel<CPL>, dim3(p.n_ctas), dim3(256), smem, stream, p);
+}
+
+cudaError_t launch_decode_rk8v4(const DecodeParams& p, cudaStream_t stream) {
+  const size_t smem = rk_smem(p.D, p.G);
+  if (p.D == 256) return launch_rk_t<8>(p, smem, stream);
+  if (p.D == 128) return launch_rk_t<4>(p, smem, stream);
+  return launch_rk_t<2>(p, smem, stream);
+}
+
+}  // namespace nk

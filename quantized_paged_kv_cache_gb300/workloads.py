@@ -42,6 +42,8 @@ class Workload:
     outlier_scale: float = 1.0
     token_norm_range: tuple[float, float] | None = None
     note: str = ""
+    # KV format of the pool: "int8" (INT8 group-64, fp32 scales) or "rk8v4"
+    fmt: str = "int8"
     # filled by tables()
     num_pages: int = 0
     max_pages: int = 0
@@ -62,11 +64,18 @@ class Workload:
     def pages_of(self, b: int) -> int:
         return (self.ctx_lens[b] + self.P - 1) // self.P
 
-    # algorithmic bytes of one attention call: int8 K/V + fp32 group scales
-    # of every visible key, bf16 Q read and bf16 O written
+    # stored bytes of one key of one kv-head: int8 K/V codes + fp32 scales per
+    # 64 channels (int8); int8 K codes + fp16 scale per 64 channels and 4-bit
+    # V codes + fp16 scale per 32 channels (rk8v4)
+    def bytes_per_key_head(self) -> int:
+        if self.fmt == "rk8v4":
+            return self.D + (self.D // 64) * 2 + self.D // 2 + (self.D // 32) * 2
+        return 2 * self.D + 2 * (self.D // 64) * 4
+
+    # algorithmic bytes of one attention call: the stored K/V of every visible
+    # key, bf16 Q read and bf16 O written
     def kv_bytes(self) -> int:
-        per_key_head = 2 * self.D + 2 * (self.D // 64) * 4
-        return sum(self.ctx_lens) * self.Hkv * per_key_head
+        return sum(self.ctx_lens) * self.Hkv * self.bytes_per_key_head()
 
     def q_bytes(self) -> int:
         return self.B * self.T * self.Hq * self.D * 2
@@ -74,14 +83,14 @@ class Workload:
     def attn_bytes(self) -> int:
         return self.kv_bytes() + 2 * self.q_bytes()
 
-    # algorithmic bytes of one append call: bf16 K and V read, int8 codes and
-    # fp32 scales written
+    # algorithmic bytes of one append call: bf16 K and V read, codes and
+    # scales written
     def append_rows(self) -> int:
         return self.B * self.append_len
 
     def append_bytes(self) -> int:
         n = self.append_rows() * self.Hkv
-        return n * (2 * self.D * 2 + 2 * self.D + 2 * (self.D // 64) * 4)
+        return n * (2 * self.D * 2 + self.bytes_per_key_head())
 
 
 def _gen(seed: int, tag: int, device) -> torch.Generator:
@@ -91,16 +100,20 @@ def _gen(seed: int, tag: int, device) -> torch.Generator:
 
 
 def make(name: str) -> Workload:
-    """The workloads: tiny, c1_decode, c8_verify, long_context, mix, and
-    c8_decode (the C8 verify contexts at T = 1: plain decode of 8 sequences)."""
+    """The workloads: tiny, c1_decode, c8_verify, long_context, mix,
+    c8_decode (the C8 verify contexts at T = 1: plain decode of 8 sequences),
+    and c1_rk8v4 (c1_decode's inputs in the rk8v4 format)."""
     if name == "tiny":
         w = Workload("tiny", B=1, T=1, Hq=2, Hkv=1, D=64, P=16, ctx_lens=[256], seed=0, append_len=1,
                      note="1 seq, 1 kv-head, 2 q-heads, head_dim 64, ctx 256, page 16, T=1")
-    elif name == "c1_decode":
-        w = Workload("c1_decode", B=1, T=1, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[32768], seed=1, append_len=1,
+    elif name in ("c1_decode", "c1_rk8v4"):
+        w = Workload(name, B=1, T=1, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[32768], seed=1, append_len=1,
                      outlier_channels=4, outlier_scale=8.0,
                      note="C1 decode: 24 q / 4 kv heads, head_dim 256, ctx 32,768, page 64, T=1, "
-                          "4 K outlier channels per head x8")
+                          "4 K outlier channels per head x8",
+                     fmt="rk8v4" if name == "c1_rk8v4" else "int8")
+        if name == "c1_rk8v4":
+            w.note += "; rk8v4 KV format"
     elif name in ("c8_verify", "c8_decode"):
         g = _gen(2, 0, "cpu")
         lens = torch.randint(4096, 65536 + 1, (8,), generator=g).tolist()
@@ -123,7 +136,8 @@ def make(name: str) -> Workload:
     return tables(w)
 
 
-CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix", "c8_decode")
+CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix", "c8_decode")  # INT8 group-64 pools
+RK8V4_CONFIGS = ("c1_rk8v4",)
 
 
 def tables(w: Workload, num_pages: int | None = None) -> Workload:

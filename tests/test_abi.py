@@ -129,3 +129,48 @@ def test_combine_rejects_bad_arguments():
     assert L.nk_attn_combine(None, FAKE, 2, 4, 64, FAKE, None) == 1
     assert L.nk_attn_combine(FAKE, FAKE, -1, 4, 64, FAKE, None) == 2
     assert L.nk_attn_combine(FAKE, FAKE, 2, 0, 64, FAKE, None) == 0
+
+
+@pytest.mark.parametrize("P,D,H,N", [(16, 64, 1, 16), (64, 256, 4, 512), (32, 128, 8, 3), (256, 256, 2, 7)])
+def test_rk8v4_pool_size_agrees_with_the_oracle_layout(P, D, H, N):
+    assert nk.rk8v4_chunk_bytes(P, D) == oracle.rk_chunk_bytes(P, D)
+    assert nk.rk8v4_pool_bytes(N, P, H, D) == oracle.rk_pool_bytes(N, P, H, D)
+    assert nk.rk8v4_chunk_bytes(P, D) % 16 == 0
+    assert nk.rk8v4_chunk_bytes(64, 100) == 0 and nk.rk8v4_chunk_bytes(0, 256) == 0
+
+
+def test_rk8v4_calls_reject_bad_arguments():
+    L = nk.lib()
+    p = pool()
+    assert L.nk_rk8v4_append(None, FAKE, 4, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 1
+    assert L.nk_rk8v4_append(ctypes.byref(p), FAKE, 0, FAKE, FAKE, 1, 1, FAKE, FAKE, None, None) == 2
+    assert L.nk_rk8v4_append(ctypes.byref(p), FAKE, 4, FAKE, FAKE, 1, 1, FAKE, FAKE + 8, None, None) == 2
+    assert L.nk_rk8v4_append(ctypes.byref(p), FAKE, 4, FAKE, FAKE, 1, 0, FAKE, FAKE, None, None) == 0
+
+    def dec(pp=p, T=1, Hq=2, B=1, max_ctx=64, q=FAKE, scale=0.125):
+        return L.nk_rk8v4_decode_attn(ctypes.byref(pp) if pp is not None else None, q, FAKE, 4, FAKE, B, T, Hq,
+                                      scale, max_ctx, 0, FAKE, 1 << 30, FAKE, None, None)
+
+    assert dec(pp=None) == 1
+    assert dec(pp=pool(P=24)) == 2
+    assert dec(T=0) == 2 and dec(T=17) == 2
+    assert dec(pp=pool(H=2), Hq=3) == 2
+    assert dec(q=FAKE + 2) == 2
+    assert dec(scale=float("nan")) == 2
+    assert dec(Hq=16) == 3  # G > 8 on CUDA cores
+    assert dec(B=0) == 0
+
+
+def test_pool_format_is_checked_by_the_binding():
+    """An INT8 pool is refused by the rk8v4 calls and the other way round
+    (the C ABI cannot tell the formats apart: the Python pool carries it)."""
+    import torch
+
+    st = torch.zeros(16, dtype=torch.uint8)
+    for fmt, other in (("int8", "rk8v4"), ("rk8v4", "int8")):
+        p = nk.KVPool(st, 1, 16, 1, 64, fmt)
+        p.need(fmt)
+        with pytest.raises(ValueError):
+            p.need(other)
+    with pytest.raises(ValueError):
+        nk.KVPool.empty(1, 16, 1, 64, device="cpu", fmt="fp8")
