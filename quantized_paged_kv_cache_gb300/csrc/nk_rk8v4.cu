@@ -23,6 +23,7 @@
 // partials unchanged.
 #include <cuda_fp16.h>
 
+#include "nk_ptx.cuh"
 #include "nk_rk8v4.cuh"
 
 namespace nk {
@@ -248,6 +249,25 @@ __device__ __forceinline__ RkRaw<CPL> rk_load(const uint8_t* kc, const uint8_t* 
   return r;
 }
 
+// The same codes from a page staged in shared memory (plain loads).
+template <int CPL>
+__device__ __forceinline__ RkRaw<CPL> rk_load_shared(const uint8_t* kc, const uint8_t* vc) {
+  RkRaw<CPL> r;
+  if constexpr (CPL == 8) {
+    const uint2 w = *reinterpret_cast<const uint2*>(kc);
+    r.k[0] = w.x;
+    r.k[1] = w.y;
+    r.v = *reinterpret_cast<const uint32_t*>(vc);
+  } else if constexpr (CPL == 4) {
+    r.k[0] = *reinterpret_cast<const uint32_t*>(kc);
+    r.v = *reinterpret_cast<const uint16_t*>(vc);
+  } else {
+    r.k[0] = *reinterpret_cast<const uint16_t*>(kc);
+    r.v = *vc;
+  }
+  return r;
+}
+
 template <int CPL>
 __global__ void __launch_bounds__(256) decode_rk8v4_kernel(const DecodeParams p) {
   chain_wait();
@@ -434,6 +454,274 @@ __global__ void __launch_bounds__(256) decode_rk8v4_kernel(const DecodeParams p)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Staged decode, used wherever the ring below holds at least three pages. The
+// CTA walks the same segments, but every (page, kv-head) chunk -- contiguous,
+// 26,112 bytes at P = 64, D = 256 -- arrives in a shared-memory ring through
+// one bulk asynchronous copy issued S pages ahead by one thread, and all the
+// warps of the CTA work on the same page: warp w takes query column
+// t = w % T and keys [sub KPW, (sub + 1) KPW) of the page (sub = w / T, KPW =
+// P / (8 / T) rounded up). Keys are taken four at a time: the four keys' warp
+// reductions are independent, so their shuffles overlap, and a row's running
+// maximum moves at most once per four keys. GM >= G is the number of query
+// heads the registers hold.
+// ---------------------------------------------------------------------------
+constexpr int kRkMaxStages = 8;
+constexpr int kRkSmemBudget = 232448 - 8192;  // opt-in shared memory per block, less the static arrays
+
+__host__ __device__ inline int rk_staged_fixed_bytes(int D, int GM) {
+  return kRkWarps * GM * D * 4 + 2 * kRkWarps * GM * 4 + 128;
+}
+
+__host__ __device__ inline int rk_staged_stages(int chunk, int D, int GM) {
+  int s = (kRkSmemBudget - rk_staged_fixed_bytes(D, GM)) / chunk;
+  return s > kRkMaxStages ? kRkMaxStages : s;
+}
+
+template <int CPL, int GM>
+__global__ void __launch_bounds__(256, 1) decode_rk8v4_staged_kernel(const DecodeParams p, int S) {
+  chain_wait();
+  chain_release();
+  extern __shared__ uint8_t rk_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rk_smem_raw) + 127) & ~uintptr_t(127));
+  __shared__ int pre[kMaxBatch + 1];
+  __shared__ int warp_tot[8];
+  __shared__ int stage_ok[kRkMaxStages];
+  __shared__ __align__(8) uint64_t full_bar[kRkMaxStages];
+  __shared__ int abort_flag;
+  constexpr int D = CPL * 32;
+  constexpr int LPG = kGroup / CPL;  // lanes per 64-channel group
+  const int G = p.G, T = p.T, M = G * T;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const SplitShape sh = p.shape();
+  const int chunk = (int)p.lay.chunk;
+  float* red_o = reinterpret_cast<float*>(smem + (size_t)S * chunk);  // [8 warps][GM][D]
+  float* red_m = red_o + kRkWarps * GM * D;                            // [8][GM]
+  float* red_l = red_m + kRkWarps * GM;                                // [8][GM]
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  flag_bad_ctx(p);
+  block_page_prefix(sh, p.ctx, p.trim, pre, warp_tot);  // ends with __syncthreads
+  const int64_t W = (int64_t)pre[p.B] * p.Hkv;
+  if (W == 0) return;
+  const int64_t x_begin = cta_begin(W, p.n_ctas, blockIdx.x);
+  const int64_t x_end = cta_begin(W, p.n_ctas, blockIdx.x + 1);
+  const int total = (int)(x_end - x_begin);
+
+  // chunk index (page * Hkv + head) of the CTA's page q, -1 for a page id out of range
+  auto coord = [&](int q) -> int {
+    const int64_t xq = x_begin + q;
+    int lo = 0, hi = p.B;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if ((int64_t)pre[mid] * p.Hkv <= xq) lo = mid; else hi = mid;
+    }
+    const int pages = pre[lo + 1] - pre[lo];
+    const int64_t off = xq - (int64_t)pre[lo] * p.Hkv;
+    const int h = (int)(off / pages), pi = (int)(off % pages);
+    const int page = __ldg(p.bt + (int64_t)lo * p.max_pages + pi);
+    return (page < 0 || page >= p.num_pages) ? -1 : page * p.Hkv + h;
+  };
+  // one thread: load the CTA's page q into its stage
+  auto issue = [&](int q) {
+    const int s = q % S;
+    const int z = coord(q);
+    const uint32_t fb = smem_u32(&full_bar[s]);
+    if (z < 0) {
+      stage_ok[s] = 0;
+      flag(p.status, NK_DEVFLAG_BAD_PAGE);
+      mbar_arrive(fb);
+      return;
+    }
+    stage_ok[s] = 1;
+    mbar_arrive_expect_tx(fb, (uint32_t)chunk);
+    bulk_load(smem_u32(smem + (size_t)s * chunk), p.pool + (int64_t)z * chunk, (uint32_t)chunk, fb);
+  };
+  int issued = 0, waited = 0;
+  if (tid == 0)
+    for (; issued < total && issued < S; ++issued) issue(issued);
+
+  const int nsub = kRkWarps / T;
+  const bool active = w < nsub * T;
+  const int t = w % T, sub = w / T;
+  const int kpw = (p.P + nsub - 1) / nsub;
+  const int kgrp = (lane * CPL) / kGroup, vgrp = (lane * CPL) / kRkVGroup;
+  int q = 0;  // the CTA's page number
+  int64_t x = x_begin;
+  Segment seg;
+  while (next_segment(sh, pre, x, x_end, seg)) {
+    const int L = p.ctx[seg.b] - p.trim;
+    const int last = L - T + t;  // last key visible to column t
+    float qf[GM][CPL], o[GM][CPL], m[GM], l[GM];
+#pragma unroll
+    for (int hg = 0; hg < GM; ++hg) {
+      m[hg] = -INFINITY;
+      l[hg] = 0.f;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) { o[hg][j] = 0.f; qf[hg][j] = 0.f; }
+      if (hg < G) {
+        const uint16_t* qr = p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * D + lane * CPL;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) qf[hg][j] = __uint_as_float((uint32_t)__ldg(qr + j) << 16);
+      }
+#pragma unroll
+      for (int h = 1; h < CPL; h <<= 1)
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+          if ((j & h) == 0) {
+            const float a = qf[hg][j], b = qf[hg][j + h];
+            qf[hg][j] = a + b;
+            qf[hg][j + h] = a - b;
+          }
+#pragma unroll
+      for (int lb = 1; lb < LPG; lb <<= 1) {
+        const bool upper = (lane & lb) != 0;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const float other = __shfl_xor_sync(0xffffffffu, qf[hg][j], lb);
+          qf[hg][j] = upper ? other - qf[hg][j] : qf[hg][j] + other;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) qf[hg][j] *= 0.125f;
+    }
+    for (int pi = seg.page_begin; pi < seg.page_end; ++pi, ++q) {
+      const int s = q % S;
+      bool ok = false;
+      if (!abort_flag) {
+        ok = mbar_wait(smem_u32(&full_bar[s]), (uint32_t)(q / S) & 1u);
+        if (ok) {
+          ++waited;
+        } else {
+          flag(p.status, NK_DEVFLAG_TIMEOUT);
+          abort_flag = 1;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);  // the warp's shuffles below run only if every lane has the page
+      const int k_lo = sub * kpw;
+      int k_hi = min(p.P, k_lo + kpw);
+      k_hi = min(k_hi, last - pi * p.P + 1);
+      if (active && ok && stage_ok[s] && k_lo < k_hi) {
+        const uint8_t* st = smem + (size_t)s * chunk;
+        const __half* ks_s = reinterpret_cast<const __half*>(st + p.lay.ks);
+        const __half* vs_s = reinterpret_cast<const __half*>(st + p.lay.vs);
+        for (int k0 = k_lo; k0 < k_hi; k0 += 4) {
+          const int nk = min(4, k_hi - k0);
+          RkRaw<CPL> raw[4];
+          float sc[4][GM], vsc[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int k = k0 + (j < nk ? j : nk - 1);  // a repeated key is never used
+            raw[j] = rk_load_shared<CPL>(st + k * D + lane * CPL, st + p.lay.vc + k * (D / 2) + lane * (CPL / 2));
+            const float ks = __half2float(ks_s[k * (D / kGroup) + kgrp]);
+            vsc[j] = __half2float(vs_s[k * (D / kRkVGroup) + vgrp]);
+            float kf[CPL];
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) kf[i] = (float)(int8_t)(raw[j].k[i / 4] >> (8 * (i % 4)));
+#pragma unroll
+            for (int hg = 0; hg < GM; ++hg) {
+              float acc = 0.f;
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) acc = fmaf(qf[hg][i], kf[i], acc);
+              sc[j][hg] = acc * ks;
+            }
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+              for (int hg = 0; hg < GM; ++hg) sc[j][hg] += __shfl_xor_sync(0xffffffffu, sc[j][hg], off);
+#pragma unroll
+          for (int hg = 0; hg < GM; ++hg) {
+            if (hg >= G) break;
+            float mx = m[hg];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              sc[j][hg] *= p.scale2;
+              if (j < nk) mx = fmaxf(mx, sc[j][hg]);
+            }
+            if (mx > m[hg]) {
+              const float alpha = exp2f(m[hg] - mx);  // 0 while the row is empty
+              l[hg] *= alpha;
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) o[hg][i] *= alpha;
+              m[hg] = mx;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j >= nk) break;
+            float vf[CPL];
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) vf[i] = (float)((int32_t)(raw[j].v << (28 - 4 * i)) >> 28);
+#pragma unroll
+            for (int hg = 0; hg < GM; ++hg) {
+              if (hg >= G) break;
+              const float pw = exp2f(sc[j][hg] - m[hg]);
+              l[hg] += pw;
+              const float pv = pw * vsc[j];
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) o[hg][i] = fmaf(pv, vf[i], o[hg][i]);
+            }
+          }
+        }
+      }
+      __syncthreads();  // every warp is done with stage s
+      if (tid == 0 && !abort_flag && issued < total) {
+        // generic-proxy reads of the stage are ordered before the bulk copy that refills it
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(issued);
+        ++issued;
+      }
+    }
+    // merge the nsub warps of each column (as in the unstaged kernel)
+#pragma unroll
+    for (int hg = 0; hg < GM; ++hg) {
+      if (hg >= G) break;
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) red_o[(w * GM + hg) * D + lane * CPL + j] = o[hg][j];
+      if (lane == 0) {
+        red_m[w * GM + hg] = active ? m[hg] : -INFINITY;
+        red_l[w * GM + hg] = active ? l[hg] : 0.f;
+      }
+    }
+    __syncthreads();
+    const int seg_slot = blockIdx.x + seg.u;
+    for (int i = tid; i < M * D; i += blockDim.x) {
+      const int r = i / D, c = i % D;
+      const int tt = r / G, hg = r % G;
+      float mx = -INFINITY;
+      for (int sb = 0; sb < nsub; ++sb) mx = fmaxf(mx, red_m[(sb * T + tt) * GM + hg]);
+      float lsum = 0.f, acc = 0.f;
+      if (mx != -INFINITY) {
+        for (int sb = 0; sb < nsub; ++sb) {
+          const int ww = sb * T + tt;
+          const float mw = red_m[ww * GM + hg];
+          if (mw == -INFINITY) continue;
+          const float f = exp2f(mw - mx);
+          lsum += red_l[ww * GM + hg] * f;
+          acc += red_o[(ww * GM + hg) * D + c] * f;
+        }
+      }
+      const float val = lsum > 0.f ? acc / lsum : 0.f;
+      if (seg.whole) {
+        p.out[(((int64_t)seg.b * p.qT + tt) * p.Hq + seg.h * G + hg) * D + c] = f32_to_bf16(val);
+      } else {
+        p.part_o[((int64_t)seg_slot * M + r) * D + c] = val;
+        if (c == 0) p.part_lse[(int64_t)seg_slot * M + r] = lsum > 0.f ? (mx + log2f(lsum)) * kLn2 : -INFINITY;
+      }
+    }
+    __syncthreads();
+  }
+  // after a timed-out wait: let the copies still in flight land before the CTA exits
+  if (tid == 0)
+    for (int qq = waited; qq < issued; ++qq) (void)mbar_wait(smem_u32(&full_bar[qq % S]), (uint32_t)(qq / S) & 1u);
+}
+
 static size_t rk_smem(int D, int G) { return (size_t)kRkWarps * G * (D + 2) * sizeof(float); }
 
 int decode_rk8v4_ctas_per_sm(int D, int G) {
@@ -454,7 +742,30 @@ static cudaError_t launch_rk_t(const DecodeParams& p, size_t smem, cudaStream_t 
   return launch_chained(decode_rk8v4_kernel<CPL>, dim3(p.n_ctas), dim3(256), smem, stream, p);
 }
 
+template <int CPL, int GM>
+static cudaError_t launch_rk_staged(const DecodeParams& p, int S, cudaStream_t stream) {
+  const size_t smem = (size_t)S * p.lay.chunk + rk_staged_fixed_bytes(CPL * 32, GM);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_rk8v4_staged_kernel<CPL, GM>), (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_chained(decode_rk8v4_staged_kernel<CPL, GM>, dim3(p.n_ctas), dim3(256), smem, stream, p, S);
+}
+
+template <int CPL>
+static cudaError_t launch_rk_staged_g(const DecodeParams& p, int S, cudaStream_t stream) {
+  if (p.G <= 2) return launch_rk_staged<CPL, 2>(p, S, stream);
+  if (p.G <= 6) return launch_rk_staged<CPL, 6>(p, S, stream);
+  return launch_rk_staged<CPL, 8>(p, S, stream);
+}
+
 cudaError_t launch_decode_rk8v4(const DecodeParams& p, cudaStream_t stream) {
+  const int GM = p.G <= 2 ? 2 : (p.G <= 6 ? 6 : 8);
+  const int S = rk_staged_stages((int)p.lay.chunk, p.D, GM);
+  if (S >= 3) {
+    if (p.D == 256) return launch_rk_staged_g<8>(p, S, stream);
+    if (p.D == 128) return launch_rk_staged_g<4>(p, S, stream);
+    return launch_rk_staged_g<2>(p, S, stream);
+  }
+  // pages too large for a ring of three: the unstaged kernel
   const size_t smem = rk_smem(p.D, p.G);
   if (p.D == 256) return launch_rk_t<8>(p, smem, stream);
   if (p.D == 128) return launch_rk_t<4>(p, smem, stream);

@@ -67,6 +67,7 @@ CASES = {
     "d256_g8_t2": (2, 2, 16, 2, 256, 16, [90, 333]),
     "d256_g6_t12": (2, 12, 24, 4, 256, 64, [12, 640]),  # two column chunks
     "d64_g1_t16": (1, 16, 4, 4, 64, 16, [400]),
+    "d256_p256": (2, 2, 12, 2, 256, 256, [300, 1100]),  # pages too large for the staged kernel's ring
 }
 
 
