@@ -213,9 +213,10 @@ cudaError_t launch_rk8v4_append(int sms, const nk_kv_pool& pool, const int32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// Decode attention. Same structure as the INT8 CUDA-core kernel: each CTA
-// walks its segments of (sequence, kv-head, page) items; warp w serves query
-// column t = w % T for pages sub, sub + nsub, ...; lane l owns channels
+// Decode attention, unstaged form (used where pages are too large for the
+// staged kernel's ring, below). Same structure as the INT8 CUDA-core kernel:
+// each CTA walks its segments of (sequence, kv-head, page) items; warp w
+// serves query column t = w % T for pages sub, sub + nsub, ...; lane l owns channels
 // [l CPL, (l + 1) CPL). The query rows are rotated once per segment (the
 // butterflies of the channel bits a lane holds in registers, then those of the
 // lane bits by shuffles); per key a warp forms the G dot products with the
