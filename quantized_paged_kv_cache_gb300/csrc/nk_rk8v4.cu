@@ -459,8 +459,9 @@ __global__ void __launch_bounds__(256) decode_rk8v4_kernel(const DecodeParams p)
 // Staged decode, used wherever the ring below holds at least three pages. The
 // CTA walks the same segments, but every (page, kv-head) chunk -- contiguous,
 // 26,112 bytes at P = 64, D = 256 -- arrives in a shared-memory ring through
-// one bulk asynchronous copy issued S pages ahead by one thread, and all the
-// warps of the CTA work on the same page: warp w takes query column
+// one bulk asynchronous copy, issued when the last of the 8 warps releases
+// the stage S pages earlier, and all the warps of the CTA work on the same
+// pages (each may run up to S pages ahead of the others): warp w takes query column
 // t = w % T and keys [sub KPW, (sub + 1) KPW) of the page (sub = w / T, KPW =
 // P / (8 / T) rounded up). Keys are taken four at a time: the four keys' warp
 // reductions are independent, so their shuffles overlap, and a row's running
@@ -489,7 +490,9 @@ __global__ void __launch_bounds__(256, 1) decode_rk8v4_staged_kernel(const Decod
   __shared__ int warp_tot[8];
   __shared__ int stage_ok[kRkMaxStages];
   __shared__ __align__(8) uint64_t full_bar[kRkMaxStages];
-  __shared__ int abort_flag;
+  __shared__ __align__(8) uint64_t empty_bar[kRkMaxStages];  // the 8 warps are done with the stage
+  __shared__ int rel_cnt[kRkMaxStages];
+  __shared__ volatile int abort_flag;
   constexpr int D = CPL * 32;
   constexpr int LPG = kGroup / CPL;  // lanes per 64-channel group
   const int G = p.G, T = p.T, M = G * T;
@@ -500,7 +503,11 @@ __global__ void __launch_bounds__(256, 1) decode_rk8v4_staged_kernel(const Decod
   float* red_m = red_o + kRkWarps * GM * D;                            // [8][GM]
   float* red_l = red_m + kRkWarps * GM;                                // [8][GM]
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), kRkWarps);
+      rel_cnt[s] = 0;
+    }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -541,9 +548,9 @@ __global__ void __launch_bounds__(256, 1) decode_rk8v4_staged_kernel(const Decod
     mbar_arrive_expect_tx(fb, (uint32_t)chunk);
     bulk_load(smem_u32(smem + (size_t)s * chunk), p.pool + (int64_t)z * chunk, (uint32_t)chunk, fb);
   };
-  int issued = 0, waited = 0;
+  int waited = 0;
   if (tid == 0)
-    for (; issued < total && issued < S; ++issued) issue(issued);
+    for (int q0 = 0; q0 < total && q0 < S; ++q0) issue(q0);
 
   const int nsub = kRkWarps / T;
   const bool active = w < nsub * T;
@@ -671,12 +678,25 @@ __global__ void __launch_bounds__(256, 1) decode_rk8v4_staged_kernel(const Decod
           }
         }
       }
-      __syncthreads();  // every warp is done with stage s
-      if (tid == 0 && !abort_flag && issued < total) {
-        // generic-proxy reads of the stage are ordered before the bulk copy that refills it
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(issued);
-        ++issued;
+      // this warp is done with stage s; the last of the 8 warps to release it
+      // loads page q + S into it (warps run up to S pages apart)
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&empty_bar[s]));
+        if (atomicAdd(&rel_cnt[s], 1) == kRkWarps - 1) {
+          rel_cnt[s] = 0;
+          const int qn = q + S;
+          if (qn < total && !abort_flag) {
+            if (mbar_wait(smem_u32(&empty_bar[s]), (uint32_t)(q / S) & 1u)) {
+              // generic-proxy reads of the stage are ordered before the bulk copy that refills it
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              issue(qn);
+            } else {
+              flag(p.status, NK_DEVFLAG_TIMEOUT);
+              abort_flag = 1;
+            }
+          }
+        }
       }
     }
     // merge the nsub warps of each column (as in the unstaged kernel)
@@ -718,9 +738,13 @@ __global__ void __launch_bounds__(256, 1) decode_rk8v4_staged_kernel(const Decod
     }
     __syncthreads();
   }
-  // after a timed-out wait: let the copies still in flight land before the CTA exits
-  if (tid == 0)
-    for (int qq = waited; qq < issued; ++qq) (void)mbar_wait(smem_u32(&full_bar[qq % S]), (uint32_t)(qq / S) & 1u);
+  // after a timed-out wait: let the copies that may still be in flight land
+  // before the CTA exits (a page is issued only once page - S is released,
+  // so at most S pages past the last one waited for)
+  if (tid == 0) {
+    const int end = min(total, waited + S);
+    for (int qq = waited; qq < end; ++qq) (void)mbar_wait(smem_u32(&full_bar[qq % S]), (uint32_t)(qq / S) & 1u);
+  }
 }
 
 static size_t rk_smem(int D, int G) { return (size_t)kRkWarps * G * (D + 2) * sizeof(float); }
