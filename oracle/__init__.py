@@ -70,6 +70,13 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_rk_attention_row.restype = I
     L.oracle_rk_paged_attention.argtypes = [P, I, I, I, I, P, I, P, I, I, I, P, D, P, P]
     L.oracle_rk_paged_attention.restype = I
+    L.oracle_i8h_quantize_group.argtypes, L.oracle_i8h_quantize_group.restype = [P, P], U16
+    L.oracle_i8h_chunk_bytes.argtypes, L.oracle_i8h_chunk_bytes.restype = [I, I], Z
+    L.oracle_bf16kv_chunk_bytes.argtypes, L.oracle_bf16kv_chunk_bytes.restype = [I, I], Z
+    L.oracle_fmt_append.argtypes = [I, P, I, I, I, I, P, I, P, P, I, P, P]
+    L.oracle_fmt_append.restype = I
+    L.oracle_fmt_paged_attention.argtypes = [I, P, I, I, I, I, P, I, P, I, I, I, P, D, P, P]
+    L.oracle_fmt_paged_attention.restype = I
     return L
 
 
@@ -336,3 +343,54 @@ def rk_chunk_view(pool: np.ndarray, num_pages, page_size, num_kv_heads, head_dim
     vc = c[:, :, o2:o3].reshape(num_pages, num_kv_heads, P, D // 2)
     vs = c[:, :, o3:].copy().view(np.uint16).reshape(num_pages, num_kv_heads, P, D // 32)
     return kc, ks, vc, vs
+
+
+# ---------------------------------------------------------------------------
+# The pages' own INT8 layout (fp16 scales) and the bf16 baseline (oracle.h)
+# ---------------------------------------------------------------------------
+FORMATS = {"int8_f16": 1, "bf16": 2}
+
+
+def i8h_quantize_group(x_bits) -> tuple[np.ndarray, int]:
+    """64 bf16 values -> (int8 codes, fp16 scale bits)."""
+    x = _bits(x_bits).reshape(-1)
+    assert x.size == 64
+    q = np.empty(64, dtype=np.int8)
+    sb = lib().oracle_i8h_quantize_group(_ptr(x), _ptr(q))
+    return q, int(sb)
+
+
+def fmt_chunk_bytes(fmt: str, page_size: int, head_dim: int) -> int:
+    f = lib().oracle_i8h_chunk_bytes if fmt == "int8_f16" else lib().oracle_bf16kv_chunk_bytes
+    return int(f(page_size, head_dim))
+
+
+def fmt_new_pool(fmt: str, num_pages, page_size, num_kv_heads, head_dim, fill: int = 0) -> np.ndarray:
+    return np.full(num_pages * num_kv_heads * fmt_chunk_bytes(fmt, page_size, head_dim), fill, dtype=np.uint8)
+
+
+def fmt_append(fmt: str, pool: np.ndarray, num_pages, page_size, num_kv_heads, head_dim, block_table,
+               start_pos, cu_new, k, v) -> int:
+    bt = i32(block_table)
+    sp, cu = i32(start_pos), i32(cu_new)
+    kb, vb = _bits(k), _bits(v)
+    assert pool.dtype == np.uint8 and pool.size >= num_pages * num_kv_heads * fmt_chunk_bytes(fmt, page_size, head_dim)
+    B = sp.size
+    assert cu.size == B + 1 and kb.size == int(cu[-1]) * num_kv_heads * head_dim and vb.size == kb.size
+    max_pages = bt.shape[1] if bt.ndim == 2 else bt.size // max(B, 1)
+    return lib().oracle_fmt_append(FORMATS[fmt], _ptr(pool), num_pages, page_size, num_kv_heads, head_dim,
+                                   _ptr(bt), max_pages, _ptr(sp), _ptr(cu), B, _ptr(kb), _ptr(vb))
+
+
+def fmt_paged_attention(fmt: str, pool, num_pages, page_size, num_kv_heads, head_dim, block_table, ctx_lens, q,
+                        T, num_q_heads, sm_scale, want_lse=False):
+    bt, cl, qb = i32(block_table), i32(ctx_lens), _bits(q)
+    B = cl.size
+    out = np.empty((B, T, num_q_heads, head_dim), dtype=np.float64)
+    lse = np.empty((B, T, num_q_heads), dtype=np.float64)
+    rc = lib().oracle_fmt_paged_attention(FORMATS[fmt], _ptr(pool), num_pages, page_size, num_kv_heads, head_dim,
+                                          _ptr(bt), bt.shape[1], _ptr(cl), B, T, num_q_heads, _ptr(qb),
+                                          float(sm_scale), _ptr(out), _ptr(lse))
+    if rc:
+        raise ValueError(f"oracle_fmt_paged_attention: {rc} rows with out-of-range data")
+    return (out, lse) if want_lse else out

@@ -494,6 +494,134 @@ int oracle_rk_paged_attention(const uint8_t* pool, int num_pages, int page_size,
   return bad;
 }
 
+/* ===========================================================================
+ * The pages' own INT8 layout (fp16 scales) and the bf16 baseline; readings
+ * in oracle.h.
+ * ======================================================================== */
+
+uint16_t oracle_i8h_quantize_group(const uint16_t* x, int8_t* q) {
+  /* the rule of the rk8v4 keys (fp16 scale of absmax / 127, fp32 quotients),
+   * applied to the bf16 values as they are: no rotation */
+  float y[GROUP];
+  for (int i = 0; i < GROUP; ++i) y[i] = (float)oracle_bf16_to_double(x[i]);
+  return oracle_rk_quantize_k(y, q);
+}
+
+size_t oracle_i8h_chunk_bytes(int page_size, int head_dim) {
+  size_t P = (size_t)page_size, D = (size_t)head_dim;
+  return 2 * (P * D + P * (D / GROUP) * 2);
+}
+
+size_t oracle_bf16kv_chunk_bytes(int page_size, int head_dim) {
+  return 2 * (size_t)page_size * (size_t)head_dim * 2;
+}
+
+static size_t fmt_chunk_bytes(int fmt, int P, int D) {
+  return fmt == 1 ? oracle_i8h_chunk_bytes(P, D) : oracle_bf16kv_chunk_bytes(P, D);
+}
+
+int oracle_fmt_append(int fmt, uint8_t* pool, int num_pages, int page_size, int num_kv_heads, int head_dim,
+                      const int32_t* block_table, int max_pages, const int32_t* start_pos,
+                      const int32_t* cu_new, int B, const uint16_t* k, const uint16_t* v) {
+  const int P = page_size, D = head_dim, H = num_kv_heads, g = D / GROUP;
+  const int total = cu_new[B];
+  int bad = 0;
+#pragma omp parallel for schedule(static) reduction(+ : bad)
+  for (int j = 0; j < total; ++j) {
+    int b = 0;
+    while (b + 1 <= B && cu_new[b + 1] <= j) ++b;
+    long pos = (long)start_pos[b] + (j - cu_new[b]);
+    if (pos < 0 || pos >= (long)max_pages * P) { ++bad; continue; }
+    int page = block_table[(size_t)b * max_pages + pos / P];
+    if (page < 0 || page >= num_pages) { ++bad; continue; }
+    int slot = (int)(pos % P);
+    for (int h = 0; h < H; ++h) {
+      uint8_t* base = pool + ((size_t)page * H + h) * fmt_chunk_bytes(fmt, P, D);
+      const uint16_t* krow = k + ((size_t)j * H + h) * D;
+      const uint16_t* vrow = v + ((size_t)j * H + h) * D;
+      if (fmt == 1) {
+        /* Kc | Ks | Vc | Vs */
+        const size_t half = (size_t)P * D + (size_t)P * g * 2;
+        for (int gr = 0; gr < g; ++gr) {
+          uint16_t sk = oracle_i8h_quantize_group(krow + gr * GROUP, (int8_t*)(base + (size_t)slot * D + gr * GROUP));
+          uint16_t sv = oracle_i8h_quantize_group(vrow + gr * GROUP,
+                                                  (int8_t*)(base + half + (size_t)slot * D + gr * GROUP));
+          memcpy(base + (size_t)P * D + ((size_t)slot * g + gr) * 2, &sk, 2);
+          memcpy(base + half + (size_t)P * D + ((size_t)slot * g + gr) * 2, &sv, 2);
+        }
+      } else {
+        /* K | V, the bf16 rows as they are */
+        memcpy(base + (size_t)slot * D * 2, krow, (size_t)D * 2);
+        memcpy(base + (size_t)P * D * 2 + (size_t)slot * D * 2, vrow, (size_t)D * 2);
+      }
+    }
+  }
+  return bad;
+}
+
+/* dequantized (or widened) K and V value of channel ch of a key's slot */
+static double fmt_kv(int fmt, const uint8_t* base, int P, int D, int slot, int ch, int want_v) {
+  if (fmt == 1) {
+    const size_t g = (size_t)D / GROUP, half = (size_t)P * D + (size_t)P * g * 2;
+    const uint8_t* part = base + (want_v ? half : 0);
+    uint16_t sb;
+    memcpy(&sb, part + (size_t)P * D + ((size_t)slot * g + ch / GROUP) * 2, 2);
+    return (double)(int8_t)part[(size_t)slot * D + ch] * oracle_f16_to_double(sb);
+  }
+  uint16_t bits;
+  memcpy(&bits, base + (want_v ? (size_t)P * D * 2 : 0) + ((size_t)slot * D + ch) * 2, 2);
+  return oracle_bf16_to_double(bits);
+}
+
+int oracle_fmt_paged_attention(int fmt, const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                               int head_dim, const int32_t* block_table, int max_pages,
+                               const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                               const uint16_t* q, double sm_scale, double* out, double* lse) {
+  const int P = page_size, D = head_dim, Hq = num_q_heads, H = num_kv_heads;
+  const long rows = (long)B * T * Hq;
+  int bad = 0;
+  if (Hq % H != 0) return (int)rows;
+  const int G = Hq / H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+  for (long r = 0; r < rows; ++r) {
+    const int i = (int)(r % Hq), t = (int)((r / Hq) % T), b = (int)(r / ((long)Hq * T));
+    const int h = i / G;
+    double* o = out + (size_t)r * D;
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    if (lse) lse[r] = -INFINITY;
+    const long L = ctx_lens[b];
+    if (L < T || L > (long)max_pages * P) { ++bad; continue; }
+    const long n1 = L - T + t + 1; /* keys 0 .. L - T + t are visible */
+    const uint16_t* qrow = q + (((size_t)b * T + t) * Hq + i) * D;
+    double* z = (double*)malloc(sizeof(double) * (size_t)n1);
+    if (!z) { ++bad; continue; }
+    int err = 0;
+    for (long n = 0; n < n1 && !err; ++n) {
+      const int page = block_table[(size_t)b * max_pages + n / P];
+      if (page < 0 || page >= num_pages) { err = 1; break; }
+      const uint8_t* base = pool + ((size_t)page * H + h) * fmt_chunk_bytes(fmt, P, D);
+      double dot = 0.0;
+      for (int ch = 0; ch < D; ++ch) dot += oracle_bf16_to_double(qrow[ch]) * fmt_kv(fmt, base, P, D, (int)(n % P), ch, 0);
+      z[n] = sm_scale * dot;
+    }
+    if (err) { free(z); ++bad; continue; }
+    double m = -INFINITY;
+    for (long n = 0; n < n1; ++n) if (z[n] > m) m = z[n];
+    double l = 0.0;
+    for (long n = 0; n < n1; ++n) {
+      const double w = exp(z[n] - m);
+      const int page = block_table[(size_t)b * max_pages + n / P];
+      const uint8_t* base = pool + ((size_t)page * H + h) * fmt_chunk_bytes(fmt, P, D);
+      for (int ch = 0; ch < D; ++ch) o[ch] += w * fmt_kv(fmt, base, P, D, (int)(n % P), ch, 1);
+      l += w;
+    }
+    for (int ch = 0; ch < D; ++ch) o[ch] /= l;
+    if (lse) lse[r] = m + log(l);
+    free(z);
+  }
+  return bad;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -147,6 +147,37 @@ int oracle_rk_paged_attention(const uint8_t* pool, int num_pages, int page_size,
                               const int32_t* ctx_lens, int B, int T, int num_q_heads,
                               const uint16_t* q, double sm_scale, double* out, double* lse);
 
+/* ---------------------------------------------------------------------------
+ * The pages' own INT8 layout ("NInfer-3090" README, "Choosing a KV format":
+ * int8 at 33,792 bytes per token on the 27B model = 16 layers x 4 kv-heads x
+ * (2 x 256 codes + 2 x 4 two-byte scales)): INT8 group-64 codes for K and V
+ * with fp16 scales, no rotation. Readings: s = RN_fp16(absmax / 127), 1 when
+ * that is 0 and 65504 past the fp16 maximum (as rk8v4's keys);
+ * q = clamp(round_half_even(fp32(x / s)), -127, 127).
+ * Chunk per (page, kv-head): Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D] int8 | Vs[P][D/64] fp16
+ *
+ * And the unquantized baseline the same table lists (bf16, 65,536 bytes per
+ * token): chunk per (page, kv-head) K[P][D] bf16 | V[P][D] bf16.
+ * ------------------------------------------------------------------------- */
+
+/* One group of 64 bf16 values -> 64 codes; returns the fp16 scale bits. */
+uint16_t oracle_i8h_quantize_group(const uint16_t* x, int8_t* q);
+size_t oracle_i8h_chunk_bytes(int page_size, int head_dim);
+size_t oracle_bf16kv_chunk_bytes(int page_size, int head_dim);
+
+/* kv_cache_append into a pool of the given format (1 = INT8 with fp16
+ * scales, 2 = bf16); arguments and result as oracle_kv_append. */
+int oracle_fmt_append(int fmt, uint8_t* pool, int num_pages, int page_size, int num_kv_heads, int head_dim,
+                      const int32_t* block_table, int max_pages, const int32_t* start_pos,
+                      const int32_t* cu_new, int B, const uint16_t* k, const uint16_t* v);
+
+/* Attention over a pool of the given format (1 or 2); arguments and results
+ * as oracle_paged_attention. */
+int oracle_fmt_paged_attention(int fmt, const uint8_t* pool, int num_pages, int page_size, int num_kv_heads,
+                               int head_dim, const int32_t* block_table, int max_pages,
+                               const int32_t* ctx_lens, int B, int T, int num_q_heads,
+                               const uint16_t* q, double sm_scale, double* out, double* lse);
+
 /* Threads the oracle's parallel loops use. */
 int oracle_num_threads(void);
 

@@ -4,7 +4,7 @@ Each mutant below is oracle.c with one plausible mistake planted in it: a
 dropped term, a wrong sign, rounding rule or bound, a wrong or transposed
 index (page, slot, group, head, query row), a swapped operand. Every mutant is
 compiled into a library of its own, and the oracle pins (the quantizer,
-attention and rk8v4 test files) run against it in a child process; each mutant must be
+attention, rk8v4 and formats test files) run against it in a child process; each mutant must be
 caught, i.e. make at least one pin fail, while the unaltered source, built the
 same way, passes all of them. The mistakes are planted in copies in a
 temporary directory: oracle.c itself is never changed.
@@ -29,11 +29,13 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = ["tests/test_oracle_quantize.py", "tests/test_oracle_attention.py", "tests/test_oracle_rk8v4.py"]
+PINS = ["tests/test_oracle_quantize.py", "tests/test_oracle_attention.py", "tests/test_oracle_rk8v4.py",
+        "tests/test_oracle_formats.py"]
 
 # (name, section, [(text in oracle.c, replacement), ...]); each text occurs
 # exactly once in its section of oracle.c: "int8" (the INT8 group-64 format,
-# the combine and the shared helpers) or "rk8v4" (the part from its banner on).
+# the combine and the shared helpers), "rk8v4" (from its banner to the next),
+# "formats" (the INT8 layout with fp16 scales and the bf16 layout).
 MUTANTS = [
     # quantizer
     ("scale divides by 128", "int8", [("(float)(a / 127.0)", "(float)(a / 128.0)")]),
@@ -141,6 +143,21 @@ MUTANTS = [
     ("rk8v4: softmax scale dropped", "rk8v4", [("z[n - n0] = sm_scale * dot;", "z[n - n0] = dot;")]),
     ("rk8v4: output not normalized", "rk8v4", [("for (int ch = 0; ch < D; ++ch) o[ch] /= l;", "")]),
     ("rk8v4: LSE without the max", "rk8v4", [("*lse = m + log(l);", "*lse = log(l);")]),
+    # the INT8 layout with fp16 scales and the bf16 layout
+    ("int8_f16: scales indexed per 32 channels", "formats",
+     [("((size_t)slot * g + ch / GROUP) * 2, 2);", "((size_t)slot * g + ch / 32) * 2, 2);")]),
+    ("int8_f16: V codes read from the K half", "formats",
+     [("const uint8_t* part = base + (want_v ? half : 0);", "const uint8_t* part = base;")]),
+    ("int8_f16: V scale stored over the K scale", "formats",
+     [("memcpy(base + half + (size_t)P * D + ((size_t)slot * g + gr) * 2, &sv, 2);",
+       "memcpy(base + (size_t)P * D + ((size_t)slot * g + gr) * 2, &sv, 2);")]),
+    ("bf16: V read from the K rows", "formats",
+     [("memcpy(&bits, base + (want_v ? (size_t)P * D * 2 : 0) + ((size_t)slot * D + ch) * 2, 2);",
+       "memcpy(&bits, base + ((size_t)slot * D + ch) * 2, 2);")]),
+    ("formats: q-head i reads kv-head i mod Hkv", "formats", [("const int h = i / G;", "const int h = i % H;")]),
+    ("formats: causal limit one key short", "formats",
+     [("const long n1 = L - T + t + 1;", "const long n1 = L - T + t;")]),
+    ("formats: output not normalized", "formats", [("for (int ch = 0; ch < D; ++ch) o[ch] /= l;", "")]),
 ]
 
 RUNNER = (
@@ -155,17 +172,20 @@ def _source() -> str:
         return f.read()
 
 
-RK_BANNER = "/* ===========================================================================\n * rk8v4"
+BANNERS = {
+    "rk8v4": "/* ===========================================================================\n * rk8v4",
+    "formats": "/* ===========================================================================\n * The pages' own INT8",
+}
 
 
 def _mutate(src: str, section: str, edits) -> str:
-    cut = src.index(RK_BANNER)
-    head, tail = src[:cut], src[cut:]
-    part = head if section == "int8" else tail
+    cuts = [0, src.index(BANNERS["rk8v4"]), src.index(BANNERS["formats"]), len(src)]
+    k = {"int8": 0, "rk8v4": 1, "formats": 2}[section]
+    head, part, tail = src[:cuts[k]], src[cuts[k]:cuts[k + 1]], src[cuts[k + 1]:]
     for old, new in edits:
         assert part.count(old) == 1, f"mutation anchor not unique or missing in {section}: {old!r}"
         part = part.replace(old, new)
-    return part + tail if section == "int8" else head + part
+    return head + part + tail
 
 
 def _build_and_run(src: str, workdir: str, tag: str):
