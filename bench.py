@@ -41,8 +41,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c1_decode",
-                    help="tiny | c1_decode | c8_verify | long_context | mix | c8_decode | c1_rk8v4")
+    ap.add_argument("--config", default="mix",
+                    help="mix (default: the largest single-GPU configuration, 8 x 1,024-row append + C8 x T4 "
+                         "attention at 131,072) | tiny | c1_decode | c8_verify | long_context | c8_decode | c1_rk8v4")
     ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -170,6 +171,13 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
                       for _ in range(replicas - 1)]
     starts, _ = wl.history_and_step(w)
     k, v, sp, cu = wl.append_batch(w, starts, [w.append_len] * w.B, device=device)
+    # copies of the append's bf16 input, rotated step by step like the pool,
+    # so that the append reads rows that are not in L2 (when they are large
+    # enough for that to matter)
+    in_bytes = 2 * k.numel() * k.element_size()
+    n_in = 1 if in_bytes >= 2 * L2_BYTES or in_bytes < 2 ** 20 else min(16, int(-(-2 * L2_BYTES // in_bytes)) + 1)
+    ks = [k] + [k.clone() for _ in range(n_in - 1)]
+    vs = [v] + [v.clone() for _ in range(n_in - 1)]
     q = wl.queries(w, device=device)
     nct = num_ctas
     ws_bytes = nk.decode_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D, nct)
@@ -178,8 +186,8 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
     torch.cuda.synchronize()
     if int(status.item()) != 0:
         raise RuntimeError(f"history append flagged device status {int(status.item())}")
-    return dict(bt=bt, ctx=ctx, status=status, pools=pools, k=k, v=v, sp=sp.to(device), cu=cu.to(device), q=q,
-                ws=ws, out=out, nct=nct, kernel=kernel, append=append)
+    return dict(bt=bt, ctx=ctx, status=status, pools=pools, k=k, v=v, ks=ks, vs=vs, n_in=n_in, sp=sp.to(device),
+                cu=cu.to(device), q=q, ws=ws, out=out, nct=nct, kernel=kernel, append=append)
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -227,12 +235,13 @@ def run_ours(args, w, rank, world, device):
 
     def step(i, what="step"):
         pool = S["pools"][i % replicas]
+        k, v = S["ks"][i % S["n_in"]], S["vs"][i % S["n_in"]]
         if what == "step" and one_call_step(args, w):  # append + attention in one call
-            nk.decode_step(pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], S["q"], S["ctx"], w.sm_scale, w.max_ctx,
+            nk.decode_step(pool, S["bt"], S["sp"], S["cu"], k, v, S["q"], S["ctx"], w.sm_scale, w.max_ctx,
                            num_ctas=S["nct"], workspace=S["ws"], out=S["out"], status=S["status"], stream=stream)
             return
         if what != "attn":
-            S["append"](pool, S["bt"], S["sp"], S["cu"], S["k"], S["v"], status=S["status"], stream=stream)
+            S["append"](pool, S["bt"], S["sp"], S["cu"], k, v, status=S["status"], stream=stream)
         if what != "append":
             dec(pool, S["q"], S["bt"], S["ctx"], w.sm_scale, w.max_ctx, num_ctas=S["nct"], workspace=S["ws"],
                 out=S["out"], status=S["status"], stream=stream)
@@ -291,7 +300,8 @@ def run_ours(args, w, rank, world, device):
         e2e = run_e2e(args, w, S, dec, replicas, step_bytes, world, device)
 
     return dict(ms=ms, attn_ms=attn_ms, append_ms=append_ms, clocks=clocks, step_bytes=step_bytes, replicas=replicas,
-                pool_bytes=pool_bytes, e2e=e2e, nct=S["nct"])
+                pool_bytes=pool_bytes, e2e=e2e, nct=S["nct"], n_in=S["n_in"],
+                in_bytes=2 * S["k"].numel() * S["k"].element_size())
 
 
 def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
@@ -501,6 +511,9 @@ def main():
     gbs = job_gbs(r["step_bytes"], r["ms"], world)
     l2 = (f"rotating {r['replicas']} pool copies ({r['replicas'] * r['pool_bytes'] / 2**20:.0f} MiB) > 2x L2"
           if r["replicas"] > 1 else f"pool {r['pool_bytes'] / 2**20:.0f} MiB > 2x L2")
+    if r["n_in"] > 1:
+        l2 += (f"; append input rotated over {r['n_in']} copies "
+               f"({r['n_in'] * r['in_bytes'] / 2**20:.0f} MiB) > 2x L2")
     out = {
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms"], 6), "higher_is_better": True, "scaling": "weak",

@@ -105,7 +105,12 @@ typedef struct nk_kv_pool {
   int32_t head_dim;     /* D: 64, 128 or 256 */
 } nk_kv_pool;
 
-/* Bytes of one (page, kv-head) chunk, and of a whole pool. 0 for bad sizes. */
+/* Bytes of one (page, kv-head) chunk, and of a whole pool. 0 for bad sizes.
+ * The pages size the INT8 cache per token ("NInfer-3090" README, "Choosing a
+ * KV format": 33,792 bytes per token on the 27B model, 16 attention layers x 4
+ * kv-heads x (2 x 256 codes + 2 x 4 two-byte scales)); this layout stores the
+ * same codes with four-byte scales, 544 bytes per (token, kv-head) at D = 256
+ * (2 x D codes + 2 x D/64 scales), and pads nothing. */
 size_t nk_kv_chunk_bytes(int32_t page_size, int32_t head_dim);
 size_t nk_kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
 
@@ -128,18 +133,35 @@ int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t
                  const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream);
 
 /*
- * Work split of nk_paged_decode_attn. The flat list of (sequence, kv-head,
- * page) items is cut into `num_ctas` near-equal contiguous ranges, one per
- * CTA; each (CTA, (sequence, kv-head)) overlap produces one partial result,
- * so there are at most num_ctas + B*Hkv - 1 partials. num_ctas <= 0 picks the
- * default (a multiple of the device's SM count, capped by the work).
+ * Work split of nk_paged_decode_attn (the pages describe no split; attention
+ * re-reads the whole cache every step -- "NInfer-3090" README, "Choosing a KV
+ * format" -- so the cache of one step is cut into page ranges that run in
+ * parallel, flash-decoding style). The flat list of (sequence, kv-head, page)
+ * items is cut into `num_splits` near-equal contiguous ranges, one per CTA;
+ * each (CTA, (sequence, kv-head)) overlap produces one partial result, so
+ * there are at most num_splits + B*Hkv - 1 partials. A "split" is one such CTA
+ * range. num_splits <= 0 (the num_ctas argument of the calls below) picks the
+ * default: a multiple of the device's SM count (of Hkv for one sequence),
+ * capped by the number of items. Host arithmetic only; returns >= 1.
+ * nk_decode_default_ctas is the same function under its earlier name.
  */
+int32_t nk_decode_default_splits(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size);
 int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size);
 
-/* Workspace bytes nk_paged_decode_attn needs for this shape and CTA count:
- * fp32 partial outputs [num_ctas + B*Hkv][T*G][D] and their LSEs. */
+/*
+ * Workspace bytes nk_paged_decode_attn needs for this shape and split count
+ * (num_splits <= 0: room for the default). The workspace is the pair of
+ * split-partial arrays, back to back:
+ *   part_o   fp32 [S][T*G][D]  at byte 0 (each partial normalized by its own
+ *                              softmax sum),
+ *   part_lse fp32 [S][T*G]     right after part_o (natural-log LSE of the
+ *                              partial's scaled scores, -inf when empty),
+ * with S = num_splits + B*Hkv partial slots and G = Hq / Hkv; the row of
+ * query column t, q-head h*G + g is t*G + g. They are what nk_attn_combine
+ * merges. The total is rounded up to 256 bytes. 0 for bad sizes.
+ */
 size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int32_t num_kv_heads,
-                                 int32_t head_dim, int32_t num_ctas);
+                                 int32_t head_dim, int32_t num_splits);
 
 /*
  * nk_paged_decode_attn -- split-KV GQA attention over the paged cache.
@@ -243,7 +265,11 @@ int nk_rk8v4_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_
  * optional status word; the arguments mean what they mean for
  * nk_paged_decode_attn.
  *   - The first call on a device looks up the array's device address once
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     (cudaGetSymbolAddress) and keeps it until the process exits; make that
+ *     first call before any stream capture. A call with B = 0 does only this
+ *     set-up (nothing is launched, and the other arguments are not read), so
+ *     it serves as the warm-up. Do not use the entry point on a device across
+ *     a cudaDeviceReset of that device.
  *   - Returns NK_ERR_WORKSPACE when nk_decode_workspace_bytes() for this shape
  *     and CTA count exceeds NK_NOALLOC_MAX_WORKSPACE.
  *   - All calls on a device share the array and it keeps the last call's
@@ -257,7 +283,12 @@ int nk_paged_decode_attn_noalloc(const nk_kv_pool* pool, const void* q_dev, cons
                                  void* out_dev, int32_t* status_dev, void* stream);
 
 /*
- * nk_attn_combine -- log-sum-exp merge of S partial results.
+ * nk_attn_combine -- log-sum-exp merge of S partial results. The pages give
+ * attention over the whole cache ("NInfer-3090" README, "Choosing a KV
+ * format") but no split or merge; this is the exact re-join of a softmax
+ * computed over disjoint key ranges: with l_s the softmax sum of range s,
+ * sum_s l_s O_s / sum_s l_s is the attention over the union, and
+ * lse_s = m_s + ln l_s carries l_s up to a common factor.
  *   part_o_dev    fp32 [S][R][D]: each partial normalized by its own softmax sum
  *   part_lse_dev  fp32 [S][R]: natural-log LSE of the partial's scaled scores,
  *                 -inf for a partial that saw no key (weight 0)

@@ -21,7 +21,7 @@ GROUP = 64
 MAX_T = 16
 
 __all__ = [
-    "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_ctas",
+    "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_splits", "decode_default_ctas",
     "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "paged_decode_attn_noalloc",
     "attn_combine", "status_string", "decode_step", "rk8v4_chunk_bytes", "rk8v4_pool_bytes", "rk8v4_append",
     "rk8v4_decode_attn",
@@ -120,7 +120,13 @@ def kv_append(pool: KVPool, block_table, start_pos, cu_new, k, v, status=None, s
     _check(rc, "nk_kv_append")
 
 
+def decode_default_splits(B: int, num_kv_heads: int, max_ctx: int, page_size: int) -> int:
+    """Default split (CTA) count of the decode calls (nk_decode_default_splits)."""
+    return int(lib().nk_decode_default_splits(B, num_kv_heads, max_ctx, page_size))
+
+
 def decode_default_ctas(B: int, num_kv_heads: int, max_ctx: int, page_size: int) -> int:
+    """The same count under its earlier name (nk_decode_default_ctas)."""
     return int(lib().nk_decode_default_ctas(B, num_kv_heads, max_ctx, page_size))
 
 

@@ -39,6 +39,7 @@ EXPORTS = (
     "nk_kv_chunk_bytes",
     "nk_kv_pool_bytes",
     "nk_kv_append",
+    "nk_decode_default_splits",
     "nk_decode_default_ctas",
     "nk_decode_workspace_bytes",
     "nk_paged_decode_attn",
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
             L.nk_kv_pool_bytes.argtypes, L.nk_kv_pool_bytes.restype = [I32, I32, I32, I32], Z
             L.nk_kv_append.argtypes = [pool_p, P, I32, P, P, I32, I32, P, P, P, P]
             L.nk_kv_append.restype = ctypes.c_int
+            L.nk_decode_default_splits.argtypes, L.nk_decode_default_splits.restype = [I32, I32, I32, I32], I32
             L.nk_decode_default_ctas.argtypes, L.nk_decode_default_ctas.restype = [I32, I32, I32, I32], I32
             L.nk_decode_workspace_bytes.argtypes = [I32, I32, I32, I32, I32, I32]
             L.nk_decode_workspace_bytes.restype = Z

@@ -254,9 +254,14 @@ int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32
   return launch_decode(p, Path::kTensor, st);
 }
 
-int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {
+int32_t nk_decode_default_splits(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {
   if (B < 1 || num_kv_heads < 1 || max_ctx < 1 || page_size < 1) return 1;
+  // one CTA per SM: the tensor-core kernels' residency (decode_mma_ctas_per_sm)
   return default_ctas(B, num_kv_heads, max_ctx, page_size, 1);
+}
+
+int32_t nk_decode_default_ctas(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {
+  return nk_decode_default_splits(B, num_kv_heads, max_ctx, page_size);
 }
 
 size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,

@@ -29,7 +29,9 @@ std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 
 // Device address of the array on the current device; looked up once per
-// device (the first call on a device does it).
+// device (the first call on a device does it) and kept until the process
+// exits, so the entry point must not be used across a cudaDeviceReset of that
+// device (the module would be reloaded at another address).
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -56,16 +58,15 @@ extern "C" int nk_paged_decode_attn_noalloc(const nk_kv_pool* pool, const void* 
                                             const int32_t* ctx_lens_dev, int32_t B, int32_t T, int32_t num_q_heads,
                                             float sm_scale, int32_t max_ctx, int32_t num_ctas, void* out_dev,
                                             int32_t* status_dev, void* stream) {
-  if (!pool) return NK_ERR_NULL;
-  if (B < 0 || T < 1 || num_q_heads < 1 || pool->num_kv_heads < 1 || pool->page_size < 1) return NK_ERR_SHAPE;
-  if (B == 0) return NK_OK;
-  // Fix the CTA count here so the scratch size is known before launching.
-  int32_t n = num_ctas > 0 ? num_ctas : nk_decode_default_ctas(B, pool->num_kv_heads, max_ctx, pool->page_size);
-  const size_t need = nk_decode_workspace_bytes(B, T, num_q_heads, pool->num_kv_heads, pool->head_dim, n);
-  if (need > kStaticBytes) return NK_ERR_WORKSPACE;
+  // The address lookup comes first, so that a call with B = 0 (which
+  // launches nothing) sets up the current device ahead of a stream capture.
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != NK_OK) return rc;
+  if (B == 0) return NK_OK;
+  // The regular entry point checks the arguments, picks the same default
+  // split count and returns NK_ERR_WORKSPACE when the partials of this shape
+  // do not fit the array.
   return nk_paged_decode_attn(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads,
-                              sm_scale, max_ctx, n, scratch, kStaticBytes, out_dev, status_dev, stream);
+                              sm_scale, max_ctx, num_ctas, scratch, kStaticBytes, out_dev, status_dev, stream);
 }

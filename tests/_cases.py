@@ -78,22 +78,42 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
+# Elements that needed the |O| >= 2 allowance of compare(), reported at the
+# end of the run (tests/conftest.py): [count, largest |O|, largest error].
+WIDE = {"elements": 0, "compared": 0, "max_abs_o": 0.0, "max_err": 0.0, "calls": []}
+
+
 def compare(gpu_bf16: torch.Tensor, ref64: np.ndarray, what=""):
-    """Tolerance of the attention output against the oracle's fp64 result
-    rounded to bf16 (ties to even): relative L2 <= 1e-3, and every element
-    within 4e-3 -- or within one bf16 ulp of the reference where that ulp is
-    larger (|O| >= 1, reached only by short contexts), since a bf16 output
-    that differs from the rounded reference differs by at least one ulp."""
+    """Tolerance of a bf16 attention output against the oracle:
+    * every element within 4e-3 of the oracle's unrounded fp64 result. A bf16
+      number can be that close only where half a bf16 ulp is below 4e-3,
+      i.e. |O| < 2; at |O| >= 2 an element may differ by half an ulp (the
+      rounding no bf16 output avoids) plus 4e-3. Those elements are counted
+      and reported at the end of the run, with their largest magnitude;
+    * relative L2 <= 1e-3 against the fp64 result rounded to bf16 (ties to
+      even): bf16 rounding alone gives ~1.6e-3 against the unrounded result,
+      so that is not the bar for the L2 norm."""
+    ref64 = np.asarray(ref64, dtype=np.float64)
     ref = oracle.bits_to_double(oracle.round_bf16(ref64))
     g = gpu_bf16.to(torch.float64).cpu().numpy().reshape(ref.shape)
+    x = ref64.reshape(ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite output"
-    err = np.abs(g - ref)
-    allow = np.maximum(ABS_TOL, bf16_ulp(ref))
-    maxabs = float(err.max())
-    worst = float((err / allow).max())
+    err = np.abs(g - x)
+    wide = np.abs(x) >= 2.0
+    allow = np.where(wide, 0.5 * bf16_ulp(x) + ABS_TOL, ABS_TOL)
+    maxabs = float(err.max()) if err.size else 0.0
+    worst = float((err / allow).max()) if err.size else 0.0
     rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300))
-    rel_exact = float(np.linalg.norm(g - ref64.reshape(ref.shape)) / max(np.linalg.norm(ref64), 1e-300))
-    assert worst <= 1.0, f"{what}: max-abs {maxabs:.3e} exceeds max(4e-3, 1 ulp) (ratio {worst:.2f})"
+    rel_exact = float(np.linalg.norm(g - x) / max(np.linalg.norm(x), 1e-300))
+    nwide = int(wide.sum())
+    WIDE["compared"] += int(err.size)
+    if nwide:
+        WIDE["elements"] += nwide
+        WIDE["max_abs_o"] = max(WIDE["max_abs_o"], float(np.abs(x[wide]).max()))
+        WIDE["max_err"] = max(WIDE["max_err"], float(err[wide].max()))
+        WIDE["calls"].append(what)
+    assert worst <= 1.0, (f"{what}: max-abs {maxabs:.3e} vs the unrounded oracle exceeds 4e-3 "
+                          f"(|O| >= 2: half an ulp + 4e-3) (ratio {worst:.2f})")
     assert rel <= REL_L2_TOL, f"{what}: rel-L2 {rel:.3e} > {REL_L2_TOL} (vs unrounded fp64: {rel_exact:.3e})"
     return maxabs, rel, rel_exact
 

@@ -29,3 +29,16 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """How many compared attention elements needed the |O| >= 2 allowance
+    (half a bf16 ulp + 4e-3 against the unrounded oracle)."""
+    mod = sys.modules.get("_cases")
+    if mod is None or not mod.WIDE["compared"]:
+        return
+    w = mod.WIDE
+    terminalreporter.write_line(
+        f"attention tolerance: {w['elements']} of {w['compared']} compared elements had |O| >= 2 and were held to "
+        f"half a bf16 ulp + 4e-3 (largest |O| {w['max_abs_o']:.3f}, largest error {w['max_err']:.3e}); "
+        f"all others to 4e-3 against the unrounded fp64 oracle")

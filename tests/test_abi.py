@@ -174,3 +174,19 @@ def test_pool_format_is_checked_by_the_binding():
             p.need(other)
     with pytest.raises(ValueError):
         nk.KVPool.empty(1, 16, 1, 64, device="cpu", fmt="fp8")
+
+
+def test_noalloc_array_size_matches_the_header():
+    src = open(os.path.join(ROOT, "include", "nk.h")).read()
+    m = re.search(r"#define\s+NK_NOALLOC_MAX_WORKSPACE\s+\((\d+)u\s*<<\s*(\d+)\)", src)
+    assert m, "NK_NOALLOC_MAX_WORKSPACE not found in nk.h"
+    assert nk.NOALLOC_MAX_WORKSPACE == int(m.group(1)) << int(m.group(2))
+
+
+def test_default_splits_is_exported_under_both_names():
+    L = nk.lib()
+    for args in [(1, 4, 32768, 64), (8, 4, 65536, 64), (1, 1, 256, 16), (3, 2, 17, 16)]:
+        n = L.nk_decode_default_splits(*args)
+        assert n == L.nk_decode_default_ctas(*args) == nk.decode_default_splits(*args)
+        assert 1 <= n <= args[0] * args[1] * ((args[2] + args[3] - 1) // args[3])
+    assert L.nk_decode_default_splits(0, 4, 100, 16) == 1
