@@ -250,7 +250,7 @@ def f16_to_double(bits: int) -> float:
 
 
 def rk_rotate64(x_bits) -> np.ndarray:
-    """R x (fp32, the append's butterfly order) of one 64-channel bf16 group."""
+    """R x of one 64-channel bf16 group: RN_fp32 of the exact H64 x / 8."""
     x = _bits(x_bits).reshape(-1)
     assert x.size == 64
     y = np.empty(64, dtype=np.float32)

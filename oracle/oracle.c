@@ -276,18 +276,79 @@ double oracle_f16_to_double(uint16_t bits) {
   return (bits & 0x8000) ? -v : v;
 }
 
+/* The rotation of one key group, y = RN_fp32(H64 x / 8), follows its plain
+ * definition: each output is the exact signed sum of the 64 inputs, rounded
+ * once to fp32 (round to nearest, ties to even).
+ *
+ * Exact sum. A finite bf16 value is an integer multiple of 2^-133 (the
+ * subnormal quantum): 128 + m times 2^(e - 1) units for a normal pattern
+ * (exponent field e, 7-bit fraction m), m units for a subnormal one. The
+ * multiples are added as base-2^16 digits held in 64-bit cells, so that no
+ * partial sum is ever rounded (|x| < 2^128 and 64 terms need fewer than 268
+ * bits; RK_DIGITS digits hold 320). */
+#define RK_DIGITS 20
+
+static void rk_add_term(int64_t* acc, uint16_t bits, int negate) {
+  const int e = (bits >> 7) & 0xff, m = bits & 0x7f;
+  const int64_t units = e == 0 ? m : 128 + m; /* times 2^shift units of 2^-133 */
+  const int shift = e == 0 ? 0 : e - 1;
+  const int64_t v = units << (shift % 16);     /* below 2^23 */
+  const int64_t sgn = ((bits & 0x8000) != 0) != (negate != 0) ? -1 : 1;
+  acc[shift / 16] += sgn * (v % 65536);
+  acc[shift / 16 + 1] += sgn * (v / 65536);
+}
+
+/* Carry every cell into the next one, so that cells 0 .. RK_DIGITS-2 lie in
+ * [0, 2^16) and the last one holds the sign of the whole number. */
+static void rk_carry(int64_t* acc) {
+  for (int k = 0; k < RK_DIGITS - 1; ++k) {
+    int64_t c = acc[k] / 65536;
+    if (acc[k] - c * 65536 < 0) c -= 1; /* floor division */
+    acc[k] -= c * 65536;
+    acc[k + 1] += c;
+  }
+}
+
+static int rk_bit(const int64_t* mag, int pos) {
+  return pos < 0 ? 0 : (int)((mag[pos / 16] >> (pos % 16)) & 1);
+}
+
+/* RN_fp32(S * 2^-136) for the integer S held in acc: 2^-133 units, and the
+ * 1/8 of the rotation. */
+static float rk_round_fp32(int64_t* acc) {
+  rk_carry(acc);
+  const int negative = acc[RK_DIGITS - 1] < 0;
+  if (negative) {
+    for (int k = 0; k < RK_DIGITS; ++k) acc[k] = -acc[k];
+    rk_carry(acc);
+  }
+  int top = -1; /* position of the leading 1 bit of |S| */
+  for (int pos = 16 * RK_DIGITS - 1; pos >= 0 && top < 0; --pos)
+    if (rk_bit(acc, pos)) top = pos;
+  if (top < 0) return 0.0f;
+  double mant = 0.0; /* the 24 leading bits (all of them when there are fewer) */
+  const int low = top - 23 > 0 ? top - 23 : 0;
+  for (int pos = top; pos >= low; --pos) mant = 2.0 * mant + rk_bit(acc, pos);
+  if (top >= 24) {
+    const int guard = rk_bit(acc, low - 1);
+    int sticky = 0;
+    for (int pos = 0; pos < low - 1; ++pos) sticky |= rk_bit(acc, pos);
+    if (guard && (sticky || fmod(mant, 2.0) == 1.0)) mant += 1.0; /* half up only to even */
+  }
+  /* mant * 2^(low - 136) is exact in double and, by construction, an fp32
+   * number (or past the fp32 range, which converts to infinity) */
+  const double y = ldexp(mant, low - 136);
+  if (y >= ldexp(1.0, 128)) return negative ? -INFINITY : INFINITY;
+  return (float)(negative ? -y : y);
+}
+
 void oracle_rk_rotate64(const uint16_t* x, float* y) {
-  float t[GROUP];
-  for (int i = 0; i < GROUP; ++i) t[i] = (float)oracle_bf16_to_double(x[i]);
-  /* butterflies over index bit 0, then 1, ..., 5; every add rounds to fp32 */
-  for (int h = 1; h < GROUP; h <<= 1)
-    for (int i = 0; i < GROUP; ++i)
-      if ((i & h) == 0) {
-        const float a = t[i], b = t[i + h];
-        t[i] = a + b;
-        t[i + h] = a - b;
-      }
-  for (int i = 0; i < GROUP; ++i) y[i] = t[i] * 0.125f;
+  for (int r = 0; r < GROUP; ++r) {
+    int64_t acc[RK_DIGITS];
+    for (int k = 0; k < RK_DIGITS; ++k) acc[k] = 0;
+    for (int j = 0; j < GROUP; ++j) rk_add_term(acc, x[j], __builtin_popcount((unsigned)(r & j)) & 1);
+    y[r] = rk_round_fp32(acc);
+  }
 }
 
 /* fp16 scale bits for a group absmax a and code bound qmax: RN_fp16(a / qmax),

@@ -101,9 +101,10 @@ void oracle_combine(const float* part_o, const float* part_lse, int S, int R, in
  *   rotation R = H64 / 8 per 64-channel group (Sylvester order,
  *     H[i][j] = (-1)^popcount(i & j); orthonormal and its own inverse), so
  *     q . k = (R q) . (R k);
- *   at append R k is evaluated in fp32 as butterflies (a + b, a - b) over
- *     index bits 0, 1, ..., 5 in that order, rounding after every add, then
- *     times 1/8 -- the precision in which the kernel takes the code decision;
+ *   at append R k is taken as its plain definition: every output is the
+ *     exact sum of the 64 signed inputs divided by 8, rounded once to fp32
+ *     (round to nearest, ties to even; past the fp32 range it is infinite);
+ *     inputs are finite bf16 values;
  *   key scale  s = RN_fp16(absmax(R k) / 127), value scale s = RN_fp16(absmax(v) / 7);
  *     s = 1 when it rounds to 0 (absmax = 0 or below the fp16 range), and
  *     s = 65504 when it rounds past the fp16 maximum;
@@ -120,7 +121,7 @@ void oracle_combine(const float* part_o, const float* part_lse, int S, int R, in
 uint16_t oracle_double_to_f16(double x);
 /* Exact widening of an fp16 bit pattern. */
 double oracle_f16_to_double(uint16_t bits);
-/* R x of one 64-channel group of bf16 values, in the fp32 order above. */
+/* R x of one 64-channel group of bf16 values: RN_fp32 of the exact H64 x / 8. */
 void oracle_rk_rotate64(const uint16_t* x, float* y);
 /* Key group: 64 rotated fp32 values -> 64 codes; returns the fp16 scale bits. */
 uint16_t oracle_rk_quantize_k(const float* y, int8_t* q);

@@ -32,6 +32,15 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PINS = ["tests/test_oracle_quantize.py", "tests/test_oracle_attention.py", "tests/test_oracle_rk8v4.py",
         "tests/test_oracle_formats.py"]
 
+ROT_LINE = ("for (int j = 0; j < GROUP; ++j) rk_add_term(acc, x[j], __builtin_popcount((unsigned)(r & j)) & 1);\n"
+            "    y[r] = rk_round_fp32(acc);")
+# the whole transform in fp32 butterflies, every add rounded, then x 1/8
+FP32_BUTTERFLIES = ("float t[GROUP];\n    for (int i = 0; i < GROUP; ++i) t[i] = (float)oracle_bf16_to_double(x[i]);\n"
+                    "    for (int h = {first}; {cond}; {step})\n"
+                    "      for (int i = 0; i < GROUP; ++i)\n"
+                    "        if ((i & h) == 0) {{ const float a = t[i], b = t[i + h]; t[i] = a + b; t[i + h] = a - b; }}\n"
+                    "    y[r] = t[r] * 0.125f; (void)acc;")
+
 # (name, section, [(text in oracle.c, replacement), ...]); each text occurs
 # exactly once in its section of oracle.c: "int8" (the INT8 group-64 format,
 # the combine and the shared helpers), "rk8v4" (from its banner to the next),
@@ -107,8 +116,20 @@ MUTANTS = [
      [("r = ldexp(nearbyint(ldexp(a, 11 - e)), e - 11);", "r = ldexp(nearbyint(ldexp(a, 10 - e)), e - 10);")]),
     ("fp16 subnormal quantum 2^-23", "rk8v4",
      [("r = nearbyint(ldexp(a, 24)) * ldexp(1.0, -24);", "r = nearbyint(ldexp(a, 23)) * ldexp(1.0, -23);")]),
-    ("rotation without the 1/8", "rk8v4", [("y[i] = t[i] * 0.125f;", "y[i] = t[i];")]),
-    ("rotation butterfly with the difference reversed", "rk8v4", [("t[i + h] = a - b;", "t[i + h] = b - a;")]),
+    ("rotation without the 1/8", "rk8v4", [("ldexp(mant, low - 136)", "ldexp(mant, low - 133)")]),
+    ("rotation sign from r | j", "rk8v4",
+     [("rk_add_term(acc, x[j], __builtin_popcount((unsigned)(r & j)) & 1)",
+       "rk_add_term(acc, x[j], __builtin_popcount((unsigned)(r | j)) & 1)")]),
+    ("rotation as fp32 butterflies over bits 0..5", "rk8v4", [(ROT_LINE, FP32_BUTTERFLIES.format(first="1", step="h <<= 1", cond="h < GROUP"))]),
+    ("rotation as fp32 butterflies over bits 5..0", "rk8v4", [(ROT_LINE, FP32_BUTTERFLIES.format(first="GROUP / 2", step="h >>= 1", cond="h >= 1"))]),
+    ("rotation summed in fp64, then rounded", "rk8v4",
+     [(ROT_LINE, "double s = 0.0;\n    for (int j = 0; j < GROUP; ++j) { const double v = oracle_bf16_to_double(x[j]); "
+                 "s += (__builtin_popcount((unsigned)(r & j)) & 1) ? -v : v; }\n    y[r] = (float)(s / 8.0);")]),
+    ("rotation rounding ignores the sticky bits", "rk8v4",
+     [("if (guard && (sticky || fmod(mant, 2.0) == 1.0)) mant += 1.0;", "if (guard && fmod(mant, 2.0) == 1.0) mant += 1.0;")]),
+    ("rotation rounds ties away from zero", "rk8v4",
+     [("if (guard && (sticky || fmod(mant, 2.0) == 1.0)) mant += 1.0;", "if (guard) mant += 1.0;")]),
+    ("rotation carries truncate instead of floor", "rk8v4", [("if (acc[k] - c * 65536 < 0) c -= 1;", "")]),
     ("keys stored unrotated", "rk8v4",
      [("oracle_rk_rotate64(krow + gr * GROUP, y);",
        "for (int ii = 0; ii < GROUP; ++ii) y[ii] = (float)oracle_bf16_to_double(krow[gr * GROUP + ii]);")]),

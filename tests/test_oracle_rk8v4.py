@@ -11,6 +11,7 @@ two non-zero entries, values q * 2^-e with |q| <= 7), plus closed forms and
 invariances of attention.
 """
 import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -59,7 +60,7 @@ def test_f16_rounding_against_numpy():
 # ---------------------------------------------------------------- rotation
 
 def test_rotation_is_scaled_hadamard_on_exact_inputs():
-    """Small integers: every fp32 butterfly is exact, so R x = H64 x / 8 exactly."""
+    """Small integers: every partial sum is exact, so R x = H64 x / 8 exactly."""
     rng = np.random.default_rng(4)
     for _ in range(200):
         x = rng.integers(-100, 101, 64).astype(np.float64) * 2.0 ** int(rng.integers(-20, 20))
@@ -67,18 +68,125 @@ def test_rotation_is_scaled_hadamard_on_exact_inputs():
         np.testing.assert_array_equal(y.astype(np.float64), H64 @ x / 8.0)
 
 
-def test_rotation_error_bound_on_general_inputs():
-    """bf16 inputs of mixed magnitude: six rounded stages stay within
-    6 * 2^-24 * sum|x| / 8 of the exact transform, and R is its own inverse
-    within the same order of error."""
+def exponent_span(x) -> int:
+    """Binades between the smallest and the largest non-zero |x| (bf16)."""
+    e = np.floor(np.log2(np.abs(x[x != 0])))
+    return int(e.max() - e.min()) if e.size else 0
+
+
+def test_rotation_rounds_once_on_general_inputs():
+    """bf16 inputs of mixed magnitude within 30 binades: each partial sum of
+    H64 x is an integer multiple of the smallest input's quantum below 2^53
+    of it, so scipy's Hadamard matrix times x in fp64 is exact, / 8 is exact,
+    and one rounding to float32 is the definition. Bit for bit equal -- a
+    rotation that rounds in between (fp32 butterflies in any order) differs
+    on most of these groups."""
     rng = np.random.default_rng(5)
-    for _ in range(300):
-        x = bf16(rng.standard_normal(64) * 10.0 ** rng.uniform(-3, 3, 64))
-        y = oracle.rk_rotate64(to_bits(x)).astype(np.float64)
-        exact = H64 @ x / 8.0
-        bound = 6 * 2.0 ** -24 * np.abs(x).sum() / 8.0
-        assert np.all(np.abs(y - exact) <= bound)
-        np.testing.assert_allclose(H64 @ exact / 8.0, x, rtol=0, atol=1e-12 * np.abs(x).max())
+    differs_from_fp32_butterflies = 0
+    for _ in range(400):
+        x = bf16(rng.choice([-1.0, 1.0], 64) * rng.uniform(1.0, 2.0, 64) * 2.0 ** rng.uniform(-15, 15, 64))
+        x[rng.random(64) < 0.05] = 0.0
+        assert exponent_span(x) <= 38
+        y = oracle.rk_rotate64(to_bits(x))
+        ref = (H64 @ x / 8.0).astype(np.float32)
+        np.testing.assert_array_equal(y, ref)
+        t = x.astype(np.float32)
+        h = 1
+        while h < 64:
+            for i in range(64):
+                if i & h == 0:
+                    t[i], t[i + h] = t[i] + t[i + h], t[i] - t[i + h]
+            h <<= 1
+        differs_from_fp32_butterflies += int(np.any(t * np.float32(0.125) != ref))
+    assert differs_from_fp32_butterflies > 300
+
+
+def fraction_to_f32(r: Fraction) -> np.float32:
+    """Round a rational to float32: nearest, ties to even, overflow to inf."""
+    if r == 0:
+        return np.float32(0.0)
+    a = abs(r)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    assert Fraction(2) ** e <= a < Fraction(2) ** (e + 1)
+    q = max(e, -126) - 23                      # quantum of float32 at |r|
+    n = round(a / Fraction(2) ** q)            # Fraction.__round__: half to even
+    mag = n * Fraction(2) ** q
+    if mag >= Fraction(2) ** 128:
+        v = np.inf
+    else:
+        v = float(n) * 2.0 ** q                # exact: n < 2^25, q >= -149
+    return np.float32(v if r > 0 else -v)
+
+
+def rotate_exact(x_bits) -> np.ndarray:
+    """H64 x / 8 in exact rational arithmetic, rounded once to float32."""
+    xs = [Fraction(float(v)) for v in oracle.bits_to_double(np.asarray(x_bits, dtype=np.uint16))]
+    return np.array([fraction_to_f32(sum((xs[j] if H64[r, j] > 0 else -xs[j]) for j in range(64)) / 8)
+                     for r in range(64)], dtype=np.float32)
+
+
+def wide_groups():
+    """Groups whose partial sums are not exact in fp64: exponent spans of up
+    to 250 binades, exact cancellation of the large terms, bf16 subnormals,
+    sums at an fp32 tie with a tiny term deciding it, float32-subnormal and
+    overflowing results."""
+    rng = np.random.default_rng(11)
+    gs = []
+    for _ in range(40):  # random magnitudes over the whole bf16 range
+        gs.append(bf16(rng.standard_normal(64) * 2.0 ** rng.uniform(-130, 125, 64)))
+    for _ in range(20):  # two clusters far apart
+        x = rng.standard_normal(64) * 2.0 ** 60
+        x[rng.random(64) < 0.5] *= 2.0 ** -110
+        gs.append(bf16(x))
+    big = 2.0 ** 90
+    x = np.zeros(64)
+    x[0], x[1] = big, big           # H rows with popcount(r & 1) = 1 cancel the large terms exactly
+    x[2] = 2.0 ** -100
+    x[5] = -3 * 2.0 ** -120
+    gs.append(x)
+    x = np.zeros(64)                # an fp32 tie (1 + 2^-24) decided by a term 2^-100 below it
+    x[0] = 8 * (1.0 + 2.0 ** -7)    # 1 + 2^-7 and 2^-24: bf16, and the group sums to a tie
+    x[1] = 8 * 2.0 ** -17
+    x[2] = 8 * 2.0 ** -24
+    x[3] = 8 * 2.0 ** -100
+    gs.append(bf16(x))
+    x[3] = -x[3]
+    gs.append(bf16(x))
+    x = np.zeros(64)                # exact ties with nothing below: to even, down then up
+    x[0], x[2] = 8 * (1.0 + 2.0 ** -7), 8 * 2.0 ** -24
+    gs.append(bf16(x))
+    x = np.zeros(64)
+    x[0], x[1], x[2] = 8 * (1.0 + 2.0 ** -7), 8 * 2.0 ** -23, 8 * 2.0 ** -24
+    gs.append(bf16(x))
+    gs.append(bf16(np.full(64, 2.0 ** -133)))                 # bf16 subnormals: fp32-subnormal results
+    gs.append(bf16(rng.choice([-1, 1], 64) * 2.0 ** -130))
+    gs.append(bf16(np.full(64, 3.0e38)))                      # the first output overflows float32
+    gs.append(bf16(np.r_[np.full(32, 3.0e38), np.full(32, -3.0e38)]))
+    return gs
+
+
+def test_rotation_rounds_once_on_wide_and_degenerate_groups():
+    for i, x in enumerate(wide_groups()):
+        bits = to_bits(x)
+        y = oracle.rk_rotate64(bits)
+        ref = rotate_exact(bits)
+        same = (y == ref) | (np.isnan(y) & np.isnan(ref))
+        assert same.all(), f"group {i}: outputs {np.nonzero(~same)[0][:8]} differ"
+
+
+def test_rotation_tie_cases_round_as_the_definition_says():
+    """The hand-built tie: the exact first output is 1 + 2^-24 + 2^-17 .. with
+    a 2^-100 term; with the tiny term positive it rounds up, negative down."""
+    gs = wide_groups()
+    up, down, even_dn, even_up = gs[-8], gs[-7], gs[-6], gs[-5]
+    y_up, y_dn = oracle.rk_rotate64(to_bits(up))[0], oracle.rk_rotate64(to_bits(down))[0]
+    assert float(y_up) - float(y_dn) == 2.0 ** -23 * 2.0 ** np.floor(np.log2(float(y_dn)))
+    # 1 + 2^-7 + 2^-24 is a tie whose lower neighbour is even: it stays down;
+    # 1 + 2^-7 + 2^-23 + 2^-24 lies between an odd and an even one: it goes up
+    assert float(oracle.rk_rotate64(to_bits(even_dn))[0]) == 1.0 + 2.0 ** -7
+    assert float(oracle.rk_rotate64(to_bits(even_up))[0]) == 1.0 + 2.0 ** -7 + 2.0 ** -22
 
 
 # ---------------------------------------------------------------- quantizers
