@@ -85,10 +85,11 @@ typedef enum {
 #define NK_DEVFLAG_BAD_POS 0x2u     /* append position outside the block table */
 #define NK_DEVFLAG_BAD_CTX 0x4u     /* ctx_len < T, > max_ctx or > table capacity */
 #define NK_DEVFLAG_TIMEOUT 0x8u     /* a bounded wait on an async copy gave up */
-#define NK_DEVFLAG_RANGE 0x10u      /* a Q value or an output left the fp16 range of the
-                                       tensor-core path (|Q| > 65504, or p * Vs > 65504);
-                                       rk8v4 append: a group scale saturated at the fp16
-                                       maximum, or a non-finite value */
+#define NK_DEVFLAG_RANGE 0x10u      /* attention: an output is not finite (a true fp32
+                                       overflow; the tensor-core kernels scale their fp16
+                                       operands by powers of two, so no finite bf16 input
+                                       leaves their range); rk8v4 append: a group scale
+                                       saturated at the fp16 maximum, or a non-finite value */
 
 /* Limits of this build. */
 #define NK_GROUP 64      /* channels per quantization group */
@@ -224,8 +225,8 @@ int nk_paged_decode_attn_simt(const nk_kv_pool* pool, const void* q_dev, const i
  * struct describes an rk8v4 pool; its storage is sized with
  * nk_rk8v4_pool_bytes and only the nk_rk8v4_* calls may touch it.
  * Quantization (the readings where the page is silent):
- *   keys:   y = R k in fp32, as butterflies (a + b, a - b) over the index
- *           bits 0, 1, ..., 5 in that order (every add rounded), then x 1/8;
+ *   keys:   y = R k = RN_fp32(H64 k / 8): the exact sum of the 64 signed
+ *           inputs, divided by 8 and rounded once to fp32 (ties to even);
  *           s = RN_fp16(max|y| / 127); q = clamp(rne(fp32(y / s)), -127, 127);
  *   values: s = RN_fp16(max|v| / 7);    q = clamp(rne(fp32(v / s)), -7, 7);
  *   a scale that rounds to 0 is stored as 1 (the codes are then 0); one past
@@ -303,6 +304,22 @@ const char* nk_status_string(int code);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int nk_version(void);
+
+/*
+ * nk_test_inject_copy_stall -- failure injection for tests of the bounded
+ * waits (the pages have no counterpart; nothing here faults or traps). While
+ * withheld_page >= 0, every tensor-core decode launched afterwards by this
+ * process (nk_paged_decode_attn, nk_decode_step, the no-alloc variant) never
+ * issues the page copies of its CTA page numbers >= withheld_page, and bounds
+ * each of its waits by wait_cycles SM clock cycles (0 keeps the default of
+ * about 2 s). A wait for a withheld page runs out, sets NK_DEVFLAG_TIMEOUT in
+ * the status word, and the kernel runs on without blocking, issues nothing
+ * more, lets the copies and tensor-core work it did issue complete, and
+ * returns; the outputs of the call are then unspecified and the device stays
+ * usable. withheld_page < 0 switches it off. Process-wide, not thread-safe
+ * against concurrent decode calls; for tests only.
+ */
+void nk_test_inject_copy_stall(int32_t withheld_page, uint64_t wait_cycles);
 
 #ifdef __cplusplus
 }

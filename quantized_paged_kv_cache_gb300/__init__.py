@@ -17,6 +17,7 @@ NK_DEVFLAG_BAD_PAGE = 0x1
 NK_DEVFLAG_BAD_POS = 0x2
 NK_DEVFLAG_BAD_CTX = 0x4
 NK_DEVFLAG_TIMEOUT = 0x8
+NK_DEVFLAG_RANGE = 0x10
 GROUP = 64
 MAX_T = 16
 
@@ -250,3 +251,9 @@ def attn_combine(part_o, part_lse, out=None, stream=None):
     rc = lib().nk_attn_combine(_ptr(part_o), _ptr(part_lse), S, R, D, _ptr(out), _stream(stream))
     _check(rc, "nk_attn_combine")
     return out
+
+
+def test_inject_copy_stall(withheld_page: int, wait_cycles: int = 0) -> None:
+    """nk_test_inject_copy_stall: failure injection for the bounded-wait tests
+    (withheld_page < 0 switches it off)."""
+    lib().nk_test_inject_copy_stall(int(withheld_page), int(wait_cycles))

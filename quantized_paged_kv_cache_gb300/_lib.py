@@ -53,6 +53,7 @@ EXPORTS = (
     "nk_rk8v4_decode_attn",
     "nk_status_string",
     "nk_version",
+    "nk_test_inject_copy_stall",
 )
 
 
@@ -92,6 +93,8 @@ def lib() -> ctypes.CDLL:
             L.nk_attn_combine.restype = ctypes.c_int
             L.nk_status_string.argtypes, L.nk_status_string.restype = [ctypes.c_int], ctypes.c_char_p
             L.nk_version.argtypes, L.nk_version.restype = [], ctypes.c_int
+            L.nk_test_inject_copy_stall.argtypes = [I32, ctypes.c_uint64]
+            L.nk_test_inject_copy_stall.restype = None
             _lib = L
     return _lib
 

@@ -6,6 +6,7 @@
 #include <atomic>
 
 #include "nk_decode.cuh"
+#include "nk_ptx.cuh"
 #include "nk_rk8v4.cuh"
 
 namespace nk {
@@ -19,6 +20,10 @@ using namespace nk;
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// nk_test_inject_copy_stall: withheld CTA page number (-1: none) and wait limit (0: the default)
+std::atomic<int> g_withhold{-1};
+std::atomic<unsigned long long> g_wait_cycles{0};
 
 bool pool_ok(const nk_kv_pool* pool, int* err) {
   if (!pool || !pool->base_dev) { *err = NK_ERR_NULL; return false; }
@@ -144,6 +149,9 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   p.qT = T;
   p.trim = 0;
   p.early = 0;
+  const unsigned long long wc = g_wait_cycles.load(std::memory_order_relaxed);
+  p.wait_cycles = wc > 0 ? wc : kWaitCycles;
+  p.withhold = g_withhold.load(std::memory_order_relaxed);
   *empty = false;
   return NK_OK;
 }
@@ -351,5 +359,10 @@ const char* nk_status_string(int code) {
 }
 
 int nk_version(void) { return 100; }
+
+void nk_test_inject_copy_stall(int32_t withheld_page, uint64_t wait_cycles) {
+  g_wait_cycles.store(withheld_page >= 0 ? wait_cycles : 0ull, std::memory_order_relaxed);
+  g_withhold.store(withheld_page >= 0 ? withheld_page : -1, std::memory_order_relaxed);
+}
 
 }  // extern "C"

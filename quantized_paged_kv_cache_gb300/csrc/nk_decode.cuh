@@ -34,6 +34,12 @@ struct DecodeParams {
   // are visible: the append itself waited for every earlier kernel before
   // this kernel could start.
   int early;
+  // Failure-detection tests (nk_test_inject_copy_stall): every bounded wait
+  // gives up after wait_cycles, and the page copies of CTA page numbers
+  // >= withhold are never issued (-1: all issued).
+  unsigned long long wait_cycles;
+  int withhold;
+  __host__ __device__ bool issuable(int q) const { return withhold < 0 || q < withhold; }
   __host__ __device__ SplitShape shape() const { return SplitShape{B, Hkv, P, T, max_ctx, max_pages}; }
 };
 

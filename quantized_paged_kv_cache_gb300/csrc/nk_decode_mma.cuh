@@ -86,7 +86,7 @@ __host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B
   g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
   const int mrows = NT * 8;
   g.merge_bytes = mrows * (D + 4) * 4 + 3 * nteams * mrows * 4 + mrows * 4;
-  const int pre_bytes = round_up((2 * B + 25) * 4, 16);  // pre[B+1], warp_tot, flags, lens[B]
+  const int pre_bytes = round_up((2 * B + 33) * 4, 16);  // pre[B+1], warp_tot, flags, lens[B], icnt[8]
   const int pid_bytes = 1024 * 4;
   const int fixed = g.xch_bytes + g.merge_bytes + pre_bytes + pid_bytes + 8 * 2 * 8 + 1024;
   int s = (kSmemLimit - fixed) / g.stage_bytes;
@@ -178,6 +178,52 @@ __device__ __forceinline__ void named_bar(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Range of the fp16 MMA operands. The method is scale-free: attention of Q,
+// K, V scaled by powers of two is the same attention (K) or the same output
+// scaled alike (V). fp16 is not: it has a 2^-14 .. 65504 normal range. Both
+// tensor-core kernels therefore carry powers of two beside their fp16 operands
+// and undo them in fp32, exactly:
+//   * a query row (or a warp's channel slice of it) enters the QK product as
+//     q 2^e with e chosen from its largest |q|, so that it lies in
+//     [2^14, 2^15); the row's fp32 scores are multiplied by 2^-e;
+//   * the probability-weighted value scales P' = p Vs of a 64-channel group
+//     enter the PV product as p Vs 2^-ev, and the accumulator holds O 2^-ev.
+//     ev follows the exponent E of the largest Vs of the page (or 16-key
+//     block): set at the first one and moved only when E - ev leaves
+//     [-10, 6] -- p <= 2^8 keeps p Vs 2^-ev below 2^15, the lower bound keeps
+//     the hi part of a key with p near 1 a normal fp16 number -- with the
+//     accumulator rescaled by 2^(ev_old - ev_new), like the softmax
+//     reference. The output is O 2^-ev times 2^ev.
+// ---------------------------------------------------------------------------
+// 2^e as fp32, -126 <= e <= 127.
+__device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// E with 2^E <= x < 2^(E+1) for a positive normal fp32 x (-127 for 0 and subnormals).
+__device__ __forceinline__ int exp_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xffu) - 127; }
+
+// Exponent that brings a query row whose largest |q| is m into [2^14, 2^15)
+// (0 for a zero row; at most 2^60, so rows below 2^-46 stay smaller).
+__device__ __forceinline__ int q_norm_exp(float m) {
+  if (!(m > 0.f)) return 0;
+  const int e = 14 - exp_of(m);
+  return e > 60 ? 60 : (e < -120 ? -120 : e);
+}
+
+constexpr int kEvUnset = -1000;  // no page of the segment seen yet
+
+// Moves the exponent ev of a group's P' when the page's largest value scale
+// (exponent E) leaves ev's window; beta = 2^(ev_old - ev_new) rescales the
+// accumulator (1 on the first page, whose accumulator is still zero).
+__device__ __forceinline__ bool ev_update(int& ev, int E, float& beta) {
+  if (ev != kEvUnset && E - ev <= 6 && E - ev >= -10) return false;
+  const int ne = E > 100 ? 100 : (E < -100 ? -100 : E);
+  const int d = ev == kEvUnset ? 0 : ev - ne;
+  beta = d < -126 ? 0.f : pow2i(d > 127 ? 127 : d);
+  ev = ne;
+  return true;
+}
+
 // Byte offset of (channel chunk16 `ch16`, row) inside one K|V box region of
 // a stage: boxes of 128 channels (64 for D = 64) x [K rows | V rows].
 template <int D>
@@ -267,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   volatile int* abort_flag = pre + (p.B + 1) + 8;
   int* cnt = pre + (p.B + 1) + 9;  // [8] consumer count per stage
   int* lens = pre + (p.B + 1) + 24;  // [B] context lengths
+  int* icnt = lens + p.B;            // [8] copies issued into each stage
   int* pid = reinterpret_cast<int*>(smem + geo.pid_off);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + geo.bar_off);
   uint64_t* empty_bar = full_bar + 8;
@@ -285,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), per_stage);
       cnt[s] = 0;
+      icnt[s] = 0;
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -324,11 +372,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   uint32_t bq[NT][NCH][2];
   float o[NCH][NT][4];
   float m_run[NT][2], l_run[NT][2];
+  int ev[GW];    // exponent of this warp's P' per group (kEvUnset before the segment's first block)
+  float sv[GW];  // 2^-ev
   int row_t[NT][2];  // verify column of each held row (T - 1 for padding rows)
 
   // Q fragments of this warp's channels, all rows of a segment's unit:
   // load_q fetches the raw bf16 pairs, convert_q turns them into fp16 pairs
-  // (exact for |q| in [2^-14, 65504]; larger values set NK_DEVFLAG_RANGE).
+  // scaled by a power of two per row (exact for elements within 2^31 of the
+  // row's largest).
   auto load_q = [&](const Segment& sg) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -385,19 +436,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       }
     }
   };
+  // Each warp scales its channel slice of a query row by 2^e (from the
+  // slice's largest |q|, over the four lanes that hold the row) before the
+  // fp16 conversion, and its partial scores by rsc = 2^-e.
+  float rsc[NT][2];
   auto convert_q = [&]() {
-    bool big = false;
+    float rq[NT];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NT; ++nt) {
+      float m = 0.f;
 #pragma unroll
       for (int c = 0; c < NCH; ++c)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float f0 = bf16_lo(bq[nt][c][h]), f1 = bf16_hi(bq[nt][c][h]);
-          big |= fmaxf(fabsf(f0), fabsf(f1)) > 65504.f;
-          bq[nt][c][h] = pack_f16(f0, f1);
-        }
-    if (big) flag(p.status, NK_DEVFLAG_RANGE);
+        for (int h = 0; h < 2; ++h) m = fmaxf(m, fmaxf(fabsf(bf16_lo(bq[nt][c][h])), fabsf(bf16_hi(bq[nt][c][h]))));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+      const int e = q_norm_exp(m);
+      const float qs = pow2i(e);
+      rq[nt] = pow2i(-e);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          bq[nt][c][h] = pack_f16(bf16_lo(bq[nt][c][h]) * qs, bf16_hi(bq[nt][c][h]) * qs);
+    }
+    // score rows are 2 t4 + e of each tile: their factors from the lanes holding them
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) rsc[nt][e2] = __shfl_sync(0xffffffffu, rq[nt], (2 * t4 + e2) * 4);
   };
 
   // Every global read of the prologue -- the first unit's Q (converted at
@@ -418,7 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   // copy, so the issuer is the last warp, whose first block is in page 1.
   if (tid == kThreads - 32) {
     const int n0 = total < S ? total : S;
-    for (int q = 0; q < n0; ++q) issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+    for (int q = 0; q < n0; ++q) {
+      if (!p.issuable(q)) break;
+      issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+      icnt[q] = 1;
+    }
   }
 
   const int bpp_sh = (BPP & (BPP - 1)) == 0 ? __ffs(BPP) - 1 : -1;  // blocks per page, as a shift
@@ -457,6 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[c][nt][k] = 0.f;
     }
+#pragma unroll
+    for (int gi = 0; gi < GW; ++gi) {
+      ev[gi] = kEvUnset;
+      sv[gi] = 1.f;
+    }
 
     // this team's blocks of the segment: CTA-wide block numbers jn = team,
     // team + NTEAMS, ... (4 blocks of 16 keys per 64-key page)
@@ -478,7 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       const float* ks_s = reinterpret_cast<const float*>(smem + s * geo.stage_bytes + 2 * P * D);
       const float* vs_s = ks_s + P * G_ALL;
       {
-        if (!*abort_flag && !mbar_wait(smem_u32(&full_bar[s]), par)) {
+        // after one wait of the CTA has run out, no wait blocks any more (the
+        // blocks run without data and nothing more is issued; the end of the
+        // kernel waits for the copies that were)
+        if (!*abort_flag && !mbar_wait(smem_u32(&full_bar[s]), par, p.wait_cycles)) {
           if (lane == 0) flag(p.status, NK_DEVFLAG_TIMEOUT);
           *abort_flag = 1;
         }
@@ -529,6 +608,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
               sc[nt][3] = fmaf(k1, acc[gi][nt][3], sc[nt][3]);
             }
           }
+          // undo the power of two of this warp's Q slice
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sc[nt][k] *= rsc[nt][k & 1];
 
           // ---- team exchange: every warp of the team sums the CS partials in warp order
           if constexpr (CS > 1) {
@@ -627,6 +711,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             float v1 = vs_s[(key0 + g + 8) * G_ALL + grp0 + gi];
             v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
             v1 = valid1 ? v1 : 0.f;
+            // exponent of the group's P' from the block's largest value scale
+            const uint32_t mxb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(v0, v1)));
+            float beta;
+            if (mxb != 0u && ev_update(ev[gi], exp_of(__uint_as_float(mxb)), beta)) {
+              sv[gi] = pow2i(-ev[gi]);
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) o[gi * 4 + cc][nt][k] *= beta;
+            }
+            v0 *= sv[gi];
+            v1 *= sv[gi];
             uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -667,18 +765,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
           mbar_arrive(smem_u32(&empty_bar[s]));
           if (atomicAdd(&cnt[s], 1) == per_stage - 1) {
             cnt[s] = 0;
-            // every reader arrived before its increment: the phase is complete
-            if (!mbar_wait(smem_u32(&empty_bar[s]), par)) flag(p.status, NK_DEVFLAG_TIMEOUT);
             const int qn = q + S;
-            if (qn < total)
-              issue_page<D>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
-                            smem_u32(&full_bar[s]));
+            if (qn < total && p.issuable(qn) && !*abort_flag) {
+              // every reader arrived before its increment: the phase is complete
+              if (mbar_wait(smem_u32(&empty_bar[s]), par, p.wait_cycles)) {
+                issue_page<D>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
+                              smem_u32(&full_bar[s]));
+                ++icnt[s];
+              } else {
+                flag(p.status, NK_DEVFLAG_TIMEOUT);
+                *abort_flag = 1;
+              }
+            }
           }
         }
       }
     }
 
     page_seq += seg_pages;
+
+    // the accumulators hold O 2^-ev per group: back to O
+#pragma unroll
+    for (int gi = 0; gi < GW; ++gi) {
+      if (ev[gi] == kEvUnset) continue;
+      const float f = pow2i(ev[gi]);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[gi * 4 + cc][nt][k] *= f;
+    }
 
     const bool last_seg = x >= x_end;
 
@@ -838,6 +955,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       stage_q();
       __syncthreads();
     }
+  }
+  // After a timed-out wait some copies may still be in flight: the last copy
+  // issued into each stage lands (bounded waits) before the CTA exits. Every
+  // issue came before the last merge's barriers. Without a timeout all of
+  // them were consumed already.
+  if (tid == kThreads - 32) {
+    for (int s2 = 0; s2 < S; ++s2)
+      if (icnt[s2] > 0) (void)mbar_wait(smem_u32(&full_bar[s2]), (uint32_t)(icnt[s2] - 1) & 1u, p.wait_cycles);
   }
 }
 

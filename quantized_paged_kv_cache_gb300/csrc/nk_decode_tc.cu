@@ -91,8 +91,8 @@ __host__ __device__ inline Layout layout(int W, int NT) {
   const int pbuf = 2 * NT * 8192;
   const int hdr = 512;
   const int xs = 2 * 2 * 64 * NT * 4 * 4;
-  const int red = (2 * 4 * 32 + 2 * 32) * 4 + 4 * 4 + 32 * 4 + 64;
-  const int pre = round_up((2 * kMaxBatch + 1 + 16 + 8 + 4) * 4, 16);  // pre, warp_tot, cnt, flag, lens
+  const int red = (2 * 4 * 32 + 2 * 32) * 4 + 4 * 4 + 32 * 4 + 64 + (16 + 4 + 32) * 4;
+  const int pre = round_up((2 * kMaxBatch + 1 + 16 + 8 + 4 + 9) * 4, 16);  // pre, warp_tot, cnt, flag, lens, icnt, last MMA
   const int pid = kPidCache * 4;
   const int bar = 32 * 8;
   const int fixed = qt + pbuf + hdr + xs + red + pre + pid + bar + 16;
@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   int* cnt = warp_tot + 16;  // [8]
   volatile int* abort_flag = cnt + 8;
   int* lens = cnt + 12;  // [kMaxBatch] context lengths
+  int* icnt = lens + kMaxBatch;  // [8] copies issued into each stage
   int* pid = reinterpret_cast<int*>(smem + LY.off_pid);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + LY.off_bar);
   uint64_t* empty_bar = full_bar + 8;
@@ -188,6 +189,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   float* mrow = lrow + 32;                                     // [32]
   int* sflag = reinterpret_cast<int*>(mrow + 32);              // [4]
   int* row_t = sflag + 4;                                      // [32]: query column of row n (T for padding)
+  float* pmx = reinterpret_cast<float*>(row_t + 32 + 16);      // [4 score warps][4 groups]: page's largest Vs
+  int* evs = reinterpret_cast<int*>(pmx + 16);                 // [4]: P' exponents at a segment's end
+  float* rsn = reinterpret_cast<float*>(evs + 4);              // [32]: 2^-e of each query row's Q scaling
   float* xs = reinterpret_cast<float*>(smem + LY.off_xs);      // [2 pages][2 sides][64 keys][NR]
   const uint32_t qt0 = smem_u32(smem + LY.off_qt);             // two Q tiles of 2W x 128 bytes
   uint8_t* pbuf = smem + LY.off_pbuf;                          // [2][4 g][2 h][NT][64][16 B]
@@ -204,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), kWarps);
       cnt[s] = 0;
+      icnt[s] = 0;
     }
+    icnt[8] = -1;  // last_mma
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&qk_bar[i]), 1);
       mbar_init(smem_u32(&accfree_bar[i]), kScoreWarps);
@@ -258,12 +264,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   if (p.early) chain_wait();  // the pages may hold the preceding append's rows
   if (tid == 0) {
     const int n0 = total < S ? total : S;
-    for (int q = 0; q < n0; ++q) issue_page<kD>(p, &tmap, pid[q], stage0 + q * kStageBytes, smem_u32(&full_bar[q]));
+    for (int q = 0; q < n0; ++q) {
+      if (!p.issuable(q)) break;
+      issue_page<kD>(p, &tmap, pid[q], stage0 + q * kStageBytes, smem_u32(&full_bar[q]));
+      icnt[q] = 1;
+    }
   }
 
+  // A bounded wait. After one wait of the CTA has run out (abort_flag), no
+  // wait blocks any more: every role runs through its remaining pages without
+  // data, no page is issued and no MMA started, and the end of the kernel
+  // waits for what was issued before it releases the tensor memory.
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
     if (*abort_flag) return;
-    if (!mbar_wait(smem_u32(bar), parity)) {
+    if (!mbar_wait(smem_u32(bar), parity, p.wait_cycles)) {
       if (lane == 0) flag(p.status, NK_DEVFLAG_TIMEOUT);
       *abort_flag = 1;
     }
@@ -276,14 +290,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       mbar_arrive(smem_u32(&empty_bar[s]));
       if (atomicAdd(&cnt[s], 1) == kWarps - 1) {
         cnt[s] = 0;
-        if (!mbar_wait(smem_u32(&empty_bar[s]), ph)) flag(p.status, NK_DEVFLAG_TIMEOUT);
         const int qn = q + S;
-        if (qn < total)
-          issue_page<kD>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn),
-                         stage0 + s * kStageBytes, smem_u32(&full_bar[s]));
+        if (qn < total && p.issuable(qn) && !*abort_flag) {
+          if (mbar_wait(smem_u32(&empty_bar[s]), ph, p.wait_cycles)) {
+            issue_page<kD>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn),
+                           stage0 + s * kStageBytes, smem_u32(&full_bar[s]));
+            ++icnt[s];
+          } else {
+            flag(p.status, NK_DEVFLAG_TIMEOUT);
+            *abort_flag = 1;
+          }
+        }
       }
     }
   };
+  int* last_mma = icnt + 8;  // CTA page number of the last QK MMAs issued (thread 0)
 
   int64_t x = x_begin;
   Segment seg;
@@ -304,29 +325,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       const int npages = seg.page_end - seg.page_begin;
       // the previous segment's MMAs still read the Q tiles: wait for the last one
       if (q0 > 0) wait_bar(&qk_bar[(q0 - 1) & 1], ((q0 - 1) >> 1) & 1);
-      // Q tile tb, row r: query row r % W, channels 128 (r / W) + 64 tb + [0, 64)
-      bool big = false;
-      for (int i = tid; i < 2 * 2 * W * 8; i += kConvWarps * 32) {
-        const int c = i & 7, r = (i >> 3) % (2 * W), tb = i / (2 * W * 8);
-        const int n = r % W, ch = 128 * (r / W) + 64 * tb + 8 * c;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < M) {
-          const int t = n / G, hg = n % G;
-          const uint4 raw =
-              *reinterpret_cast<const uint4*>(p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * kD + ch);
-          const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t hw[4];
+      // Q tile tb, row r: query row r % W, channels 128 (r / W) + 64 tb + [0, 64).
+      // Thread (row n, quarter qq) converts channels [64 qq, 64 qq + 64) of
+      // row n, scaled by the row's power of two (q_norm_exp over the four
+      // threads of the row), into tile qq & 1, row (qq >> 1) W + n.
+      {
+        const int n = tid >> 2, qq = tid & 3;
+        uint4 raw[8];
+        float m = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float f0 = bf16_lo(rw[j]), f1 = bf16_hi(rw[j]);
-            big |= fmaxf(fabsf(f0), fabsf(f1)) > 65504.f;
-            hw[j] = pack_f16(f0, f1);
+        for (int c = 0; c < 8; ++c) {
+          raw[c] = make_uint4(0u, 0u, 0u, 0u);
+          if (n < M) {
+            const int t = n / G, hg = n % G;
+            raw[c] = *reinterpret_cast<const uint4*>(p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * kD +
+                                                     64 * qq + 8 * c);
           }
-          v = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          const uint32_t rw[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(rw[j])), fabsf(bf16_hi(rw[j]))));
         }
-        *reinterpret_cast<uint4*>(smem + LY.off_qt + tb * (2 * W * 128) + r * 128 + ((c ^ (r & 7)) << 4)) = v;
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const float qs = pow2i(q_norm_exp(m));
+        if (n < W) {
+          const int r = (qq >> 1) * W + n, tb = qq & 1;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t rw[4] = {raw[c].x, raw[c].y, raw[c].z, raw[c].w};
+            uint32_t hw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) hw[j] = pack_f16(bf16_lo(rw[j]) * qs, bf16_hi(rw[j]) * qs);
+            *reinterpret_cast<uint4*>(smem + LY.off_qt + tb * (2 * W * 128) + r * 128 + ((c ^ (r & 7)) << 4)) =
+                make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          }
+        }
       }
-      if (big) flag(p.status, NK_DEVFLAG_RANGE);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q writes -> tensor-core reads
       named_bar(1, kConvWarps * 32);
       // the next unit's Q lines, kQAhead pages before this segment ends
@@ -364,6 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         named_bar(1, kConvWarps * 32);
         if (tid == 0) {
           wait_bar(&accfree_bar[q & 1], ((q >> 1) & 1) ^ 1);  // scores of page q - 2 read
+        }
+        if (tid == 0 && !*abort_flag) {
           tc_fence_after();
           constexpr uint32_t idesc = idesc_f16_f32(128, 2 * W);
           const uint32_t acc = tmem + kColAcc + (q & 1) * (4 * W);
@@ -374,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
               mma_tmem_a(acc + tb * (2 * W), tmem + kColA + (q & 1) * 64 + tb * 32 + ks * 8,
                          sdesc_sw128(qt0 + tb * (2 * W * 128) + ks * 32), idesc, ks > 0);
           mma_commit(smem_u32(&qk_bar[q & 1]));
+          *last_mma = q;
         }
         release_stage(q, s, ph);
         next_stage();
@@ -386,6 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // ======================= score warps: scores, softmax, P'
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
     float m_ref[NR], l_part[NR];
+    int ev[4];  // exponents of the P' of the four 64-channel groups (identical in the four warps)
+    float sv[4];
     while (next_segment(sh, pre, x, x_end, seg)) {
       const int L = lens[seg.b];
       const int npages = seg.page_end - seg.page_begin;
@@ -393,6 +432,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       for (int i = 0; i < NR; ++i) {
         m_ref[i] = -INFINITY;
         l_part[i] = 0.f;
+      }
+#pragma unroll
+      for (int g4 = 0; g4 < 4; ++g4) {
+        ev[g4] = kEvUnset;
+        sv[g4] = 1.f;
+      }
+      {
+        // the query rows' powers of two, computed from the same rows as the
+        // convert warps' Q tile (so no exchange is needed), as 2^-e per row
+        const int ts = tid - kConvWarps * 32, n = ts >> 2, qq = ts & 3;
+        float m = 0.f;
+        if (n < M) {
+          const int t = n / G, hg = n % G;
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.q + (((int64_t)seg.b * p.qT + t) * p.Hq + seg.h * G + hg) * kD + 64 * qq);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 w4 = src[c];
+            const uint32_t rw[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(rw[j])), fabsf(bf16_hi(rw[j]))));
+          }
+        }
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        if (qq == 0) rsn[n] = pow2i(-q_norm_exp(m));
+        named_bar(2, kScoreWarps * 32);
       }
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
@@ -442,10 +508,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const float4 rcv = *reinterpret_cast<const float4*>(theirs + nt * 4);
-            sc[nt * 4 + 0] += rcv.x;
-            sc[nt * 4 + 1] += rcv.y;
-            sc[nt * 4 + 2] += rcv.z;
-            sc[nt * 4 + 3] += rcv.w;
+            const float4 f = *reinterpret_cast<const float4*>(rsn + 8 * nt + 4 * half);  // undo the Q scaling
+            sc[nt * 4 + 0] = (sc[nt * 4 + 0] + rcv.x) * f.x;
+            sc[nt * 4 + 1] = (sc[nt * 4 + 1] + rcv.y) * f.y;
+            sc[nt * 4 + 2] = (sc[nt * 4 + 2] + rcv.z) * f.z;
+            sc[nt * 4 + 3] = (sc[nt * 4 + 3] + rcv.w) * f.w;
           }
         }
         // ---- causal / context mask: only pages that reach past L - T (padding rows
@@ -464,8 +531,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         for (int i = 0; i < NR; ++i) over |= sc[i] > m_ref[i] + 8.f;
         const unsigned vote = __ballot_sync(0xffffffffu, over);
         if (lane == 0) sflag[quad] = vote != 0;
+        // the page's largest value scale per group: this warp's 32 keys, then the other warp's
+        float vsk[4];
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          vsk[g4] = key_valid ? vs_s[key * 4 + g4] : 0.f;  // slots past ctx_len may hold NaN scales
+          const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(vsk[g4]));
+          if (lane == 0) pmx[quad * 4 + g4] = __uint_as_float(mx);
+        }
         named_bar(3 + half, 64);
         const bool raise = sflag[2 * half] | sflag[2 * half + 1];
+        bool rebased = false;
+        float beta[4];
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+          beta[g4] = 1.f;
+          const float mx = fmaxf(pmx[(2 * half) * 4 + g4], pmx[(2 * half + 1) * 4 + g4]);
+          if (mx > 0.f && ev_update(ev[g4], exp_of(mx), beta[g4])) {
+            sv[g4] = pow2i(-ev[g4]);
+            rebased = true;
+          }
+        }
         float al[NR];
 #pragma unroll
         for (int i = 0; i < NR; ++i) al[i] = 1.f;
@@ -498,17 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           l_part[i] += pr[i];
         }
         wait_bar(&pempty_bar[q & 1], ((q >> 1) & 1) ^ 1);
-        float* alpha = hdr + (q & 1) * 40;  // [32 alpha | side flags]
+        float* alpha = hdr + (q & 1) * 48;  // [32 alpha | 2 side flags | 2 pad | 4 beta | rebase flag]
         if ((quad & 1) == 0 && lane == 0) {
-          // the PV warps rescale their accumulators by alpha before adding this page
+          // the PV warps rescale their accumulators by alpha (rows) and beta
+          // (groups) before adding this page
 #pragma unroll
           for (int i = 0; i < NR; ++i) alpha[8 * (i >> 2) + 4 * half + (i & 3)] = al[i];
           reinterpret_cast<int*>(alpha + 32)[half] = raise ? 1 : 0;
+          if (half == 0) {
+#pragma unroll
+            for (int g4 = 0; g4 < 4; ++g4) alpha[36 + g4] = beta[g4];
+            reinterpret_cast<int*>(alpha + 40)[0] = rebased ? 1 : 0;
+          }
         }
         uint8_t* pb = pbuf + (q & 1) * (NT * 8192);
 #pragma unroll
         for (int gq = 0; gq < 4; ++gq) {
-          const float vs = key_valid ? vs_s[key * 4 + gq] : 0.f;  // slots past ctx_len may hold NaN scales
+          const float vs = vsk[gq] * sv[gq];  // P' = p Vs 2^-ev
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             // hi = the value cut to 11 significant bits (exact in fp16 for
@@ -549,6 +641,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           lrow[n] = red_l[quad * 32 + i] + red_l[(quad + 1) * 32 + i];
           mrow[n] = m_ref[i];
         }
+        if (half == 0) {
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) evs[g4] = ev[g4];
+        }
       }
       named_bar(5, (kScoreWarps + kPvWarps) * 32);
       named_bar(5, (kScoreWarps + kPvWarps) * 32);  // the PV warps have read lrow / mrow
@@ -573,8 +669,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const int q = q0 + j;
         wait_bar(&full_bar[s], ph);
         wait_bar(&pfull_bar[q & 1], (q >> 1) & 1);
-        const float* alpha = hdr + (q & 1) * 40;
+        const float* alpha = hdr + (q & 1) * 48;
         const int* sf = reinterpret_cast<const int*>(alpha + 32);
+        if (reinterpret_cast<const int*>(alpha + 40)[0]) {  // P' exponent of a group moved
+          const float bt = alpha[36 + gq];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) o[cc][nt][k] *= bt;
+        }
         if (sf[0] | sf[1]) {
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -627,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       named_bar(5, (kScoreWarps + kPvWarps) * 32);
       named_bar(5, (kScoreWarps + kPvWarps) * 32);
       const int64_t slot = (int64_t)blockIdx.x + seg.u;
+      const float unscale = evs[gq] == kEvUnset ? 1.f : pow2i(evs[gq]);  // o holds O 2^-ev
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -634,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const int n = 8 * nt + 2 * t4 + e;
           if (n >= M) continue;
           const float lsum = lrow[n];
-          const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+          const float inv = lsum > 0.f ? unscale / lsum : 0.f;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int ch = 32 * pw + 16 * cc + 2 * g_lane;
@@ -659,6 +765,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
   // release tensor memory
   tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    // After a timed-out wait some copies or MMAs may still be in flight:
+    // the last copy issued into each stage and the last QK MMAs complete
+    // (bounded waits, whatever abort_flag says) before the tensor memory is
+    // released and the CTA exits. Without a timeout all of them are done.
+    for (int s2 = 0; s2 < S; ++s2)
+      if (icnt[s2] > 0) (void)mbar_wait(smem_u32(&full_bar[s2]), (uint32_t)(icnt[s2] - 1) & 1u, p.wait_cycles);
+    const int lm = *last_mma;
+    if (lm >= 0) (void)mbar_wait(smem_u32(&qk_bar[lm & 1]), (uint32_t)(lm >> 1) & 1u, p.wait_cycles);
+  }
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();

@@ -8,8 +8,7 @@
 //
 // Quantization (both sides of the parity tests take these decisions in the
 // same precision):
-//   keys   y = R k in fp32: butterflies (a + b, a - b) over index bits 0..5 in
-//          that order, each add rounded, then times 1/8;
+//   keys   y = R k = RN_fp32(H64 k / 8), one rounding of the exact sum;
 //          s = RN_fp16(fp32(max|y| / 127)), q = clamp(rne(fp32(y / s)), +-127);
 //   values s = RN_fp16(fp32(max|v| / 7)),   q = clamp(rne(fp32(v / s)), +-7);
 //   a scale that rounds to 0 becomes 1 (its codes are then 0), one past the
@@ -46,33 +45,143 @@ __device__ __forceinline__ uint32_t rk_code(float x, float s, int qmax) {
   return (uint32_t)q;
 }
 
+// ---------------------------------------------------------------------------
+// The key rotation y = RN_fp32(H64 x / 8): every output is the exact signed
+// sum of the group's 64 bf16 values, divided by 8 and rounded once.
+//
+// A finite bf16 value is an integer multiple of the quantum of its exponent
+// (2^(e-134) for exponent field e >= 1, 2^-133 for e = 0). When the group's
+// non-zero values have exponent fields within 39 of each other, every partial
+// sum of up to 64 of them is an integer multiple of the smallest quantum and
+// below 2^53 of it, so fp64 butterflies (a + b, a - b) are exact, the 1/8 is
+// exact, and one conversion to fp32 gives the correctly rounded value. Wider
+// groups (a rare, degenerate input) take rk_rotate_wide: an exact integer
+// sum in 32-bit limbs and an explicit round to nearest even.
+// ---------------------------------------------------------------------------
+constexpr int kWideLimbs = 10;  // 320 bits: |x| < 2^128 in 2^-133 units, times 64
+
+// a += units * 2^shift (units < 2^8): the magnitude sum of one sign.
+__device__ __forceinline__ void wide_add(uint32_t (&a)[kWideLimbs], uint32_t units, int shift) {
+  int k = shift >> 5;
+  const uint64_t v = (uint64_t)units << (shift & 31);
+  uint64_t cur = (uint64_t)a[k] + (uint32_t)v;
+  a[k] = (uint32_t)cur;
+  uint64_t carry = (cur >> 32) + (v >> 32);
+  for (++k; k < kWideLimbs && carry; ++k) {
+    cur = (uint64_t)a[k] + carry;
+    a[k] = (uint32_t)cur;
+    carry = cur >> 32;
+  }
+}
+
+// Bit `pos` of a (0 below bit 0).
+__device__ __forceinline__ uint32_t wide_bit(const uint32_t (&a)[kWideLimbs], int pos) {
+  return pos < 0 ? 0u : (a[pos >> 5] >> (pos & 31)) & 1u;
+}
+
+// fp32 bits of RN(m * 2^-136) for the magnitude m in `a`, sign `neg`.
+__device__ uint32_t wide_round(const uint32_t (&a)[kWideLimbs], bool neg) {
+  int top = -1;
+  for (int k = kWideLimbs - 1; k >= 0 && top < 0; --k)
+    if (a[k]) top = 32 * k + 31 - __clz(a[k]);
+  const uint32_t sign = neg ? 0x80000000u : 0u;
+  if (top < 0) return 0u;
+  if (top < 24) {  // exact: fewer than 25 significant bits
+    const uint32_t m = a[0];
+    if (top < 10) return sign | (m << 13);  // fp32 subnormal: m * 2^-136 = (m << 13) * 2^-149
+    return sign | ((uint32_t)(top - 9) << 23) | ((m << (23 - top)) & 0x7fffffu);
+  }
+  const int low = top - 23;
+  uint32_t m = 0;
+  for (int b = 23; b >= 0; --b) m = (m << 1) | wide_bit(a, low + b);
+  const uint32_t guard = wide_bit(a, low - 1);
+  bool sticky = false;
+  for (int b = 0; b < low - 1; ++b) sticky |= wide_bit(a, b) != 0u;
+  if (guard && (sticky || (m & 1u))) ++m;
+  int e = top - 9;  // biased exponent of the leading bit 2^(top - 136)
+  if (m == (1u << 24)) {
+    m >>= 1;
+    ++e;
+  }
+  if (e >= 255) return sign | 0x7f800000u;
+  return sign | ((uint32_t)e << 23) | (m & 0x7fffffu);
+}
+
+// R x of one group whose exponents span more than 39 binades, exactly.
+__device__ void rk_rotate_wide(const uint16_t (&xb)[kGroup], float (&y)[kGroup]) {
+  for (int r = 0; r < kGroup; ++r) {
+    uint32_t pos[kWideLimbs], ng[kWideLimbs];
+    for (int k = 0; k < kWideLimbs; ++k) pos[k] = ng[k] = 0u;
+    for (int j = 0; j < kGroup; ++j) {
+      const uint32_t b = xb[j], e = (b >> 7) & 0xffu, f = b & 0x7fu;
+      if (e == 0u && f == 0u) continue;
+      const uint32_t units = e == 0u ? f : 128u + f;
+      const int shift = e == 0u ? 0 : (int)e - 1;
+      const bool minus = ((b >> 15) ^ (__popc((uint32_t)(r & j)) & 1u)) != 0u;
+      wide_add(minus ? ng : pos, units, shift);
+    }
+    // |pos - ng| and its sign
+    bool neg = false;
+    for (int k = kWideLimbs - 1; k >= 0; --k)
+      if (pos[k] != ng[k]) {
+        neg = ng[k] > pos[k];
+        break;
+      }
+    uint32_t d[kWideLimbs];
+    uint32_t borrow = 0u;
+    for (int k = 0; k < kWideLimbs; ++k) {
+      const uint64_t hi = neg ? ng[k] : pos[k], lo = (uint64_t)(neg ? pos[k] : ng[k]) + borrow;
+      d[k] = (uint32_t)(hi - lo);
+      borrow = hi < lo ? 1u : 0u;
+    }
+    y[r] = __uint_as_float(wide_round(d, neg));
+  }
+}
+
 // One key group: 64 bf16 channels -> 64 int8 codes of R k and the fp16 scale.
 __device__ __forceinline__ void rk_key_group(const uint4* src, uint4* dst, uint16_t* scale, bool& range) {
-  float t[kGroup];
+  uint16_t xb[kGroup];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const uint4 w = __ldg(src + c);
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      t[8 * c + 2 * i] = bf16_lo(ws[i]);
-      t[8 * c + 2 * i + 1] = bf16_hi(ws[i]);
+      xb[8 * c + 2 * i] = (uint16_t)(ws[i] & 0xffffu);
+      xb[8 * c + 2 * i + 1] = (uint16_t)(ws[i] >> 16);
     }
   }
+  int emax = 0, emin = 255;  // exponent fields of the non-zero values (subnormals count as 1)
 #pragma unroll
-  for (int h = 1; h < kGroup; h <<= 1)
+  for (int i = 0; i < kGroup; ++i) {
+    if ((xb[i] & 0x7fffu) == 0u) continue;
+    const int e = max(1, (xb[i] >> 7) & 0xff);
+    emax = max(emax, e);
+    emin = min(emin, e);
+  }
+  float t[kGroup];
+  if (emax - emin <= 39) {
+    double d[kGroup];
 #pragma unroll
-    for (int i = 0; i < kGroup; ++i)
-      if ((i & h) == 0) {
-        const float a = t[i], b = t[i + h];
-        t[i] = __fadd_rn(a, b);
-        t[i + h] = __fsub_rn(a, b);
-      }
+    for (int i = 0; i < kGroup; ++i) d[i] = (double)__uint_as_float((uint32_t)xb[i] << 16);
+#pragma unroll
+    for (int h = 1; h < kGroup; h <<= 1)
+#pragma unroll
+      for (int i = 0; i < kGroup; ++i)
+        if ((i & h) == 0) {
+          const double a = d[i], b = d[i + h];
+          d[i] = __dadd_rn(a, b);
+          d[i + h] = __dsub_rn(a, b);
+        }
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i) t[i] = __double2float_rn(__dmul_rn(d[i], 0.125));
+  } else {
+    rk_rotate_wide(xb, t);
+  }
   float amax = 0.f;
   bool finite = true;
 #pragma unroll
   for (int i = 0; i < kGroup; ++i) {
-    t[i] = __fmul_rn(t[i], 0.125f);
     finite &= isfinite(t[i]);
     amax = fmaxf(amax, fabsf(t[i]));
   }

@@ -14,7 +14,9 @@ rounded to bf16 (round to nearest even), then shaped per config:
   * c1_decode: 4 fixed K channels per kv-head scaled x8 (outliers that stress
     the group scales);
   * long_context: K and V rows each scaled by an independent U(0.5, 2) factor
-    per (token, kv-head) (per-token norm spread).
+    per (token, kv-head) (per-token norm spread);
+  * any workload: Q, K or V multiplied by a power of two (q_scale, k_scale,
+    v_scale), to move the inputs off unit scale.
 """
 from __future__ import annotations
 
@@ -44,6 +46,11 @@ class Workload:
     note: str = ""
     # KV format of the pool: "int8" (INT8 group-64, fp32 scales) or "rk8v4"
     fmt: str = "int8"
+    # powers of two the drawn Q, K and V values are multiplied by (before the
+    # bf16 rounding): the range tests move the inputs off unit scale
+    q_scale: float = 1.0
+    k_scale: float = 1.0
+    v_scale: float = 1.0
     # filled by tables()
     num_pages: int = 0
     max_pages: int = 0
@@ -157,10 +164,12 @@ def tables(w: Workload, num_pages: int | None = None) -> Workload:
 
 
 def custom(name="custom", *, B, T, Hq, Hkv, D, P, ctx_lens, seed, append_len=None, num_pages=None,
-           outlier_channels=0, outlier_scale=1.0, token_norm_range=None) -> Workload:
+           outlier_channels=0, outlier_scale=1.0, token_norm_range=None, q_scale=1.0, k_scale=1.0,
+           v_scale=1.0) -> Workload:
     w = Workload(name, B=B, T=T, Hq=Hq, Hkv=Hkv, D=D, P=P, ctx_lens=list(ctx_lens), seed=seed,
                  append_len=T if append_len is None else append_len, outlier_channels=outlier_channels,
-                 outlier_scale=outlier_scale, token_norm_range=token_norm_range)
+                 outlier_scale=outlier_scale, token_norm_range=token_norm_range, q_scale=q_scale, k_scale=k_scale,
+                 v_scale=v_scale)
     return tables(w, num_pages)
 
 
@@ -200,8 +209,8 @@ def kv_rows(w: Workload, b: int, start: int, n: int, device="cpu") -> tuple[torc
             vv *= uv
         a = max(start, k * blk) - k * blk
         e = min(start + n, (k + 1) * blk) - k * blk
-        ks.append(kk[a:e].to(torch.bfloat16))
-        vs.append(vv[a:e].to(torch.bfloat16))
+        ks.append((kk[a:e] * w.k_scale).to(torch.bfloat16))
+        vs.append((vv[a:e] * w.v_scale).to(torch.bfloat16))
     if not ks:
         z = torch.empty((0, w.Hkv, w.D), dtype=torch.bfloat16, device=device)
         return z, z.clone()
@@ -211,7 +220,8 @@ def kv_rows(w: Workload, b: int, start: int, n: int, device="cpu") -> tuple[torc
 def queries(w: Workload, device="cpu") -> torch.Tensor:
     """bf16 Q [B][T][Hq][D]."""
     g = _gen(w.seed, 3, device)
-    return torch.randn((w.B, w.T, w.Hq, w.D), generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+    q = torch.randn((w.B, w.T, w.Hq, w.D), generator=g, device=device, dtype=torch.float32)
+    return (q * w.q_scale).to(torch.bfloat16)
 
 
 def history_and_step(w: Workload):

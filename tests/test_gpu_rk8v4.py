@@ -108,6 +108,49 @@ def test_append_ragged_batch_in_one_call():
     assert np.array_equal(pool.storage.cpu().numpy(), opool)
 
 
+def wide_key_rows(n, H, D, seed):
+    """Key rows whose 64-channel groups span far more than 39 binades (values
+    from 2^-133 to 2^120, two clusters 2^100 apart, exact cancellations), so
+    that the append rotates them by its exact integer route; the rest of the
+    rows are ordinary groups (fp64 route)."""
+    rng = np.random.default_rng(seed)
+    k = rng.standard_normal((n, H, D // 64, 64))
+    kind = rng.integers(0, 4, size=(n, H, D // 64))
+    wide = 2.0 ** rng.uniform(-133, 120, size=k.shape)
+    clusters = np.where(rng.random(k.shape) < 0.5, 2.0 ** 40, 2.0 ** -60)
+    k = np.where((kind == 1)[..., None], k * wide, k)
+    k = np.where((kind == 2)[..., None], k * clusters, k)
+    # kind 3: channel pairs (0, 1) equal, so half of the outputs cancel them exactly
+    k3 = k.copy()
+    k3[..., 0] = 2.0 ** 70
+    k3[..., 1] = 2.0 ** 70
+    k3[..., 2:] *= 2.0 ** -40
+    k = np.where((kind == 3)[..., None], k3, k)
+    return torch.from_numpy(k.reshape(n, H, D)).to(torch.bfloat16)
+
+
+def test_append_wide_exponent_key_groups_bit_exact():
+    """Both routes of the key rotation against the oracle's exact rotation
+    rounded once: codes and scales bit for bit; saturated scales may flag."""
+    n, H, D, P = 256, 2, 256, 64
+    k = wide_key_rows(n, H, D, seed=21)
+    v = torch.randn((n, H, D)).to(torch.bfloat16)
+    num_pages = n // P
+    bt = torch.arange(num_pages, dtype=torch.int32)[None].contiguous()
+    cu = torch.tensor([0, n], dtype=torch.int32)
+    sp = torch.tensor([0], dtype=torch.int32)
+    pool = nk.KVPool.empty(num_pages, P, H, D, fill=0x11, fmt="rk8v4")
+    opool = oracle.rk_new_pool(num_pages, P, H, D, fill=0x11)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nk.rk8v4_append(pool, bt.cuda(), sp.cuda(), cu.cuda(), k.cuda(), v.cuda(), status=status)
+    assert oracle.rk_append(opool, num_pages, P, H, D, bt, sp, cu, k, v) == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) & ~0x10 == 0
+    got = pool.storage.cpu().numpy()
+    diff = np.flatnonzero(got != opool)
+    assert diff.size == 0, f"{diff.size} pool bytes differ, first at {diff[:8]}"
+
+
 def sweep_rows():
     """K and V rows whose group maxima sweep the scale's range: every positive
     finite bf16 value below 458,000 is the absmax of one value group (its
