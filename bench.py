@@ -43,7 +43,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="mix",
                     help="mix (default: the largest single-GPU configuration, 8 x 1,024-row append + C8 x T4 "
-                         "attention at 131,072) | tiny | c1_decode | c8_verify | long_context | c8_decode | c1_rk8v4")
+                         "attention at 131,072) | tiny | c1_decode | c8_verify | long_context | c8_decode | c1_rk8v4 "
+                         "| c1_i8f16 | c1_bf16 | c8_i8f16 | c8_bf16")
     ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -156,7 +157,7 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
     bt = wl.block_table(w).to(device)
     ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    append = nk.rk8v4_append if w.fmt == "rk8v4" else nk.kv_append
+    append = {"rk8v4": nk.rk8v4_append, "i8f16": nk.i8f16_append, "bf16": nk.bf16kv_append}.get(w.fmt, nk.kv_append)
     base = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, device=device, fill=0, fmt=w.fmt)
     hist, _ = wl.history_and_step(w)
     for b in range(w.B):
@@ -211,8 +212,8 @@ def attention_call(args, w):
     kernel of an INT8 pool, or the rk8v4 kernel of an rk8v4 pool."""
     import quantized_paged_kv_cache_gb300 as nk
 
-    if w.fmt == "rk8v4":
-        return nk.rk8v4_decode_attn
+    if w.fmt != "int8":
+        return {"rk8v4": nk.rk8v4_decode_attn, "i8f16": nk.i8f16_decode_attn, "bf16": nk.bf16kv_decode_attn}[w.fmt]
     return nk.paged_decode_attn if args.kernel == "mma" else nk.paged_decode_attn_simt
 
 
@@ -226,7 +227,8 @@ def run_ours(args, w, rank, world, device):
 
     import quantized_paged_kv_cache_gb300 as nk
 
-    sizer = nk.rk8v4_pool_bytes if w.fmt == "rk8v4" else nk.kv_pool_bytes
+    sizer = {"rk8v4": nk.rk8v4_pool_bytes, "i8f16": nk.i8f16_pool_bytes, "bf16": nk.bf16kv_pool_bytes}.get(
+        w.fmt, nk.kv_pool_bytes)
     pool_bytes = sizer(w.num_pages, w.P, w.Hkv, w.D)
     replicas = 1 if pool_bytes >= 2 * L2_BYTES else int(-(-2 * L2_BYTES // pool_bytes)) + 1
     S = setup_gpu(w, device, replicas, args.num_ctas, args.kernel)
@@ -382,11 +384,19 @@ class OracleStep:
 
         self.w, self.oracle, self.np = w, oracle, np
         rk = w.fmt == "rk8v4"
-        self.append = oracle.rk_append if rk else oracle.kv_append
-        self.attention = oracle.rk_paged_attention if rk else oracle.paged_attention
-        self.attention_row = oracle.rk_attention_row if rk else oracle.attention_row
+        self.fmt = {"i8f16": "int8_f16", "bf16": "bf16"}.get(w.fmt)  # the oracle's other formats
+        if self.fmt:
+            f = self.fmt
+            self.append = lambda *a: oracle.fmt_append(f, *a)
+            self.attention = lambda *a: oracle.fmt_paged_attention(f, *a)
+            self.attention_row = None  # rows are sampled as whole sequences
+            self.pool = oracle.fmt_new_pool(f, w.num_pages, w.P, w.Hkv, w.D)
+        else:
+            self.append = oracle.rk_append if rk else oracle.kv_append
+            self.attention = oracle.rk_paged_attention if rk else oracle.paged_attention
+            self.attention_row = oracle.rk_attention_row if rk else oracle.attention_row
+            self.pool = (oracle.rk_new_pool if rk else oracle.new_pool)(w.num_pages, w.P, w.Hkv, w.D)
         self.bt = wl.block_table(w)
-        self.pool = (oracle.rk_new_pool if rk else oracle.new_pool)(w.num_pages, w.P, w.Hkv, w.D)
         hist, _ = wl.history_and_step(w)
         for b in range(w.B):
             pos = 0
@@ -400,6 +410,11 @@ class OracleStep:
         self.q = wl.queries(w, device="cpu")
         all_rows = [(b, t, i) for b in range(w.B) for t in range(w.T) for i in range(w.Hq)]
         self.rows = all_rows if max_rows is None else all_rows[:max_rows]
+        self.nseq = w.B
+        if self.fmt and len(self.rows) < len(all_rows):
+            # the other formats' oracle attends whole sequences: the first ones
+            self.nseq = max(1, len(self.rows) // (w.T * w.Hq))
+            self.rows = all_rows[:self.nseq * w.T * w.Hq]
         self.frac_rows = len(self.rows) / len(all_rows)
         self.threads = oracle.num_threads()
         # algorithmic bytes of this sample: the whole append, and the KV bytes
@@ -413,6 +428,10 @@ class OracleStep:
         if self.frac_rows == 1.0:
             self.attention(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T, w.Hq,
                            w.sm_scale)
+        elif self.fmt:
+            n = self.nseq
+            self.attention(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt[:n].contiguous(), w.ctx_lens[:n],
+                           self.q[:n].contiguous(), w.T, w.Hq, w.sm_scale)
         else:
             for (b, t, i) in self.rows:
                 self.attention_row(self.pool, w.num_pages, w.P, w.Hkv, w.D, self.bt, w.ctx_lens, self.q, w.T,
@@ -518,8 +537,10 @@ def main():
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms"], 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": ("i8 K / i4 V KV (fp16 scales), f32 CUDA-core arithmetic" if w.fmt == "rk8v4"
-                  else "i8 KV, f16 MMA operands, f32 accumulate"),
+        "dtype": {"rk8v4": "i8 K / i4 V KV (fp16 scales), f32 CUDA-core arithmetic",
+                  "i8f16": "i8 KV (fp16 scales), f16 MMA operands, f32 accumulate",
+                  "bf16": "bf16 KV, bf16 MMA operands, f32 accumulate"}.get(
+                      w.fmt, "i8 KV, f16 MMA operands, f32 accumulate"),
         "data": "synthetic",
         "config": config_dict(w, l2),
         "us_per_call": round(us, 3), "attn_us_per_call": round(attn_us, 3),
@@ -532,12 +553,14 @@ def main():
         "append_gbs": round(w.append_bytes() / (append_us * 1e-6) / 1e9, 2),
         "attn_gbs": round(achieved, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
-        "kernel": "rk8v4" if w.fmt == "rk8v4" else args.kernel, "num_ctas": r["nct"] or "default",
+        "kernel": args.kernel if w.fmt == "int8" else w.fmt, "num_ctas": r["nct"] or "default",
         "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": 3 * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("rk8v4 split kernel + combine (one nk_rk8v4_decode_attn call)" if w.fmt == "rk8v4"
-                                else "paged_decode split kernel + combine (one nk_paged_decode_attn call)"),
+                     "kernel": ("paged_decode split kernel + combine (one nk_paged_decode_attn call)"
+                                if w.fmt == "int8" else
+                                f"{w.fmt} split kernel + combine (one nk_{'bf16kv' if w.fmt == 'bf16' else w.fmt}"
+                                "_decode_attn call)"),
                      "peak_source": f"{src} hbm_gbs", "bytes_per_launch": w.attn_bytes()},
     }
     if not args.no_cpu_baseline and world == 1 and not args.profile:

@@ -254,6 +254,51 @@ int nk_rk8v4_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_
                          size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream);
 
 /*
+ * The pages' own INT8 layout and the unquantized bf16 baseline ("NInfer-3090"
+ * README, "Choosing a KV format": int8 at 33,792 and bf16 at 65,536 bytes per
+ * token on the 27B model, 16 attention layers x 4 kv-heads x 256 channels).
+ * Chunks per (page, kv-head), pool = [num_pages][num_kv_heads][chunk]:
+ *   int8 with fp16 scales (i8f16):
+ *     Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D] int8 | Vs[P][D/64] fp16
+ *     (528 bytes per (token, kv-head) at D = 256: the page's 33,792 per token);
+ *   bf16 (bf16kv): K[P][D] bf16 | V[P][D] bf16 (the page's 65,536 per token).
+ * i8f16 quantization (the rule of the rk8v4 keys, without the rotation):
+ *   s = RN_fp16(max|x| / 127), 1 when that is 0, 65504 past the fp16 maximum
+ *   (NK_DEVFLAG_RANGE); q = clamp(round_half_even(fp32(x / s)), -127, 127).
+ * bf16kv stores the rows as they are. The nk_kv_pool struct describes these
+ * pools too; size them with their own *_pool_bytes, and only the calls of a
+ * format may touch its pool.
+ */
+size_t nk_i8f16_chunk_bytes(int32_t page_size, int32_t head_dim);
+size_t nk_i8f16_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+size_t nk_bf16kv_chunk_bytes(int32_t page_size, int32_t head_dim);
+size_t nk_bf16kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim);
+
+/* kv_cache_append into an i8f16 or a bf16kv pool: arguments, checks, device
+ * flags, ordering and ownership exactly as nk_kv_append. */
+int nk_i8f16_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                    const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                    const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream);
+int nk_bf16kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                     const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                     const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream);
+
+/* Split-KV decode / verify attention over an i8f16 or a bf16kv pool:
+ * arguments, checks, workspace (nk_decode_workspace_bytes), column chunks,
+ * causal mask, output and device flags exactly as nk_paged_decode_attn, on the
+ * same tensor-core kernels (i8f16: the tcgen05 and mma.sync kernels with fp16
+ * scales; bf16kv: the mma.sync kernel with bf16 operands). */
+int nk_i8f16_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                         int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                         int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                         size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream);
+int nk_bf16kv_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                          void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
+                          void* stream);
+
+/*
  * nk_paged_decode_attn_noalloc -- nk_paged_decode_attn for callers that
  * cannot allocate device memory (the pages have no counterpart of this entry
  * point). Some callers cannot call cudaMalloc or pass a scratch buffer: hosts

@@ -25,7 +25,8 @@ __all__ = [
     "KVPool", "NKError", "kv_chunk_bytes", "kv_pool_bytes", "kv_append", "decode_default_splits", "decode_default_ctas",
     "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "paged_decode_attn_noalloc",
     "attn_combine", "status_string", "decode_step", "rk8v4_chunk_bytes", "rk8v4_pool_bytes", "rk8v4_append",
-    "rk8v4_decode_attn",
+    "rk8v4_decode_attn", "i8f16_chunk_bytes", "i8f16_pool_bytes", "i8f16_append", "i8f16_decode_attn",
+    "bf16kv_chunk_bytes", "bf16kv_pool_bytes", "bf16kv_append", "bf16kv_decode_attn", "test_inject_copy_stall",
 ]
 
 
@@ -62,6 +63,22 @@ def kv_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: i
     return int(lib().nk_kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
 
 
+def i8f16_chunk_bytes(page_size: int, head_dim: int) -> int:
+    return int(lib().nk_i8f16_chunk_bytes(page_size, head_dim))
+
+
+def i8f16_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().nk_i8f16_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
+def bf16kv_chunk_bytes(page_size: int, head_dim: int) -> int:
+    return int(lib().nk_bf16kv_chunk_bytes(page_size, head_dim))
+
+
+def bf16kv_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().nk_bf16kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim))
+
+
 def rk8v4_chunk_bytes(page_size: int, head_dim: int) -> int:
     return int(lib().nk_rk8v4_chunk_bytes(page_size, head_dim))
 
@@ -73,9 +90,10 @@ def rk8v4_pool_bytes(num_pages: int, page_size: int, num_kv_heads: int, head_dim
 @dataclass
 class KVPool:
     """A caller-owned pool: ``storage`` is a uint8 CUDA tensor laid out as
-    [page][kv-head][chunk], in the INT8 group-64 format (``fmt="int8"``,
-    ``kv_pool_bytes(...)`` bytes) or the rk8v4 format (``fmt="rk8v4"``,
-    ``rk8v4_pool_bytes(...)`` bytes)."""
+    [page][kv-head][chunk], in the INT8 group-64 format with fp32 scales
+    (``fmt="int8"``, ``kv_pool_bytes(...)`` bytes), the rk8v4 format
+    (``"rk8v4"``), the pages' INT8 layout with fp16 scales (``"i8f16"``) or
+    bf16 rows (``"bf16"``), each sized by its own ``*_pool_bytes``."""
 
     storage: "object"
     num_pages: int
@@ -89,12 +107,11 @@ class KVPool:
               fmt: str = "int8"):
         import torch
 
-        if fmt == "int8":
-            n = kv_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
-        elif fmt == "rk8v4":
-            n = rk8v4_pool_bytes(num_pages, page_size, num_kv_heads, head_dim)
-        else:
+        sizers = {"int8": kv_pool_bytes, "rk8v4": rk8v4_pool_bytes, "i8f16": i8f16_pool_bytes,
+                  "bf16": bf16kv_pool_bytes}
+        if fmt not in sizers:
             raise ValueError(f"unknown KV format {fmt!r}")
+        n = sizers[fmt](num_pages, page_size, num_kv_heads, head_dim)
         st = torch.empty(n, dtype=torch.uint8, device=device)
         if fill is not None:
             st.fill_(fill)
@@ -257,3 +274,40 @@ def test_inject_copy_stall(withheld_page: int, wait_cycles: int = 0) -> None:
     """nk_test_inject_copy_stall: failure injection for the bounded-wait tests
     (withheld_page < 0 switches it off)."""
     lib().nk_test_inject_copy_stall(int(withheld_page), int(wait_cycles))
+
+
+def _fmt_append(fn, name, fmt, pool, block_table, start_pos, cu_new, k, v, status, stream):
+    _need_cuda(block_table, start_pos, cu_new, k, v, status)
+    pool.need(fmt)
+    B = int(start_pos.numel())
+    total = int(k.shape[0]) if k.dim() > 0 else 0
+    ps = pool.c_struct()
+    rc = fn(ctypes.byref(ps), _ptr(block_table), int(block_table.shape[-1]), _ptr(start_pos), _ptr(cu_new), B, total,
+            _ptr(k), _ptr(v), _ptr(status), _stream(stream))
+    _check(rc, name)
+
+
+def i8f16_append(pool: KVPool, block_table, start_pos, cu_new, k, v, status=None, stream=None) -> None:
+    """Quantize k/v rows into a pool of the pages' INT8 layout with fp16 scales (nk_i8f16_append)."""
+    _fmt_append(lib().nk_i8f16_append, "nk_i8f16_append", "i8f16", pool, block_table, start_pos, cu_new, k, v,
+                status, stream)
+
+
+def bf16kv_append(pool: KVPool, block_table, start_pos, cu_new, k, v, status=None, stream=None) -> None:
+    """Scatter bf16 k/v rows into a bf16 pool (nk_bf16kv_append)."""
+    _fmt_append(lib().nk_bf16kv_append, "nk_bf16kv_append", "bf16", pool, block_table, start_pos, cu_new, k, v,
+                status, stream)
+
+
+def i8f16_decode_attn(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int, num_ctas: int = 0,
+                      workspace=None, out=None, status=None, stream=None):
+    """Split-KV paged attention over an INT8 pool with fp16 scales (nk_i8f16_decode_attn)."""
+    return _decode(lib().nk_i8f16_decode_attn, "nk_i8f16_decode_attn", pool, q, block_table, ctx_lens, sm_scale,
+                   max_ctx, num_ctas, workspace, out, status, stream, fmt="i8f16")
+
+
+def bf16kv_decode_attn(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int, num_ctas: int = 0,
+                       workspace=None, out=None, status=None, stream=None):
+    """Split-KV paged attention over a bf16 pool (nk_bf16kv_decode_attn)."""
+    return _decode(lib().nk_bf16kv_decode_attn, "nk_bf16kv_decode_attn", pool, q, block_table, ctx_lens, sm_scale,
+                   max_ctx, num_ctas, workspace, out, status, stream, fmt="bf16")

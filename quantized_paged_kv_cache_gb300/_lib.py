@@ -51,6 +51,14 @@ EXPORTS = (
     "nk_rk8v4_pool_bytes",
     "nk_rk8v4_append",
     "nk_rk8v4_decode_attn",
+    "nk_i8f16_chunk_bytes",
+    "nk_i8f16_pool_bytes",
+    "nk_i8f16_append",
+    "nk_i8f16_decode_attn",
+    "nk_bf16kv_chunk_bytes",
+    "nk_bf16kv_pool_bytes",
+    "nk_bf16kv_append",
+    "nk_bf16kv_decode_attn",
     "nk_status_string",
     "nk_version",
     "nk_test_inject_copy_stall",
@@ -89,6 +97,13 @@ def lib() -> ctypes.CDLL:
             L.nk_rk8v4_append.argtypes = [pool_p, P, I32, P, P, I32, I32, P, P, P, P]
             L.nk_rk8v4_append.restype = ctypes.c_int
             L.nk_rk8v4_decode_attn.argtypes, L.nk_rk8v4_decode_attn.restype = dec, ctypes.c_int
+            for fmt in ("i8f16", "bf16kv"):
+                for name, args, res in ((f"nk_{fmt}_chunk_bytes", [I32, I32], Z),
+                                        (f"nk_{fmt}_pool_bytes", [I32, I32, I32, I32], Z),
+                                        (f"nk_{fmt}_append", [pool_p, P, I32, P, P, I32, I32, P, P, P, P], ctypes.c_int),
+                                        (f"nk_{fmt}_decode_attn", dec, ctypes.c_int)):
+                    fn = getattr(L, name)
+                    fn.argtypes, fn.restype = args, res
             L.nk_attn_combine.argtypes = [P, P, I32, I32, I32, P, P]
             L.nk_attn_combine.restype = ctypes.c_int
             L.nk_status_string.argtypes, L.nk_status_string.restype = [ctypes.c_int], ctypes.c_char_p

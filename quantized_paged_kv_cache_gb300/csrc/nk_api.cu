@@ -10,9 +10,9 @@
 #include "nk_rk8v4.cuh"
 
 namespace nk {
-cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
-                             const int32_t* cu_new, int B, int total_new, const void* k, const void* v,
-                             int32_t* status, cudaStream_t stream);
+cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, int fmt, const int32_t* bt, int max_pages,
+                             const int32_t* start_pos, const int32_t* cu_new, int B, int total_new, const void* k,
+                             const void* v, int32_t* status, cudaStream_t stream);
 }
 
 using namespace nk;
@@ -73,29 +73,37 @@ int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per
 // dim 256, 64-key pages) chunks of at most 24 rows, where that kernel is
 // fastest; on the mma.sync shapes at most 48 rows, fewer where a larger
 // page leaves no room for them; on CUDA cores 8 columns.
-int chunk_cols(bool simt, int D, int T, int G, int P) {
+int chunk_cols(bool simt, int fmt, int D, int T, int G, int P) {
   if (simt) return T < 8 ? T : 8;
-  if (decode_tc_supported(D, T, G, P)) return T;
-  const bool tc_shape = D == 256 && P == 64;  // the tcgen05 kernel's head dim and page size
-  if (!tc_shape && decode_mma_supported(D, T, G, P)) return T;
+  if (decode_tc_supported(fmt, D, T, G, P)) return T;
+  const bool tc_shape = D == 256 && P == 64 && fmt != kFmtBf16;  // the tcgen05 kernel's head dim, page, formats
+  if (!tc_shape && decode_mma_supported(fmt, D, T, G, P)) return T;
   int c = (tc_shape ? 24 : 48) / G;
   if (c < 1) c = 1;
   if (c > T) c = T;
-  while (c > 1 && !decode_tc_supported(D, c, G, P) && !decode_mma_supported(D, c, G, P)) --c;
+  while (c > 1 && !decode_tc_supported(fmt, D, c, G, P) && !decode_mma_supported(fmt, D, c, G, P)) --c;
   return c;
 }
 
 // Which split kernel a decode call runs: the tensor-core kernels or the fp32
-// CUDA-core kernel on an INT8 group-64 pool, or the CUDA-core kernel of the
-// rk8v4 format on an rk8v4 pool.
-enum class Path { kTensor, kSimt, kRk8v4 };
+// CUDA-core kernel on an INT8 group-64 pool (fp32 scales), the tensor-core
+// kernels on a pool of the pages' INT8 layout (fp16 scales) or of bf16 rows,
+// or the CUDA-core kernel of the rk8v4 format on an rk8v4 pool.
+enum class Path { kTensor, kSimt, kRk8v4, kTensorF16, kBf16 };
+
+int path_fmt(Path path) {
+  return path == Path::kTensorF16 ? kFmtI8F16 : (path == Path::kBf16 ? kFmtBf16 : kFmtI8F32);
+}
+
+// the paths on the tensor-core kernels (tcgen05 / mma.sync)
+bool tensor_path(Path path) { return path == Path::kTensor || path == Path::kTensorF16 || path == Path::kBf16; }
 
 // Checks the decode arguments and fills `p`; *empty = nothing to launch.
 int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int32_t max_pages, const int32_t* ctx,
                    int32_t B, int32_t T, int32_t Hq, float sm_scale, int32_t max_ctx, int32_t num_ctas,
                    void* workspace, size_t workspace_bytes, void* out, int32_t* status, Path path, DecodeParams* pp,
                    bool* empty) {
-  const bool simt = path != Path::kTensor;
+  const bool simt = !tensor_path(path);
   *empty = true;
   int err = NK_OK;
   if (!pool_ok(pool, &err)) return err;
@@ -109,11 +117,12 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   if (max_pages < 1 || max_ctx < T || (int64_t)max_ctx > (int64_t)max_pages * P) return NK_ERR_SHAPE;
   if (!isfinite(sm_scale)) return NK_ERR_SHAPE;
   if (!aligned(q, 16) || !aligned(out, 16)) return NK_ERR_SHAPE;
-  const int Tc = chunk_cols(simt, D, T, G, P);
+  const int fmt = path_fmt(path);
+  const int Tc = chunk_cols(simt, fmt, D, T, G, P);
   if (simt) {
     if (G > 8) return NK_ERR_UNSUPPORTED;
   } else {
-    if (!decode_tc_supported(D, Tc, G, P) && !decode_mma_supported(D, Tc, G, P)) return NK_ERR_UNSUPPORTED;
+    if (!decode_tc_supported(fmt, D, Tc, G, P) && !decode_mma_supported(fmt, D, Tc, G, P)) return NK_ERR_UNSUPPORTED;
   }
   const int per_sm = path == Path::kRk8v4 ? decode_rk8v4_ctas_per_sm(D, G)
                      : (simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G));
@@ -128,7 +137,8 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   p.P = P;
   p.Hkv = Hkv;
   p.D = D;
-  p.lay = path == Path::kRk8v4 ? rk8v4_layout(P, D) : ChunkLayout::make(P, D);
+  p.lay = path == Path::kRk8v4 ? rk8v4_layout(P, D) : layout_of(fmt, P, D);
+  p.fmt = fmt;
   p.q = reinterpret_cast<const uint16_t*>(q);
   p.bt = bt;
   p.max_pages = max_pages;
@@ -157,8 +167,8 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
 }
 
 int launch_decode(const DecodeParams& p0, Path path, cudaStream_t st) {
-  const bool simt = path != Path::kTensor;
-  const int Tc = chunk_cols(simt, p0.D, p0.T, p0.G, p0.P);
+  const bool simt = !tensor_path(path);
+  const int Tc = chunk_cols(simt, p0.fmt, p0.D, p0.T, p0.G, p0.P);
   const int64_t slots = (int64_t)p0.n_ctas + (int64_t)p0.B * p0.Hkv;
   for (int t0 = 0; t0 < p0.T; t0 += Tc) {
     DecodeParams p = p0;
@@ -173,7 +183,8 @@ int launch_decode(const DecodeParams& p0, Path path, cudaStream_t st) {
     // 32 rows per kv-head; the mma.sync kernel for the other shapes
     cudaError_t e = path == Path::kRk8v4 ? launch_decode_rk8v4(p, st)
                     : path == Path::kSimt   ? launch_decode_simt(p, st)
-                    : (decode_tc_supported(p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st) : launch_decode_mma(p, st));
+                    : (decode_tc_supported(p.fmt, p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st)
+                                                                     : launch_decode_mma(p, st));
     if (e != cudaSuccess) return NK_ERR_CUDA;
     e = launch_decode_combine(p, st);
     if (e != cudaSuccess) return NK_ERR_CUDA;
@@ -229,7 +240,7 @@ int nk_kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t
   const int err = check_append(pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B, total_new,
                                k_dev, v_dev, &empty);
   if (err != NK_OK || empty) return err;
-  const cudaError_t e = launch_kv_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev,
+  const cudaError_t e = launch_kv_append(sm_count(), *pool, kFmtI8F32, block_table_dev, max_pages_per_seq, start_pos_dev,
                                          cu_new_dev, B, total_new, k_dev, v_dev, status_dev,
                                          reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;
@@ -251,7 +262,7 @@ int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32
   if (err != NK_OK) return err;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (!no_append) {
-    const cudaError_t e = launch_kv_append(sm_count(), *pool, block_table_dev, max_pages_per_seq, start_pos_dev,
+    const cudaError_t e = launch_kv_append(sm_count(), *pool, kFmtI8F32, block_table_dev, max_pages_per_seq, start_pos_dev,
                                            cu_new_dev, B, total_new, k_dev, v_dev, status_dev, st);
     if (e != cudaSuccess) return NK_ERR_CUDA;
   }
@@ -329,6 +340,68 @@ int nk_rk8v4_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_
                          size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream) {
   return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
                       max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kRk8v4);
+}
+
+size_t nk_i8f16_chunk_bytes(int32_t page_size, int32_t head_dim) {
+  if (page_size < 1 || head_dim < kGroup || head_dim % kGroup != 0) return 0;
+  return (size_t)i8f16_layout(page_size, head_dim).chunk;
+}
+
+size_t nk_i8f16_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_pages < 0 || num_kv_heads < 1) return 0;
+  return (size_t)num_pages * (size_t)num_kv_heads * nk_i8f16_chunk_bytes(page_size, head_dim);
+}
+
+size_t nk_bf16kv_chunk_bytes(int32_t page_size, int32_t head_dim) {
+  if (page_size < 1 || head_dim < kGroup || head_dim % kGroup != 0) return 0;
+  return (size_t)bf16kv_layout(page_size, head_dim).chunk;
+}
+
+size_t nk_bf16kv_pool_bytes(int32_t num_pages, int32_t page_size, int32_t num_kv_heads, int32_t head_dim) {
+  if (num_pages < 0 || num_kv_heads < 1) return 0;
+  return (size_t)num_pages * (size_t)num_kv_heads * nk_bf16kv_chunk_bytes(page_size, head_dim);
+}
+
+static int append_fmt(int fmt, const nk_kv_pool* pool, const int32_t* bt, int32_t max_pages, const int32_t* start_pos,
+                      const int32_t* cu_new, int32_t B, int32_t total_new, const void* k, const void* v,
+                      int32_t* status, void* stream) {
+  bool empty = true;
+  const int err = check_append(pool, bt, max_pages, start_pos, cu_new, B, total_new, k, v, &empty);
+  if (err != NK_OK || empty) return err;
+  const cudaError_t e = launch_kv_append(sm_count(), *pool, fmt, bt, max_pages, start_pos, cu_new, B, total_new, k, v,
+                                         status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? NK_OK : NK_ERR_CUDA;
+}
+
+int nk_i8f16_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                    const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                    const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream) {
+  return append_fmt(kFmtI8F16, pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B, total_new,
+                    k_dev, v_dev, status_dev, stream);
+}
+
+int nk_bf16kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                     const int32_t* start_pos_dev, const int32_t* cu_new_dev, int32_t B, int32_t total_new,
+                     const void* k_dev, const void* v_dev, int32_t* status_dev, void* stream) {
+  return append_fmt(kFmtBf16, pool, block_table_dev, max_pages_per_seq, start_pos_dev, cu_new_dev, B, total_new,
+                    k_dev, v_dev, status_dev, stream);
+}
+
+int nk_i8f16_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                         int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                         int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
+                         size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream) {
+  return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kTensorF16);
+}
+
+int nk_bf16kv_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
+                          void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
+                          void* stream) {
+  return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
+                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kBf16);
 }
 
 int nk_attn_combine(const float* part_o_dev, const float* part_lse_dev, int32_t num_splits, int32_t rows,

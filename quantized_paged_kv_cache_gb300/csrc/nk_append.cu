@@ -119,6 +119,65 @@ __device__ __forceinline__ float quantize64(const uint32_t (&w)[32], uint32_t (&
   return s;
 }
 
+// The same for a group with an fp16 scale (the pages' INT8 layout):
+// s = RN_fp16(a / 127) -- fp32(a / 127) rounded again to fp16 is that
+// correctly rounded quotient, as for the rk8v4 keys -- stored as 1 when it
+// rounds to 0 and as 65504 (with `range` set) past the fp16 maximum. The codes
+// come from the same refined quotient with y = RN(1/s), replayed on the CPU
+// for fp16 scales too (tests/quotient_check.c); a group whose scale is an fp16
+// subnormal or saturated, where |x / s| can pass 127, divides per element and
+// clamps. Returns the scale's fp16 bits.
+__device__ __forceinline__ uint32_t quantize64_f16(const uint32_t (&w)[32], uint32_t (&packed)[16], bool& range) {
+  uint32_t m2 = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m2 = __vmaxu2(m2, w[i] & 0x7fff7fffu);
+  const uint32_t abits = max(m2 << 16, m2 & 0xffff0000u);  // fp32 bits of a
+  uint32_t sb = 0x3c00u;  // a = 0: scale 1, every code 0
+  bool per_element = false;
+  if (abits != 0u) {
+    sb = __half_as_ushort(__float2half_rn(__fdiv_rn(__uint_as_float(abits), 127.f)));
+    if ((sb & 0x7fffu) == 0u) {
+      sb = 0x3c00u;  // below the fp16 range: |x| < 2^-17, every code 0
+    } else if ((sb & 0x7fffu) >= 0x7c00u) {
+      sb = 0x7bffu;
+      range = true;
+      per_element = true;
+    } else if ((sb & 0x7c00u) == 0u) {
+      per_element = true;  // subnormal scale: relative rounding beyond 2^-11
+    }
+  }
+  const float s = __half2float(__ushort_as_half((unsigned short)sb));
+  if (per_element) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t wv = w[2 * k + (e >> 1)];
+        word |= quantize_exact((e & 1) ? bf16_hi(wv) : bf16_lo(wv), s) << (8 * e);
+      }
+      packed[k] = word;
+    }
+    return sb;
+  }
+  const float y = __frcp_rn(s), ns = -s;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    uint32_t tb[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t wv = w[2 * k + (e >> 1)];
+      const float x = (e & 1) ? bf16_hi(wv) : bf16_lo(wv);
+      const float q0 = __fmul_rn(x, y);
+      const float r = __fmaf_rn(ns, q0, x);
+      const float q = __fmaf_rn(r, y, q0);
+      tb[e] = __float_as_uint(__fadd_rn(q, 12582912.f));
+    }
+    packed[k] = __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
+  }
+  return sb;
+}
+
 constexpr int kAppendThreads = 128;     // one 64-channel group per thread and chunk
 constexpr int kAppendStages = 3;
 constexpr int kAppendBlocksPerSM = 3;
@@ -149,7 +208,7 @@ struct __align__(128) AppendSmem {
 // [K|V][row][D] buffer; after one block barrier the stage is refilled and the
 // block stores the codes with coalesced 16-byte writes, one row of one tensor
 // being D contiguous bytes of its page.
-template <int D>
+template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_kernel(const AppendParams p) {
   chain_wait();
   chain_release();
@@ -250,6 +309,25 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
       flag(p.status, NK_DEVFLAG_TIMEOUT);
       return;
     }
+    if constexpr (FMT == kFmtBf16) {
+      // the rows as they are: 16-byte pieces straight from the stage into
+      // their pages (one row of one tensor is D bf16 values of its page)
+#pragma unroll
+      for (int i = 0; i < 2 * kChunkBytes / (16 * kAppendThreads); ++i) {
+        const int o = (i * kAppendThreads + t) * 16;
+        const int tv = o / kChunkBytes, rem = o % kChunkBytes, r = rem / (2 * D), col = rem % (2 * D);
+        const int2 dd = dest[r];
+        if (r < rows && dd.x >= 0)
+          *reinterpret_cast<uint4*>(p.pool + (int64_t)dd.x * p.lay.chunk + (tv ? p.lay.vc : 0) + dd.y * (2 * D) +
+                                    col) = *reinterpret_cast<const uint4*>(sm.stage[st] + o);
+      }
+      __syncthreads();  // stage st fully read
+      if (t == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue(k + kAppendStages);
+      }
+      continue;
+    }
     // load the group (pieces in rotated order), quantize
     uint32_t w[32];
     const uint8_t* src = sm.stage[st] + isv * kChunkBytes + gk * 128;
@@ -260,7 +338,11 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
       w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
     uint32_t packed[16];  // codes of the pieces in the same rotated order
-    const float s = quantize64<true>(w, packed, sm.tab);
+    bool range = false;
+    float s = 0.f;
+    uint32_t sb16 = 0u;
+    if constexpr (FMT == kFmtI8F16) sb16 = quantize64_f16(w, packed, range);
+    else s = quantize64<true>(w, packed, sm.tab);
     uint8_t* codes = sm.codes[k & 1];
     uint8_t* cdst = codes + isv * (R * D) + row * D + grp * kGroup;
 #pragma unroll
@@ -269,9 +351,15 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
       *reinterpret_cast<uint2*>(cdst + piece * 8) = make_uint2(packed[2 * i], packed[2 * i + 1]);
     }
     const int2 d = dest[row];
-    if (row < rows && d.x >= 0)
-      *reinterpret_cast<float*>(p.pool + (int64_t)d.x * p.lay.chunk + (isv ? p.lay.vs : p.lay.ks) +
-                                (d.y * GPR + grp) * 4) = s;
+    if (row < rows && d.x >= 0) {
+      uint8_t* sdst = p.pool + (int64_t)d.x * p.lay.chunk + (isv ? p.lay.vs : p.lay.ks);
+      if constexpr (FMT == kFmtI8F16) {
+        *reinterpret_cast<uint16_t*>(sdst + (d.y * GPR + grp) * 2) = (uint16_t)sb16;
+        if (range) flag(p.status, NK_DEVFLAG_RANGE);
+      } else {
+        *reinterpret_cast<float*>(sdst + (d.y * GPR + grp) * 4) = s;
+      }
+    }
     __syncthreads();  // stage st fully read, codes of chunk k complete, codes of chunk k - 1 stored
     if (t == 0) {
       // generic-proxy reads of the stage are ordered before the bulk copy that refills it
@@ -300,7 +388,7 @@ constexpr int64_t kSmallMaxGroups = 4096;  // appends up to this many groups tak
 // (binary search over cu_new, block-table entry) runs while they are in
 // flight; s = fp32(a / 127) and RN(1/s) come from IEEE division; the codes
 // from the same exact quotient as the streaming kernel.
-template <int D>
+template <int D, int FMT>
 __global__ void __launch_bounds__(kSmallThreads) kv_append_small_kernel(const AppendParams p) {
   chain_wait();
   chain_release();
@@ -354,7 +442,11 @@ __global__ void __launch_bounds__(kSmallThreads) kv_append_small_kernel(const Ap
   if (!live) return;
   const int64_t pos64 = (int64_t)st0 + ((int)j - c0);
   uint32_t packed[16];
-  const float s = quantize64<false>(w, packed, nullptr);
+  bool range = false;
+  float s = 0.f;
+  uint32_t sb16 = 0u;
+  if constexpr (FMT == kFmtI8F16) sb16 = quantize64_f16(w, packed, range);
+  else if constexpr (FMT == kFmtI8F32) s = quantize64<false>(w, packed, nullptr);
   if (pos64 < 0 || pos64 >= (int64_t)p.max_pages * p.P || pos64 > 0x7fffffff) {
     if (flagger) flag(p.status, NK_DEVFLAG_BAD_POS);
     return;
@@ -368,22 +460,57 @@ __global__ void __launch_bounds__(kSmallThreads) kv_append_small_kernel(const Ap
   }
   const int slot = p.p_shift >= 0 ? (pos & (p.P - 1)) : (int)((uint32_t)pos % (uint32_t)p.P);
   uint8_t* chunk = p.pool + ((int64_t)page * p.Hkv + h) * p.lay.chunk;
+  if constexpr (FMT == kFmtBf16) {
+    uint4* dst = reinterpret_cast<uint4*>(chunk + (isv ? p.lay.vc : 0) + slot * (2 * D) + grp * (2 * kGroup));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    return;
+  }
   uint4* dst = reinterpret_cast<uint4*>(chunk + (isv ? p.lay.vc : 0) + slot * D + grp * kGroup);
 #pragma unroll
   for (int i = 0; i < 4; ++i) dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-  *reinterpret_cast<float*>(chunk + (isv ? p.lay.vs : p.lay.ks) + (slot * GPR + grp) * 4) = s;
+  if constexpr (FMT == kFmtI8F16) {
+    *reinterpret_cast<uint16_t*>(chunk + (isv ? p.lay.vs : p.lay.ks) + (slot * GPR + grp) * 2) = (uint16_t)sb16;
+    if (range) flag(p.status, NK_DEVFLAG_RANGE);
+  } else {
+    *reinterpret_cast<float*>(chunk + (isv ? p.lay.vs : p.lay.ks) + (slot * GPR + grp) * 4) = s;
+  }
 }
 
-cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages, const int32_t* start_pos,
-                             const int32_t* cu_new, int B, int total_new, const void* k, const void* v,
-                             int32_t* status, cudaStream_t stream) {
+template <int D, int FMT>
+static cudaError_t launch_append_d(int sms, const AppendParams& p, int64_t groups, int64_t pairs, cudaStream_t stream) {
+  if (groups <= kSmallMaxGroups) {
+    const unsigned g = (unsigned)((groups + kSmallThreads - 1) / kSmallThreads);
+    return launch_chained(kv_append_small_kernel<D, FMT>, dim3(g), dim3(kSmallThreads), 0, stream, p);
+  }
+  if (sms < 1) sms = 1;
+  const int64_t rows_per_chunk = kChunkBytes / (2 * D);
+  const int64_t nchunks = (pairs + rows_per_chunk - 1) / rows_per_chunk;
+  const int64_t grid = nchunks < (int64_t)sms * kAppendBlocksPerSM ? nchunks : (int64_t)sms * kAppendBlocksPerSM;
+  const int smem = (int)sizeof(AppendSmem);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<D, FMT>), smem);
+  if (e != cudaSuccess) return e;
+  return launch_chained(kv_append_kernel<D, FMT>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
+}
+
+template <int FMT>
+static cudaError_t launch_append_fmt(int sms, const AppendParams& p, int64_t groups, int64_t pairs,
+                                     cudaStream_t stream) {
+  if (p.D == 256) return launch_append_d<256, FMT>(sms, p, groups, pairs, stream);
+  if (p.D == 128) return launch_append_d<128, FMT>(sms, p, groups, pairs, stream);
+  return launch_append_d<64, FMT>(sms, p, groups, pairs, stream);
+}
+
+cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, int fmt, const int32_t* bt, int max_pages,
+                             const int32_t* start_pos, const int32_t* cu_new, int B, int total_new, const void* k,
+                             const void* v, int32_t* status, cudaStream_t stream) {
   AppendParams p;
   p.pool = reinterpret_cast<uint8_t*>(pool.base_dev);
   p.num_pages = pool.num_pages;
   p.P = pool.page_size;
   p.Hkv = pool.num_kv_heads;
   p.D = pool.head_dim;
-  p.lay = ChunkLayout::make(p.P, p.D);
+  p.lay = layout_of(fmt, p.P, p.D);
   p.bt = bt;
   p.max_pages = max_pages;
   p.start_pos = start_pos;
@@ -404,32 +531,9 @@ cudaError_t launch_kv_append(int sms, const nk_kv_pool& pool, const int32_t* bt,
   if (pairs * 2 * (p.D / kGroup) >= ((int64_t)1 << 31)) return cudaErrorInvalidValue;  // 32-bit numbering
   if (pairs == 0) return cudaSuccess;
   const int64_t groups = pairs * 2 * (p.D / kGroup);
-  if (groups <= kSmallMaxGroups) {
-    const unsigned g = (unsigned)((groups + kSmallThreads - 1) / kSmallThreads);
-    if (p.D == 256) return launch_chained(kv_append_small_kernel<256>, dim3(g), dim3(kSmallThreads), 0, stream, p);
-    if (p.D == 128) return launch_chained(kv_append_small_kernel<128>, dim3(g), dim3(kSmallThreads), 0, stream, p);
-    return launch_chained(kv_append_small_kernel<64>, dim3(g), dim3(kSmallThreads), 0, stream, p);
-  }
-  if (sms < 1) sms = 1;
-  const int64_t rows_per_chunk = kChunkBytes / (2 * p.D);
-  const int64_t nchunks = (pairs + rows_per_chunk - 1) / rows_per_chunk;
-  const int64_t grid = nchunks < (int64_t)sms * kAppendBlocksPerSM ? nchunks : (int64_t)sms * kAppendBlocksPerSM;
-  const int smem = (int)sizeof(AppendSmem);
-  cudaError_t e;
-  if (p.D == 256) {
-    e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<256>), smem);
-    if (e == cudaSuccess)
-      e = launch_chained(kv_append_kernel<256>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
-  } else if (p.D == 128) {
-    e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<128>), smem);
-    if (e == cudaSuccess)
-      e = launch_chained(kv_append_kernel<128>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
-  } else {
-    e = set_smem_limit(reinterpret_cast<const void*>(kv_append_kernel<64>), smem);
-    if (e == cudaSuccess)
-      e = launch_chained(kv_append_kernel<64>, dim3((unsigned)grid), dim3(kAppendThreads), smem, stream, p);
-  }
-  return e;
+  if (fmt == kFmtI8F16) return launch_append_fmt<kFmtI8F16>(sms, p, groups, pairs, stream);
+  if (fmt == kFmtBf16) return launch_append_fmt<kFmtBf16>(sms, p, groups, pairs, stream);
+  return launch_append_fmt<kFmtI8F32>(sms, p, groups, pairs, stream);
 }
 
 }  // namespace nk

@@ -34,6 +34,40 @@ struct ChunkLayout {
   }
 };
 
+// KV formats a pool can hold (the same nk_kv_pool struct describes each; the
+// calls of a format take only pools sized for it):
+//   kFmtI8F32  INT8 group-64 codes with fp32 scales (nk_kv_*);
+//   kFmtI8F16  the same codes with fp16 scales, the layout whose size the
+//              "NInfer-3090" README's "Choosing a KV format" table gives
+//              (nk_i8f16_*);
+//   kFmtBf16   the unquantized bf16 rows of the same table (nk_bf16kv_*).
+enum KvFmt : int { kFmtI8F32 = 0, kFmtI8F16 = 1, kFmtBf16 = 2 };
+
+// Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D] int8 | Vs[P][D/64] fp16
+__host__ __device__ inline ChunkLayout i8f16_layout(int P, int D) {
+  ChunkLayout c;
+  const int64_t g = D / kGroup;
+  c.ks = (int64_t)P * D;
+  c.vc = c.ks + (int64_t)P * g * 2;
+  c.vs = c.vc + (int64_t)P * D;
+  c.chunk = c.vs + (int64_t)P * g * 2;
+  return c;
+}
+
+// K[P][D] bf16 | V[P][D] bf16 (no scales: ks = vs = 0)
+__host__ __device__ inline ChunkLayout bf16kv_layout(int P, int D) {
+  ChunkLayout c;
+  c.ks = 0;
+  c.vc = (int64_t)P * D * 2;
+  c.vs = 0;
+  c.chunk = 2 * c.vc;
+  return c;
+}
+
+__host__ __device__ inline ChunkLayout layout_of(int fmt, int P, int D) {
+  return fmt == kFmtI8F16 ? i8f16_layout(P, D) : (fmt == kFmtBf16 ? bf16kv_layout(P, D) : ChunkLayout::make(P, D));
+}
+
 // Programmatic dependent launch. Every kernel of the library is launched
 // with programmatic stream serialization (launch_chained), so it may become
 // resident while the previous kernel on the stream is still running. Each one

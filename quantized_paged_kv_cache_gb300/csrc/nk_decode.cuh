@@ -34,6 +34,7 @@ struct DecodeParams {
   // are visible: the append itself waited for every earlier kernel before
   // this kernel could start.
   int early;
+  int fmt;  // KvFmt of the pool (the rk8v4 kernel ignores it)
   // Failure-detection tests (nk_test_inject_copy_stall): every bounded wait
   // gives up after wait_cycles, and the page copies of CTA page numbers
   // >= withhold are never issued (-1: all issued).
@@ -55,12 +56,12 @@ __device__ __forceinline__ void flag_bad_ctx(const DecodeParams& p) {
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
-bool decode_tc_supported(int D, int T, int G, int P);
+bool decode_tc_supported(int fmt, int D, int T, int G, int P);
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_attn_combine(const float* part_o, const float* part_lse, int S, int R, int D, uint16_t* out,
                                 cudaStream_t stream);
 int decode_simt_ctas_per_sm(int D, int G);
 int decode_mma_ctas_per_sm(int D, int T, int G);
-bool decode_mma_supported(int D, int T, int G, int P);
+bool decode_mma_supported(int fmt, int D, int T, int G, int P);
 
 }  // namespace nk

@@ -43,31 +43,35 @@ cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map) {
   // host work on the critical path of every call)
   struct Cached {
     const void* base;
-    int num_pages, P, Hkv, D;
+    int num_pages, P, Hkv, D, fmt;
     CUtensorMap map;
   };
   thread_local Cached cache[8];
   thread_local int used = 0, next = 0;
   for (int i = 0; i < used; ++i) {
     const Cached& c = cache[i];
-    if (c.base == p.pool && c.num_pages == p.num_pages && c.P == p.P && c.Hkv == p.Hkv && c.D == p.D) {
+    if (c.base == p.pool && c.num_pages == p.num_pages && c.P == p.P && c.Hkv == p.Hkv && c.D == p.D &&
+        c.fmt == p.fmt) {
       *map = c.map;
       return cudaSuccess;
     }
   }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
+  // bf16 pools: 2-byte elements, boxes of 64 channels (128-byte rows)
+  const bool bf = p.fmt == kFmtBf16;
+  const cuuint64_t esize = bf ? 2 : 1;
   cuuint64_t dims[4] = {(cuuint64_t)p.D, (cuuint64_t)p.P, 2, (cuuint64_t)p.num_pages * p.Hkv};
-  cuuint64_t strides[3] = {(cuuint64_t)p.D, (cuuint64_t)p.lay.vc, (cuuint64_t)p.lay.chunk};
-  cuuint32_t box[4] = {(cuuint32_t)(p.D < 128 ? p.D : 128), (cuuint32_t)p.P, 2, 1};
+  cuuint64_t strides[3] = {(cuuint64_t)p.D * esize, (cuuint64_t)p.lay.vc, (cuuint64_t)p.lay.chunk};
+  cuuint32_t box[4] = {(cuuint32_t)(bf ? 64 : (p.D < 128 ? p.D : 128)), (cuuint32_t)p.P, 2, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(p.pool), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        p.D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = fn(map, bf ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                        const_cast<uint8_t*>(p.pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        (p.D == 64 && !bf) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   Cached& c = cache[next];
-  c = Cached{p.pool, p.num_pages, p.P, p.Hkv, p.D, *map};
+  c = Cached{p.pool, p.num_pages, p.P, p.Hkv, p.D, p.fmt, *map};
   next = (next + 1) % 8;
   if (used < 8) ++used;
   return cudaSuccess;
@@ -79,12 +83,12 @@ cudaError_t launch_d64(const CUtensorMap& map, const DecodeParams& p, int NT, cu
 
 }  // namespace mma
 
-bool decode_mma_supported(int D, int T, int G, int P) {
+bool decode_mma_supported(int fmt, int D, int T, int G, int P) {
   const int M = G * T;
   if (M < 1 || M > 48 || P % 16 != 0 || P > 256) return false;
   if (!(D == 64 || D == 128 || D == 256)) return false;
   const int NT = (M + 7) / 8;
-  const mma::Geometry g = mma::geometry(D, NT, mma::channel_split(D, NT), P, kMaxBatch);
+  const mma::Geometry g = mma::geometry(fmt, D, NT, mma::channel_split(D, NT), P, kMaxBatch);
   return g.stages >= 2;
 }
 

@@ -76,12 +76,13 @@ struct Geometry {
 
 __host__ __device__ inline int round_up(int x, int a) { return (x + a - 1) / a * a; }
 
-// Shared-memory plan. Needs D, NT, CS, P (and B for the prefix array).
-__host__ __device__ inline Geometry geometry(int D, int NT, int CS, int P, int B) {
+// Shared-memory plan. Needs the pool format, D, NT, CS, P (and B for the
+// prefix array). A bf16 pool stages 2-byte K|V values and no scales.
+__host__ __device__ inline Geometry geometry(int fmt, int D, int NT, int CS, int P, int B) {
   Geometry g;
   const int nteams = kConsumerWarps / CS;
-  const int kv_bytes = 2 * P * D;
-  const int sc_bytes = 2 * P * (D / kGroup) * 4;
+  const int kv_bytes = 2 * P * D * (fmt == kFmtBf16 ? 2 : 1);
+  const int sc_bytes = fmt == kFmtBf16 ? 0 : 2 * P * (D / kGroup) * (fmt == kFmtI8F16 ? 2 : 4);
   g.stage_bytes = round_up(kv_bytes + sc_bytes, 1024);
   g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
   const int mrows = NT * 8;
@@ -147,6 +148,14 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -196,6 +205,15 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 //     accumulator rescaled by 2^(ev_old - ev_new), like the softmax
 //     reference. The output is O 2^-ev times 2^ev.
 // ---------------------------------------------------------------------------
+// Bytes of one group scale in a pool of format fmt: fp32 for the INT8 layout
+// with fp32 scales, fp16 for the pages' own INT8 layout.
+__host__ __device__ inline int scale_bytes(int fmt) { return fmt == kFmtI8F16 ? 2 : 4; }
+
+// Scale number idx of a page's scale array (fp32 or fp16 elements).
+__device__ __forceinline__ float ld_scale(const uint8_t* arr, int idx, int sb) {
+  return sb == 2 ? __half2float(reinterpret_cast<const __half*>(arr)[idx]) : reinterpret_cast<const float*>(arr)[idx];
+}
+
 // 2^e as fp32, -126 <= e <= 127.
 __device__ __forceinline__ float pow2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
@@ -262,12 +280,24 @@ __device__ __forceinline__ int page_coord(const DecodeParams& p, const SplitShap
 
 // Load the CTA's page number q into its stage: TMA boxes of the K|V codes
 // plus bulk copies of the two scale arrays, all completing on full_bar.
-template <int D>
+template <int D, bool BF = false>
 __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensorMap* tmap, int z, uint32_t dst,
                                            uint32_t fb) {
   const int P = p.P;
+  if constexpr (BF) {
+    // bf16 rows: boxes of [64 channels][P keys][K|V] (128-byte rows), no scales
+    if (z < 0) {
+      flag(p.status, NK_DEVFLAG_BAD_PAGE);
+      mbar_arrive(fb);
+      return;
+    }
+    mbar_arrive_expect_tx(fb, 2 * P * D * 2);
+#pragma unroll
+    for (int bx = 0; bx < D / 64; ++bx) tma_load_4d(dst + bx * 2 * P * 128, tmap, fb, bx * 64, 0, 0, z);
+    return;
+  }
   const int kv_bytes = 2 * P * D;
-  const int sc_bytes = P * (D / kGroup) * 4;
+  const int sc_bytes = P * (D / kGroup) * scale_bytes(p.fmt);
   if (z < 0) {
     flag(p.status, NK_DEVFLAG_BAD_PAGE);
     mbar_arrive(fb);  // release the consumers; the stage keeps stale data
@@ -288,7 +318,10 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, int NT, int CS>
+// BF: the pool holds bf16 rows (the unquantized layout): K and V enter the
+// MMAs as they are (bf16 operands, Q bf16 too), there are no scales, and P
+// enters the PV product as bf16 hi + lo.
+template <int D, int NT, int CS, bool BF>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                  const DecodeParams p) {
   // the tensor map is a launch parameter (no earlier kernel writes it): its
@@ -306,8 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Geometry geo = geometry(D, NT, CS, p.P, p.B);
+  const Geometry geo = geometry(p.fmt, D, NT, CS, p.P, p.B);
   const int S = geo.stages;
+  const int sb = scale_bytes(p.fmt);
   int* pre = reinterpret_cast<int*>(smem + geo.pre_off);
   int* warp_tot = pre + (p.B + 1);
   volatile int* abort_flag = pre + (p.B + 1) + 8;
@@ -368,12 +402,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
     for (int q2 = 0; q2 < 2; ++q2) loff[gi][q2] = box_off<D>(P, 0, lm_key, (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk);
+  // bf16 stage: boxes of 64 channels, 128-byte rows (K rows, then V rows),
+  // 128-byte swizzle. K fragments of a 16-channel chunk: matrices (keys 0-7 |
+  // 8-15) x (channels 0-7 | 8-15); V^T fragments (transposed loads): matrices
+  // (channels 0-7 | 8-15) x (keys 0-7 | 8-15).
+  auto bf_off = [&](int row, int ch8) -> uint32_t {
+    return (uint32_t)((ch8 >> 3) * (2 * P * 128) + row * 128 + (((ch8 & 7) ^ (row & 7)) << 4));
+  };
+  uint32_t kof[BF ? NCH : 1], vof[BF ? NCH : 1];
+  if constexpr (BF) {
+    const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      kof[c] = bf_off((mi & 1) * 8 + r8, (ch0 >> 3) + 2 * c + (mi >> 1));
+      vof[c] = bf_off(P + (mi >> 1) * 8 + r8, (ch0 >> 3) + 2 * c + (mi & 1));
+    }
+  }
 
   uint32_t bq[NT][NCH][2];
   float o[NCH][NT][4];
   float m_run[NT][2], l_run[NT][2];
-  int ev[GW];    // exponent of this warp's P' per group (kEvUnset before the segment's first block)
-  float sv[GW];  // 2^-ev
+  float sv[GW];  // 2^-ev of this warp's P' per group (0 before the segment's first block)
   int row_t[NT][2];  // verify column of each held row (T - 1 for padding rows)
 
   // Q fragments of this warp's channels, all rows of a segment's unit:
@@ -389,8 +438,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         uint2 raw = make_uint2(0u, 0u);
         if (r < M) {
           const int t = r / G, hg = r % G;
-          raw = *reinterpret_cast<const uint2*>(p.q + (((int64_t)sg.b * p.qT + t) * p.Hq + sg.h * G + hg) * D + ch0 +
-                                                c * 16 + t4 * 4);
+          const uint16_t* qr = p.q + (((int64_t)sg.b * p.qT + t) * p.Hq + sg.h * G + hg) * D + ch0 + c * 16;
+          if constexpr (BF)  // the standard B layout: channels 2 t4, 2 t4 + 1 and 2 t4 + 8, 2 t4 + 9
+            raw = make_uint2(*reinterpret_cast<const uint32_t*>(qr + 2 * t4),
+                             *reinterpret_cast<const uint32_t*>(qr + 2 * t4 + 8));
+          else
+            raw = *reinterpret_cast<const uint2*>(qr + t4 * 4);
         }
         bq[nt][c][0] = raw.x;
         bq[nt][c][1] = raw.y;
@@ -430,41 +483,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
       for (int c = 0; c < NCH; ++c) {
         uint2 raw = make_uint2(0u, 0u);
-        if (r < M) raw = *reinterpret_cast<const uint2*>(qstage + r * kQRow + (ch0 + c * 16 + t4 * 4) * 2);
+        if (r < M) {
+          if constexpr (BF)
+            raw = make_uint2(*reinterpret_cast<const uint32_t*>(qstage + r * kQRow + (ch0 + c * 16 + 2 * t4) * 2),
+                             *reinterpret_cast<const uint32_t*>(qstage + r * kQRow + (ch0 + c * 16 + 2 * t4 + 8) * 2));
+          else
+            raw = *reinterpret_cast<const uint2*>(qstage + r * kQRow + (ch0 + c * 16 + t4 * 4) * 2);
+        }
         bq[nt][c][0] = raw.x;
         bq[nt][c][1] = raw.y;
       }
     }
   };
-  // Each warp scales its channel slice of a query row by 2^e (from the
-  // slice's largest |q|, over the four lanes that hold the row) before the
-  // fp16 conversion, and its partial scores by rsc = 2^-e.
-  float rsc[NT][2];
+  // Each warp scales its channel slice of the unit's query rows by one power
+  // of two 2^e (from the slice's largest |q| over all rows) before the fp16
+  // conversion; kq = sm_scale log2(e) 2^-e undoes it on the partial scores
+  // (folded into the key scales: no work per block).
+  float kq = p.scale2;
   auto convert_q = [&]() {
-    float rq[NT];
+    kq = p.scale2;
+    if constexpr (BF) return;  // bf16 operands as they are, no scaling
+    float m = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float m = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int h = 0; h < 2; ++h) m = fmaxf(m, fmaxf(fabsf(bf16_lo(bq[nt][c][h])), fabsf(bf16_hi(bq[nt][c][h]))));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-      const int e = q_norm_exp(m);
-      const float qs = pow2i(e);
-      rq[nt] = pow2i(-e);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int e = q_norm_exp(m);
+    const float qs = pow2i(e);
+    kq = p.scale2 * pow2i(-e);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           bq[nt][c][h] = pack_f16(bf16_lo(bq[nt][c][h]) * qs, bf16_hi(bq[nt][c][h]) * qs);
-    }
-    // score rows are 2 t4 + e of each tile: their factors from the lanes holding them
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) rsc[nt][e2] = __shfl_sync(0xffffffffu, rq[nt], (2 * t4 + e2) * 4);
   };
 
   // Every global read of the prologue -- the first unit's Q (converted at
@@ -487,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     const int n0 = total < S ? total : S;
     for (int q = 0; q < n0; ++q) {
       if (!p.issuable(q)) break;
-      issue_page<D>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+      issue_page<D, BF>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
       icnt[q] = 1;
     }
   }
@@ -529,10 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         for (int k = 0; k < 4; ++k) o[c][nt][k] = 0.f;
     }
 #pragma unroll
-    for (int gi = 0; gi < GW; ++gi) {
-      ev[gi] = kEvUnset;
-      sv[gi] = 1.f;
-    }
+    for (int gi = 0; gi < GW; ++gi) sv[gi] = BF ? 1.f : 0.f;
 
     // this team's blocks of the segment: CTA-wide block numbers jn = team,
     // team + NTEAMS, ... (4 blocks of 16 keys per 64-key page)
@@ -551,8 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       const int s = s_cur;
       const uint32_t par = par_cur;
       const uint32_t st = stage0 + s * geo.stage_bytes;
-      const float* ks_s = reinterpret_cast<const float*>(smem + s * geo.stage_bytes + 2 * P * D);
-      const float* vs_s = ks_s + P * G_ALL;
+      const uint8_t* ks_s = smem + s * geo.stage_bytes + 2 * P * D;  // [P][G_ALL], fp32 or fp16
+      const uint8_t* vs_s = ks_s + P * G_ALL * sb;
       {
         // after one wait of the CTA has run out, no wait blocks any more (the
         // blocks run without data and nothing more is issued; the end of the
@@ -565,14 +619,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         const int pos0 = pi * P + key0;  // sequence position of the block's key 0
         if (pos0 < L) {
           // ---- QK: per-group fp32 partial dot products (GW*NT independent accumulators)
-          uint32_t kw[GW][4][2];  // [group][chunk][keys 0-7 | 8-15]
-          const uint32_t kbase = st + key0 * RB;
-#pragma unroll
-          for (int gi = 0; gi < GW; ++gi)
-#pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2)
-              ldsm_x4(kbase + loff[gi][q2], kw[gi][q2 * 2][0], kw[gi][q2 * 2][1], kw[gi][q2 * 2 + 1][0],
-                      kw[gi][q2 * 2 + 1][1]);
           float acc[GW][NT][4];
 #pragma unroll
           for (int gi = 0; gi < GW; ++gi)
@@ -580,17 +626,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int k = 0; k < 4; ++k) acc[gi][nt][k] = 0.f;
+          if constexpr (BF) {
+            // bf16 K fragments straight from the tile, one ldmatrix per 16 channels
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
+            for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-            for (int gi = 0; gi < GW; ++gi) {
-              const uint32_t lo = kw[gi][cc][0] ^ bias, hi = kw[gi][cc][1] ^ bias;
-              const uint32_t a0 = i8x2_to_f16x2(lo, 0x4140), a2 = i8x2_to_f16x2(lo, 0x4342);
-              const uint32_t a1 = i8x2_to_f16x2(hi, 0x4140), a3 = i8x2_to_f16x2(hi, 0x4342);
+              for (int cc = 0; cc < 4; ++cc) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(st + key0 * 128 + kof[gi * 4 + cc], a0, a1, a2, a3);
 #pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma16816(acc[gi][nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
-            }
+                for (int nt = 0; nt < NT; ++nt)
+                  mma16816_bf16(acc[gi][nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
+              }
+          } else {
+            uint32_t kw[GW][4][2];  // [group][chunk][keys 0-7 | 8-15]
+            const uint32_t kbase = st + key0 * RB;
+#pragma unroll
+            for (int gi = 0; gi < GW; ++gi)
+#pragma unroll
+              for (int q2 = 0; q2 < 2; ++q2)
+                ldsm_x4(kbase + loff[gi][q2], kw[gi][q2 * 2][0], kw[gi][q2 * 2][1], kw[gi][q2 * 2 + 1][0],
+                        kw[gi][q2 * 2 + 1][1]);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int gi = 0; gi < GW; ++gi) {
+                const uint32_t lo = kw[gi][cc][0] ^ bias, hi = kw[gi][cc][1] ^ bias;
+                const uint32_t a0 = i8x2_to_f16x2(lo, 0x4140), a2 = i8x2_to_f16x2(lo, 0x4342);
+                const uint32_t a1 = i8x2_to_f16x2(hi, 0x4140), a3 = i8x2_to_f16x2(hi, 0x4342);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma16816(acc[gi][nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
+              }
+          }
           float sc[NT][4];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
@@ -598,8 +666,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             for (int k = 0; k < 4; ++k) sc[nt][k] = 0.f;
 #pragma unroll
           for (int gi = 0; gi < GW; ++gi) {
-            const float k0 = ks_s[(key0 + g) * G_ALL + grp0 + gi] * p.scale2;
-            const float k1 = ks_s[(key0 + g + 8) * G_ALL + grp0 + gi] * p.scale2;
+            const float k0 = BF ? p.scale2 : ld_scale(ks_s, (key0 + g) * G_ALL + grp0 + gi, sb) * kq;
+            const float k1 = BF ? p.scale2 : ld_scale(ks_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb) * kq;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               sc[nt][0] = fmaf(k0, acc[gi][nt][0], sc[nt][0]);
@@ -608,11 +676,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
               sc[nt][3] = fmaf(k1, acc[gi][nt][3], sc[nt][3]);
             }
           }
-          // undo the power of two of this warp's Q slice
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) sc[nt][k] *= rsc[nt][k & 1];
 
           // ---- team exchange: every warp of the team sums the CS partials in warp order
           if constexpr (CS > 1) {
@@ -699,64 +762,127 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             l_run[nt][1] += pr[nt][1] + pr[nt][3];
           }
 
+          if constexpr (BF) {
+            // ---- PV with P as bf16 hi + lo (16 significant bits) and the bf16 V^T
+            uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const __nv_bfloat162 h01 = __floats2bfloat162_rn(pr[nt][0], pr[nt][1]);
+              const __nv_bfloat162 h23 = __floats2bfloat162_rn(pr[nt][2], pr[nt][3]);
+              const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+              const __nv_bfloat162 l01 = __floats2bfloat162_rn(pr[nt][0] - f01.x, pr[nt][1] - f01.y);
+              const __nv_bfloat162 l23 = __floats2bfloat162_rn(pr[nt][2] - f23.x, pr[nt][3] - f23.y);
+              bh[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h01));
+              bh[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h23));
+              bl[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&l01));
+              bl[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&l23));
+            }
+            // slots past ctx_len may hold any bits (NaN): their V is zeroed, not
+            // multiplied by p = 0. This thread's keys: 2 t4 + {0, 1} (a0, a1) and
+            // 2 t4 + 8 + {0, 1} (a2, a3) of the block.
+            uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+            if (need_mask) {
+              const int kq = pos0 + 2 * t4;
+              vmask_lo = (kq < L ? 0x0000ffffu : 0u) | (kq + 1 < L ? 0xffff0000u : 0u);
+              vmask_hi = (kq + 8 < L ? 0x0000ffffu : 0u) | (kq + 9 < L ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_t(st + key0 * 128 + vof[c], a0, a1, a2, a3);
+              a0 &= vmask_lo;
+              a1 &= vmask_lo;
+              a2 &= vmask_hi;
+              a3 &= vmask_hi;
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma16816_bf16(o[c][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) mma16816_bf16(o[c][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+            }
+          } else {
           // ---- PV with P' = p * Vs split into fp16 hi + lo
+            // P' window of each of this warp's groups (bits as in ev_update's
+            // window: a Vs 2^-ev above 2^6, or one at least 2^-10); the
+            // exponents move only when a group leaves it
+            {
+              uint32_t wb = 0u;
 #pragma unroll
-          for (int gi = 0; gi < GW; ++gi) {
-            uint32_t vw[4][2];  // [chunk][keys 0-7 | 8-15], transposed fragments
-            const uint32_t vbase = st + (P + key0) * RB;
+              for (int gi = 0; gi < GW; ++gi) {
+                const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * G_ALL + grp0 + gi, sb) : 0.f;
+                const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb) : 0.f;
+                const float tv = fmaxf(a0, a1) * sv[gi];
+                wb |= (tv > 64.f ? 1u : 0u) << gi;
+                wb |= (tv >= 0.0009765625f ? 1u : 0u) << (4 + gi);
+              }
+              wb = __reduce_or_sync(0xffffffffu, wb);
+              const uint32_t moving = ((wb & 0xfu) | (~(wb >> 4) & 0xfu)) & ((1u << GW) - 1u);
+              if (moving) {
 #pragma unroll
-            for (int q2 = 0; q2 < 2; ++q2)
-              ldsm_x4_t(vbase + loff[gi][q2], vw[q2 * 2][0], vw[q2 * 2][1], vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
-            float v0 = vs_s[(key0 + g) * G_ALL + grp0 + gi];
-            float v1 = vs_s[(key0 + g + 8) * G_ALL + grp0 + gi];
-            v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
-            v1 = valid1 ? v1 : 0.f;
-            // exponent of the group's P' from the block's largest value scale
-            const uint32_t mxb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(v0, v1)));
-            float beta;
-            if (mxb != 0u && ev_update(ev[gi], exp_of(__uint_as_float(mxb)), beta)) {
-              sv[gi] = pow2i(-ev[gi]);
+                for (int gi = 0; gi < GW; ++gi) {
+                  if (!((moving >> gi) & 1u)) continue;
+                  const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * G_ALL + grp0 + gi, sb) : 0.f;
+                  const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb) : 0.f;
+                  const uint32_t mxb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(a0, a1)));
+                  int ev = sv[gi] == 0.f ? kEvUnset : -exp_of(sv[gi]);
+                  float beta;
+                  if (mxb != 0u && ev_update(ev, exp_of(__uint_as_float(mxb)), beta)) {
+                    sv[gi] = pow2i(-ev);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) o[gi * 4 + cc][nt][k] *= beta;
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int gi = 0; gi < GW; ++gi) {
+              uint32_t vw[4][2];  // [chunk][keys 0-7 | 8-15], transposed fragments
+              const uint32_t vbase = st + (P + key0) * RB;
+#pragma unroll
+              for (int q2 = 0; q2 < 2; ++q2)
+                ldsm_x4_t(vbase + loff[gi][q2], vw[q2 * 2][0], vw[q2 * 2][1], vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
+              float v0 = ld_scale(vs_s, (key0 + g) * G_ALL + grp0 + gi, sb);
+              float v1 = ld_scale(vs_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb);
+              v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
+              v1 = valid1 ? v1 : 0.f;
+              v0 *= sv[gi];
+              v1 *= sv[gi];
+              uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
+                const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
+                const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+                const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
+                bh[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h01));
+                bh[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h23));
+                bl[nt][0] = movmatrix_t(l01);
+                bl[nt][1] = movmatrix_t(l23);
+              }
+              uint32_t av[4][4];
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                const uint32_t w0 = vw[cc][0] ^ bias, w1 = vw[cc][1] ^ bias;
+                av[cc][0] = i8x2_to_f16x2(w0, 0x4240);
+                av[cc][1] = i8x2_to_f16x2(w0, 0x4341);
+                av[cc][2] = i8x2_to_f16x2(w1, 0x4240);
+                av[cc][3] = i8x2_to_f16x2(w1, 0x4341);
+              }
+              // all hi products first, then all lo: 4*NT independent accumulators between dependent pairs
 #pragma unroll
               for (int cc = 0; cc < 4; ++cc)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
+                  mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bh[nt][0], bh[nt][1]);
 #pragma unroll
-                  for (int k = 0; k < 4; ++k) o[gi * 4 + cc][nt][k] *= beta;
+              for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bl[nt][0], bl[nt][1]);
             }
-            v0 *= sv[gi];
-            v1 *= sv[gi];
-            uint32_t bh[NT][2], bl[NT][2];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
-              const __half2 h01 = __floats2half2_rn(q0, q1), h23 = __floats2half2_rn(q2, q3);
-              const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-              const uint32_t l01 = pack_f16(q0 - f01.x, q1 - f01.y), l23 = pack_f16(q2 - f23.x, q3 - f23.y);
-              bh[nt][0] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h01));
-              bh[nt][1] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&h23));
-              bl[nt][0] = movmatrix_t(l01);
-              bl[nt][1] = movmatrix_t(l23);
-            }
-            uint32_t av[4][4];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-              const uint32_t w0 = vw[cc][0] ^ bias, w1 = vw[cc][1] ^ bias;
-              av[cc][0] = i8x2_to_f16x2(w0, 0x4240);
-              av[cc][1] = i8x2_to_f16x2(w0, 0x4341);
-              av[cc][2] = i8x2_to_f16x2(w1, 0x4240);
-              av[cc][3] = i8x2_to_f16x2(w1, 0x4341);
-            }
-            // all hi products first, then all lo: 4*NT independent accumulators between dependent pairs
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bh[nt][0], bh[nt][1]);
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bl[nt][0], bl[nt][1]);
           }
         }
         // ---- release the stage; its last reader loads the page S ahead into it
@@ -769,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             if (qn < total && p.issuable(qn) && !*abort_flag) {
               // every reader arrived before its increment: the phase is complete
               if (mbar_wait(smem_u32(&empty_bar[s]), par, p.wait_cycles)) {
-                issue_page<D>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
+                issue_page<D, BF>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
                               smem_u32(&full_bar[s]));
                 ++icnt[s];
               } else {
@@ -787,8 +913,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     // the accumulators hold O 2^-ev per group: back to O
 #pragma unroll
     for (int gi = 0; gi < GW; ++gi) {
-      if (ev[gi] == kEvUnset) continue;
-      const float f = pow2i(ev[gi]);
+      if (BF || sv[gi] == 0.f) continue;
+      const float f = pow2i(-exp_of(sv[gi]));
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc)
 #pragma unroll

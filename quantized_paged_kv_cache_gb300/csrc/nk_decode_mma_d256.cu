@@ -5,13 +5,19 @@
 namespace nk {
 namespace mma {
 
+template <int D, int NT, int CS, bool BF>
+static cudaError_t launch_tb(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
+  const Geometry geo = geometry(p.fmt, D, NT, CS, p.P, p.B);
+  if (geo.stages < 2 || geo.total > kSmemLimit) return cudaErrorInvalidConfiguration;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_mma_kernel<D, NT, CS, BF>), geo.total);
+  if (e != cudaSuccess) return e;
+  return launch_chained(decode_mma_kernel<D, NT, CS, BF>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
+}
+
+// INT8 pools (fp32 or fp16 scales) and bf16 pools
 template <int D, int NT, int CS>
 static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
-  const Geometry geo = geometry(D, NT, CS, p.P, p.B);
-  if (geo.stages < 2 || geo.total > kSmemLimit) return cudaErrorInvalidConfiguration;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_mma_kernel<D, NT, CS>), geo.total);
-  if (e != cudaSuccess) return e;
-  return launch_chained(decode_mma_kernel<D, NT, CS>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
+  return p.fmt == kFmtBf16 ? launch_tb<D, NT, CS, true>(map, p, st) : launch_tb<D, NT, CS, false>(map, p, st);
 }
 
 cudaError_t launch_d256(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st) {

@@ -61,7 +61,9 @@ constexpr int kConvWarps = 4, kScoreWarps = 4, kPvWarps = 8;
 constexpr int kWarps = kConvWarps + kScoreWarps + kPvWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTmemCols = 512;
-constexpr int kStageBytes = 2 * kP * kD + 2 * kP * (kD / kGroup) * 4;  // 34816, a multiple of 1024
+// one page: the K|V code boxes, then both scale arrays (34,816 bytes with
+// fp32 scales, 33,792 with fp16 ones: multiples of 1024 either way)
+__host__ __device__ constexpr int stage_bytes(int sb) { return 2 * kP * kD + 2 * kP * (kD / kGroup) * sb; }
 constexpr int kPidCache = 512;
 constexpr int kColA = 0;      // tensor-memory columns of the two K buffers (64 each)
 constexpr int kColAcc = 128;  // the two accumulator buffers (4W each)
@@ -79,27 +81,29 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
 }
 
 struct Layout {
+  int stage_bytes;
   int stages;
   int off_qt, off_pbuf, off_hdr, off_xs, off_red, off_pre, off_pid, off_bar, off_tmem;
   int total;
 };
 
-__host__ __device__ inline Layout layout(int W, int NT) {
+__host__ __device__ inline Layout layout(int W, int NT, int sb) {
   Layout L;
+  L.stage_bytes = stage_bytes(sb);
   int off = 0;
   const int qt = 2 * (2 * W) * 128;
   const int pbuf = 2 * NT * 8192;
   const int hdr = 512;
   const int xs = 2 * 2 * 64 * NT * 4 * 4;
-  const int red = (2 * 4 * 32 + 2 * 32) * 4 + 4 * 4 + 32 * 4 + 64 + (16 + 4 + 32) * 4;
+  const int red = (2 * 4 * 32 + 2 * 32) * 4 + 4 * 4 + 32 * 4 + 64 + (16 + 4 + 8 + 16 + 4) * 4;
   const int pre = round_up((2 * kMaxBatch + 1 + 16 + 8 + 4 + 9) * 4, 16);  // pre, warp_tot, cnt, flag, lens, icnt, last MMA
   const int pid = kPidCache * 4;
   const int bar = 32 * 8;
   const int fixed = qt + pbuf + hdr + xs + red + pre + pid + bar + 16;
-  int s = (kSmemLimit - 1024 - fixed) / kStageBytes;
+  int s = (kSmemLimit - 1024 - fixed) / L.stage_bytes;
   if (s > 8) s = 8;
   L.stages = s;
-  off = s * kStageBytes;
+  off = s * L.stage_bytes;
   L.off_qt = off; off += qt;
   L.off_pbuf = off; off += pbuf;
   L.off_hdr = off; off += hdr;
@@ -154,6 +158,35 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// The rare step of the score warps' P' window (out of line, so that its
+// registers do not weigh on the page loop): the page's largest Vs of each
+// group -- this warp's 32 keys, then the other warp's of the same channel half
+// -- moves the exponent of the groups in `moving` (ev_update); lane g of each
+// warp updates its copy sva[quad][g], and warp 0 leaves the accumulator
+// factors in bva for the PV warps. key < 0: this lane's slot is past ctx_len.
+__device__ __noinline__ void rebase_pv_exponents(const uint8_t* vs_s, int key, int sb, uint32_t moving, float* pmx,
+                                                 float* sva, float* bva, int quad, int half, int lane) {
+#pragma unroll
+  for (int g4 = 0; g4 < 4; ++g4) {
+    const float v = key >= 0 ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f;
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v));
+    if (lane == 0) pmx[quad * 4 + g4] = __uint_as_float(mx);
+  }
+  named_bar(3 + half, 64);
+  __syncwarp();
+  if (lane < 4) {
+    float sv = sva[quad * 4 + lane], beta = 1.f;
+    if ((moving >> lane) & 1u) {
+      const float mx = fmaxf(pmx[(2 * half) * 4 + lane], pmx[(2 * half + 1) * 4 + lane]);
+      int ev = sv == 0.f ? kEvUnset : -exp_of(sv);
+      if (mx > 0.f && ev_update(ev, exp_of(mx), beta)) sv = pow2i(-ev);
+    }
+    sva[quad * 4 + lane] = sv;
+    if (quad == 0) bva[lane] = beta;
+  }
+  __syncwarp();
+}
+
 // W: padded query rows per channel half of the QK operand (16 or 32);
 // NT: 8-row tiles of the PV product (ceil(G*T / 8) <= W / 8).
 template <int W, int NT>
@@ -167,8 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   constexpr int NR = NT * 4;  // rows a score thread finishes (half of each 8-row tile)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Layout LY = layout(W, NT);
+  const int sb = scale_bytes(p.fmt);
+  const Layout LY = layout(W, NT, sb);
   const int S = LY.stages;
+  const int kStageBytes = LY.stage_bytes;
   int* pre = reinterpret_cast<int*>(smem + LY.off_pre);
   int* warp_tot = pre + (kMaxBatch + 1);
   int* cnt = warp_tot + 16;  // [8]
@@ -191,7 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   int* row_t = sflag + 4;                                      // [32]: query column of row n (T for padding)
   float* pmx = reinterpret_cast<float*>(row_t + 32 + 16);      // [4 score warps][4 groups]: page's largest Vs
   int* evs = reinterpret_cast<int*>(pmx + 16);                 // [4]: P' exponents at a segment's end
-  float* rsn = reinterpret_cast<float*>(evs + 4);              // [32]: 2^-e of each query row's Q scaling
+  float* qmx = reinterpret_cast<float*>(evs + 4);              // [2 roles][4 warps]: largest |q| of the unit
+  float* sva = qmx + 8;                                        // [4 score warps][4 groups]: 2^-ev of P' (0: unset)
+  float* bva = sva + 16;                                       // [4 groups]: accumulator factors of a rebase
   float* xs = reinterpret_cast<float*>(smem + LY.off_xs);      // [2 pages][2 sides][64 keys][NR]
   const uint32_t qt0 = smem_u32(smem + LY.off_qt);             // two Q tiles of 2W x 128 bytes
   uint8_t* pbuf = smem + LY.off_pbuf;                          // [2][4 g][2 h][NT][64][16 B]
@@ -327,8 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (q0 > 0) wait_bar(&qk_bar[(q0 - 1) & 1], ((q0 - 1) >> 1) & 1);
       // Q tile tb, row r: query row r % W, channels 128 (r / W) + 64 tb + [0, 64).
       // Thread (row n, quarter qq) converts channels [64 qq, 64 qq + 64) of
-      // row n, scaled by the row's power of two (q_norm_exp over the four
-      // threads of the row), into tile qq & 1, row (qq >> 1) W + n.
+      // row n, scaled by the unit's power of two (q_norm_exp of the largest
+      // |q| of the unit's M rows, which the score warps compute alike), into
+      // tile qq & 1, row (qq >> 1) W + n.
       {
         const int n = tid >> 2, qq = tid & 3;
         uint4 raw[8];
@@ -345,9 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
           for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(rw[j])), fabsf(bf16_hi(rw[j]))));
         }
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        const float qs = pow2i(q_norm_exp(m));
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) qmx[quad] = m;
+        named_bar(1, kConvWarps * 32);
+        const float qs = pow2i(q_norm_exp(fmaxf(fmaxf(qmx[0], qmx[1]), fmaxf(qmx[2], qmx[3]))));
         if (n < W) {
           const int r = (qq >> 1) * W + n, tb = qq & 1;
 #pragma unroll
@@ -423,8 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // ======================= score warps: scores, softmax, P'
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
     float m_ref[NR], l_part[NR];
-    int ev[4];  // exponents of the P' of the four 64-channel groups (identical in the four warps)
-    float sv[4];
+    // sva[quad]: 2^-ev of the P' of the four 64-channel groups (0: not set
+    // yet in the segment), a copy per warp (identical in the four), read once
+    // per page
     while (next_segment(sh, pre, x, x_end, seg)) {
       const int L = lens[seg.b];
       const int npages = seg.page_end - seg.page_begin;
@@ -433,14 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         m_ref[i] = -INFINITY;
         l_part[i] = 0.f;
       }
-#pragma unroll
-      for (int g4 = 0; g4 < 4; ++g4) {
-        ev[g4] = kEvUnset;
-        sv[g4] = 1.f;
-      }
+      if (lane < 4) sva[quad * 4 + lane] = 0.f;
+      float kq;  // sm_scale log2(e) 2^-e: undoes the Q tile's power of two in the scores
       {
-        // the query rows' powers of two, computed from the same rows as the
-        // convert warps' Q tile (so no exchange is needed), as 2^-e per row
+        // the unit's power of two, from the same rows as the convert warps'
+        // Q tile (so no exchange with them is needed)
         const int ts = tid - kConvWarps * 32, n = ts >> 2, qq = ts & 3;
         float m = 0.f;
         if (n < M) {
@@ -455,10 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(rw[j])), fabsf(bf16_hi(rw[j]))));
           }
         }
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        if (qq == 0) rsn[n] = pow2i(-q_norm_exp(m));
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) qmx[4 + quad] = m;
         named_bar(2, kScoreWarps * 32);
+        kq = p.scale2 * pow2i(-q_norm_exp(fmaxf(fmaxf(qmx[4], qmx[5]), fmaxf(qmx[6], qmx[7]))));
       }
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
@@ -466,9 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
         tc_fence_after();
         const uint8_t* st = smem + s * kStageBytes;
-        const float* ks_s = reinterpret_cast<const float*>(st + 2 * kP * kD);
-        const float* vs_s = ks_s + kP * (kD / kGroup);
-        const float ka = ks_s[key * 4 + 2 * half] * p.scale2, kb = ks_s[key * 4 + 2 * half + 1] * p.scale2;
+        const uint8_t* ks_s = st + 2 * kP * kD;           // [64 keys][4 groups], fp32 or fp16
+        const uint8_t* vs_s = ks_s + kP * (kD / kGroup) * sb;
+        const float ka = ld_scale(ks_s, key * 4 + 2 * half, sb) * kq;
+        const float kb = ld_scale(ks_s, key * 4 + 2 * half + 1, sb) * kq;
         // ---- this lane's accumulator rows (groups 2 half, 2 half + 1), 16 query rows at a time;
         // half of the rows go to the thread holding the other channel half of the key
         float* xq = xs + (q & 1) * (2 * 64 * NR);  // by page parity: a side rewrites it only two pages later
@@ -508,11 +548,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const float4 rcv = *reinterpret_cast<const float4*>(theirs + nt * 4);
-            const float4 f = *reinterpret_cast<const float4*>(rsn + 8 * nt + 4 * half);  // undo the Q scaling
-            sc[nt * 4 + 0] = (sc[nt * 4 + 0] + rcv.x) * f.x;
-            sc[nt * 4 + 1] = (sc[nt * 4 + 1] + rcv.y) * f.y;
-            sc[nt * 4 + 2] = (sc[nt * 4 + 2] + rcv.z) * f.z;
-            sc[nt * 4 + 3] = (sc[nt * 4 + 3] + rcv.w) * f.w;
+            sc[nt * 4 + 0] += rcv.x;
+            sc[nt * 4 + 1] += rcv.y;
+            sc[nt * 4 + 2] += rcv.z;
+            sc[nt * 4 + 3] += rcv.w;
           }
         }
         // ---- causal / context mask: only pages that reach past L - T (padding rows
@@ -529,29 +568,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         bool over = false;
 #pragma unroll
         for (int i = 0; i < NR; ++i) over |= sc[i] > m_ref[i] + 8.f;
-        const unsigned vote = __ballot_sync(0xffffffffu, over);
-        if (lane == 0) sflag[quad] = vote != 0;
-        // the page's largest value scale per group: this warp's 32 keys, then the other warp's
-        float vsk[4];
+        // P' window of each group: bit g set when a key's Vs 2^-ev passes
+        // 2^6 (p Vs 2^-ev could reach 2^15), bit 4 + g when one is at least
+        // 2^-10; a group whose ev is not set yet has neither
+        uint32_t wbits = 0u;
+        __syncwarp();
+        {
+          const float4 sv4 = *reinterpret_cast<const float4*>(sva + quad * 4);
+          const float sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
 #pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          vsk[g4] = key_valid ? vs_s[key * 4 + g4] : 0.f;  // slots past ctx_len may hold NaN scales
-          const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(vsk[g4]));
-          if (lane == 0) pmx[quad * 4 + g4] = __uint_as_float(mx);
-        }
-        named_bar(3 + half, 64);
-        const bool raise = sflag[2 * half] | sflag[2 * half + 1];
-        bool rebased = false;
-        float beta[4];
-#pragma unroll
-        for (int g4 = 0; g4 < 4; ++g4) {
-          beta[g4] = 1.f;
-          const float mx = fmaxf(pmx[(2 * half) * 4 + g4], pmx[(2 * half + 1) * 4 + g4]);
-          if (mx > 0.f && ev_update(ev[g4], exp_of(mx), beta[g4])) {
-            sv[g4] = pow2i(-ev[g4]);
-            rebased = true;
+          for (int g4 = 0; g4 < 4; ++g4) {
+            // slots past ctx_len may hold NaN scales
+            const float tv = (key_valid ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f) * sv[g4];
+            wbits |= (tv > 64.f ? 1u : 0u) << g4;
+            wbits |= (tv >= 0.0009765625f ? 1u : 0u) << (4 + g4);
           }
         }
+        wbits = __reduce_or_sync(0xffffffffu, wbits);
+        const unsigned vote = __ballot_sync(0xffffffffu, over);
+        if (lane == 0) sflag[quad] = (int)((vote != 0 ? 1u : 0u) | (wbits << 1));
+        named_bar(3 + half, 64);
+        const uint32_t fl = (uint32_t)(sflag[2 * half] | sflag[2 * half + 1]);
+        const bool raise = (fl & 1u) != 0u;
+        // groups whose ev moves: a Vs 2^-ev above the window, or none in it
+        const uint32_t moving = ((fl >> 1) & 0xfu) | (~(fl >> 5) & 0xfu);
+        if (moving) rebase_pv_exponents(vs_s, key_valid ? key : -1, sb, moving, pmx, sva, bva, quad, half, lane);
         float al[NR];
 #pragma unroll
         for (int i = 0; i < NR; ++i) al[i] = 1.f;
@@ -592,15 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           for (int i = 0; i < NR; ++i) alpha[8 * (i >> 2) + 4 * half + (i & 3)] = al[i];
           reinterpret_cast<int*>(alpha + 32)[half] = raise ? 1 : 0;
           if (half == 0) {
+            if (moving) {
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) alpha[36 + g4] = beta[g4];
-            reinterpret_cast<int*>(alpha + 40)[0] = rebased ? 1 : 0;
+              for (int g4 = 0; g4 < 4; ++g4) alpha[36 + g4] = bva[g4];
+            }
+            reinterpret_cast<int*>(alpha + 40)[0] = moving ? 1 : 0;
           }
         }
         uint8_t* pb = pbuf + (q & 1) * (NT * 8192);
+        const float4 sv4 = *reinterpret_cast<const float4*>(sva + quad * 4);
+        const float svp[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
 #pragma unroll
         for (int gq = 0; gq < 4; ++gq) {
-          const float vs = vsk[gq] * sv[gq];  // P' = p Vs 2^-ev
+          // P' = p Vs 2^-ev (slots past ctx_len may hold NaN scales)
+          const float vs = (key_valid ? ld_scale(vs_s, key * 4 + gq, sb) : 0.f) * svp[gq];
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             // hi = the value cut to 11 significant bits (exact in fp16 for
@@ -643,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         if (half == 0) {
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) evs[g4] = ev[g4];
+          for (int g4 = 0; g4 < 4; ++g4) evs[g4] = sva[g4] == 0.f ? kEvUnset : -exp_of(sva[g4]);
         }
       }
       named_bar(5, (kScoreWarps + kPvWarps) * 32);
@@ -785,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
 template <int W, int NT>
 static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
-  const Layout LY = layout(W, NT);
+  const Layout LY = layout(W, NT, scale_bytes(p.fmt));
   if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT>), LY.total);
   if (e != cudaSuccess) return e;
@@ -797,9 +843,9 @@ static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaS
 // At G * T <= 8 (one 8-row tile, e.g. plain decode at G = 6) the QK product is
 // small and the mma.sync kernel's shorter per-page chain is faster (C1 32K:
 // 34.7 us against 37.3 us for split + combine), so this kernel takes 9 to 32 rows.
-bool decode_tc_supported(int D, int T, int G, int P) {
+bool decode_tc_supported(int fmt, int D, int T, int G, int P) {
   const int M = G * T;
-  return D == tc::kD && P == tc::kP && M > 8 && M <= 32;
+  return (fmt == kFmtI8F32 || fmt == kFmtI8F16) && D == tc::kD && P == tc::kP && M > 8 && M <= 32;
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream) {

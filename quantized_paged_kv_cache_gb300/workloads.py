@@ -44,7 +44,8 @@ class Workload:
     outlier_scale: float = 1.0
     token_norm_range: tuple[float, float] | None = None
     note: str = ""
-    # KV format of the pool: "int8" (INT8 group-64, fp32 scales) or "rk8v4"
+    # KV format of the pool: "int8" (INT8 group-64, fp32 scales), "rk8v4",
+    # "i8f16" (the pages' INT8 layout, fp16 scales) or "bf16" (unquantized)
     fmt: str = "int8"
     # powers of two the drawn Q, K and V values are multiplied by (before the
     # bf16 rounding): the range tests move the inputs off unit scale
@@ -77,6 +78,10 @@ class Workload:
     def bytes_per_key_head(self) -> int:
         if self.fmt == "rk8v4":
             return self.D + (self.D // 64) * 2 + self.D // 2 + (self.D // 32) * 2
+        if self.fmt == "i8f16":
+            return 2 * self.D + 2 * (self.D // 64) * 2
+        if self.fmt == "bf16":
+            return 2 * self.D * 2
         return 2 * self.D + 2 * (self.D // 64) * 4
 
     # algorithmic bytes of one attention call: the stored K/V of every visible
@@ -113,14 +118,19 @@ def make(name: str) -> Workload:
     if name == "tiny":
         w = Workload("tiny", B=1, T=1, Hq=2, Hkv=1, D=64, P=16, ctx_lens=[256], seed=0, append_len=1,
                      note="1 seq, 1 kv-head, 2 q-heads, head_dim 64, ctx 256, page 16, T=1")
-    elif name in ("c1_decode", "c1_rk8v4"):
+    elif name in ("c1_decode", "c1_rk8v4", "c1_i8f16", "c1_bf16"):
+        fmt = {"c1_rk8v4": "rk8v4", "c1_i8f16": "i8f16", "c1_bf16": "bf16"}.get(name, "int8")
         w = Workload(name, B=1, T=1, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[32768], seed=1, append_len=1,
                      outlier_channels=4, outlier_scale=8.0,
                      note="C1 decode: 24 q / 4 kv heads, head_dim 256, ctx 32,768, page 64, T=1, "
-                          "4 K outlier channels per head x8",
-                     fmt="rk8v4" if name == "c1_rk8v4" else "int8")
-        if name == "c1_rk8v4":
-            w.note += "; rk8v4 KV format"
+                          "4 K outlier channels per head x8", fmt=fmt)
+        if fmt != "int8":
+            w.note += f"; {fmt} KV format"
+    elif name in ("c8_i8f16", "c8_bf16"):
+        g = _gen(2, 0, "cpu")
+        lens = torch.randint(4096, 65536 + 1, (8,), generator=g).tolist()
+        w = Workload(name, B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=lens, seed=2, append_len=4,
+                     note=f"MTP3 verify C8 (c8_verify's inputs) in the {name[3:]} KV format", fmt=name[3:])
     elif name in ("c8_verify", "c8_decode"):
         g = _gen(2, 0, "cpu")
         lens = torch.randint(4096, 65536 + 1, (8,), generator=g).tolist()
@@ -145,6 +155,7 @@ def make(name: str) -> Workload:
 
 CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix", "c8_decode")  # INT8 group-64 pools
 RK8V4_CONFIGS = ("c1_rk8v4",)
+FORMAT_CONFIGS = ("c1_i8f16", "c1_bf16", "c8_i8f16", "c8_bf16")  # the pages' INT8 layout and bf16 KV
 
 
 def tables(w: Workload, num_pages: int | None = None) -> Workload:

@@ -17,8 +17,8 @@
  * mantissas), or of every exponent with a few mantissas, and every bf16 x
  * with |x| <= a, both signs. Scaling a and x by a power of two scales every
  * step exactly (no overflow or underflow in this range), so a handful of
- * exponents stands for all of them. Prints "tested N bad M"; exit status 1 if
- * M > 0.
+ * exponents stands for all of them. A second part does the same for fp16
+ * group scales (below). Prints "tested N bad M"; exit status 1 if M > 0.
  */
 #include <math.h>
 #include <stdint.h>
@@ -81,6 +81,42 @@ static void check_max(uint32_t ab) {
   }
 }
 
+/* The same steps with an fp16 group scale s (the pages' INT8 layout):
+ * s = RN_fp16(a / 127) is a normal fp16 number, y = RN(1/s) by IEEE division,
+ * and x runs over every bf16 value with |x| <= 127 s (1 + 2^-11), the largest
+ * element a group with that scale can hold. The kernel sends groups whose
+ * scale is an fp16 subnormal, or saturated, to the per-element division. */
+static float f16(uint32_t h) {
+  const int e = (int)((h >> 10) & 0x1f), m = (int)(h & 0x3ff);
+  return e == 0 ? ldexpf((float)m, -24) : ldexpf((float)(1024 + m), e - 25);
+}
+
+static void check_f16_scale(uint32_t sbits) {
+  const volatile float s = f16(sbits);
+  const volatile float y = 1.0f / s;
+  const double bound = 127.0 * (double)s * (1.0 + ldexp(1.0, -11));
+  for (uint32_t xb = 0; xb < 0x7f80u; ++xb) {
+    if ((double)bf16(xb) > bound) break;
+    for (int neg = 0; neg < 2; ++neg) {
+      const volatile float x = neg ? -bf16(xb) : bf16(xb);
+      float e = x / s;
+      if (e > 127.0f) e = 127.0f;
+      if (e < -127.0f) e = -127.0f;
+      const int32_t want = (int32_t)nearbyintf(e);
+      const volatile float q0 = x * y;
+      const volatile float r = fmaf(-s, q0, x);
+      const volatile float q = fmaf(r, y, q0);
+      const volatile float t = q + 12582912.0f;
+      const uint32_t code = bits(t) & 0xffu;
+      ++tested;
+      if (code != ((uint32_t)want & 0xffu)) {
+        if (bad < 5) printf("fp16 s=%a x=%a want=%d got=%u\n", (double)s, (double)x, want, code);
+        ++bad;
+      }
+    }
+  }
+}
+
 int main(void) {
   for (uint32_t m = 0; m < 128; ++m) {
     const volatile float sm = (1.0f + (float)m * 0.0078125f) / 127.0f;
@@ -104,6 +140,13 @@ int main(void) {
   static const uint32_t mants[] = {0, 1, 63, 64, 126, 127};
   for (uint32_t be = 40; be < 255; ++be)
     for (unsigned i = 0; i < sizeof(mants) / sizeof(mants[0]); ++i) check_max(be << 7 | mants[i]);
+  /* fp16 scales: every mantissa at exponent 0, and the smallest and largest
+   * normal binades (bf16 elements down to the subnormals) */
+  for (uint32_t m = 0; m < 1024; ++m) check_f16_scale(15u << 10 | m);
+  for (uint32_t m = 0; m < 1024; m += 17) {
+    check_f16_scale(1u << 10 | m);
+    check_f16_scale(30u << 10 | m);
+  }
   printf("tested %ld bad %ld\n", tested, bad);
   return bad != 0;
 }
