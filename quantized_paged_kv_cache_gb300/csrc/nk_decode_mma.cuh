@@ -321,9 +321,11 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
 // BF: the pool holds bf16 rows (the unquantized layout): K and V enter the
 // MMAs as they are (bf16 operands, Q bf16 too), there are no scales, and P
 // enters the PV product as bf16 hi + lo.
-template <int D, int NT, int CS, bool BF>
+// FMT: the pool's KvFmt (compile time, so that scale loads need no branch).
+template <int D, int NT, int CS, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                  const DecodeParams p) {
+  constexpr bool BF = FMT == kFmtBf16;
   // the tensor map is a launch parameter (no earlier kernel writes it): its
   // descriptor fetch can start before the wait for the previous kernel
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
@@ -339,9 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const Geometry geo = geometry(p.fmt, D, NT, CS, p.P, p.B);
+  const Geometry geo = geometry(FMT, D, NT, CS, p.P, p.B);
   const int S = geo.stages;
-  const int sb = scale_bytes(p.fmt);
+  constexpr int sb = FMT == kFmtI8F16 ? 2 : 4;
   int* pre = reinterpret_cast<int*>(smem + geo.pre_off);
   int* warp_tot = pre + (p.B + 1);
   volatile int* abort_flag = pre + (p.B + 1) + 8;
@@ -924,6 +926,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     }
 
     const bool last_seg = x >= x_end;
+    // channel (within its 16-channel chunk) of accumulator element k: INT8
+    // 2 g + (k >> 1) (the V fragments' byte order), bf16 g + 8 (k >> 1)
+    auto och = [&](int k) { return BF ? g + 8 * (k >> 1) : 2 * g + (k >> 1); };
 
     // ---- merge the teams of this segment and write the result
     // row sums: reduce the per-lane partial l over the 8 lanes of a row
@@ -957,15 +962,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     const bool parked = last_seg && (size_t)NTEAMS * kSlot * 4 <= (size_t)S * geo.stage_bytes;
     float* acc_buf = parked ? reinterpret_cast<float*>(smem) + team * kSlot : mo;
     if (parked) {
-      // fragment elements k and k + 2 are adjacent channels of one row
+      // INT8: fragment elements k and k + 2 are adjacent channels of one row
+      // (16 c + 2 g, + 1: the V fragments' byte order); bf16: channels
+      // 16 c + g and 16 c + g + 8 (ldmatrix order)
 #pragma unroll
       for (int c = 0; c < NCH; ++c)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 2; ++e)
-            *reinterpret_cast<float2*>(acc_buf + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16 + 2 * g) =
-                make_float2(o[c][nt][e], o[c][nt][e + 2]);
+          for (int e = 0; e < 2; ++e) {
+            float* row = acc_buf + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16;
+            if constexpr (BF) {
+              row[g] = o[c][nt][e];
+              row[g + 8] = o[c][nt][e + 2];
+            } else {
+              *reinterpret_cast<float2*>(row + 2 * g) = make_float2(o[c][nt][e], o[c][nt][e + 2]);
+            }
+          }
     }
     __syncthreads();
     // team weights of each row: NTEAMS consecutive lanes per row, reduced by shuffles
@@ -1009,10 +1022,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                // fragment elements e and e + 2 are adjacent channels of one row
-                float2* dst = reinterpret_cast<float2*>(mo + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16 + 2 * g);
-                const float2 prev = rd == 0 ? make_float2(0.f, 0.f) : *dst;
-                *dst = make_float2(fmaf(o[c][nt][e], f[nt][e], prev.x), fmaf(o[c][nt][e + 2], f[nt][e], prev.y));
+                float* row = mo + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16;
+                if constexpr (BF) {  // channels 16 c + g, 16 c + g + 8
+                  const float p0 = rd == 0 ? 0.f : row[g], p1 = rd == 0 ? 0.f : row[g + 8];
+                  row[g] = fmaf(o[c][nt][e], f[nt][e], p0);
+                  row[g + 8] = fmaf(o[c][nt][e + 2], f[nt][e], p1);
+                } else {
+                  // fragment elements e and e + 2 are adjacent channels of one row
+                  float2* dst = reinterpret_cast<float2*>(row + 2 * g);
+                  const float2 prev = rd == 0 ? make_float2(0.f, 0.f) : *dst;
+                  *dst = make_float2(fmaf(o[c][nt][e], f[nt][e], prev.x), fmaf(o[c][nt][e + 2], f[nt][e], prev.y));
+                }
               }
           }
           __syncthreads();
@@ -1029,13 +1049,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  prev[nt][k] =
-                      (tm == 0) ? 0.f : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)];
+                  prev[nt][k] = (tm == 0) ? 0.f : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + och(k)];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + 2 * g + (k >> 1)] =
+                  mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + och(k)] =
                       fmaf(o[c][nt][k], f[nt][k & 1], prev[nt][k]);
             }
           }

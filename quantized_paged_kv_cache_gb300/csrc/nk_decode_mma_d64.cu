@@ -5,19 +5,21 @@
 namespace nk {
 namespace mma {
 
-template <int D, int NT, int CS, bool BF>
+template <int D, int NT, int CS, int FMT>
 static cudaError_t launch_tb(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
-  const Geometry geo = geometry(p.fmt, D, NT, CS, p.P, p.B);
+  const Geometry geo = geometry(FMT, D, NT, CS, p.P, p.B);
   if (geo.stages < 2 || geo.total > kSmemLimit) return cudaErrorInvalidConfiguration;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_mma_kernel<D, NT, CS, BF>), geo.total);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_mma_kernel<D, NT, CS, FMT>), geo.total);
   if (e != cudaSuccess) return e;
-  return launch_chained(decode_mma_kernel<D, NT, CS, BF>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
+  return launch_chained(decode_mma_kernel<D, NT, CS, FMT>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
 }
 
-// INT8 pools (fp32 or fp16 scales) and bf16 pools
+// INT8 pools with fp32 or fp16 scales, and bf16 pools
 template <int D, int NT, int CS>
 static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
-  return p.fmt == kFmtBf16 ? launch_tb<D, NT, CS, true>(map, p, st) : launch_tb<D, NT, CS, false>(map, p, st);
+  if (p.fmt == kFmtBf16) return launch_tb<D, NT, CS, kFmtBf16>(map, p, st);
+  if (p.fmt == kFmtI8F16) return launch_tb<D, NT, CS, kFmtI8F16>(map, p, st);
+  return launch_tb<D, NT, CS, kFmtI8F32>(map, p, st);
 }
 
 cudaError_t launch_d64(const CUtensorMap& map, const DecodeParams& p, int NT, cudaStream_t st) {

@@ -158,38 +158,10 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// The rare step of the score warps' P' window (out of line, so that its
-// registers do not weigh on the page loop): the page's largest Vs of each
-// group -- this warp's 32 keys, then the other warp's of the same channel half
-// -- moves the exponent of the groups in `moving` (ev_update); lane g of each
-// warp updates its copy sva[quad][g], and warp 0 leaves the accumulator
-// factors in bva for the PV warps. key < 0: this lane's slot is past ctx_len.
-__device__ __noinline__ void rebase_pv_exponents(const uint8_t* vs_s, int key, int sb, uint32_t moving, float* pmx,
-                                                 float* sva, float* bva, int quad, int half, int lane) {
-#pragma unroll
-  for (int g4 = 0; g4 < 4; ++g4) {
-    const float v = key >= 0 ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f;
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v));
-    if (lane == 0) pmx[quad * 4 + g4] = __uint_as_float(mx);
-  }
-  named_bar(3 + half, 64);
-  __syncwarp();
-  if (lane < 4) {
-    float sv = sva[quad * 4 + lane], beta = 1.f;
-    if ((moving >> lane) & 1u) {
-      const float mx = fmaxf(pmx[(2 * half) * 4 + lane], pmx[(2 * half + 1) * 4 + lane]);
-      int ev = sv == 0.f ? kEvUnset : -exp_of(sv);
-      if (mx > 0.f && ev_update(ev, exp_of(mx), beta)) sv = pow2i(-ev);
-    }
-    sva[quad * 4 + lane] = sv;
-    if (quad == 0) bva[lane] = beta;
-  }
-  __syncwarp();
-}
-
 // W: padded query rows per channel half of the QK operand (16 or 32);
 // NT: 8-row tiles of the PV product (ceil(G*T / 8) <= W / 8).
-template <int W, int NT>
+// SB: bytes of a group scale (4: fp32 scales; 2: the pages' fp16 scales).
+template <int W, int NT, int SB>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const DecodeParams p) {
   // the tensor map is a launch parameter: its descriptor fetch can start
@@ -200,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   constexpr int NR = NT * 4;  // rows a score thread finishes (half of each 8-row tile)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int sb = scale_bytes(p.fmt);
+  constexpr int sb = SB;
   const Layout LY = layout(W, NT, sb);
   const int S = LY.stages;
   const int kStageBytes = LY.stage_bytes;
@@ -592,7 +564,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const bool raise = (fl & 1u) != 0u;
         // groups whose ev moves: a Vs 2^-ev above the window, or none in it
         const uint32_t moving = ((fl >> 1) & 0xfu) | (~(fl >> 5) & 0xfu);
-        if (moving) rebase_pv_exponents(vs_s, key_valid ? key : -1, sb, moving, pmx, sva, bva, quad, half, lane);
+        if (moving) {  // rare: the page's largest Vs of each group moves its exponent (ev_update)
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            const float v = key_valid ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f;
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v));
+            if (lane == 0) pmx[quad * 4 + g4] = __uint_as_float(mx);
+          }
+          named_bar(3 + half, 64);
+          __syncwarp();
+          if (lane < 4) {  // lane g moves group g; warp 0 leaves the accumulator factors for the PV warps
+            float sv = sva[quad * 4 + lane], beta = 1.f;
+            if ((moving >> lane) & 1u) {
+              const float mx = fmaxf(pmx[(2 * half) * 4 + lane], pmx[(2 * half + 1) * 4 + lane]);
+              int ev = sv == 0.f ? kEvUnset : -exp_of(sv);
+              if (mx > 0.f && ev_update(ev, exp_of(mx), beta)) sv = pow2i(-ev);
+            }
+            sva[quad * 4 + lane] = sv;
+            if (quad == 0) bva[lane] = beta;
+          }
+          __syncwarp();
+        }
         float al[NR];
 #pragma unroll
         for (int i = 0; i < NR; ++i) al[i] = 1.f;
@@ -829,13 +821,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   }
 }
 
+template <int W, int NT, int SB>
+static cudaError_t launch_ts(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
+  const Layout LY = layout(W, NT, SB);
+  if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT, SB>), LY.total);
+  if (e != cudaSuccess) return e;
+  return launch_chained(decode_tc_kernel<W, NT, SB>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
+}
+
 template <int W, int NT>
 static cudaError_t launch_t(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
-  const Layout LY = layout(W, NT, scale_bytes(p.fmt));
-  if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT>), LY.total);
-  if (e != cudaSuccess) return e;
-  return launch_chained(decode_tc_kernel<W, NT>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
+  return scale_bytes(p.fmt) == 2 ? launch_ts<W, NT, 2>(map, p, st) : launch_ts<W, NT, 4>(map, p, st);
 }
 
 }  // namespace tc
