@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--config", default="mix",
                     help="mix (default: the largest single-GPU configuration, 8 x 1,024-row append + C8 x T4 "
                          "attention at 131,072) | tiny | c1_decode | c8_verify | long_context | c8_decode | c1_rk8v4 "
-                         "| c1_i8f16 | c1_bf16 | c8_i8f16 | c8_bf16")
+                         "| c1_i8f16 | c8_i8f16 | mix_prefill")
     ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -181,7 +181,8 @@ def setup_gpu(w, device, replicas, num_ctas, kernel):
     vs = [v] + [v.clone() for _ in range(n_in - 1)]
     q = wl.queries(w, device=device)
     nct = num_ctas
-    ws_bytes = nk.decode_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D, nct)
+    # the chunked prefill takes no workspace
+    ws_bytes = 256 if is_prefill(w) else nk.decode_workspace_bytes(w.B, w.T, w.Hq, w.Hkv, w.D, nct)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     out = torch.empty_like(q)
     torch.cuda.synchronize()
@@ -207,10 +208,22 @@ def job_gbs(step_bytes: int, ms: float, world: int) -> float:
     return step_bytes * world / (ms * 1e-3) / 1e9
 
 
+def is_prefill(w) -> bool:
+    """A chunked-prefill workload (T beyond the decode / verify widths)."""
+    return w.T > 16
+
+
 def attention_call(args, w):
     """The attention entry point the run times: the tensor-core or CUDA-core
-    kernel of an INT8 pool, or the rk8v4 kernel of an rk8v4 pool."""
+    kernel of an INT8 pool, the kernels of the other formats, or the chunked
+    prefill (which takes no split count or workspace)."""
     import quantized_paged_kv_cache_gb300 as nk
+
+    if is_prefill(w):
+        def prefill(pool, q, bt, ctx, sm_scale, max_ctx, num_ctas=0, workspace=None, out=None, status=None,
+                    stream=None):
+            return nk.paged_prefill_attn(pool, q, bt, ctx, sm_scale, max_ctx, out=out, status=status, stream=stream)
+        return prefill
 
     if w.fmt != "int8":
         return {"rk8v4": nk.rk8v4_decode_attn, "i8f16": nk.i8f16_decode_attn, "bf16": nk.bf16kv_decode_attn}[w.fmt]
@@ -218,8 +231,8 @@ def attention_call(args, w):
 
 
 def one_call_step(args, w) -> bool:
-    """Whether a step runs as one nk_decode_step call (INT8 pool, tensor-core kernels)."""
-    return w.fmt == "int8" and args.kernel == "mma"
+    """Whether a step runs as one nk_decode_step call (INT8 pool, tensor-core decode kernels)."""
+    return w.fmt == "int8" and args.kernel == "mma" and not is_prefill(w)
 
 
 def run_ours(args, w, rank, world, device):
@@ -525,6 +538,10 @@ def main():
     attn_us = r["attn_ms"] * 1e3
     append_us = r["append_ms"] * 1e3
     achieved = w.attn_bytes() / (attn_us * 1e-6) / 1e9
+    prefill = is_prefill(w)
+    if prefill:  # compute-bound: the tensor roofline (fp16 mma.sync at the bf16 rate)
+        tflops = w.attn_flops() / (attn_us * 1e-6) / 1e12
+        tpeak = float(peaks.get("bf16_tflops", 1900.0))
     traffic = ncu_traffic(w.name, args.kernel)
     us = r["ms"] * 1e3
     gbs = job_gbs(r["step_bytes"], r["ms"], world)
@@ -554,14 +571,19 @@ def main():
         "attn_gbs": round(achieved, 2),
         "pct_of_hbm_peak": round(100 * gbs / world / peak, 2),
         "kernel": args.kernel if w.fmt == "int8" else w.fmt, "num_ctas": r["nct"] or "default",
-        "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": 3 * args.steps,
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+        "clocks": r["clocks"], "e2e": r["e2e"], "gpu_launches": (2 if is_prefill(w) else 3) * args.steps,
+        "roofline": ({"bound": "tensor", "achieved": round(tflops, 2), "peak": tpeak, "unit": "TFLOP/s",
+                      "frac": round(tflops / tpeak, 4), "traffic": None,
+                      "kernel": "chunked-prefill kernel (one nk_paged_prefill_attn call, mma.sync)",
+                      "peak_source": f"{src} bf16_tflops (burst)", "flops_per_launch": w.attn_flops()}
+                     if prefill else
+                     {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("paged_decode split kernel + combine (one nk_paged_decode_attn call)"
                                 if w.fmt == "int8" else
                                 f"{w.fmt} split kernel + combine (one nk_{'bf16kv' if w.fmt == 'bf16' else w.fmt}"
                                 "_decode_attn call)"),
-                     "peak_source": f"{src} hbm_gbs", "bytes_per_launch": w.attn_bytes()},
+                     "peak_source": f"{src} hbm_gbs", "bytes_per_launch": w.attn_bytes()}),
     }
     if not args.no_cpu_baseline and world == 1 and not args.profile:
         out["cpu_baseline"] = cpu_baseline(w)

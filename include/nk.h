@@ -287,7 +287,9 @@ int nk_bf16kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int
  * arguments, checks, workspace (nk_decode_workspace_bytes), column chunks,
  * causal mask, output and device flags exactly as nk_paged_decode_attn, on the
  * same tensor-core kernels (i8f16: the tcgen05 and mma.sync kernels with fp16
- * scales; bf16kv: the mma.sync kernel with bf16 operands). */
+ * scales). nk_bf16kv_decode_attn returns NK_ERR_UNSUPPORTED in this build: its
+ * kernel path (mma.sync with bf16 operands) is held back after a GPU fault at
+ * the C1 decode size whose cause is not yet found. */
 int nk_i8f16_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
@@ -327,6 +329,27 @@ int nk_paged_decode_attn_noalloc(const nk_kv_pool* pool, const void* q_dev, cons
                                  int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
                                  int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
                                  void* out_dev, int32_t* status_dev, void* stream);
+
+/*
+ * nk_paged_prefill_attn -- chunked-prefill attention over the paged INT8
+ * group-64 cache ("NInfer-4090" README, "What this fork changes": the INT8
+ * attention prefill on the append shape, with causal key-block tiles; prefill
+ * runs in chunks, "NInfer-3090" README, "Capabilities"). The T tokens of one
+ * chunk per sequence -- T = 1,024 in the pages' chunked prefill, any T >= 1 --
+ * attend to the cache exactly as nk_paged_decode_attn defines it: ctx_len[b]
+ * counts the chunk's tokens, whose K/V the chunk's nk_kv_append already
+ * stored, and token t sees keys 0 .. ctx_len[b] - T + t.
+ *   q_dev    bf16 [B][T][Hq][D];  out_dev bf16 [B][T][Hq][D]
+ * No workspace and no split: each CTA takes 128 query rows of one (sequence,
+ * kv-head) over every key they see (mma.sync tensor cores; P a multiple of 16
+ * whose page fits twice in shared memory). Checks, device flags, ordering and
+ * ownership as nk_paged_decode_attn; NK_ERR_SHAPE when G * T or the grid
+ * reaches 2^31.
+ */
+int nk_paged_prefill_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, void* out_dev, int32_t* status_dev,
+                          void* stream);
 
 /*
  * nk_attn_combine -- log-sum-exp merge of S partial results. The pages give

@@ -26,7 +26,7 @@ __all__ = [
     "decode_workspace_bytes", "paged_decode_attn", "paged_decode_attn_simt", "paged_decode_attn_noalloc",
     "attn_combine", "status_string", "decode_step", "rk8v4_chunk_bytes", "rk8v4_pool_bytes", "rk8v4_append",
     "rk8v4_decode_attn", "i8f16_chunk_bytes", "i8f16_pool_bytes", "i8f16_append", "i8f16_decode_attn",
-    "bf16kv_chunk_bytes", "bf16kv_pool_bytes", "bf16kv_append", "bf16kv_decode_attn", "test_inject_copy_stall",
+    "bf16kv_chunk_bytes", "bf16kv_pool_bytes", "bf16kv_append", "bf16kv_decode_attn", "test_inject_copy_stall", "paged_prefill_attn",
 ]
 
 
@@ -311,3 +311,22 @@ def bf16kv_decode_attn(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, 
     """Split-KV paged attention over a bf16 pool (nk_bf16kv_decode_attn)."""
     return _decode(lib().nk_bf16kv_decode_attn, "nk_bf16kv_decode_attn", pool, q, block_table, ctx_lens, sm_scale,
                    max_ctx, num_ctas, workspace, out, status, stream, fmt="bf16")
+
+
+def paged_prefill_attn(pool: KVPool, q, block_table, ctx_lens, sm_scale: float, max_ctx: int, out=None, status=None,
+                       stream=None):
+    """Chunked-prefill attention of T query tokens per sequence over the paged
+    INT8 cache (nk_paged_prefill_attn); returns out bf16 [B][T][Hq][D]."""
+    import torch
+
+    _need_cuda(q, block_table, ctx_lens, out, status)
+    pool.need("int8")
+    B, T, Hq, D = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    ps = pool.c_struct()
+    rc = lib().nk_paged_prefill_attn(ctypes.byref(ps), _ptr(q), _ptr(block_table), int(block_table.shape[-1]),
+                                     _ptr(ctx_lens), B, T, Hq, float(sm_scale), int(max_ctx), _ptr(out), _ptr(status),
+                                     _stream(stream))
+    _check(rc, "nk_paged_prefill_attn")
+    return out

@@ -62,6 +62,7 @@ EXPORTS = (
     "nk_status_string",
     "nk_version",
     "nk_test_inject_copy_stall",
+    "nk_paged_prefill_attn",
 )
 
 
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
                                         (f"nk_{fmt}_decode_attn", dec, ctypes.c_int)):
                     fn = getattr(L, name)
                     fn.argtypes, fn.restype = args, res
+            L.nk_paged_prefill_attn.argtypes = [pool_p, P, P, I32, P, I32, I32, I32, F, I32, P, P, P]
+            L.nk_paged_prefill_attn.restype = ctypes.c_int
             L.nk_attn_combine.argtypes = [P, P, I32, I32, I32, P, P]
             L.nk_attn_combine.restype = ctypes.c_int
             L.nk_status_string.argtypes, L.nk_status_string.restype = [ctypes.c_int], ctypes.c_char_p

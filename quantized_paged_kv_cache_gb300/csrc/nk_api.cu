@@ -400,8 +400,61 @@ int nk_bf16kv_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32
                           int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas,
                           void* workspace_dev, size_t workspace_bytes, void* out_dev, int32_t* status_dev,
                           void* stream) {
-  return paged_decode(pool, q_dev, block_table_dev, max_pages_per_seq, ctx_lens_dev, B, T, num_q_heads, sm_scale,
-                      max_ctx, num_ctas, workspace_dev, workspace_bytes, out_dev, status_dev, stream, Path::kBf16);
+  // The bf16 path of the mma.sync kernel ended with a GPU fault at the C1
+  // decode size (32,768 keys, 152 CTAs) whose cause is not found yet; until it
+  // is, no kernel is launched for a bf16 pool.
+  (void)pool; (void)q_dev; (void)block_table_dev; (void)max_pages_per_seq; (void)ctx_lens_dev; (void)B; (void)T;
+  (void)num_q_heads; (void)sm_scale; (void)max_ctx; (void)num_ctas; (void)workspace_dev; (void)workspace_bytes;
+  (void)out_dev; (void)status_dev; (void)stream;
+  return NK_ERR_UNSUPPORTED;
+}
+
+int nk_paged_prefill_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
+                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
+                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, void* out_dev, int32_t* status_dev,
+                          void* stream) {
+  int err = NK_OK;
+  if (!pool_ok(pool, &err)) return err;
+  if (B < 0 || T < 1 || num_q_heads < 1) return NK_ERR_SHAPE;
+  if (B == 0) return NK_OK;
+  if (!q_dev || !block_table_dev || !ctx_lens_dev || !out_dev) return NK_ERR_NULL;
+  const int Hkv = pool->num_kv_heads, D = pool->head_dim, P = pool->page_size;
+  if (num_q_heads % Hkv != 0) return NK_ERR_SHAPE;
+  if (max_pages_per_seq < 1 || max_ctx < T || (int64_t)max_ctx > (int64_t)max_pages_per_seq * P) return NK_ERR_SHAPE;
+  if (!isfinite(sm_scale)) return NK_ERR_SHAPE;
+  if (!aligned(q_dev, 16) || !aligned(out_dev, 16)) return NK_ERR_SHAPE;
+  if (!prefill_supported(kFmtI8F32, D, P)) return NK_ERR_UNSUPPORTED;
+  const int G = num_q_heads / Hkv;
+  const int64_t tiles = ((int64_t)G * T + prefill_rows_per_cta() - 1) / prefill_rows_per_cta();
+  const int64_t grid = (int64_t)B * Hkv * tiles;
+  if ((int64_t)G * T >= ((int64_t)1 << 31) || grid >= ((int64_t)1 << 31)) return NK_ERR_SHAPE;
+  DecodeParams p = {};
+  p.pool = reinterpret_cast<const uint8_t*>(pool->base_dev);
+  p.num_pages = pool->num_pages;
+  p.P = P;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.lay = ChunkLayout::make(P, D);
+  p.fmt = kFmtI8F32;
+  p.q = reinterpret_cast<const uint16_t*>(q_dev);
+  p.bt = block_table_dev;
+  p.max_pages = max_pages_per_seq;
+  p.ctx = ctx_lens_dev;
+  p.B = B;
+  p.T = T;
+  p.qT = T;
+  p.Hq = num_q_heads;
+  p.G = G;
+  p.sm_scale = sm_scale;
+  p.scale2 = sm_scale * kLog2e;
+  p.max_ctx = max_ctx;
+  p.n_ctas = (int)grid;
+  p.out = reinterpret_cast<uint16_t*>(out_dev);
+  p.status = status_dev;
+  const unsigned long long wc = g_wait_cycles.load(std::memory_order_relaxed);
+  p.wait_cycles = wc > 0 ? wc : kWaitCycles;
+  p.withhold = g_withhold.load(std::memory_order_relaxed);
+  return launch_prefill(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? NK_OK : NK_ERR_CUDA;
 }
 
 int nk_attn_combine(const float* part_o_dev, const float* part_lse_dev, int32_t num_splits, int32_t rows,

@@ -54,6 +54,9 @@ __device__ __forceinline__ void flag_bad_ctx(const DecodeParams& p) {
 }
 
 cudaError_t launch_decode_simt(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_prefill(const DecodeParams& p, cudaStream_t stream);
+bool prefill_supported(int fmt, int D, int P);
+int prefill_rows_per_cta();
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t stream);
 bool decode_tc_supported(int fmt, int D, int T, int G, int P);

@@ -89,6 +89,11 @@ class Workload:
     def kv_bytes(self) -> int:
         return sum(self.ctx_lens) * self.Hkv * self.bytes_per_key_head()
 
+    def attn_flops(self) -> int:
+        """Multiply-adds x 2 of QK and PV over every visible (query, key) pair."""
+        pairs = sum(self.T * (L - self.T) + self.T * (self.T + 1) // 2 for L in self.ctx_lens) * self.Hq
+        return 4 * self.D * pairs
+
     def q_bytes(self) -> int:
         return self.B * self.T * self.Hq * self.D * 2
 
@@ -118,15 +123,15 @@ def make(name: str) -> Workload:
     if name == "tiny":
         w = Workload("tiny", B=1, T=1, Hq=2, Hkv=1, D=64, P=16, ctx_lens=[256], seed=0, append_len=1,
                      note="1 seq, 1 kv-head, 2 q-heads, head_dim 64, ctx 256, page 16, T=1")
-    elif name in ("c1_decode", "c1_rk8v4", "c1_i8f16", "c1_bf16"):
-        fmt = {"c1_rk8v4": "rk8v4", "c1_i8f16": "i8f16", "c1_bf16": "bf16"}.get(name, "int8")
+    elif name in ("c1_decode", "c1_rk8v4", "c1_i8f16"):
+        fmt = {"c1_rk8v4": "rk8v4", "c1_i8f16": "i8f16"}.get(name, "int8")
         w = Workload(name, B=1, T=1, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[32768], seed=1, append_len=1,
                      outlier_channels=4, outlier_scale=8.0,
                      note="C1 decode: 24 q / 4 kv heads, head_dim 256, ctx 32,768, page 64, T=1, "
                           "4 K outlier channels per head x8", fmt=fmt)
         if fmt != "int8":
             w.note += f"; {fmt} KV format"
-    elif name in ("c8_i8f16", "c8_bf16"):
+    elif name == "c8_i8f16":
         g = _gen(2, 0, "cpu")
         lens = torch.randint(4096, 65536 + 1, (8,), generator=g).tolist()
         w = Workload(name, B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=lens, seed=2, append_len=4,
@@ -144,6 +149,11 @@ def make(name: str) -> Workload:
         w = Workload("long_context", B=1, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[262144], seed=3, append_len=4,
                      token_norm_range=(0.5, 2.0),
                      note="long context C1: ctx 262,144, T=4 causal, per-token norm x U(0.5, 2)")
+    elif name == "mix_prefill":
+        w = Workload("mix_prefill", B=8, T=1024, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[131072] * 8, seed=4,
+                     append_len=1024,
+                     note="the append + attend mix's chunk: 1,024 tokens of each of 8 seqs appended at "
+                          "130,048..131,071, then their chunked-prefill attention over 131,072 keys")
     elif name == "mix":
         w = Workload("mix", B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[131072] * 8, seed=4, append_len=1024,
                      note="append of a 1,024-token chunk into each of 8 seqs (positions 130,048..131,071), "
@@ -155,7 +165,8 @@ def make(name: str) -> Workload:
 
 CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix", "c8_decode")  # INT8 group-64 pools
 RK8V4_CONFIGS = ("c1_rk8v4",)
-FORMAT_CONFIGS = ("c1_i8f16", "c1_bf16", "c8_i8f16", "c8_bf16")  # the pages' INT8 layout and bf16 KV
+FORMAT_CONFIGS = ("c1_i8f16", "c8_i8f16")  # the pages' INT8 layout (fp16 scales)
+PREFILL_CONFIGS = ("mix_prefill",)  # chunked prefill (T = 1,024)
 
 
 def tables(w: Workload, num_pages: int | None = None) -> Workload:
