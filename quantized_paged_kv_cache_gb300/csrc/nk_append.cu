@@ -179,7 +179,7 @@ __device__ __forceinline__ uint32_t quantize64_f16(const uint32_t (&w)[32], uint
 }
 
 constexpr int kAppendThreads = 128;     // one 64-channel group per thread and chunk
-constexpr int kAppendStages = 3;
+constexpr int kAppendStages = 4;
 constexpr int kAppendBlocksPerSM = 3;
 constexpr int kChunkBytes = 8192;       // bf16 bytes of K (and of V) per chunk
 constexpr int kDestEntries = 512;       // (row, head) destinations a block looks up at once
@@ -187,9 +187,12 @@ constexpr int kAppendSmemSeqs = 256;    // sequences whose cu_new/start_pos a bl
 
 struct __align__(128) AppendSmem {
   uint8_t stage[kAppendStages][2 * kChunkBytes];  // K rows | V rows of one chunk, bf16
-  uint8_t codes[2][kChunkBytes];                  // [K|V][row][D] int8 of a chunk, double-buffered
   int2 dest[kDestEntries];                        // per (chunk of a batch, row): (page * Hkv + head or -1, slot)
   uint64_t full[kAppendStages];
+  uint64_t empty[kAppendStages];                  // the 4 warps done with a stage
+  int cnt[kAppendStages];
+  int abort;
+  int issued;  // the highest chunk number issued so far
   ScaleEntry tab[128];
   int cu[kAppendSmemSeqs + 1];
   int start[kAppendSmemSeqs];
@@ -197,17 +200,18 @@ struct __align__(128) AppendSmem {
 
 // Persistent grid, a whole number of blocks per SM. The (row, kv-head) pairs
 // are cut into chunks of R = 8 KB / (2 D) consecutive pairs; block b takes
-// chunks b, b + grid, ... Thread 0 streams the K rows and the V rows of a
-// chunk into a stage of a 3-deep shared-memory ring with two bulk copies
-// (cp.async.bulk, completing on the stage's mbarrier). The destinations of
-// up to kDestEntries / R of the block's chunks (binary search over cu_new,
+// chunks b, b + grid, ... The K rows and the V rows of a chunk stream into a
+// stage of a 4-deep shared-memory ring with two bulk copies (cp.async.bulk,
+// completing on the stage's "full" mbarrier). The destinations of up to
+// kDestEntries / R of the block's chunks (binary search over cu_new,
 // block-table entry) are looked up together, one pair per thread, so their
 // global loads overlap. Per chunk, thread t quantizes group t (K groups, then
 // V groups), reading its 128 bytes in a lane-rotated order so the eight lanes
-// of a quarter-warp hit distinct banks, and puts its 64 codes into a
-// [K|V][row][D] buffer; after one block barrier the stage is refilled and the
-// block stores the codes with coalesced 16-byte writes, one row of one tensor
-// being D contiguous bytes of its page.
+// of a quarter-warp hit distinct banks, and stores its 64 codes straight into
+// the page row (eight 8-byte pieces in the same rotated order; the four
+// groups of a row are 256 contiguous bytes). There is no block barrier per
+// chunk: each warp releases the stage on its "empty" mbarrier, and the last of
+// the four loads the chunk S ahead into it.
 template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_kernel(const AppendParams p) {
   chain_wait();
@@ -278,7 +282,13 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
   };
 
   if (t == 0) {
-    for (int st = 0; st < kAppendStages; ++st) mbar_init(smem_u32(&sm.full[st]), 1);
+    for (int st = 0; st < kAppendStages; ++st) {
+      mbar_init(smem_u32(&sm.full[st]), 1);
+      mbar_init(smem_u32(&sm.empty[st]), kAppendThreads / 32);
+      sm.cnt[st] = 0;
+    }
+    sm.abort = 0;
+    sm.issued = (int)min((uint32_t)kAppendStages, my_chunks) - 1;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int k = 0; k < kAppendStages; ++k) issue(k);
   }
@@ -295,6 +305,7 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
   // this thread's group in a chunk: tensor, pair row, group in the row
   const int isv = t / (R * GPR), gk = t % (R * GPR), row = gk / GPR, grp = gk % GPR;
   const int rot = lane & 7;  // 16-byte piece read first
+  volatile int* abort_flag = &sm.abort;
   for (uint32_t k = 0; k < my_chunks; ++k) {
     if (k % CB == 0) {
       if (k > 0) __syncthreads();  // the previous batch's entries are no longer read
@@ -303,11 +314,15 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
     }
     const uint32_t c = blockIdx.x + k * grid;
     const int st = (int)(k % kAppendStages);
+    const uint32_t ph = (k / kAppendStages) & 1u;
     const int rows = rows_of(c);
     const int2* dest = sm.dest + (k % CB) * R;
-    if (!mbar_wait(smem_u32(&sm.full[st]), (k / kAppendStages) & 1)) {
+    // after one wait has run out nothing waits any more: the chunks run
+    // without data, and nothing more is issued (the copies issued so far land
+    // before the block exits)
+    if (!*abort_flag && !mbar_wait(smem_u32(&sm.full[st]), ph)) {
       flag(p.status, NK_DEVFLAG_TIMEOUT);
-      return;
+      *abort_flag = 1;
     }
     if constexpr (FMT == kFmtBf16) {
       // the rows as they are: 16-byte pieces straight from the stage into
@@ -321,61 +336,66 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
           *reinterpret_cast<uint4*>(p.pool + (int64_t)dd.x * p.lay.chunk + (tv ? p.lay.vc : 0) + dd.y * (2 * D) +
                                     col) = *reinterpret_cast<const uint4*>(sm.stage[st] + o);
       }
-      __syncthreads();  // stage st fully read
-      if (t == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        issue(k + kAppendStages);
+    } else {
+      // load the group (pieces in rotated order), quantize
+      uint32_t w[32];
+      const uint8_t* src = sm.stage[st] + isv * kChunkBytes + gk * 128;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int piece = (i + rot) & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(src + piece * 16);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
       }
-      continue;
-    }
-    // load the group (pieces in rotated order), quantize
-    uint32_t w[32];
-    const uint8_t* src = sm.stage[st] + isv * kChunkBytes + gk * 128;
+      uint32_t packed[16];  // codes of the pieces in the same rotated order
+      bool range = false;
+      float s = 0.f;
+      uint32_t sb16 = 0u;
+      if constexpr (FMT == kFmtI8F16) sb16 = quantize64_f16(w, packed, range);
+      else s = quantize64<true>(w, packed, sm.tab);
+      const int2 d = dest[row];
+      if (row < rows && d.x >= 0) {
+        uint8_t* chunk = p.pool + (int64_t)d.x * p.lay.chunk;
+        uint8_t* cdst = chunk + (isv ? p.lay.vc : 0) + d.y * D + grp * kGroup;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int piece = (i + rot) & 7;
-      const uint4 v = *reinterpret_cast<const uint4*>(src + piece * 16);
-      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-    }
-    uint32_t packed[16];  // codes of the pieces in the same rotated order
-    bool range = false;
-    float s = 0.f;
-    uint32_t sb16 = 0u;
-    if constexpr (FMT == kFmtI8F16) sb16 = quantize64_f16(w, packed, range);
-    else s = quantize64<true>(w, packed, sm.tab);
-    uint8_t* codes = sm.codes[k & 1];
-    uint8_t* cdst = codes + isv * (R * D) + row * D + grp * kGroup;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int piece = (i + rot) & 7;
-      *reinterpret_cast<uint2*>(cdst + piece * 8) = make_uint2(packed[2 * i], packed[2 * i + 1]);
-    }
-    const int2 d = dest[row];
-    if (row < rows && d.x >= 0) {
-      uint8_t* sdst = p.pool + (int64_t)d.x * p.lay.chunk + (isv ? p.lay.vs : p.lay.ks);
-      if constexpr (FMT == kFmtI8F16) {
-        *reinterpret_cast<uint16_t*>(sdst + (d.y * GPR + grp) * 2) = (uint16_t)sb16;
-        if (range) flag(p.status, NK_DEVFLAG_RANGE);
-      } else {
-        *reinterpret_cast<float*>(sdst + (d.y * GPR + grp) * 4) = s;
+        for (int i = 0; i < 8; ++i) {
+          const int piece = (i + rot) & 7;
+          *reinterpret_cast<uint2*>(cdst + piece * 8) = make_uint2(packed[2 * i], packed[2 * i + 1]);
+        }
+        uint8_t* sdst = chunk + (isv ? p.lay.vs : p.lay.ks);
+        if constexpr (FMT == kFmtI8F16) {
+          *reinterpret_cast<uint16_t*>(sdst + (d.y * GPR + grp) * 2) = (uint16_t)sb16;
+          if (range) flag(p.status, NK_DEVFLAG_RANGE);
+        } else {
+          *reinterpret_cast<float*>(sdst + (d.y * GPR + grp) * 4) = s;
+        }
       }
     }
-    __syncthreads();  // stage st fully read, codes of chunk k complete, codes of chunk k - 1 stored
-    if (t == 0) {
-      // generic-proxy reads of the stage are ordered before the bulk copy that refills it
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(k + kAppendStages);
+    // this warp is done with the stage; the last of the four refills it
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(smem_u32(&sm.empty[st]));
+      if (atomicAdd(&sm.cnt[st], 1) == kAppendThreads / 32 - 1) {
+        sm.cnt[st] = 0;
+        if (k + kAppendStages < my_chunks && !*abort_flag) {
+          if (mbar_wait(smem_u32(&sm.empty[st]), ph)) {
+            // generic-proxy reads of the stage are ordered before the bulk copy that refills it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(k + kAppendStages);
+            sm.issued = (int)(k + kAppendStages);
+          } else {
+            flag(p.status, NK_DEVFLAG_TIMEOUT);
+            *abort_flag = 1;
+          }
+        }
+      }
     }
-    // coalesced stores: 16 bytes per thread and step, rows of D bytes
-#pragma unroll
-    for (int i = 0; i < kChunkBytes / (16 * kAppendThreads); ++i) {
-      const int o = (i * kAppendThreads + t) * 16;
-      const int tv = o / (R * D), rem = o % (R * D), r = rem / D, col = rem % D;
-      const int2 dd = dest[r];
-      if (r < rows && dd.x >= 0)
-        *reinterpret_cast<uint4*>(p.pool + (int64_t)dd.x * p.lay.chunk + (tv ? p.lay.vc : 0) + dd.y * D + col) =
-            *reinterpret_cast<const uint4*>(codes + o);
-    }
+  }
+  // copies still in flight after a timed-out wait land before the block exits
+  __syncthreads();
+  if (t == 0 && *abort_flag) {
+    // the last chunk issued into each stage is one of the last S issued
+    for (int kk = max(0, sm.issued - kAppendStages + 1); kk <= sm.issued; ++kk)
+      (void)mbar_wait(smem_u32(&sm.full[kk % kAppendStages]), (uint32_t)(kk / kAppendStages) & 1u);
   }
 }
 

