@@ -61,6 +61,14 @@ constexpr int kConvWarps = 4, kScoreWarps = 4, kPvWarps = 8;
 constexpr int kWarps = kConvWarps + kScoreWarps + kPvWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTmemCols = 512;
+// Registers per thread: the kernel launches with 128 (512 threads, one CTA
+// per SM: the whole register file). Each role's warpgroup(s) then move to
+// their own share with setmaxnreg; the shares add up to the launch total, so
+// no increase ever waits for registers that are not there (checked on the
+// host against the compiled count before the first launch).
+constexpr int kLaunchRegs = 128, kRegsConv = 144, kRegsScore = 144, kRegsPv = 112;
+static_assert(kConvWarps == 4 && kScoreWarps == 4 && kPvWarps == 8, "one warpgroup per role, two for PV");
+static_assert(kRegsConv + kRegsScore + 2 * kRegsPv == 4 * kLaunchRegs, "register shares = the launch's registers");
 // one page: the K|V code boxes, then both scale arrays (34,816 bytes with
 // fp32 scales, 33,792 with fp16 ones: multiples of 1024 either way)
 __host__ __device__ constexpr int stage_bytes(int sb) { return 2 * kP * kD + 2 * kP * (kD / kGroup) * sb; }
@@ -328,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
   };
   if (role == 0) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConv) : "memory");
     // ======================= convert warps: K codes -> tensor memory, QK MMAs
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
     while (next_segment(sh, pre, x, x_end, seg)) {
@@ -432,6 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // all MMAs done before the tensor memory is released
     if (q0 > 0) wait_bar(&qk_bar[(q0 - 1) & 1], ((q0 - 1) >> 1) & 1);
   } else if (role == 1) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsScore) : "memory");
     // ======================= score warps: scores, softmax, P'
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
     float m_ref[NR], l_part[NR];
@@ -474,11 +484,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
         wait_bar(&full_bar[s], ph);  // scale arrays of the page visible
-        wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
-        tc_fence_after();
         const uint8_t* st = smem + s * kStageBytes;
         const uint8_t* ks_s = st + 2 * kP * kD;           // [64 keys][4 groups], fp32 or fp16
         const uint8_t* vs_s = ks_s + kP * (kD / kGroup) * sb;
+        const int pos = (seg.page_begin + j) * kP + key;
+        const bool key_valid = pos < L;
+        // P' window of each group, while the page's QK runs: bit g set when a
+        // key's Vs 2^-ev passes 2^6 (p Vs 2^-ev could reach 2^15), bit 4 + g
+        // when one is at least 2^-10; a group whose ev is not set yet has
+        // neither. Slots past ctx_len may hold NaN scales: their Vs is 0.
+        float vk[4];
+        uint32_t wbits = 0u;
+        __syncwarp();  // sva as the previous page left it
+        {
+          const float4 sv4 = *reinterpret_cast<const float4*>(sva + quad * 4);
+          const float sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            vk[g4] = key_valid ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f;
+            const float tv = vk[g4] * sv[g4];
+            wbits |= (tv > 64.f ? 1u : 0u) << g4;
+            wbits |= (tv >= 0.0009765625f ? 1u : 0u) << (4 + g4);
+          }
+        }
+        wbits = __reduce_or_sync(0xffffffffu, wbits);
+        wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
+        tc_fence_after();
         const float ka = ld_scale(ks_s, key * 4 + 2 * half, sb) * kq;
         const float kb = ld_scale(ks_s, key * 4 + 2 * half + 1, sb) * kq;
         // ---- this lane's accumulator rows (groups 2 half, 2 half + 1), 16 query rows at a time;
@@ -528,8 +559,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         // ---- causal / context mask: only pages that reach past L - T (padding rows
         // hold zero queries and are never written out, so they need no mask)
-        const int pos = (seg.page_begin + j) * kP + key;
-        const bool key_valid = pos < L;
         if ((seg.page_begin + j + 1) * kP > L - T) {
           const int lim = pos - (L - T);  // visible to column t when lim <= t
 #pragma unroll
@@ -540,23 +569,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         bool over = false;
 #pragma unroll
         for (int i = 0; i < NR; ++i) over |= sc[i] > m_ref[i] + 8.f;
-        // P' window of each group: bit g set when a key's Vs 2^-ev passes
-        // 2^6 (p Vs 2^-ev could reach 2^15), bit 4 + g when one is at least
-        // 2^-10; a group whose ev is not set yet has neither
-        uint32_t wbits = 0u;
-        __syncwarp();
-        {
-          const float4 sv4 = *reinterpret_cast<const float4*>(sva + quad * 4);
-          const float sv[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
-#pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            // slots past ctx_len may hold NaN scales
-            const float tv = (key_valid ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f) * sv[g4];
-            wbits |= (tv > 64.f ? 1u : 0u) << g4;
-            wbits |= (tv >= 0.0009765625f ? 1u : 0u) << (4 + g4);
-          }
-        }
-        wbits = __reduce_or_sync(0xffffffffu, wbits);
         const unsigned vote = __ballot_sync(0xffffffffu, over);
         if (lane == 0) sflag[quad] = (int)((vote != 0 ? 1u : 0u) | (wbits << 1));
         named_bar(3 + half, 64);
@@ -567,8 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (moving) {  // rare: the page's largest Vs of each group moves its exponent (ev_update)
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4) {
-            const float v = key_valid ? ld_scale(vs_s, key * 4 + g4, sb) : 0.f;
-            const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(v));
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(vk[g4]));
             if (lane == 0) pmx[quad * 4 + g4] = __uint_as_float(mx);
           }
           named_bar(3 + half, 64);
@@ -637,8 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         const float svp[4] = {sv4.x, sv4.y, sv4.z, sv4.w};
 #pragma unroll
         for (int gq = 0; gq < 4; ++gq) {
-          // P' = p Vs 2^-ev (slots past ctx_len may hold NaN scales)
-          const float vs = (key_valid ? ld_scale(vs_s, key * 4 + gq, sb) : 0.f) * svp[gq];
+          const float vs = vk[gq] * svp[gq];  // P' = p Vs 2^-ev
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             // hi = the value cut to 11 significant bits (exact in fp16 for
@@ -688,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       named_bar(5, (kScoreWarps + kPvWarps) * 32);  // the PV warps have read lrow / mrow
     }
   } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsPv) : "memory");
     // ======================= PV warps
     const int pw = warp - kConvWarps - kScoreWarps;
     const int g_lane = lane >> 2, t4 = lane & 3;
@@ -827,6 +838,15 @@ static cudaError_t launch_ts(const CUtensorMap& map, const DecodeParams& p, cuda
   if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT, SB>), LY.total);
   if (e != cudaSuccess) return e;
+  // the register shares assume the launch count they were split from
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, decode_tc_kernel<W, NT, SB>);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   return launch_chained(decode_tc_kernel<W, NT, SB>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
 }
 
