@@ -554,7 +554,7 @@ def main():
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(r["ms"], 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {"rk8v4": "i8 K / i4 V KV (fp16 scales), f32 CUDA-core arithmetic",
+        "dtype": {"rk8v4": "i8 K / i4 V KV (fp16 scales), f16 MMA operands (rotated Q hi + lo), f32 accumulate",
                   "i8f16": "i8 KV (fp16 scales), f16 MMA operands, f32 accumulate",
                   "bf16": "bf16 KV, bf16 MMA operands, f32 accumulate"}.get(
                       w.fmt, "i8 KV, f16 MMA operands, f32 accumulate"),

@@ -245,9 +245,12 @@ int nk_rk8v4_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int3
  * workspace (nk_decode_workspace_bytes), causal mask, output and device
  * flags exactly as nk_paged_decode_attn. Each query row is rotated by R
  * inside the kernel and scored against the stored rotated keys
- * (q . k = (R q) . (R k)); values are dequantized as code * scale. fp32
- * CUDA-core kernel; G = Hq / Hkv <= 8; verifies wider than 8 columns run as
- * column chunks. */
+ * (q . k = (R q) . (R k)); values are dequantized as code * scale. Head dim
+ * 128 or 256 with up to 32 query rows (G * T) per kv-head: tensor cores (the
+ * rotated row as fp16 hi + lo against the INT8 key codes; the 4-bit value
+ * codes widened exactly; a wider verify runs as column chunks of up to 32
+ * rows). Other shapes: an fp32 CUDA-core kernel with G = Hq / Hkv <= 8 and
+ * column chunks of 8. */
 int nk_rk8v4_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
                          int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,

@@ -74,6 +74,17 @@ int32_t default_ctas(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P, int per
 // fastest; on the mma.sync shapes at most 48 rows, fewer where a larger
 // page leaves no room for them; on CUDA cores 8 columns.
 int chunk_cols(bool simt, int fmt, int D, int T, int G, int P) {
+  if (fmt == kFmtRk8v4) {
+    // rk8v4: the tensor-core kernel where it holds the rows (up to 32 per
+    // kv-head), else the CUDA-core kernel's 8 columns
+    if (decode_mma_supported(fmt, D, T, G, P)) return T;
+    int c = 32 / G;
+    if (c < 1) c = 1;
+    if (c > T) c = T;
+    while (c > 1 && !decode_mma_supported(fmt, D, c, G, P)) --c;
+    if (decode_mma_supported(fmt, D, c, G, P)) return c;
+    return T < 8 ? T : 8;
+  }
   if (simt) return T < 8 ? T : 8;
   if (decode_tc_supported(fmt, D, T, G, P)) return T;
   const bool tc_shape = D == 256 && P == 64 && fmt != kFmtBf16;  // the tcgen05 kernel's head dim, page, formats
@@ -88,11 +99,17 @@ int chunk_cols(bool simt, int fmt, int D, int T, int G, int P) {
 // Which split kernel a decode call runs: the tensor-core kernels or the fp32
 // CUDA-core kernel on an INT8 group-64 pool (fp32 scales), the tensor-core
 // kernels on a pool of the pages' INT8 layout (fp16 scales) or of bf16 rows,
-// or the CUDA-core kernel of the rk8v4 format on an rk8v4 pool.
+// or on an rk8v4 pool the tensor-core kernel (up to 32 rows per kv-head) or
+// the rk8v4 CUDA-core kernel.
 enum class Path { kTensor, kSimt, kRk8v4, kTensorF16, kBf16 };
 
 int path_fmt(Path path) {
-  return path == Path::kTensorF16 ? kFmtI8F16 : (path == Path::kBf16 ? kFmtBf16 : kFmtI8F32);
+  switch (path) {
+    case Path::kTensorF16: return kFmtI8F16;
+    case Path::kBf16: return kFmtBf16;
+    case Path::kRk8v4: return kFmtRk8v4;
+    default: return kFmtI8F32;
+  }
 }
 
 // the paths on the tensor-core kernels (tcgen05 / mma.sync)
@@ -119,12 +136,14 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   if (!aligned(q, 16) || !aligned(out, 16)) return NK_ERR_SHAPE;
   const int fmt = path_fmt(path);
   const int Tc = chunk_cols(simt, fmt, D, T, G, P);
-  if (simt) {
+  const bool rk_tc = path == Path::kRk8v4 && decode_mma_supported(fmt, D, Tc, G, P);
+  if (simt && !rk_tc) {
     if (G > 8) return NK_ERR_UNSUPPORTED;
-  } else {
+  } else if (!rk_tc) {
     if (!decode_tc_supported(fmt, D, Tc, G, P) && !decode_mma_supported(fmt, D, Tc, G, P)) return NK_ERR_UNSUPPORTED;
   }
-  const int per_sm = path == Path::kRk8v4 ? decode_rk8v4_ctas_per_sm(D, G)
+  const int per_sm = rk_tc ? decode_mma_ctas_per_sm(D, T, G)
+                     : path == Path::kRk8v4 ? decode_rk8v4_ctas_per_sm(D, G)
                      : (simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G));
   const int32_t n = num_ctas > 0 ? num_ctas : default_ctas(B, Hkv, max_ctx, P, per_sm);
   const size_t need = nk_decode_workspace_bytes(B, T, Hq, Hkv, D, n);
@@ -137,7 +156,7 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
   p.P = P;
   p.Hkv = Hkv;
   p.D = D;
-  p.lay = path == Path::kRk8v4 ? rk8v4_layout(P, D) : layout_of(fmt, P, D);
+  p.lay = layout_of(fmt, P, D);
   p.fmt = fmt;
   p.q = reinterpret_cast<const uint16_t*>(q);
   p.bt = bt;
@@ -181,7 +200,8 @@ int launch_decode(const DecodeParams& p0, Path path, cudaStream_t st) {
     if (t0 > 0) p.early = 0;  // the predecessor is the previous chunk's combine
     // tensor-core path: tcgen05 QK for head_dim 256, 64-key pages and 9 to
     // 32 rows per kv-head; the mma.sync kernel for the other shapes
-    cudaError_t e = path == Path::kRk8v4 ? launch_decode_rk8v4(p, st)
+    cudaError_t e = path == Path::kRk8v4 ? (decode_mma_supported(p.fmt, p.D, p.T, p.G, p.P) ? launch_decode_mma(p, st)
+                                                                                          : launch_decode_rk8v4(p, st))
                     : path == Path::kSimt   ? launch_decode_simt(p, st)
                     : (decode_tc_supported(p.fmt, p.D, p.T, p.G, p.P) ? launch_decode_tc(p, st)
                                                                      : launch_decode_mma(p, st));

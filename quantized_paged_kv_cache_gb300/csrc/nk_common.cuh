@@ -41,7 +41,7 @@ struct ChunkLayout {
 //              "NInfer-3090" README's "Choosing a KV format" table gives
 //              (nk_i8f16_*);
 //   kFmtBf16   the unquantized bf16 rows of the same table (nk_bf16kv_*).
-enum KvFmt : int { kFmtI8F32 = 0, kFmtI8F16 = 1, kFmtBf16 = 2 };
+enum KvFmt : int { kFmtI8F32 = 0, kFmtI8F16 = 1, kFmtBf16 = 2, kFmtRk8v4 = 3 };
 
 // Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D] int8 | Vs[P][D/64] fp16
 __host__ __device__ inline ChunkLayout i8f16_layout(int P, int D) {
@@ -64,8 +64,26 @@ __host__ __device__ inline ChunkLayout bf16kv_layout(int P, int D) {
   return c;
 }
 
+constexpr int kRkVGroup = 32;  // rk8v4 value channels per scale
+
+// rk8v4: Kc[P][D] int8 | Ks[P][D/64] fp16 | Vc[P][D/2] (channel 2j in the low
+// nibble of byte j, 2j + 1 in the high one) | Vs[P][D/32] fp16
+__host__ __device__ inline ChunkLayout rk8v4_layout(int P, int D) {
+  ChunkLayout c;
+  c.ks = (int64_t)P * D;
+  c.vc = c.ks + (int64_t)P * (D / kGroup) * 2;
+  c.vs = c.vc + (int64_t)P * (D / 2);
+  c.chunk = c.vs + (int64_t)P * (D / kRkVGroup) * 2;
+  return c;
+}
+
 __host__ __device__ inline ChunkLayout layout_of(int fmt, int P, int D) {
-  return fmt == kFmtI8F16 ? i8f16_layout(P, D) : (fmt == kFmtBf16 ? bf16kv_layout(P, D) : ChunkLayout::make(P, D));
+  switch (fmt) {
+    case kFmtI8F16: return i8f16_layout(P, D);
+    case kFmtBf16: return bf16kv_layout(P, D);
+    case kFmtRk8v4: return rk8v4_layout(P, D);
+    default: return ChunkLayout::make(P, D);
+  }
 }
 
 // Programmatic dependent launch. Every kernel of the library is launched

@@ -81,8 +81,11 @@ __host__ __device__ inline int round_up(int x, int a) { return (x + a - 1) / a *
 __host__ __device__ inline Geometry geometry(int fmt, int D, int NT, int CS, int P, int B) {
   Geometry g;
   const int nteams = kConsumerWarps / CS;
-  const int kv_bytes = 2 * P * D * (fmt == kFmtBf16 ? 2 : 1);
-  const int sc_bytes = fmt == kFmtBf16 ? 0 : 2 * P * (D / kGroup) * (fmt == kFmtI8F16 ? 2 : 4);
+  // rk8v4: D key bytes and D / 2 value bytes per key, fp16 scales per 64
+  // key channels and per 32 value channels
+  const int kv_bytes = fmt == kFmtRk8v4 ? 3 * P * D / 2 : 2 * P * D * (fmt == kFmtBf16 ? 2 : 1);
+  const int sc_bytes = fmt == kFmtRk8v4 ? P * (D / kGroup) * 2 + P * (D / kRkVGroup) * 2
+                       : (fmt == kFmtBf16 ? 0 : 2 * P * (D / kGroup) * (fmt == kFmtI8F16 ? 2 : 4));
   g.stage_bytes = round_up(kv_bytes + sc_bytes, 1024);
   g.xch_bytes = CS > 1 ? nteams * 2 * CS * NT * 4 * 32 * 4 : 0;
   const int mrows = NT * 8;
@@ -117,6 +120,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
       "[%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
 
@@ -171,6 +182,26 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t wb, uint32_t sel) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// Two's-complement 4-bit codes: w holds, per 16-bit half, two bytes of one
+// key's value row (channels 4u .. 4u + 3, low nibble first), the low half one
+// key and the high half the next. nib_lo: the low nibbles of the halves' low
+// bytes as an exact fp16 pair (1024 + (n ^ 8) - 1032 = n); nib_hi: their high
+// nibbles (1024 + 16 (n ^ 8), times 1/16, minus 72). w >> 8 gives the same for
+// the halves' high bytes (channels 4u + 2, 4u + 3).
+__device__ __forceinline__ uint32_t nib_lo(uint32_t w) {
+  const uint32_t h = (w & 0x000f000fu) ^ 0x64086408u;
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&h), __halves2half2(__ushort_as_half(0x6408),
+                                                                                    __ushort_as_half(0x6408)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t nib_hi(uint32_t w) {
+  const uint32_t h = (w & 0x00f000f0u) ^ 0x64806480u;
+  const __half2 r = __hfma2(*reinterpret_cast<const __half2*>(&h),
+                            __halves2half2(__ushort_as_half(0x2c00), __ushort_as_half(0x2c00)),   // 1/16
+                            __halves2half2(__ushort_as_half(0xd480), __ushort_as_half(0xd480)));  // -72
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
 // 2^x on the SFU (relative error ~2^-22); ex2(-inf) = 0.
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -206,8 +237,8 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 //     reference. The output is O 2^-ev times 2^ev.
 // ---------------------------------------------------------------------------
 // Bytes of one group scale in a pool of format fmt: fp32 for the INT8 layout
-// with fp32 scales, fp16 for the pages' own INT8 layout.
-__host__ __device__ inline int scale_bytes(int fmt) { return fmt == kFmtI8F16 ? 2 : 4; }
+// with fp32 scales, fp16 for the pages' own INT8 layout and for rk8v4.
+__host__ __device__ inline int scale_bytes(int fmt) { return (fmt == kFmtI8F16 || fmt == kFmtRk8v4) ? 2 : 4; }
 
 // Scale number idx of a page's scale array (fp32 or fp16 elements).
 __device__ __forceinline__ float ld_scale(const uint8_t* arr, int idx, int sb) {
@@ -315,6 +346,28 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
   bulk_load(dst + kv_bytes + sc_bytes, chunk + p.lay.vs, sc_bytes, fb);
 }
 
+// The same for an rk8v4 pool: the key codes as boxes of [128 channels][P]
+// (one per 128 channels), the value codes as one box of [D / 2 bytes][P],
+// then Ks and Vs (fp16) by bulk copies. Stage: K boxes | V box | Ks | Vs.
+template <int D>
+__device__ __forceinline__ void issue_page_rk(const DecodeParams& p, const CUtensorMap* tk, const CUtensorMap* tv, int z,
+                                              uint32_t dst, uint32_t fb) {
+  const int P = p.P;
+  const int ks_bytes = P * (D / kGroup) * 2, vs_bytes = P * (D / kRkVGroup) * 2;
+  if (z < 0) {
+    flag(p.status, NK_DEVFLAG_BAD_PAGE);
+    mbar_arrive(fb);
+    return;
+  }
+  mbar_arrive_expect_tx(fb, 3 * P * D / 2 + ks_bytes + vs_bytes);
+#pragma unroll
+  for (int bx = 0; bx < D / 128; ++bx) tma_load_3d(dst + bx * P * 128, tk, fb, bx * 128, 0, z);
+  tma_load_3d(dst + P * D, tv, fb, 0, 0, z);
+  const uint8_t* chunk = p.pool + (int64_t)z * p.lay.chunk;
+  bulk_load(dst + 3 * P * D / 2, chunk + p.lay.ks, ks_bytes, fb);
+  bulk_load(dst + 3 * P * D / 2 + ks_bytes, chunk + p.lay.vs, vs_bytes, fb);
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -322,13 +375,21 @@ __device__ __forceinline__ void issue_page(const DecodeParams& p, const CUtensor
 // MMAs as they are (bf16 operands, Q bf16 too), there are no scales, and P
 // enters the PV product as bf16 hi + lo.
 // FMT: the pool's KvFmt (compile time, so that scale loads need no branch).
+// RK: an rk8v4 pool: tmap covers the key codes and tmapv the value codes (for
+// the other formats tmapv is unused); each query row is rotated by H64 / 8
+// and enters the QK product as fp16 hi + lo; the 4-bit values are widened
+// from their nibbles; P' carries one scale per 32 value channels.
 template <int D, int NT, int CS, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                 const __grid_constant__ CUtensorMap tmapv,
                                                                  const DecodeParams p) {
   constexpr bool BF = FMT == kFmtBf16;
+  constexpr bool RK = FMT == kFmtRk8v4;
+  static_assert(!RK || D >= 128, "rk8v4: head_dim 128 or 256");
   // the tensor map is a launch parameter (no earlier kernel writes it): its
   // descriptor fetch can start before the wait for the previous kernel
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmap)) : "memory");
+  if constexpr (RK) asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmapv)) : "memory");
   if (!p.early) chain_wait();  // (early: waits below, before the first page load)
   chain_release();
   constexpr int NTEAMS = kConsumerWarps / CS;
@@ -338,12 +399,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   constexpr int G_ALL = D / kGroup;
   constexpr int MROWS = NT * 8;
   static_assert(DW % kGroup == 0, "a warp owns whole 64-channel groups");
+  // P' groups of a warp (value channels per scale: 64, rk8v4 32) and the
+  // accumulator chunks of one
+  constexpr int GP = RK ? DW / kRkVGroup : GW;
+  constexpr int CPG = RK ? 2 : 4;
+  constexpr int GV_ALL = RK ? D / kRkVGroup : G_ALL;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Geometry geo = geometry(FMT, D, NT, CS, p.P, p.B);
   const int S = geo.stages;
-  constexpr int sb = FMT == kFmtI8F16 ? 2 : 4;
+  constexpr int sb = (FMT == kFmtI8F16 || RK) ? 2 : 4;
   int* pre = reinterpret_cast<int*>(smem + geo.pre_off);
   int* warp_tot = pre + (p.B + 1);
   volatile int* abort_flag = pre + (p.B + 1) + 8;
@@ -403,7 +469,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
   for (int gi = 0; gi < GW; ++gi)
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) loff[gi][q2] = box_off<D>(P, 0, lm_key, (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk);
+    for (int q2 = 0; q2 < 2; ++q2) {
+      const int ch16 = (ch0 >> 4) + gi * 4 + q2 * 2 + lm_chunk;
+      // rk8v4 key boxes hold P rows of 128 bytes (no value rows)
+      loff[gi][q2] = RK ? (uint32_t)((ch16 >> 3) * (P * 128) + lm_key * 128 + (((ch16 & 7) ^ (lm_key & 7)) << 4))
+                        : box_off<D>(P, 0, lm_key, ch16);
+    }
+  // rk8v4 value rows: D / 2 bytes (32 channels per 16-byte chunk) after the
+  // key boxes, 128-byte swizzle (64-byte at head_dim 128); matrices (keys
+  // 0-7 | 8-15) x (chunks of two consecutive value groups)
+  constexpr int RBV = D / 2;
+  uint32_t vloff[RK ? GP / 2 : 1];
+  if constexpr (RK) {
+#pragma unroll
+    for (int pv = 0; pv < GP / 2; ++pv) {
+      const int c = (ch0 >> 5) + 2 * pv + lm_chunk;
+      const int sw = RBV == 128 ? (c ^ (lm_key & 7)) : (c ^ ((lm_key >> 1) & 3));
+      vloff[pv] = (uint32_t)(P * D + lm_key * RBV + (sw << 4));
+    }
+  }
   // bf16 stage: boxes of 64 channels, 128-byte rows (K rows, then V rows),
   // 128-byte swizzle. K fragments of a 16-channel chunk: matrices (keys 0-7 |
   // 8-15) x (channels 0-7 | 8-15); V^T fragments (transposed loads): matrices
@@ -422,9 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   }
 
   uint32_t bq[NT][NCH][2];
+  uint32_t bql[RK ? NT : 1][RK ? NCH : 1][2];  // rk8v4: the low fp16 part of the rotated rows
   float o[NCH][NT][4];
   float m_run[NT][2], l_run[NT][2];
-  float sv[GW];  // 2^-ev of this warp's P' per group (0 before the segment's first block)
+  float sv[GP];  // 2^-ev of this warp's P' per group (0 before the segment's first block)
   int row_t[NT][2];  // verify column of each held row (T - 1 for padding rows)
 
   // Q fragments of this warp's channels, all rows of a segment's unit:
@@ -502,9 +587,83 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
   // conversion; kq = sm_scale log2(e) 2^-e undoes it on the partial scores
   // (folded into the key scales: no work per block).
   float kq = p.scale2;
+  // rk8v4: each 64-channel group of a row becomes H64 q / 8 (butterflies in
+  // fp32 over the channel-index bits: bits 0, 1 and 4, 5 are the thread's
+  // own registers -- channel 16 cc + 4 t4 + 2 h + j of a group sits in
+  // bq[.][4 gi + cc][h], half j -- and bits 2, 3 its t4 neighbours'), then
+  // scaled like the other formats and split into fp16 hi + lo.
+  auto convert_q_rk = [&]() {
+    float qf[NT][GW][16];  // [row tile][group][cc * 4 + h * 2 + j]
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int gi = 0; gi < GW; ++gi)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            qf[nt][gi][cc * 4 + h * 2] = bf16_lo(bq[nt][gi * 4 + cc][h]);
+            qf[nt][gi][cc * 4 + h * 2 + 1] = bf16_hi(bq[nt][gi * 4 + cc][h]);
+          }
+    float m = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int gi = 0; gi < GW; ++gi) {
+        float* v = qf[nt][gi];
+        // register bits: j (stride 1), h (stride 2), cc (strides 4, 8)
+#pragma unroll
+        for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if ((i & st) == 0) {
+              const float a = v[i], b = v[i + st];
+              v[i] = a + b;
+              v[i + st] = a - b;
+            }
+        // lane bits: t4 bit 0 (channel bit 2), t4 bit 1 (channel bit 3)
+#pragma unroll
+        for (int lb = 1; lb <= 2; lb <<= 1) {
+          const bool upper = (t4 & lb) != 0;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float o2 = __shfl_xor_sync(0xffffffffu, v[i], lb);
+            v[i] = upper ? o2 - v[i] : v[i] + o2;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          v[i] *= 0.125f;
+          m = fmaxf(m, fabsf(v[i]));
+        }
+      }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const int e = q_norm_exp(m);
+    const float qs = pow2i(e);
+    kq = p.scale2 * pow2i(-e);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int gi = 0; gi < GW; ++gi)
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float x0 = qf[nt][gi][cc * 4 + h * 2] * qs, x1 = qf[nt][gi][cc * 4 + h * 2 + 1] * qs;
+            const __half2 hh = __floats2half2_rn(x0, x1);
+            const float2 hf = __half22float2(hh);
+            bq[nt][gi * 4 + cc][h] = *reinterpret_cast<const uint32_t*>(&hh);
+            if constexpr (RK) bql[nt][gi * 4 + cc][h] = pack_f16(x0 - hf.x, x1 - hf.y);
+          }
+  };
   auto convert_q = [&]() {
     kq = p.scale2;
     if constexpr (BF) return;  // bf16 operands as they are, no scaling
+    if constexpr (RK) {
+      convert_q_rk();
+      return;
+    }
     float m = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -546,7 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
     const int n0 = total < S ? total : S;
     for (int q = 0; q < n0; ++q) {
       if (!p.issuable(q)) break;
-      issue_page<D, BF>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+      if constexpr (RK)
+        issue_page_rk<D>(p, &tmap, &tmapv, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
+      else
+        issue_page<D, BF>(p, &tmap, pid[q], stage0 + q * geo.stage_bytes, smem_u32(&full_bar[q]));
       icnt[q] = 1;
     }
   }
@@ -588,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         for (int k = 0; k < 4; ++k) o[c][nt][k] = 0.f;
     }
 #pragma unroll
-    for (int gi = 0; gi < GW; ++gi) sv[gi] = BF ? 1.f : 0.f;
+    for (int gi = 0; gi < GP; ++gi) sv[gi] = BF ? 1.f : 0.f;
 
     // this team's blocks of the segment: CTA-wide block numbers jn = team,
     // team + NTEAMS, ... (4 blocks of 16 keys per 64-key page)
@@ -607,7 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
       const int s = s_cur;
       const uint32_t par = par_cur;
       const uint32_t st = stage0 + s * geo.stage_bytes;
-      const uint8_t* ks_s = smem + s * geo.stage_bytes + 2 * P * D;  // [P][G_ALL], fp32 or fp16
+      // [P][G_ALL] key scales (fp32 or fp16), then [P][GV_ALL] value scales
+      const uint8_t* ks_s = smem + s * geo.stage_bytes + (RK ? 3 * P * D / 2 : 2 * P * D);
       const uint8_t* vs_s = ks_s + P * G_ALL * sb;
       {
         // after one wait of the CTA has run out, no wait blocks any more (the
@@ -659,6 +822,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
                   mma16816(acc[gi][nt], a0, a1, a2, a3, bq[nt][gi * 4 + cc][0], bq[nt][gi * 4 + cc][1]);
+                if constexpr (RK) {  // the rotated rows' low parts
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt)
+                    mma16816(acc[gi][nt], a0, a1, a2, a3, bql[nt][gi * 4 + cc][0], bql[nt][gi * 4 + cc][1]);
+                }
               }
           }
           float sc[NT][4];
@@ -806,53 +974,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             // P' window of each of this warp's groups (bits as in ev_update's
             // window: a Vs 2^-ev above 2^6, or one at least 2^-10); the
             // exponents move only when a group leaves it
+            const int vgrp0 = RK ? ch0 / kRkVGroup : grp0;
             {
               uint32_t wb = 0u;
 #pragma unroll
-              for (int gi = 0; gi < GW; ++gi) {
-                const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * G_ALL + grp0 + gi, sb) : 0.f;
-                const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb) : 0.f;
+              for (int gi = 0; gi < GP; ++gi) {
+                const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb) : 0.f;
+                const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb) : 0.f;
                 const float tv = fmaxf(a0, a1) * sv[gi];
                 wb |= (tv > 64.f ? 1u : 0u) << gi;
-                wb |= (tv >= 0.0009765625f ? 1u : 0u) << (4 + gi);
+                wb |= (tv >= 0.0009765625f ? 1u : 0u) << (8 + gi);
               }
               wb = __reduce_or_sync(0xffffffffu, wb);
-              const uint32_t moving = ((wb & 0xfu) | (~(wb >> 4) & 0xfu)) & ((1u << GW) - 1u);
+              const uint32_t moving = ((wb & 0xffu) | (~(wb >> 8) & 0xffu)) & ((1u << GP) - 1u);
               if (moving) {
 #pragma unroll
-                for (int gi = 0; gi < GW; ++gi) {
+                for (int gi = 0; gi < GP; ++gi) {
                   if (!((moving >> gi) & 1u)) continue;
-                  const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * G_ALL + grp0 + gi, sb) : 0.f;
-                  const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb) : 0.f;
+                  const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb) : 0.f;
+                  const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb) : 0.f;
                   const uint32_t mxb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(a0, a1)));
                   int ev = sv[gi] == 0.f ? kEvUnset : -exp_of(sv[gi]);
                   float beta;
                   if (mxb != 0u && ev_update(ev, exp_of(__uint_as_float(mxb)), beta)) {
                     sv[gi] = pow2i(-ev);
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
+                    for (int cc = 0; cc < CPG; ++cc)
 #pragma unroll
                       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) o[gi * 4 + cc][nt][k] *= beta;
+                        for (int k = 0; k < 4; ++k) o[gi * CPG + cc][nt][k] *= beta;
                   }
                 }
               }
             }
-#pragma unroll
-            for (int gi = 0; gi < GW; ++gi) {
-              uint32_t vw[4][2];  // [chunk][keys 0-7 | 8-15], transposed fragments
-              const uint32_t vbase = st + (P + key0) * RB;
-#pragma unroll
-              for (int q2 = 0; q2 < 2; ++q2)
-                ldsm_x4_t(vbase + loff[gi][q2], vw[q2 * 2][0], vw[q2 * 2][1], vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
-              float v0 = ld_scale(vs_s, (key0 + g) * G_ALL + grp0 + gi, sb);
-              float v1 = ld_scale(vs_s, (key0 + g + 8) * G_ALL + grp0 + gi, sb);
+            // P' of group gi as the B fragments of the product (hi, lo)
+            auto p_frags = [&](int gi, uint32_t (&bh)[NT][2], uint32_t (&bl)[NT][2]) {
+              float v0 = ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb);
+              float v1 = ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb);
               v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
               v1 = valid1 ? v1 : 0.f;
               v0 *= sv[gi];
               v1 *= sv[gi];
-              uint32_t bh[NT][2], bl[NT][2];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
@@ -864,26 +1027,75 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
                 bl[nt][0] = movmatrix_t(l01);
                 bl[nt][1] = movmatrix_t(l23);
               }
-              uint32_t av[4][4];
+            };
+            if constexpr (RK) {
+              // Two value groups (two 16-byte chunks of 32 channels) per
+              // transposed load: register vw[j][h] holds, for keys 2 t4 and
+              // 2 t4 + 1 (+ 8 h), bytes 2 g and 2 g + 1 of chunk j, i.e.
+              // channels 4 g .. 4 g + 3. Accumulator chunk 2 gi + u holds
+              // channels 32 gi + 4 g + 2 u (rows g) and + 1 (rows g + 8).
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                const uint32_t w0 = vw[cc][0] ^ bias, w1 = vw[cc][1] ^ bias;
-                av[cc][0] = i8x2_to_f16x2(w0, 0x4240);
-                av[cc][1] = i8x2_to_f16x2(w0, 0x4341);
-                av[cc][2] = i8x2_to_f16x2(w1, 0x4240);
-                av[cc][3] = i8x2_to_f16x2(w1, 0x4341);
+              for (int pv = 0; pv < GP / 2; ++pv) {
+                uint32_t vw[2][2];
+                ldsm_x4_t(st + key0 * RBV + vloff[pv], vw[0][0], vw[0][1], vw[1][0], vw[1][1]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const int gi = 2 * pv + j;
+                  uint32_t bh[NT][2], bl[NT][2];
+                  p_frags(gi, bh, bl);
+                  const uint32_t w0 = vw[j][0], w1 = vw[j][1], w08 = w0 >> 8, w18 = w1 >> 8;
+                  uint32_t av[2][4];
+                  av[0][0] = nib_lo(w0);
+                  av[0][1] = nib_hi(w0);
+                  av[0][2] = nib_lo(w1);
+                  av[0][3] = nib_hi(w1);
+                  av[1][0] = nib_lo(w08);
+                  av[1][1] = nib_hi(w08);
+                  av[1][2] = nib_lo(w18);
+                  av[1][3] = nib_hi(w18);
+#pragma unroll
+                  for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                      mma16816(o[gi * 2 + u][nt], av[u][0], av[u][1], av[u][2], av[u][3], bh[nt][0], bh[nt][1]);
+#pragma unroll
+                  for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                      mma16816(o[gi * 2 + u][nt], av[u][0], av[u][1], av[u][2], av[u][3], bl[nt][0], bl[nt][1]);
+                }
               }
-              // all hi products first, then all lo: 4*NT independent accumulators between dependent pairs
+            } else {
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc)
+              for (int gi = 0; gi < GW; ++gi) {
+                uint32_t vw[4][2];  // [chunk][keys 0-7 | 8-15], transposed fragments
+                const uint32_t vbase = st + (P + key0) * RB;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                  mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bh[nt][0], bh[nt][1]);
+                for (int q2 = 0; q2 < 2; ++q2)
+                  ldsm_x4_t(vbase + loff[gi][q2], vw[q2 * 2][0], vw[q2 * 2][1], vw[q2 * 2 + 1][0], vw[q2 * 2 + 1][1]);
+                uint32_t bh[NT][2], bl[NT][2];
+                p_frags(gi, bh, bl);
+                uint32_t av[4][4];
 #pragma unroll
-              for (int cc = 0; cc < 4; ++cc)
+                for (int cc = 0; cc < 4; ++cc) {
+                  const uint32_t w0 = vw[cc][0] ^ bias, w1 = vw[cc][1] ^ bias;
+                  av[cc][0] = i8x2_to_f16x2(w0, 0x4240);
+                  av[cc][1] = i8x2_to_f16x2(w0, 0x4341);
+                  av[cc][2] = i8x2_to_f16x2(w1, 0x4240);
+                  av[cc][3] = i8x2_to_f16x2(w1, 0x4341);
+                }
+                // all hi products first, then all lo: 4*NT independent accumulators between dependent pairs
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                  mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bl[nt][0], bl[nt][1]);
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt)
+                    mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bh[nt][0], bh[nt][1]);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+                  for (int nt = 0; nt < NT; ++nt)
+                    mma16816(o[gi * 4 + cc][nt], av[cc][0], av[cc][1], av[cc][2], av[cc][3], bl[nt][0], bl[nt][1]);
+              }
             }
           }
         }
@@ -897,8 +1109,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             if (qn < total && p.issuable(qn) && !*abort_flag) {
               // every reader arrived before its increment: the phase is complete
               if (mbar_wait(smem_u32(&empty_bar[s]), par, p.wait_cycles)) {
-                issue_page<D, BF>(p, &tmap, qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn), st,
-                              smem_u32(&full_bar[s]));
+                const int zn = qn < kPidCache ? pid[qn] : page_coord(p, sh, pre, x_begin, qn);
+                if constexpr (RK)
+                  issue_page_rk<D>(p, &tmap, &tmapv, zn, st, smem_u32(&full_bar[s]));
+                else
+                  issue_page<D, BF>(p, &tmap, zn, st, smem_u32(&full_bar[s]));
                 ++icnt[s];
               } else {
                 flag(p.status, NK_DEVFLAG_TIMEOUT);
@@ -914,21 +1129,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 
     // the accumulators hold O 2^-ev per group: back to O
 #pragma unroll
-    for (int gi = 0; gi < GW; ++gi) {
+    for (int gi = 0; gi < GP; ++gi) {
       if (BF || sv[gi] == 0.f) continue;
       const float f = pow2i(-exp_of(sv[gi]));
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
+      for (int cc = 0; cc < CPG; ++cc)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int k = 0; k < 4; ++k) o[gi * 4 + cc][nt][k] *= f;
+          for (int k = 0; k < 4; ++k) o[gi * CPG + cc][nt][k] *= f;
     }
 
     const bool last_seg = x >= x_end;
-    // channel (within its 16-channel chunk) of accumulator element k: INT8
-    // 2 g + (k >> 1) (the V fragments' byte order), bf16 g + 8 (k >> 1)
-    auto och = [&](int k) { return BF ? g + 8 * (k >> 1) : 2 * g + (k >> 1); };
+    // channel (from the warp's first) of accumulator chunk c, element k: INT8
+    // 16 c + 2 g + (k >> 1) (the V fragments' byte order), rk8v4
+    // 32 (c >> 1) + 4 g + 2 (c & 1) + (k >> 1) (the nibble order), bf16
+    // 16 c + g + 8 (k >> 1). INT8 and rk8v4 keep elements k and k + 2 in
+    // adjacent channels (cpair: the first of the two).
+    auto cpair = [&](int c) { return RK ? 32 * (c >> 1) + 4 * g + 2 * (c & 1) : 16 * c + 2 * g; };
+    auto och = [&](int c, int k) { return BF ? 16 * c + g + 8 * (k >> 1) : cpair(c) + (k >> 1); };
 
     // ---- merge the teams of this segment and write the result
     // row sums: reduce the per-lane partial l over the 8 lanes of a row
@@ -971,12 +1190,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            float* row = acc_buf + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16;
+            float* row = acc_buf + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0;
             if constexpr (BF) {
-              row[g] = o[c][nt][e];
-              row[g + 8] = o[c][nt][e + 2];
+              row[c * 16 + g] = o[c][nt][e];
+              row[c * 16 + g + 8] = o[c][nt][e + 2];
             } else {
-              *reinterpret_cast<float2*>(row + 2 * g) = make_float2(o[c][nt][e], o[c][nt][e + 2]);
+              *reinterpret_cast<float2*>(row + cpair(c)) = make_float2(o[c][nt][e], o[c][nt][e + 2]);
             }
           }
     }
@@ -1022,14 +1241,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                float* row = mo + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0 + c * 16;
+                float* row = mo + (nt * 8 + 2 * t4 + e) * (D + 4) + ch0;
                 if constexpr (BF) {  // channels 16 c + g, 16 c + g + 8
-                  const float p0 = rd == 0 ? 0.f : row[g], p1 = rd == 0 ? 0.f : row[g + 8];
-                  row[g] = fmaf(o[c][nt][e], f[nt][e], p0);
-                  row[g + 8] = fmaf(o[c][nt][e + 2], f[nt][e], p1);
+                  const float p0 = rd == 0 ? 0.f : row[c * 16 + g], p1 = rd == 0 ? 0.f : row[c * 16 + g + 8];
+                  row[c * 16 + g] = fmaf(o[c][nt][e], f[nt][e], p0);
+                  row[c * 16 + g + 8] = fmaf(o[c][nt][e + 2], f[nt][e], p1);
                 } else {
                   // fragment elements e and e + 2 are adjacent channels of one row
-                  float2* dst = reinterpret_cast<float2*>(row + 2 * g);
+                  float2* dst = reinterpret_cast<float2*>(row + cpair(c));
                   const float2 prev = rd == 0 ? make_float2(0.f, 0.f) : *dst;
                   *dst = make_float2(fmaf(o[c][nt][e], f[nt][e], prev.x), fmaf(o[c][nt][e + 2], f[nt][e], prev.y));
                 }
@@ -1049,12 +1268,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  prev[nt][k] = (tm == 0) ? 0.f : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + och(k)];
+                  prev[nt][k] = (tm == 0) ? 0.f : mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + och(c, k)];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + c * 16 + och(k)] =
+                  mo[(nt * 8 + 2 * t4 + (k & 1)) * (D + 4) + ch0 + och(c, k)] =
                       fmaf(o[c][nt][k], f[nt][k & 1], prev[nt][k]);
             }
           }

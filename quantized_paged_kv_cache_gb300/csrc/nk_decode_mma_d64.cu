@@ -11,7 +11,8 @@ static cudaError_t launch_tb(const CUtensorMap& map, const DecodeParams& p, cuda
   if (geo.stages < 2 || geo.total > kSmemLimit) return cudaErrorInvalidConfiguration;
   cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_mma_kernel<D, NT, CS, FMT>), geo.total);
   if (e != cudaSuccess) return e;
-  return launch_chained(decode_mma_kernel<D, NT, CS, FMT>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, p);
+  return launch_chained(decode_mma_kernel<D, NT, CS, FMT>, dim3(p.n_ctas), dim3(kThreads), geo.total, st, map, map,
+                        p);
 }
 
 // INT8 pools with fp32 or fp16 scales, and bf16 pools

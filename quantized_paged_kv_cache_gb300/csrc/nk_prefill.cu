@@ -38,7 +38,7 @@
 
 namespace nk {
 namespace mma {
-cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map);
+cudaError_t make_pool_map(const DecodeParams& p, CUtensorMap* map, int part = 0);
 }
 
 namespace pf {
