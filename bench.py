@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--config", default="mix",
                     help="mix (default: the largest single-GPU configuration, 8 x 1,024-row append + C8 x T4 "
                          "attention at 131,072) | tiny | c1_decode | c8_verify | long_context | c8_decode | c1_rk8v4 "
-                         "| c1_i8f16 | c8_i8f16 | mix_prefill")
+                         "| c1_i8f16 | c8_i8f16 | mix_prefill | prefill_32k")
     ap.add_argument("--kernel", choices=["mma", "simt"], default="mma", help="attention kernel of our arm")
     ap.add_argument("--num-ctas", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -72,13 +72,13 @@ def _code_only(text: str) -> str:
 
 
 def source_hash() -> str:
-    """Hash of the code of the decode split kernels' sources and the headers
-    they include (the kernels whose ncu traffic profiles/ncu_traffic.json
-    records), comments excluded."""
+    """Hash of the code of the decode split kernels' and the prefill kernel's
+    sources and the headers they include (the kernels whose ncu traffic
+    profiles/ncu_traffic.json records), comments excluded."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_paged_kv_cache_gb300", "csrc")
     for fn in sorted(os.listdir(d)):
-        if fn.startswith("nk_decode") or fn in ("nk_common.cuh", "nk_ptx.cuh"):
+        if fn.startswith(("nk_decode", "nk_prefill")) or fn in ("nk_common.cuh", "nk_ptx.cuh"):
             with open(os.path.join(d, fn), encoding="utf-8") as f:
                 h.update(fn.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]

@@ -154,6 +154,11 @@ def make(name: str) -> Workload:
                      append_len=1024,
                      note="the append + attend mix's chunk: 1,024 tokens of each of 8 seqs appended at "
                           "130,048..131,071, then their chunked-prefill attention over 131,072 keys")
+    elif name == "prefill_32k":
+        w = Workload("prefill_32k", B=2, T=1024, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[32768] * 2, seed=5,
+                     append_len=1024,
+                     note="a smaller chunked prefill for profiling: 1,024 tokens of each of 2 seqs at "
+                          "31,744..32,767, attending to 32,768 keys (142 MB of cache, above the L2)")
     elif name == "mix":
         w = Workload("mix", B=8, T=4, Hq=24, Hkv=4, D=256, P=64, ctx_lens=[131072] * 8, seed=4, append_len=1024,
                      note="append of a 1,024-token chunk into each of 8 seqs (positions 130,048..131,071), "
@@ -166,7 +171,7 @@ def make(name: str) -> Workload:
 CONFIGS = ("tiny", "c1_decode", "c8_verify", "long_context", "mix", "c8_decode")  # INT8 group-64 pools
 RK8V4_CONFIGS = ("c1_rk8v4",)
 FORMAT_CONFIGS = ("c1_i8f16", "c8_i8f16")  # the pages' INT8 layout (fp16 scales)
-PREFILL_CONFIGS = ("mix_prefill",)  # chunked prefill (T = 1,024)
+PREFILL_CONFIGS = ("mix_prefill", "prefill_32k")  # chunked prefill (T = 1,024)
 
 
 def tables(w: Workload, num_pages: int | None = None) -> Workload:

@@ -2,11 +2,13 @@
 baseline against the oracle ("NInfer-3090" README, "Choosing a KV format":
 the int8 and bf16 rows of the table, 33,792 and 65,536 bytes per token).
 
-The append must reproduce the oracle's pool bytes exactly; attention must meet
-the tolerance of the INT8 path against the oracle's fp64 result, on the
-tcgen05 kernel (i8f16 at head_dim 256, 64-key pages, 9..32 rows per kv-head)
-and on the mma.sync kernel (every other shape; every bf16 shape). Slots past
-the context hold 0xFF bytes (NaN scales or values), which must not matter.
+The append must reproduce the oracle's pool bytes exactly (both formats);
+i8f16 attention must meet the tolerance of the INT8 path against the
+oracle's fp64 result, on the tcgen05 kernel (head_dim 256, 64-key pages,
+9..32 rows per kv-head) and on the mma.sync kernel (every other shape). The
+bf16 decode launches no kernel in this build and must say so
+(NK_ERR_UNSUPPORTED). Slots past the context hold 0xFF bytes (NaN scales or
+values), which must not matter.
 """
 import numpy as np
 import pytest
