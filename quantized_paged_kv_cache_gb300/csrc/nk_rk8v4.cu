@@ -51,12 +51,16 @@ __device__ __forceinline__ uint32_t rk_code(float x, float s, int qmax) {
 //
 // A finite bf16 value is an integer multiple of the quantum of its exponent
 // (2^(e-134) for exponent field e >= 1, 2^-133 for e = 0). When the group's
-// non-zero values have exponent fields within 39 of each other, every partial
-// sum of up to 64 of them is an integer multiple of the smallest quantum and
-// below 2^53 of it, so fp64 butterflies (a + b, a - b) are exact, the 1/8 is
-// exact, and one conversion to fp32 gives the correctly rounded value. Wider
-// groups (a rare, degenerate input) take rk_rotate_wide: an exact integer
-// sum in 32-bit limbs and an explicit round to nearest even.
+// non-zero values have exponent fields within 39 of each other, each is an
+// integer below 2^47 in units of the smallest one, every partial sum of up
+// to 64 of them is an integer below 2^53, so int64 butterflies (a + b,
+// a - b) are exact; one int64 -> fp32 conversion rounds to nearest even and
+// the unit 2^(emin-137) (the 1/8 included) is applied to the exponent
+// field, exact while the result is a normal fp32 number (and an infinity
+// where it overflows). Wider groups and results in the fp32 subnormal range
+// (rare, degenerate inputs) take rk_rotate_wide: an exact integer sum in
+// 32-bit limbs and an explicit round to nearest even. (GB300 runs fp64 at a
+// small fraction of its integer rate, so the butterflies stay integer.)
 // ---------------------------------------------------------------------------
 constexpr int kWideLimbs = 10;  // 320 bits: |x| < 2^128 in 2^-133 units, times 64
 
@@ -160,24 +164,44 @@ __device__ __forceinline__ void rk_key_group(const uint4* src, uint4* dst, uint1
     emin = min(emin, e);
   }
   float t[kGroup];
-  if (emax - emin <= 39) {
-    double d[kGroup];
+  bool wide = emax - emin > 39;
+  if (!wide) {
+    long long d[kGroup];
 #pragma unroll
-    for (int i = 0; i < kGroup; ++i) d[i] = (double)__uint_as_float((uint32_t)xb[i] << 16);
+    for (int i = 0; i < kGroup; ++i) {
+      const uint32_t mag = xb[i] & 0x7fffu, e = mag >> 7;
+      const long long m = mag == 0u ? 0ll
+                                    : (long long)((mag & 0x7fu) | (e != 0u ? 0x80u : 0u))
+                                          << ((e != 0u ? (int)e : 1) - emin);
+      d[i] = (xb[i] & 0x8000u) ? -m : m;
+    }
 #pragma unroll
     for (int h = 1; h < kGroup; h <<= 1)
 #pragma unroll
       for (int i = 0; i < kGroup; ++i)
         if ((i & h) == 0) {
-          const double a = d[i], b = d[i + h];
-          d[i] = __dadd_rn(a, b);
-          d[i + h] = __dsub_rn(a, b);
+          const long long a = d[i], b = d[i + h];
+          d[i] = a + b;
+          d[i + h] = a - b;
         }
+    const int k = emin - 137;  // y = d 2^k
 #pragma unroll
-    for (int i = 0; i < kGroup; ++i) t[i] = __double2float_rn(__dmul_rn(d[i], 0.125));
-  } else {
-    rk_rotate_wide(xb, t);
+    for (int i = 0; i < kGroup; ++i) {
+      if (d[i] == 0) {
+        t[i] = 0.f;
+        continue;
+      }
+      const uint32_t fb = __float_as_uint(__ll2float_rn(d[i]));  // |d| >= 1: a normal number
+      const int ne = (int)((fb >> 23) & 0xffu) + k;
+      if (ne >= 255)
+        t[i] = __uint_as_float((fb & 0x80000000u) | 0x7f800000u);
+      else if (ne >= 1)
+        t[i] = __uint_as_float((uint32_t)((int)fb + k * (1 << 23)));
+      else
+        wide = true;  // an fp32 subnormal result: rounded in the wide path
+    }
   }
+  if (wide) rk_rotate_wide(xb, t);
   float amax = 0.f;
   bool finite = true;
 #pragma unroll
