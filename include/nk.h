@@ -379,8 +379,9 @@ int nk_version(void);
 /*
  * nk_test_inject_copy_stall -- failure injection for tests of the bounded
  * waits (the pages have no counterpart; nothing here faults or traps). While
- * withheld_page >= 0, every tensor-core decode launched afterwards by this
- * process (nk_paged_decode_attn, nk_decode_step, the no-alloc variant) never
+ * withheld_page >= 0, every tensor-core decode and prefill launched
+ * afterwards by this process (nk_paged_decode_attn, nk_decode_step, the
+ * no-alloc variant, the other formats' decodes, nk_paged_prefill_attn) never
  * issues the page copies of its CTA page numbers >= withheld_page, and bounds
  * each of its waits by wait_cycles SM clock cycles (0 keeps the default of
  * about 2 s). A wait for a withheld page runs out, sets NK_DEVFLAG_TIMEOUT in

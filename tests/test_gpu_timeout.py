@@ -1,7 +1,7 @@
-"""Failure detection of the decode kernels' bounded waits (GPU), without a
-fault: the copies of some pages are simply never issued.
+"""Failure detection of the decode and prefill kernels' bounded waits (GPU),
+without a fault: the copies of some pages are simply never issued.
 
-nk_test_inject_copy_stall makes the tensor-core decode kernels skip the page
+nk_test_inject_copy_stall makes the tensor-core kernels skip the page
 copies of CTA page numbers >= k and bounds every wait by a short limit. A wait
 for such a page runs out: the call must report NK_DEVFLAG_TIMEOUT in the
 status word, return within a fraction of a second, and leave the device
@@ -82,3 +82,33 @@ def test_decode_step_reports_the_timeout():
     st = int(status.item())
     assert st & nk.NK_DEVFLAG_TIMEOUT, f"status {st}: no timeout reported"
     assert st & ~(nk.NK_DEVFLAG_TIMEOUT | nk.NK_DEVFLAG_RANGE) == 0, f"status {st}"
+
+
+def test_prefill_reports_the_timeout_and_the_device_recovers():
+    """The chunked prefill's page ring: copies of the CTAs' pages 2 and on are
+    withheld; the call reports the timeout quickly (a non-finite output may be
+    flagged too: the stages hold stale bytes), and the next call gives the
+    oracle's result."""
+    w = wl.custom("pf_timeout", B=1, T=64, Hq=8, Hkv=2, D=128, P=32, ctx_lens=[1500], seed=57,
+                  num_pages=(1500 + 31) // 32 + 1)
+    c = build(w)
+    ref = oracle_attention_full(c)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nk.paged_prefill_attn(c.pool, c.q, c.bt, c.ctx, w.sm_scale, w.max_ctx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    nk.test_inject_copy_stall(2, WAIT)
+    t0 = time.perf_counter()
+    nk.paged_prefill_attn(c.pool, c.q, c.bt, c.ctx, w.sm_scale, w.max_ctx, status=status)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    nk.test_inject_copy_stall(-1)
+    st = int(status.item())
+    assert st & nk.NK_DEVFLAG_TIMEOUT, f"status {st}: no timeout reported"
+    assert st & ~(nk.NK_DEVFLAG_TIMEOUT | nk.NK_DEVFLAG_RANGE) == 0, f"status {st}"
+    assert elapsed < 1.0, f"the call took {elapsed:.3f} s"
+    status.zero_()
+    out = nk.paged_prefill_attn(c.pool, c.q, c.bt, c.ctx, w.sm_scale, w.max_ctx, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(out, ref, "prefill after the timed-out call")
