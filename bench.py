@@ -350,6 +350,30 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
     stream = torch.cuda.current_stream()
     bi = h_buf.numel()  # the one host->device copy of a step (inputs + alignment padding)
     bo = out_h.numel() * out_h.element_size()
+    via = "Python API: one pinned host->device copy, the step's calls, the output read back"
+    if one_call_step(args, w):
+        # the library's host-memory step: one C call copies the inputs in,
+        # runs the step, copies the output and the status word out, and waits
+        B, T, Hq = int(S["q"].shape[0]), int(S["q"].shape[1]), int(S["q"].shape[2])
+        total = int(S["k"].shape[0])
+        nbytes, offs = nk.step_host_layout(B, total, T, Hq, w.Hkv, w.D)
+        h_in = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+        for name, o in zip(("k", "v", "q", "sp", "cu", "ctx"), offs):
+            t = S[name]
+            n = t.numel() * t.element_size()
+            h_in[o:o + n].view(t.dtype).view(t.shape).copy_(t.cpu())
+        staging = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        st_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+        bi, bo = nbytes, bo + 4
+        via = "nk_decode_step_host: one C call per step (host->device copy, append + attention, output and status read back, stream wait)"
+
+        def step(i):
+            pool = S["pools"][i % replicas]
+            nk.decode_step_host(pool, S["bt"], B, total, T, Hq, w.sm_scale, w.max_ctx, h_in, staging, S["out"],
+                                out_h, num_ctas=S["nct"], workspace=S["ws"], status=S["status"], status_host=st_h,
+                                stream=stream)
+
+        return _time_e2e(args, step, step_bytes, world, device, bi, bo, via)
 
     def step(i):
         d_buf.copy_(h_buf, non_blocking=True)
@@ -365,6 +389,12 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
         out_h.copy_(S["out"], non_blocking=True)
         stream.synchronize()
 
+    return _time_e2e(args, step, step_bytes, world, device, bi, bo, via)
+
+
+def _time_e2e(args, step, step_bytes, world, device, bi, bo, via):
+    import torch
+
     for i in range(max(args.warmup, 3)):
         step(i)
     K = args.steps
@@ -376,7 +406,7 @@ def run_e2e(args, w, S, dec, replicas, step_bytes, world, device):
     el = max_over_ranks((time.perf_counter() - t0) * 1e3 / K, world, device)
     return {"value": round(job_gbs(step_bytes, el, world), 3), "unit": "GB/s",
             "ms_per_step": round(el, 5), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "sync": "host waits for each step's output"}
+            "sync": "host waits for each step's output", "via": via}
 
 
 # ---------------------------------------------------------------------------

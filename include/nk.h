@@ -31,8 +31,10 @@
  *   - Pointers named *_dev are device pointers; everything else is host.
  *   - bf16 tensors are raw 16-bit bf16 bit patterns in device memory.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
- *   - The library allocates no memory and never synchronizes. All buffers
- *     (pool, tables, Q, outputs, workspace, status word) belong to the caller.
+ *   - The library allocates no memory and never synchronizes (except
+ *     nk_decode_step_host, the host-memory step, which waits for its stream).
+ *     All buffers (pool, tables, Q, outputs, workspace, status word) belong
+ *     to the caller.
  *   - Host-checkable argument errors return an NK_ERR_* code before anything
  *     is launched. Errors in device-resident data (a page id outside the
  *     pool, a position beyond the block table, ctx_len < T or > max_ctx) are
@@ -203,6 +205,36 @@ int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32
                    const void* v_dev, const void* q_dev, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
                    int32_t num_q_heads, float sm_scale, int32_t max_ctx, int32_t num_ctas, void* workspace_dev,
                    size_t workspace_bytes, void* out_dev, int32_t* status_dev, void* stream);
+
+/*
+ * nk_decode_step_host -- nk_decode_step from host memory, end to end: the
+ * step's inputs are read from one host buffer in_host laid out by
+ * nk_step_host_layout (pinned memory makes the transfer asynchronous),
+ * copied in one transfer into the caller's device staging buffer staging_dev
+ * (the same layout; 16-byte aligned), the step runs on `stream` exactly as
+ * nk_decode_step with those device copies, and the B*T*num_q_heads*head_dim
+ * bf16 output rows (written to out_dev) are copied to out_host, the status
+ * word *status_dev (when both it and status_host are given) to *status_host.
+ * The call then waits for the stream: this is the one entry point that
+ * synchronizes. Arguments and checks as nk_decode_step; NK_ERR_NULL for a
+ * missing in_host, staging_dev or out_host; a failed copy or wait returns
+ * NK_ERR_CUDA. The pages have no counterpart; it is the step a serving loop
+ * makes when its inputs live on the host.
+ */
+int nk_decode_step_host(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                        int32_t B, int32_t total_new, int32_t T, int32_t num_q_heads, float sm_scale,
+                        int32_t max_ctx, int32_t num_ctas, const void* in_host, void* staging_dev,
+                        void* workspace_dev, size_t workspace_bytes, void* out_dev, void* out_host,
+                        int32_t* status_dev, int32_t* status_host, void* stream);
+
+/* Layout of nk_decode_step_host's input buffer (host and device alike):
+ * offsets[0] new K rows [total_new][num_kv_heads][head_dim] bf16,
+ * offsets[1] new V rows (same), offsets[2] Q [B][T][num_q_heads][head_dim]
+ * bf16, offsets[3] start_pos [B] int32, offsets[4] cu_new [B + 1] int32,
+ * offsets[5] ctx_lens [B] int32; each region starts at a multiple of 256
+ * bytes. Returns the total size in bytes (0 for an invalid shape). */
+size_t nk_step_host_layout(int32_t B, int32_t total_new, int32_t T, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, size_t offsets[6]);
 
 /* Same contract and result, computed by the fp32 CUDA-core kernel that the
  * tensor-core path is measured against. */

@@ -215,6 +215,45 @@ def decode_step(pool: KVPool, block_table, start_pos, cu_new, k, v, q, ctx_lens,
     return out
 
 
+def step_host_layout(B: int, total_new: int, T: int, num_q_heads: int, num_kv_heads: int, head_dim: int):
+    """(total bytes, offsets of k, v, q, start_pos, cu_new, ctx_lens) of
+    decode_step_host's input buffer (nk_step_host_layout)."""
+    offs = (ctypes.c_size_t * 6)()
+    total = lib().nk_step_host_layout(int(B), int(total_new), int(T), int(num_q_heads), int(num_kv_heads),
+                                      int(head_dim), offs)
+    if total == 0:
+        raise ValueError("invalid shape for the host step layout")
+    return int(total), tuple(int(o) for o in offs)
+
+
+def decode_step_host(pool: KVPool, block_table, B: int, total_new: int, T: int, num_q_heads: int, sm_scale: float,
+                     max_ctx: int, in_host, staging, out, out_host, num_ctas: int = 0, workspace=None, status=None,
+                     status_host=None, stream=None):
+    """nk_decode_step_host: one step from host memory. in_host is a host
+    uint8 tensor (pinned for an asynchronous transfer) in the
+    step_host_layout layout; staging a device buffer of at least that size;
+    out the device output [B][T][Hq][D] bf16 and out_host its host copy;
+    status_host an int32 host tensor of one element. Waits for the stream."""
+    import torch
+
+    _need_cuda(block_table, staging, out, workspace, status)
+    pool.need("int8")
+    if in_host.is_cuda or out_host.is_cuda or (status_host is not None and status_host.is_cuda):
+        raise ValueError("in_host, out_host and status_host must be host tensors")
+    D = pool.head_dim
+    if workspace is None:
+        nbytes = decode_workspace_bytes(B, T, num_q_heads, pool.num_kv_heads, D, num_ctas)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=staging.device)
+    ps = pool.c_struct()
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = lib().nk_decode_step_host(ctypes.byref(ps), _ptr(block_table), int(block_table.shape[-1]), int(B),
+                                   int(total_new), int(T), int(num_q_heads), float(sm_scale), int(max_ctx),
+                                   int(num_ctas), _ptr(in_host), _ptr(staging), _ptr(workspace), wbytes, _ptr(out),
+                                   _ptr(out_host), _ptr(status), _ptr(status_host), _stream(stream))
+    _check(rc, "nk_decode_step_host")
+    return out_host
+
+
 NOALLOC_MAX_WORKSPACE = 8 << 20
 
 

@@ -46,6 +46,8 @@ EXPORTS = (
     "nk_paged_decode_attn_simt",
     "nk_paged_decode_attn_noalloc",
     "nk_decode_step",
+    "nk_decode_step_host",
+    "nk_step_host_layout",
     "nk_attn_combine",
     "nk_rk8v4_chunk_bytes",
     "nk_rk8v4_pool_bytes",
@@ -93,6 +95,11 @@ def lib() -> ctypes.CDLL:
             L.nk_decode_step.argtypes = [pool_p, P, I32, P, P, I32, P, P, P, P, I32, I32, I32, F, I32, I32, P, Z, P,
                                          P, P]
             L.nk_decode_step.restype = ctypes.c_int
+            L.nk_decode_step_host.argtypes = [pool_p, P, I32, I32, I32, I32, I32, F, I32, I32, P, P, P, Z, P, P, P,
+                                              P, P]
+            L.nk_decode_step_host.restype = ctypes.c_int
+            L.nk_step_host_layout.argtypes = [I32, I32, I32, I32, I32, I32, ctypes.POINTER(ctypes.c_size_t)]
+            L.nk_step_host_layout.restype = Z
             L.nk_rk8v4_chunk_bytes.argtypes, L.nk_rk8v4_chunk_bytes.restype = [I32, I32], Z
             L.nk_rk8v4_pool_bytes.argtypes, L.nk_rk8v4_pool_bytes.restype = [I32, I32, I32, I32], Z
             L.nk_rk8v4_append.argtypes = [pool_p, P, I32, P, P, I32, I32, P, P, P, P]

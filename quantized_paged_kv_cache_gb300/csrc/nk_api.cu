@@ -293,6 +293,53 @@ int nk_decode_step(const nk_kv_pool* pool, const int32_t* block_table_dev, int32
   return launch_decode(p, Path::kTensor, st);
 }
 
+size_t nk_step_host_layout(int32_t B, int32_t total_new, int32_t T, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, size_t offsets[6]) {
+  if (B < 1 || total_new < 0 || T < 1 || num_q_heads < 1 || num_kv_heads < 1 || head_dim < 1 || !offsets) return 0;
+  const size_t rows = (size_t)total_new * num_kv_heads * head_dim * 2;
+  const size_t qbytes = (size_t)B * T * num_q_heads * head_dim * 2;
+  const size_t sizes[6] = {rows, rows, qbytes, (size_t)B * 4, (size_t)(B + 1) * 4, (size_t)B * 4};
+  size_t off = 0;
+  for (int i = 0; i < 6; ++i) {
+    offsets[i] = off;
+    off += (sizes[i] + 255) / 256 * 256;
+  }
+  return off;
+}
+
+int nk_decode_step_host(const nk_kv_pool* pool, const int32_t* block_table_dev, int32_t max_pages_per_seq,
+                        int32_t B, int32_t total_new, int32_t T, int32_t num_q_heads, float sm_scale,
+                        int32_t max_ctx, int32_t num_ctas, const void* in_host, void* staging_dev,
+                        void* workspace_dev, size_t workspace_bytes, void* out_dev, void* out_host,
+                        int32_t* status_dev, int32_t* status_host, void* stream) {
+  int err = NK_OK;
+  if (!pool_ok(pool, &err)) return err;
+  if (!in_host || !staging_dev || !out_host) return NK_ERR_NULL;
+  if (!aligned(staging_dev, 16)) return NK_ERR_SHAPE;
+  size_t off[6];
+  const size_t bytes = nk_step_host_layout(B, total_new, T, num_q_heads, pool->num_kv_heads, pool->head_dim, off);
+  if (bytes == 0) return NK_ERR_SHAPE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* sb = reinterpret_cast<uint8_t*>(staging_dev);
+  // the step's arguments are checked (nk_decode_step) after the transfer is
+  // queued; on an error nothing is launched and the call waits for the copy
+  if (cudaMemcpyAsync(sb, in_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return NK_ERR_CUDA;
+  err = nk_decode_step(pool, block_table_dev, max_pages_per_seq, reinterpret_cast<const int32_t*>(sb + off[3]),
+                       reinterpret_cast<const int32_t*>(sb + off[4]), total_new, sb + off[0], sb + off[1], sb + off[2],
+                       reinterpret_cast<const int32_t*>(sb + off[5]), B, T, num_q_heads, sm_scale, max_ctx, num_ctas,
+                       workspace_dev, workspace_bytes, out_dev, status_dev, stream);
+  if (err != NK_OK) {
+    (void)cudaStreamSynchronize(st);
+    return err;
+  }
+  const size_t obytes = (size_t)B * T * num_q_heads * pool->head_dim * 2;
+  if (cudaMemcpyAsync(out_host, out_dev, obytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return NK_ERR_CUDA;
+  if (status_dev && status_host &&
+      cudaMemcpyAsync(status_host, status_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return NK_ERR_CUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? NK_OK : NK_ERR_CUDA;
+}
+
 int32_t nk_decode_default_splits(int32_t B, int32_t num_kv_heads, int32_t max_ctx, int32_t page_size) {
   if (B < 1 || num_kv_heads < 1 || max_ctx < 1 || page_size < 1) return 1;
   // one CTA per SM: the tensor-core kernels' residency (decode_mma_ctas_per_sm)

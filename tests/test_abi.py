@@ -190,3 +190,18 @@ def test_default_splits_is_exported_under_both_names():
         assert n == L.nk_decode_default_ctas(*args) == nk.decode_default_splits(*args)
         assert 1 <= n <= args[0] * args[1] * ((args[2] + args[3] - 1) // args[3])
     assert L.nk_decode_default_splits(0, 4, 100, 16) == 1
+
+
+def test_host_step_layout():
+    """nk_step_host_layout: six regions in order, each at a multiple of 256
+    bytes and large enough for its tensor; bad shapes give 0."""
+    B, total, T, Hq, Hkv, D = 3, 7, 4, 24, 4, 256
+    nbytes, offs = nk.step_host_layout(B, total, T, Hq, Hkv, D)
+    sizes = [total * Hkv * D * 2, total * Hkv * D * 2, B * T * Hq * D * 2, B * 4, (B + 1) * 4, B * 4]
+    assert all(o % 256 == 0 for o in offs)
+    for i in range(6):
+        end = offs[i + 1] if i < 5 else nbytes
+        assert end - offs[i] >= sizes[i]
+        assert end - offs[i] < sizes[i] + 256
+    with pytest.raises(ValueError):
+        nk.step_host_layout(0, total, T, Hq, Hkv, D)

@@ -174,3 +174,44 @@ def test_graph_replay_matches_eager(fused):
     refs = oracle_steps(c)
     for i in range(STEPS):
         compare(outs[i], refs[i], f"graph step {i}")
+
+
+@pytest.mark.parametrize("T,lens", [(1, [130, 2000]), (4, [5, 640])], ids=["t1", "t4"])
+def test_host_step_equals_device_step(T, lens):
+    """nk_decode_step_host (inputs from one pinned host buffer, output and
+    status read back, the stream waited for) leaves the same pool bytes and
+    returns the same outputs, bit for bit, as nk_decode_step on device copies
+    of the same inputs, step after step; and the outputs match the oracle."""
+    c = chain_case(T, lens, seed=120 + T)
+    w = c.w_final
+    refs = oracle_steps(c)
+    n = nk.decode_default_ctas(w.B, w.Hkv, max(a for a in w.ctx_lens), w.P)
+    ins = device_inputs(c)
+    ws = workspace(c)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hist = c.pool.storage.clone()
+    # device path
+    outs = [torch.empty_like(a["q"]) for a in ins]
+    enqueue(c, ins, ws, outs, status, torch.cuda.current_stream(), fused=True, num_ctas=n)
+    torch.cuda.synchronize()
+    pool_dev = c.pool.storage.clone()
+    # host path
+    c.pool.storage.copy_(hist)
+    total = int(ins[0]["k"].shape[0])
+    nbytes, offs = nk.step_host_layout(w.B, total, T, w.Hq, w.Hkv, w.D)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out_dev = torch.empty_like(ins[0]["q"])
+    st_h = torch.zeros(1, dtype=torch.int32).pin_memory()
+    for i, a in enumerate(ins):
+        h_in = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+        for name, o in zip(("k", "v", "q", "sp", "cu", "ctx"), offs):
+            t = a[name]
+            nb = t.numel() * t.element_size()
+            h_in[o:o + nb].view(t.dtype).view(t.shape).copy_(t.cpu())
+        out_h = torch.empty(a["q"].shape, dtype=a["q"].dtype).pin_memory()
+        nk.decode_step_host(c.pool, c.bt_full, w.B, total, T, w.Hq, w.sm_scale, a["max_ctx"], h_in, staging, out_dev,
+                            out_h, num_ctas=n, workspace=ws, status=status, status_host=st_h)
+        assert int(st_h.item()) == 0
+        assert torch.equal(out_h, outs[i].cpu()), f"step {i}: host-step output differs"
+        compare(out_h.cuda(), refs[i], f"host step {i}")
+    assert torch.equal(c.pool.storage, pool_dev), "pool bytes differ"
