@@ -975,12 +975,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             // window: a Vs 2^-ev above 2^6, or one at least 2^-10); the
             // exponents move only when a group leaves it
             const int vgrp0 = RK ? ch0 / kRkVGroup : grp0;
+            // the value scales of this thread's two keys (g, g + 8), once per
+            // block for the window and P' (stale slots past ctx_len may hold
+            // NaN scales: 0 there)
+            float vsk[GP][2];
+#pragma unroll
+            for (int gi = 0; gi < GP; ++gi) {
+              vsk[gi][0] = valid0 ? ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb) : 0.f;
+              vsk[gi][1] = valid1 ? ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb) : 0.f;
+            }
             {
               uint32_t wb = 0u;
 #pragma unroll
               for (int gi = 0; gi < GP; ++gi) {
-                const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb) : 0.f;
-                const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb) : 0.f;
+                const float a0 = vsk[gi][0], a1 = vsk[gi][1];
                 const float tv = fmaxf(a0, a1) * sv[gi];
                 wb |= (tv > 64.f ? 1u : 0u) << gi;
                 wb |= (tv >= 0.0009765625f ? 1u : 0u) << (8 + gi);
@@ -991,8 +999,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
 #pragma unroll
                 for (int gi = 0; gi < GP; ++gi) {
                   if (!((moving >> gi) & 1u)) continue;
-                  const float a0 = valid0 ? ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb) : 0.f;
-                  const float a1 = valid1 ? ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb) : 0.f;
+                  const float a0 = vsk[gi][0], a1 = vsk[gi][1];
                   const uint32_t mxb = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(a0, a1)));
                   int ev = sv[gi] == 0.f ? kEvUnset : -exp_of(sv[gi]);
                   float beta;
@@ -1010,12 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const __grid_co
             }
             // P' of group gi as the B fragments of the product (hi, lo)
             auto p_frags = [&](int gi, uint32_t (&bh)[NT][2], uint32_t (&bl)[NT][2]) {
-              float v0 = ld_scale(vs_s, (key0 + g) * GV_ALL + vgrp0 + gi, sb);
-              float v1 = ld_scale(vs_s, (key0 + g + 8) * GV_ALL + vgrp0 + gi, sb);
-              v0 = valid0 ? v0 : 0.f;  // stale slots past ctx_len may hold NaN scales
-              v1 = valid1 ? v1 : 0.f;
-              v0 *= sv[gi];
-              v1 *= sv[gi];
+              const float v0 = vsk[gi][0] * sv[gi], v1 = vsk[gi][1] * sv[gi];
 #pragma unroll
               for (int nt = 0; nt < NT; ++nt) {
                 const float q0 = pr[nt][0] * v0, q1 = pr[nt][1] * v0, q2 = pr[nt][2] * v1, q3 = pr[nt][3] * v1;
