@@ -205,3 +205,24 @@ def test_host_step_layout():
         assert end - offs[i] < sizes[i] + 256
     with pytest.raises(ValueError):
         nk.step_host_layout(0, total, T, Hq, Hkv, D)
+
+
+def test_prefill_rejects_bad_arguments():
+    """nk_paged_prefill_attn's host checks, all before any launch."""
+    L = nk.lib()
+    p = pool(P=64, D=128, H=2)
+
+    def pf(pp=p, q=FAKE, out=FAKE, B=1, T=32, Hq=4, max_pages=4, max_ctx=64, scale=0.125):
+        return L.nk_paged_prefill_attn(ctypes.byref(pp) if pp is not None else None, q, FAKE, max_pages, FAKE, B, T,
+                                       Hq, scale, max_ctx, out, None, None)
+
+    assert pf(pp=None) == 1
+    assert pf(q=None) == 1 and pf(out=None) == 1
+    assert pf(T=0) == 2 and pf(B=-1) == 2
+    assert pf(Hq=3) == 2                      # Hq not a multiple of Hkv
+    assert pf(max_ctx=16) == 2                # max_ctx < T
+    assert pf(max_pages=0) == 2 and pf(max_ctx=300) == 2
+    assert pf(q=FAKE + 8) == 2                # misaligned Q
+    assert pf(scale=float("inf")) == 2
+    assert pf(pp=pool(P=64, D=96, H=2)) != 0  # head dim outside 64 / 128 / 256
+    assert pf(B=0) == 0                       # nothing to do
