@@ -54,6 +54,23 @@ __device__ __noinline__ uint32_t quantize_exact(float x, float s) {
   return (uint32_t)__float2int_rn(e) & 0xffu;
 }
 
+// The 64 codes of a group from its scale s and y = RN(1/s) (the quotient
+// steps described below, on pairs of values: each fp32x2 operation rounds its
+// two lanes as the scalar one does).
+__device__ __forceinline__ void codes64(const uint32_t (&w)[32], uint32_t (&packed)[16], float s, float y) {
+  const float2 y2 = make_float2(y, y), ns2 = make_float2(-s, -s), mg2 = make_float2(12582912.f, 12582912.f);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float2 xa = make_float2(bf16_lo(w[2 * k]), bf16_hi(w[2 * k]));
+    const float2 xb = make_float2(bf16_lo(w[2 * k + 1]), bf16_hi(w[2 * k + 1]));
+    const float2 qa0 = __fmul2_rn(xa, y2), qb0 = __fmul2_rn(xb, y2);
+    const float2 ra = __ffma2_rn(ns2, qa0, xa), rb = __ffma2_rn(ns2, qb0, xb);
+    const float2 ta = __fadd2_rn(__ffma2_rn(ra, y2, qa0), mg2), tb = __fadd2_rn(__ffma2_rn(rb, y2, qb0), mg2);
+    packed[k] = __byte_perm(__byte_perm(__float_as_uint(ta.x), __float_as_uint(ta.y), 0x0040),
+                            __byte_perm(__float_as_uint(tb.x), __float_as_uint(tb.y), 0x0040), 0x5410);
+  }
+}
+
 // Quantize one 64-channel group held as 32 raw bf16 pairs; returns the
 // group's scale and writes the 64 int8 codes packed into 16 words.
 //
@@ -101,21 +118,7 @@ __device__ __forceinline__ float quantize64(const uint32_t (&w)[32], uint32_t (&
       y = __frcp_rn(s);
     }
   }
-  const float ns = -s;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    uint32_t tb[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t wv = w[2 * k + (e >> 1)];
-      const float x = (e & 1) ? bf16_hi(wv) : bf16_lo(wv);
-      const float q0 = __fmul_rn(x, y);
-      const float r = __fmaf_rn(ns, q0, x);
-      const float q = __fmaf_rn(r, y, q0);
-      tb[e] = __float_as_uint(__fadd_rn(q, 12582912.f));
-    }
-    packed[k] = __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
-  }
+  codes64(w, packed, s, y);
   return s;
 }
 
@@ -160,27 +163,13 @@ __device__ __forceinline__ uint32_t quantize64_f16(const uint32_t (&w)[32], uint
     }
     return sb;
   }
-  const float y = __frcp_rn(s), ns = -s;
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    uint32_t tb[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t wv = w[2 * k + (e >> 1)];
-      const float x = (e & 1) ? bf16_hi(wv) : bf16_lo(wv);
-      const float q0 = __fmul_rn(x, y);
-      const float r = __fmaf_rn(ns, q0, x);
-      const float q = __fmaf_rn(r, y, q0);
-      tb[e] = __float_as_uint(__fadd_rn(q, 12582912.f));
-    }
-    packed[k] = __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
-  }
+  codes64(w, packed, s, __frcp_rn(s));
   return sb;
 }
 
 constexpr int kAppendThreads = 128;     // one 64-channel group per thread and chunk
-constexpr int kAppendStages = 4;
-constexpr int kAppendBlocksPerSM = 3;
+constexpr int kAppendStages = 2;
+constexpr int kAppendBlocksPerSM = 4;
 constexpr int kChunkBytes = 8192;       // bf16 bytes of K (and of V) per chunk
 constexpr int kDestEntries = 512;       // (row, head) destinations a block looks up at once
 constexpr int kAppendSmemSeqs = 256;    // sequences whose cu_new/start_pos a block stages in shared memory
@@ -198,20 +187,21 @@ struct __align__(128) AppendSmem {
   int start[kAppendSmemSeqs];
 };
 
-// Persistent grid, a whole number of blocks per SM. The (row, kv-head) pairs
-// are cut into chunks of R = 8 KB / (2 D) consecutive pairs; block b takes
-// chunks b, b + grid, ... The K rows and the V rows of a chunk stream into a
-// stage of a 4-deep shared-memory ring with two bulk copies (cp.async.bulk,
-// completing on the stage's "full" mbarrier). The destinations of up to
-// kDestEntries / R of the block's chunks (binary search over cu_new,
-// block-table entry) are looked up together, one pair per thread, so their
-// global loads overlap. Per chunk, thread t quantizes group t (K groups, then
-// V groups), reading its 128 bytes in a lane-rotated order so the eight lanes
-// of a quarter-warp hit distinct banks, and stores its 64 codes straight into
-// the page row (eight 8-byte pieces in the same rotated order; the four
-// groups of a row are 256 contiguous bytes). There is no block barrier per
-// chunk: each warp releases the stage on its "empty" mbarrier, and the last of
-// the four loads the chunk S ahead into it.
+// Persistent grid, four blocks per SM: the quotient's dependent steps are
+// latency-bound, and more resident warps hide them better than a deeper ring
+// (measured on the 8 x 1,024-row MIX append: 2 stages x 4 blocks 12.2 us,
+// 4 x 3 13.9 us, 3 x 4 13.1 us). The (row, kv-head) pairs are cut into chunks
+// of R = 8 KB / (2 D) consecutive pairs; block b takes chunks b, b + grid, ...
+// The K rows and the V rows of a chunk stream into a stage of a 2-deep
+// shared-memory ring with two bulk copies (cp.async.bulk, completing on the
+// stage's "full" mbarrier). The destinations of up to kDestEntries / R of the
+// block's chunks (binary search over cu_new, block-table entry) are looked up
+// together, one pair per thread, so their global loads overlap. Per chunk,
+// thread t quantizes group t (K groups, then V groups), reading its 128 bytes
+// in a lane-rotated order so the eight lanes of a quarter-warp hit distinct
+// banks; the warp's codes then go out as whole page rows (below). There is no
+// block barrier per chunk: each warp releases the stage on its "empty"
+// mbarrier, and the last of the four loads the chunk S ahead into it.
 template <int D, int FMT>
 __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_kernel(const AppendParams p) {
   chain_wait();
@@ -352,21 +342,68 @@ __global__ void __launch_bounds__(kAppendThreads, kAppendBlocksPerSM) kv_append_
       uint32_t sb16 = 0u;
       if constexpr (FMT == kFmtI8F16) sb16 = quantize64_f16(w, packed, range);
       else s = quantize64<true>(w, packed, sm.tab);
-      const int2 d = dest[row];
-      if (row < rows && d.x >= 0) {
-        uint8_t* chunk = p.pool + (int64_t)d.x * p.lay.chunk;
-        uint8_t* cdst = chunk + (isv ? p.lay.vc : 0) + d.y * D + grp * kGroup;
+      // The warp's 2 KB of codes (its 2048 / D rows, lane L's group at bytes
+      // 64 L) go through the part of the stage whose bf16 rows it has just
+      // read, then out as whole rows: 16-byte pieces, D / 16 lanes per row, so
+      // every 32-byte sector of a page row is written by one store (against
+      // eight 8-byte pieces per group stored straight from each thread:
+      // 13.9 against 15.2 us on the MIX append).
+      uint8_t* wst = sm.stage[st] + isv * kChunkBytes + (gk - lane) * 128;
+      __syncwarp();  // every lane's bf16 reads of the area are done
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int piece = (i + rot) & 7;
-          *reinterpret_cast<uint2*>(cdst + piece * 8) = make_uint2(packed[2 * i], packed[2 * i + 1]);
+      for (int i = 0; i < 8; ++i) {
+        const int piece = (i + rot) & 7;
+        *reinterpret_cast<uint2*>(wst + lane * 64 + piece * 8) = make_uint2(packed[2 * i], packed[2 * i + 1]);
+      }
+      // generic-proxy writes of the stage are ordered before the bulk copy that refills it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      {
+        constexpr int LPR = D / 16;  // lanes per row
+        constexpr int RPI = 32 / LPR;
+        const int r0 = (gk - lane) / GPR;  // the warp's first row of the chunk
+        const int off = (lane % LPR) * 16;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int rl = i * RPI + lane / LPR;
+          const uint4 v = *reinterpret_cast<const uint4*>(wst + rl * D + off);
+          const int2 dd = dest[r0 + rl];
+          if (r0 + rl < rows && dd.x >= 0)
+            *reinterpret_cast<uint4*>(p.pool + (int64_t)dd.x * p.lay.chunk + (isv ? p.lay.vc : 0) + dd.y * D + off) = v;
         }
-        uint8_t* sdst = chunk + (isv ? p.lay.vs : p.lay.ks);
-        if constexpr (FMT == kFmtI8F16) {
-          *reinterpret_cast<uint16_t*>(sdst + (d.y * GPR + grp) * 2) = (uint16_t)sb16;
+      }
+      // the row's GPR scales from its first group's lane, in one store
+      const int2 d = dest[row];
+      if constexpr (FMT == kFmtI8F16) {
+        uint32_t sw[GPR];
+#pragma unroll
+        for (int g2 = 0; g2 < GPR; ++g2) sw[g2] = __shfl_sync(0xffffffffu, sb16, (lane & ~(GPR - 1)) + g2);
+        if (row < rows && d.x >= 0) {
+          uint8_t* sdst = p.pool + (int64_t)d.x * p.lay.chunk + (isv ? p.lay.vs : p.lay.ks) + d.y * GPR * 2;
+          if (grp == 0) {
+            if constexpr (GPR == 4) {
+              *reinterpret_cast<uint2*>(sdst) = make_uint2(sw[0] | (sw[1] << 16), sw[2] | (sw[3] << 16));
+            } else if constexpr (GPR == 2) {
+              *reinterpret_cast<uint32_t*>(sdst) = sw[0] | (sw[1] << 16);
+            } else {
+              *reinterpret_cast<uint16_t*>(sdst) = (uint16_t)sw[0];
+            }
+          }
           if (range) flag(p.status, NK_DEVFLAG_RANGE);
-        } else {
-          *reinterpret_cast<float*>(sdst + (d.y * GPR + grp) * 4) = s;
+        }
+      } else {
+        float sv[GPR];
+#pragma unroll
+        for (int g2 = 0; g2 < GPR; ++g2) sv[g2] = __shfl_sync(0xffffffffu, s, (lane & ~(GPR - 1)) + g2);
+        if (row < rows && d.x >= 0 && grp == 0) {
+          uint8_t* sdst = p.pool + (int64_t)d.x * p.lay.chunk + (isv ? p.lay.vs : p.lay.ks) + d.y * GPR * 4;
+          if constexpr (GPR == 4) {
+            *reinterpret_cast<float4*>(sdst) = make_float4(sv[0], sv[1], sv[2], sv[3]);
+          } else if constexpr (GPR == 2) {
+            *reinterpret_cast<float2*>(sdst) = make_float2(sv[0], sv[1]);
+          } else {
+            *reinterpret_cast<float*>(sdst) = sv[0];
+          }
         }
       }
     }

@@ -117,6 +117,32 @@ def test_append_ragged_starts_and_empty_sequences():
     assert np.array_equal(pool.storage.cpu().numpy(), opool)
 
 
+@pytest.mark.parametrize("nseq", [5, 300])
+def test_append_streaming_many_sequences(nseq):
+    """The streaming kernel (more than 4,096 groups) over several sequences
+    with unaligned starts and one empty sequence: up to 256 sequences its
+    destination search reads cu_new from shared memory, beyond that from
+    global memory."""
+    rng = np.random.default_rng(nseq)
+    lens = [int(x) for x in rng.integers(20, 200, nseq)]
+    lens[1] = 0
+    starts = [int(x) for x in rng.integers(0, 100, nseq)]
+    P, D, Hkv = 16, 256, 4
+    ctx = [s + n + 1 for s, n in zip(starts, lens)]
+    w = small("stream_many", nseq, 1, 8, Hkv, D, P, ctx, seed=nseq, num_pages=sum((L + P - 1) // P for L in ctx) + 3)
+    assert sum(lens) * Hkv * 2 * (D // 64) > 4096
+    bt = wl.block_table(w).cuda()
+    pool = nk.KVPool.empty(w.num_pages, w.P, w.Hkv, w.D, fill=0)
+    opool = oracle.new_pool(w.num_pages, w.P, w.Hkv, w.D)
+    k, v, sp, cu = wl.append_batch(w, starts, lens, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nk.kv_append(pool, bt, sp.cuda(), cu.cuda(), k, v, status=status)
+    torch.cuda.synchronize()
+    assert oracle.kv_append(opool, w.num_pages, w.P, w.Hkv, w.D, wl.block_table(w), sp, cu, k.cpu(), v.cpu()) == 0
+    assert int(status.item()) == 0
+    assert np.array_equal(pool.storage.cpu().numpy(), opool)
+
+
 def _bits_to_bf16(x: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(x.astype(np.uint16).view(np.int16)).view(torch.bfloat16)
 
