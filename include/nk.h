@@ -75,7 +75,7 @@ typedef enum {
   NK_OK = 0,
   NK_ERR_NULL = 1,        /* a required pointer is NULL */
   NK_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
-  NK_ERR_UNSUPPORTED = 3, /* a size this build has no kernel for */
+  NK_ERR_UNSUPPORTED = 3, /* a size the library has no kernel for */
   NK_ERR_WORKSPACE = 4,   /* the workspace is too small */
   NK_ERR_CUDA = 5,        /* a CUDA call failed (launch or attribute) */
   NK_ERR_DEVICE_DATA = 6, /* used by callers to report a nonzero status word */
@@ -93,7 +93,7 @@ typedef enum {
                                        leaves their range); rk8v4 append: a group scale
                                        saturated at the fp16 maximum, or a non-finite value */
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define NK_GROUP 64      /* channels per quantization group */
 #define NK_MAX_T 16      /* query tokens per sequence (decode + MTP verify) */
 #define NK_MAX_HEAD_DIM 256
@@ -322,7 +322,7 @@ int nk_bf16kv_append(const nk_kv_pool* pool, const int32_t* block_table_dev, int
  * arguments, checks, workspace (nk_decode_workspace_bytes), column chunks,
  * causal mask, output and device flags exactly as nk_paged_decode_attn, on the
  * same tensor-core kernels (i8f16: the tcgen05 and mma.sync kernels with fp16
- * scales). nk_bf16kv_decode_attn returns NK_ERR_UNSUPPORTED in this build: its
+ * scales). nk_bf16kv_decode_attn returns NK_ERR_UNSUPPORTED: its
  * kernel path (mma.sync with bf16 operands) is held back after a GPU fault at
  * the C1 decode size whose cause is not yet found. */
 int nk_i8f16_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,

@@ -6,7 +6,7 @@ The append must reproduce the oracle's pool bytes exactly (both formats);
 i8f16 attention must meet the tolerance of the INT8 path against the
 oracle's fp64 result, on the tcgen05 kernel (head_dim 256, 64-key pages,
 9..32 rows per kv-head) and on the mma.sync kernel (every other shape). The
-bf16 decode launches no kernel in this build and must say so
+bf16 decode launches no kernel and must say so
 (NK_ERR_UNSUPPORTED). Slots past the context hold 0xFF bytes (NaN scales or
 values), which must not matter.
 """
@@ -99,7 +99,7 @@ def test_append_bit_exact(built):
 def test_decode_matches_oracle(built):
     c, w = built, built.w
     if c.fmt == "bf16":
-        # this build launches no kernel for a bf16 pool (see nk.h)
+        # the library launches no kernel for a bf16 pool (see nk.h)
         with pytest.raises(nk.NKError) as ei:
             DECODE[c.fmt](c.pool, c.q, c.bt, c.ctx, w.sm_scale, w.max_ctx)
         assert ei.value.code == 3
