@@ -318,6 +318,152 @@ __global__ void __launch_bounds__(128) rk8v4_append_kernel(const RkAppendParams 
   }
 }
 
+// Destination of row j of the batch (kv-head h): the chunk and slot, or
+// nullptr after flagging a position or page id out of range.
+__device__ __forceinline__ uint8_t* rk_dest(const RkAppendParams& p, int j, int h, int& slot, bool flagger) {
+  int lo = 0, hi = p.B;  // sequence b of row j: cu_new[b] <= j < cu_new[b + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.cu_new + mid) <= j) lo = mid; else hi = mid;
+  }
+  const int b = lo;
+  const int64_t pos = (int64_t)__ldg(p.start_pos + b) + (j - __ldg(p.cu_new + b));
+  if (pos < 0 || pos >= (int64_t)p.max_pages * p.P) {
+    if (flagger) flag(p.status, NK_DEVFLAG_BAD_POS);
+    return nullptr;
+  }
+  const int page = __ldg(p.bt + (int64_t)b * p.max_pages + pos / p.P);
+  if (page < 0 || page >= p.num_pages) {
+    if (flagger) flag(p.status, NK_DEVFLAG_BAD_PAGE);
+    return nullptr;
+  }
+  slot = (int)(pos % p.P);
+  return p.pool + ((int64_t)page * p.Hkv + h) * p.lay.chunk;
+}
+
+__device__ __forceinline__ long long shfl_xor_ll(long long v, int m) {
+  const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)(unsigned long long)v, m);
+  const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)((unsigned long long)v >> 32), m);
+  return (long long)(((unsigned long long)hi << 32) | lo);
+}
+
+// Small appends (decode and verify steps: a few rows). The thread-per-item
+// kernel above then runs only a few dozen threads, each through a whole key
+// group's rotation; here a warp takes a key group, lane l holding channels
+// 2l and 2l + 1: the first butterfly stage runs in the lane, the five others
+// across lanes by shuffle, on the same exact integer sums (so the same
+// bits), then each lane rounds and codes its two outputs. A group whose
+// exponents span more than 39 binades, or with an output in the fp32
+// subnormal range, is rotated by lane 0 alone in the exact wide path (all of
+// it, as the thread-per-item kernel does). Value groups: one thread each, in
+// the warps after the key groups'.
+__global__ void __launch_bounds__(128) rk8v4_append_small_kernel(const RkAppendParams p) {
+  chain_wait();
+  chain_release();
+  const int kg = p.D / kGroup, vg = p.D / kRkVGroup;
+  const int64_t nkey = (int64_t)p.total_new * p.Hkv * kg;  // key groups: one warp each
+  const int64_t nval = (int64_t)p.total_new * p.Hkv * vg;  // value groups: one thread each
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gw >= nkey) {
+    const int64_t it = (gw - nkey) * 32 + lane;
+    if (it >= nval) return;
+    const int64_t rh = it / vg;
+    const int g = (int)(it % vg), j = (int)(rh / p.Hkv), h = (int)(rh % p.Hkv);
+    int slot = 0;
+    uint8_t* chunk = rk_dest(p, j, h, slot, g == 0);
+    if (!chunk) return;
+    bool range = false;
+    rk_value_group(reinterpret_cast<const uint4*>(p.v + ((int64_t)j * p.Hkv + h) * p.D + g * kRkVGroup),
+                   reinterpret_cast<uint4*>(chunk + p.lay.vc + (int64_t)slot * (p.D / 2) + g * (kRkVGroup / 2)),
+                   reinterpret_cast<uint16_t*>(chunk + p.lay.vs) + slot * vg + g, range);
+    if (range) flag(p.status, NK_DEVFLAG_RANGE);
+    return;
+  }
+  // one key group per warp (every lane takes the same branches up to the shuffles)
+  const int64_t rh = gw / kg;
+  const int r = (int)(gw % kg), j = (int)(rh / p.Hkv), h = (int)(rh % p.Hkv);
+  int slot = 0;
+  uint8_t* chunk = rk_dest(p, j, h, slot, r == 0 && lane == 0);
+  if (!chunk) return;
+  const uint16_t* src = p.k + ((int64_t)j * p.Hkv + h) * p.D + r * kGroup;
+  uint8_t* dst = chunk + (int64_t)slot * p.D + r * kGroup;
+  uint16_t* sdst = reinterpret_cast<uint16_t*>(chunk + p.lay.ks) + slot * kg + r;
+  const uint32_t wv = __ldg(reinterpret_cast<const uint32_t*>(src) + lane);
+  const uint16_t xb[2] = {(uint16_t)(wv & 0xffffu), (uint16_t)(wv >> 16)};
+  int emax = 0, emin = 255;  // exponent fields of the non-zero values (subnormals count as 1)
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if ((xb[c] & 0x7fffu) == 0u) continue;
+    const int e = max(1, (xb[c] >> 7) & 0xff);
+    emax = max(emax, e);
+    emin = min(emin, e);
+  }
+  emax = __reduce_max_sync(0xffffffffu, emax);
+  emin = __reduce_min_sync(0xffffffffu, emin);
+  bool wide = emax - emin > 39;
+  float t[2] = {0.f, 0.f};
+  if (!wide) {
+    long long d[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t mag = xb[c] & 0x7fffu, e = mag >> 7;
+      const long long m = mag == 0u ? 0ll
+                                    : (long long)((mag & 0x7fu) | (e != 0u ? 0x80u : 0u))
+                                          << ((e != 0u ? (int)e : 1) - emin);
+      d[c] = (xb[c] & 0x8000u) ? -m : m;
+    }
+    {  // distance 1: channels 2l, 2l + 1
+      const long long a = d[0], b = d[1];
+      d[0] = a + b;
+      d[1] = a - b;
+    }
+#pragma unroll
+    for (int hl = 1; hl < 32; hl <<= 1) {  // distance 2 hl: lane l ^ hl holds the partner
+      const bool upper = (lane & hl) != 0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const long long q = shfl_xor_ll(d[c], hl);
+        d[c] = upper ? q - d[c] : d[c] + q;
+      }
+    }
+    const int k = emin - 137;  // y = d 2^k
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      if (d[c] == 0) continue;
+      const uint32_t fb = __float_as_uint(__ll2float_rn(d[c]));  // |d| >= 1: a normal number
+      const int ne = (int)((fb >> 23) & 0xffu) + k;
+      if (ne >= 255)
+        t[c] = __uint_as_float((fb & 0x80000000u) | 0x7f800000u);
+      else if (ne >= 1)
+        t[c] = __uint_as_float((uint32_t)((int)fb + k * (1 << 23)));
+      else
+        wide = true;  // an fp32 subnormal result: the wide path
+    }
+  }
+  if (__any_sync(0xffffffffu, wide)) {
+    if (lane == 0) {
+      bool range = false;
+      rk_key_group(reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), sdst, range);
+      if (range) flag(p.status, NK_DEVFLAG_RANGE);
+    }
+    return;
+  }
+  bool range = !__all_sync(0xffffffffu, isfinite(t[0]) && isfinite(t[1]));
+  const float amax = __uint_as_float(
+      __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(fabsf(t[0]), fabsf(t[1])))));
+  const uint16_t sb = rk_scale_bits(amax, 127.f, range);
+  const float s = __half2float(__ushort_as_half(sb));
+  reinterpret_cast<uint16_t*>(dst)[lane] =
+      (uint16_t)((rk_code(t[0], s, 127) & 0xffu) | ((rk_code(t[1], s, 127) & 0xffu) << 8));
+  if (lane == 0) {
+    *sdst = sb;
+    if (range) flag(p.status, NK_DEVFLAG_RANGE);
+  }
+}
+
+constexpr int64_t kRkSmallKeyGroups = 2048;  // appends up to this many key groups take the warp-per-group kernel
+
 cudaError_t launch_rk8v4_append(int sms, const nk_kv_pool& pool, const int32_t* bt, int max_pages,
                                 const int32_t* start_pos, const int32_t* cu_new, int B, int total_new, const void* k,
                                 const void* v, int32_t* status, cudaStream_t stream) {
@@ -337,6 +483,12 @@ cudaError_t launch_rk8v4_append(int sms, const nk_kv_pool& pool, const int32_t* 
   p.k = reinterpret_cast<const uint16_t*>(k);
   p.v = reinterpret_cast<const uint16_t*>(v);
   p.status = status;
+  const int64_t nkey = (int64_t)total_new * p.Hkv * (p.D / kGroup);
+  if (nkey <= kRkSmallKeyGroups) {  // decode and verify steps: a warp per key group
+    const int64_t warps = nkey + ((int64_t)total_new * p.Hkv * (p.D / kRkVGroup) + 31) / 32;
+    const int64_t nb = (warps * 32 + 127) / 128;
+    return launch_chained(rk8v4_append_small_kernel, dim3((unsigned)(nb < 1 ? 1 : nb)), dim3(128), 0, stream, p);
+  }
   const int64_t items = (int64_t)total_new * p.Hkv * (p.D / kGroup + p.D / kRkVGroup);
   int64_t blocks = (items + 127) / 128;
   const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 16;

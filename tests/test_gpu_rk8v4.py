@@ -129,10 +129,13 @@ def wide_key_rows(n, H, D, seed):
     return torch.from_numpy(k.reshape(n, H, D)).to(torch.bfloat16)
 
 
-def test_append_wide_exponent_key_groups_bit_exact():
+@pytest.mark.parametrize("n", [256, 512])
+def test_append_wide_exponent_key_groups_bit_exact(n):
     """Both routes of the key rotation against the oracle's exact rotation
-    rounded once: codes and scales bit for bit; saturated scales may flag."""
-    n, H, D, P = 256, 2, 256, 64
+    rounded once: codes and scales bit for bit; saturated scales may flag.
+    256 rows (2,048 key groups) take the warp-per-group kernel of small
+    appends, 512 rows the thread-per-item kernel."""
+    H, D, P = 2, 256, 64
     k = wide_key_rows(n, H, D, seed=21)
     v = torch.randn((n, H, D)).to(torch.bfloat16)
     num_pages = n // P
@@ -175,18 +178,25 @@ def sweep_rows():
     return k, v
 
 
-def test_append_scale_sweep_bit_exact():
+@pytest.mark.parametrize("rows_per_call", [0, 64])
+def test_append_scale_sweep_bit_exact(rows_per_call):
+    """The whole sweep in one call (thread-per-item kernel) or in calls of 64
+    rows (1,024 key groups each: the warp-per-group kernel)."""
     k, v = sweep_rows()
     n, H, D = k.shape
     P = 64
     num_pages = (n + P - 1) // P
     bt = torch.arange(num_pages, dtype=torch.int32).flip(0)[None].contiguous()
-    sp, cu = torch.zeros(1, dtype=torch.int32), torch.tensor([0, n], dtype=torch.int32)
     pool = nk.KVPool.empty(num_pages, P, H, D, fill=0, fmt="rk8v4")
     opool = oracle.rk_new_pool(num_pages, P, H, D, fill=0)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    nk.rk8v4_append(pool, bt.cuda(), sp.cuda(), cu.cuda(), k.cuda(), v.cuda(), status=status)
-    assert oracle.rk_append(opool, num_pages, P, H, D, bt, sp, cu, k, v) == 0
+    step = rows_per_call or n
+    for r0 in range(0, n, step):
+        r1 = min(n, r0 + step)
+        sp, cu = torch.tensor([r0], dtype=torch.int32), torch.tensor([0, r1 - r0], dtype=torch.int32)
+        kk, vv = k[r0:r1].contiguous(), v[r0:r1].contiguous()
+        nk.rk8v4_append(pool, bt.cuda(), sp.cuda(), cu.cuda(), kk.cuda(), vv.cuda(), status=status)
+        assert oracle.rk_append(opool, num_pages, P, H, D, bt, sp, cu, kk, vv) == 0
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got = pool.storage.cpu().numpy()
