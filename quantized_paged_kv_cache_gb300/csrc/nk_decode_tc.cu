@@ -508,32 +508,37 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           }
         }
         wbits = __reduce_or_sync(0xffffffffu, wbits);
-        wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
-        tc_fence_after();
         const float ka = ld_scale(ks_s, key * 4 + 2 * half, sb) * kq;
         const float kb = ld_scale(ks_s, key * 4 + 2 * half + 1, sb) * kq;
+        wait_bar(&qk_bar[q & 1], (q >> 1) & 1);
+        tc_fence_after();
         // ---- this lane's accumulator rows (groups 2 half, 2 half + 1), 16 query rows at a time;
         // half of the rows go to the thread holding the other channel half of the key
         float* xq = xs + (q & 1) * (2 * 64 * NR);  // by page parity: a side rewrites it only two pages later
         float* mine = xq + (half * 64 + key) * NR;
         float sc[NR];
         {
+          // every load of the page's columns in flight before the one wait
+          constexpr int NC = (NT * 8 + 15) / 16;
           const uint32_t base = tmem + ((uint32_t)(quad * 32) << 16) + kColAcc + (q & 1) * (4 * W) + half * W;
+          float ta[NC][16], tb[NC][16];
 #pragma unroll
-          for (int c = 0; c < NT * 8; c += 16) {
-            float ta[16], tb[16];
-            tmem_ld_x16(base + c, ta);
-            tmem_ld_x16(base + 2 * W + c, tb);
-            tmem_wait_ld();
+          for (int ci = 0; ci < NC; ++ci) {
+            tmem_ld_x16(base + 16 * ci, ta[ci]);
+            tmem_ld_x16(base + 2 * W + 16 * ci, tb[ci]);
+          }
+          tmem_wait_ld();
+#pragma unroll
+          for (int ci = 0; ci < NC; ++ci) {
 #pragma unroll
             for (int nt2 = 0; nt2 < 2; ++nt2) {
-              const int nt = c / 8 + nt2;
+              const int nt = 2 * ci + nt2;
               if (nt >= NT) break;
               float keep[4], send[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const float lo = fmaf(kb, tb[nt2 * 8 + i], ka * ta[nt2 * 8 + i]);
-                const float hi = fmaf(kb, tb[nt2 * 8 + 4 + i], ka * ta[nt2 * 8 + 4 + i]);
+                const float lo = fmaf(kb, tb[ci][nt2 * 8 + i], ka * ta[ci][nt2 * 8 + i]);
+                const float hi = fmaf(kb, tb[ci][nt2 * 8 + 4 + i], ka * ta[ci][nt2 * 8 + 4 + i]);
                 keep[i] = half ? hi : lo;
                 send[i] = half ? lo : hi;
                 sc[nt * 4 + i] = keep[i];
