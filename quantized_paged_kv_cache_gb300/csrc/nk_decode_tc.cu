@@ -412,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
               r[c4 * 8 + 2 * i + 1] = i8x2_to_f16x2(w[i], 0x4342);
             }
           }
+          // the MMAs' reads of the buffer (seen complete through qk_bar) are
+          // ordered before the stores; late, so the loads above overlap
+          if (hc == 0) tc_fence_after();
           tmem_st_x32(taddr + hc * 32, r);
         }
         tmem_wait_st();
