@@ -392,8 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       for (int j = 0; j < npages; ++j) {
         const int q = q0 + j;
         if (j == j_pf && has_next) prefetch_q(sn);
+        // MMAs of page q - 2 (same K buffer) done, and the stores below
+        // ordered after their reads of it; fenced before the wait for the
+        // page's data, which usually lasts longer than the fence
+        wait_bar(&qk_bar[q & 1], ((q >> 1) & 1) ^ 1);
+        tc_fence_after();
         wait_bar(&full_bar[s], ph);
-        wait_bar(&qk_bar[q & 1], ((q >> 1) & 1) ^ 1);  // MMAs of page q - 2 (same K buffer) done
         const uint8_t* st = smem + s * kStageBytes;
         const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + kColA + (q & 1) * 64;
 #pragma unroll
@@ -412,9 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
               r[c4 * 8 + 2 * i + 1] = i8x2_to_f16x2(w[i], 0x4342);
             }
           }
-          // the MMAs' reads of the buffer (seen complete through qk_bar) are
-          // ordered before the stores; late, so the loads above overlap
-          if (hc == 0) tc_fence_after();
           tmem_st_x32(taddr + hc * 32, r);
         }
         tmem_wait_st();
