@@ -100,6 +100,27 @@ def test_decode_is_deterministic_and_cta_count_independent(case, impl):
         compare(o, case.ref, f"{case.w.name}/{impl}/ctas={n}")
 
 
+@pytest.mark.parametrize("shape", [
+    ("b1024_mma", 1, 8, 2, 128, 16),   # mma.sync kernel
+    ("b1024_tc", 4, 24, 4, 256, 64),   # tcgen05 kernel (24 rows per kv-head)
+], ids=lambda s: s[0])
+def test_decode_at_the_batch_limit(shape):
+    """1,024 sequences, the most one call takes (their page prefix sums live
+    in shared memory), with short ragged contexts down to T keys, against the
+    oracle on both tensor-core paths and the CUDA-core kernel."""
+    name, T, Hq, Hkv, D, P = shape
+    rng = np.random.default_rng(1024 + T)
+    lens = [int(x) for x in rng.integers(T, 100, 1024)]
+    lens[0], lens[-1] = T, 2 * P + 3
+    w = small(name, 1024, T, Hq, Hkv, D, P, lens, seed=11, num_pages=sum((L + P - 1) // P for L in lens) + 4)
+    c = build(w, fill=0)
+    ref = oracle_attention_full(c)
+    for impl in IMPLS:
+        out = run_decode(c, impl)
+        torch.cuda.synchronize()
+        compare(out, ref, f"{name}/{impl}")
+
+
 def test_append_ragged_starts_and_empty_sequences():
     """Several sequences, unaligned starts, one sequence with no new rows."""
     w = small("ragged", 4, 1, 8, 2, 128, 16, [50, 37, 90, 17], seed=5, num_pages=20)
