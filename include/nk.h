@@ -181,7 +181,9 @@ size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int3
  * than 48 otherwise -- the columns run as consecutive chunks (at most 24
  * and 48 rows respectively), each a split kernel and a combine over the same
  * pages with its own causal limits. The workspace size for T covers every
- * chunk.
+ * chunk. A page too large for two stages of the kernels' shared-memory ring
+ * (256-key pages at head_dim 256) returns NK_ERR_UNSUPPORTED before anything
+ * is launched; nk_paged_decode_attn_simt takes pages of any size.
  */
 int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,

@@ -87,6 +87,7 @@ def test_decode_rejects_bad_arguments():
     assert decode(pool(), q=0) == 1
     assert decode(pool(), B=2000) == 3                         # beyond the batch limit
     assert decode(pool(), B=1025) == 3                         # one past it (1,024 sequences)
+    assert decode(pool(P=256, D=256), max_pages=1) == 3        # a 256-key page of head_dim 256: no two-stage ring
     assert decode(pool(), B=0) == 0                            # nothing to do
     assert E.lib().nk_paged_decode_attn_simt(ctypes.byref(pool()), FAKE, FAKE, 4, FAKE, 1, 1, 16, 0.1, 64, 0,
                                              FAKE, 1 << 30, FAKE, None, None) == 3  # G > 8 on CUDA cores
