@@ -66,9 +66,14 @@ constexpr int kTmemCols = 512;
 // their own share with setmaxnreg; the shares add up to the launch total, so
 // no increase ever waits for registers that are not there (checked on the
 // host against the compiled count before the first launch).
-constexpr int kLaunchRegs = 128, kRegsConv = 144, kRegsScore = 144, kRegsPv = 112;
+// The folding instance (below) gives the PV warps 8 more registers for the
+// total's load/store and takes them from the convert warps.
+constexpr int kLaunchRegs = 128, kRegsScore = 144;
+__host__ __device__ constexpr int regs_conv(bool fold) { return fold ? 128 : 144; }
+__host__ __device__ constexpr int regs_pv(bool fold) { return fold ? 120 : 112; }
 static_assert(kConvWarps == 4 && kScoreWarps == 4 && kPvWarps == 8, "one warpgroup per role, two for PV");
-static_assert(kRegsConv + kRegsScore + 2 * kRegsPv == 4 * kLaunchRegs, "register shares = the launch's registers");
+static_assert(regs_conv(false) + kRegsScore + 2 * regs_pv(false) == 4 * kLaunchRegs, "shares = the launch's registers");
+static_assert(regs_conv(true) + kRegsScore + 2 * regs_pv(true) == 4 * kLaunchRegs, "shares = the launch's registers");
 // one page: the K|V code boxes, then both scale arrays (34,816 bytes with
 // fp32 scales, 33,792 with fp16 ones: multiples of 1024 either way)
 __host__ __device__ constexpr int stage_bytes(int sb) { return 2 * kP * kD + 2 * kP * (kD / kGroup) * sb; }
@@ -76,6 +81,12 @@ constexpr int kPidCache = 512;
 constexpr int kColA = 0;      // tensor-memory columns of the two K buffers (64 each)
 constexpr int kColAcc = 128;  // the two accumulator buffers (4W each)
 constexpr int kQAhead = 4;    // pages before a segment's end at which the next unit's Q is prefetched
+constexpr int kColTot = 384;  // the folded PV totals (32 columns per warp, two warps per lane quadrant)
+// Folding: a PV accumulator restarts from zero every kFoldPages pages (8,192
+// keys). The host takes the folding instance when one CTA may run more than
+// kNoFoldPages pages of one kv-head through its accumulators.
+constexpr int kFoldPages = 128;
+constexpr int kNoFoldPages = 512;
 
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);  // fp16 A/B, K-major, fp32 D
@@ -148,6 +159,24 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -169,7 +198,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // W: padded query rows per channel half of the QK operand (16 or 32);
 // NT: 8-row tiles of the PV product (ceil(G*T / 8) <= W / 8).
 // SB: bytes of a group scale (4: fp32 scales; 2: the pages' fp16 scales).
-template <int W, int NT, int SB>
+// FOLD: the PV accumulators are folded into a tensor-memory total every
+// kFoldPages pages.
+template <int W, int NT, int SB, bool FOLD>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const DecodeParams p) {
   // the tensor map is a launch parameter: its descriptor fetch can start
@@ -336,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     }
   };
   if (role == 0) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsConv) : "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(regs_conv(FOLD)) : "memory");
     // ======================= convert warps: K codes -> tensor memory, QK MMAs
     const int half = quad >> 1, key = 32 * (quad & 1) + lane;
     while (next_segment(sh, pre, x, x_end, seg)) {
@@ -707,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       named_bar(5, (kScoreWarps + kPvWarps) * 32);  // the PV warps have read lrow / mrow
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsPv) : "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(regs_pv(FOLD)) : "memory");
     // ======================= PV warps
     const int pw = warp - kConvWarps - kScoreWarps;
     const int g_lane = lane >> 2, t4 = lane & 3;
@@ -715,8 +746,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int lm_key = ((lane >> 3) & 1) * 8 + (lane & 7);
     const uint32_t loff = box_off<kD>(kP, 0, lm_key, 2 * pw + (lane >> 4));
     float o[2][NT][4];
+    // The fp32 sums of mma.sync are not rounded to nearest, and the error
+    // they leave grows with the products one accumulator takes in. In the
+    // folding instance each thread adds its accumulator every kFoldPages
+    // pages into a total kept in its own tensor-memory lane and columns (one
+    // rounded add per value and fold) and restarts it from zero; when the
+    // row references or a group's P' exponent move, the total is rescaled in
+    // place like the accumulator.
+    const uint32_t tot = tmem + ((uint32_t)(quad * 32) << 16) + kColTot + (uint32_t)(pw >> 2) * 32;
+    bool has_total = false;
+    auto fold = [&](bool final_fold) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {  // one 8-column row tile at a time (few live registers)
+        float v[8];
+        tmem_ld_x8(tot + 8 * nt, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float& a = o[cc][nt][k];
+            if (final_fold) {
+              a += v[cc * 4 + k];
+            } else {
+              v[cc * 4 + k] += a;
+              a = 0.f;
+            }
+          }
+        if (!final_fold) tmem_st_x8(tot + 8 * nt, v);
+      }
+      if (!final_fold) tmem_wait_st();
+    };
+    // total *= beta (this warp's group) times alpha of each row (when `rows`)
+    auto rescale_total = [&](const float* alpha, float beta, bool rows) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float v[8];
+        tmem_ld_x8(tot + 8 * nt, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) v[cc * 4 + k] *= rows ? beta * alpha[8 * nt + 2 * t4 + (k & 1)] : beta;
+        tmem_st_x8(tot + 8 * nt, v);
+      }
+      tmem_wait_st();
+    };
     while (next_segment(sh, pre, x, x_end, seg)) {
       const int npages = seg.page_end - seg.page_begin;
+      has_total = false;
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
@@ -751,6 +829,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
               }
             }
         }
+        if (FOLD && has_total) {
+          const bool mv = reinterpret_cast<const int*>(alpha + 40)[0] != 0, rw = (sf[0] | sf[1]) != 0;
+          if (mv || rw) rescale_total(alpha, mv ? alpha[36 + gq] : 1.f, rw);
+        }
         const uint32_t st = stage0 + s * kStageBytes;
         const uint32_t pb = smem_u32(pbuf + (q & 1) * (NT * 8192));
 #pragma unroll
@@ -784,8 +866,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (lane == 0) mbar_arrive(smem_u32(&pempty_bar[q & 1]));
         release_stage(q, s, ph);
         next_stage();
+        if (FOLD && (j + 1) % kFoldPages == 0 && j + 1 < npages) {
+          if (has_total) {
+            fold(false);
+          } else {  // the first fold stores the accumulator as the total
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              float v[8];
+#pragma unroll
+              for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  v[cc * 4 + k] = o[cc][nt][k];
+                  o[cc][nt][k] = 0.f;
+                }
+              tmem_st_x8(tot + 8 * nt, v);
+            }
+            tmem_wait_st();
+            has_total = true;
+          }
+        }
       }
       q0 += npages;
+      if (FOLD && has_total) fold(true);
       // ---- segment result: wait for the row statistics, then write the rows
       named_bar(5, (kScoreWarps + kPvWarps) * 32);
       named_bar(5, (kScoreWarps + kPvWarps) * 32);
@@ -841,22 +944,38 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   }
 }
 
-template <int W, int NT, int SB>
-static cudaError_t launch_ts(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
+template <int W, int NT, int SB, bool FOLD>
+static cudaError_t launch_tsf(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
   const Layout LY = layout(W, NT, SB);
   if (LY.stages < 2 || LY.total > kSmemLimit) return cudaErrorInvalidConfiguration;
-  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT, SB>), LY.total);
+  cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(decode_tc_kernel<W, NT, SB, FOLD>), LY.total);
   if (e != cudaSuccess) return e;
   // the register shares assume the launch count they were split from
   static int regs = -1;
   if (regs < 0) {
     cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, decode_tc_kernel<W, NT, SB>);
+    e = cudaFuncGetAttributes(&fa, decode_tc_kernel<W, NT, SB, FOLD>);
     if (e != cudaSuccess) return e;
     regs = fa.numRegs;
   }
   if (regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  return launch_chained(decode_tc_kernel<W, NT, SB>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
+  return launch_chained(decode_tc_kernel<W, NT, SB, FOLD>, dim3(p.n_ctas), dim3(kThreads), LY.total, st, map, p);
+}
+
+// The most pages of one kv-head a CTA may run: a CTA takes at most
+// ceil(items / CTAs) consecutive (page, kv-head) items, and a kv-head of a
+// sequence holds at most ceil(max_ctx / P) pages.
+static int64_t max_run_pages(const DecodeParams& p) {
+  const int64_t unit = ((int64_t)p.max_ctx + kP - 1) / kP;
+  const int64_t items = unit * p.B * p.Hkv;
+  const int64_t per_cta = (items + p.n_ctas - 1) / p.n_ctas;
+  return per_cta < unit ? per_cta : unit;
+}
+
+template <int W, int NT, int SB>
+static cudaError_t launch_ts(const CUtensorMap& map, const DecodeParams& p, cudaStream_t st) {
+  return max_run_pages(p) > kNoFoldPages ? launch_tsf<W, NT, SB, true>(map, p, st)
+                                         : launch_tsf<W, NT, SB, false>(map, p, st);
 }
 
 template <int W, int NT>

@@ -82,3 +82,30 @@ def test_full_size(name, impl):
             f.write(json.dumps({"workload": name, "kernel": impl, "rows": len(rows), "max_abs": maxabs,
                                 "rel_l2_vs_bf16_oracle": rel, "rel_l2_vs_fp64_oracle": rel_exact,
                                 "codes_scales": "bit-exact", "pool_bytes": int(pool.storage.numel())}) + "\n")
+
+
+@pytest.fixture(scope="module")
+def long_pool():
+    w = wl.make("long_context")
+    return (w,) + build_like_bench(w)
+
+
+# (T, CTAs): 4 CTAs over one 262,144-key sequence put 4,096 pages of one
+# kv-head through one CTA's PV accumulators; T = 2 and 4 run the tcgen05
+# kernel (its folding instance), T = 1 the mma.sync kernel.
+@pytest.mark.parametrize("T,ctas", [(1, 4), (2, 4), (4, 4), (4, 16)])
+def test_coarse_split_long_context(long_pool, T, ctas):
+    w0, pool, opool, bt, bt_cpu = long_pool
+    w = wl.custom(f"long_T{T}", B=1, T=T, Hq=w0.Hq, Hkv=w0.Hkv, D=w0.D, P=w0.P, ctx_lens=w0.ctx_lens, seed=17)
+    q = wl.queries(w, device="cuda")
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = nk.paged_decode_attn(pool, q, bt, ctx, w.sm_scale, w.max_ctx, num_ctas=ctas, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = [(0, w.T - 1, i) for i in range(w.Hq)]
+    q_cpu = q.cpu()
+    ref = np.stack([oracle.attention_row(opool, w0.num_pages, w.P, w.Hkv, w.D, bt_cpu, w.ctx_lens, q_cpu, w.T, w.Hq,
+                                         w.sm_scale, b, t, i)[0] for (b, t, i) in rows])
+    got = torch.stack([out[b, t, i] for (b, t, i) in rows])
+    compare(got, ref, f"long_context T={T} ctas={ctas}")
