@@ -184,6 +184,11 @@ size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int3
  * chunk. A page too large for two stages of the kernels' shared-memory ring
  * (256-key pages at head_dim 256) returns NK_ERR_UNSUPPORTED before anything
  * is launched; nk_paged_decode_attn_simt takes pages of any size.
+ * On the tcgen05 shapes, when a CTA may run more than 512 pages of one
+ * kv-head (a caller-chosen split much coarser than the default, or under the
+ * default split one sequence beyond about 1.2 million keys), the split
+ * kernel runs an instance that folds its fp32 accumulators every 128 pages
+ * (about 2% slower), so that coarse splits keep the accuracy of fine ones.
  */
 int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
