@@ -44,6 +44,9 @@
 //   MMAs).
 // At the end of a segment the row sums are reduced and the PV warps write
 // bf16 rows (whole unit) or fp32 partials with their LSE.
+// A second instance of the kernel (FOLD) adds the PV accumulators into a
+// total in tensor memory every 128 pages; the host takes it when a CTA may
+// run more than 512 pages of one kv-head.
 // Every mbarrier wait is bounded; a timeout sets NK_DEVFLAG_TIMEOUT.
 #include "nk_decode_mma.cuh"
 
