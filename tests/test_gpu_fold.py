@@ -52,3 +52,37 @@ def test_fold_instance_i8f16(T):
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         compare(out, ref, f"{w.name}/ctas={n}")
+
+
+def test_fold_instance_in_column_chunks():
+    # T = 12 at G = 6: three launches of 4 columns, each over the same pages
+    # with its own causal limits, each taking the folding instance in one CTA
+    w = wl.custom("fold_t12", B=2, T=12, Hq=6, Hkv=1, D=256, P=64, ctx_lens=LENS, seed=33,
+                  num_pages=sum((L + 63) // 64 for L in LENS) + 2)
+    c = build(w)
+    ref = oracle_attention_full(c)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = nk.paged_decode_attn(c.pool, c.q, c.bt, c.ctx, w.sm_scale, w.max_ctx, num_ctas=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(out, ref, f"{w.name}/ctas=1")
+
+
+def test_fold_instance_in_the_step_call():
+    # nk_decode_step: the step's rows (the last T of each sequence, appended
+    # again with the same values) and the attention, one CTA
+    T = 4
+    w = wl.custom("fold_step", B=2, T=T, Hq=6, Hkv=1, D=256, P=64, ctx_lens=LENS, seed=34,
+                  num_pages=sum((L + 63) // 64 for L in LENS) + 2)
+    c = build(w)
+    ref = oracle_attention_full(c)
+    rows = [wl.kv_rows(w, b, L - T, T, device="cuda") for b, L in enumerate(LENS)]
+    k = torch.cat([r[0] for r in rows]).contiguous()
+    v = torch.cat([r[1] for r in rows]).contiguous()
+    start = torch.tensor([L - T for L in LENS], dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, T, 2 * T], dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = nk.decode_step(c.pool, c.bt, start, cu, k, v, c.q, c.ctx, w.sm_scale, w.max_ctx, num_ctas=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    compare(out, ref, f"{w.name}/ctas=1")
