@@ -189,6 +189,9 @@ size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int3
  * default split one sequence beyond about 1.2 million keys), the split
  * kernel runs an instance that folds its fp32 accumulators every 128 pages
  * (about 2% slower), so that coarse splits keep the accuracy of fine ones.
+ * The mma.sync shapes have no such instance: their error also grows with the
+ * pages one CTA runs (relative L2 7e-4 against the oracle at 4,096 pages of
+ * one kv-head per CTA, T = 1), and runs beyond that were not measured.
  */
 int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,
