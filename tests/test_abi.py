@@ -228,3 +228,24 @@ def test_prefill_rejects_bad_arguments():
     assert pf(scale=float("inf")) == 2
     assert pf(pp=pool(P=64, D=96, H=2)) != 0  # head dim outside 64 / 128 / 256
     assert pf(B=0) == 0                       # nothing to do
+
+
+def test_plain_c_program_compiles_and_links_against_the_library(tmp_path):
+    # the header is plain C (C99, no C++): tests/abi_step.c, a decode loop that
+    # includes only include/nk.h and the CUDA runtime header, builds with the
+    # host C compiler and links against libnk.so with no unresolved symbol
+    import shutil
+    import subprocess
+
+    from quantized_paged_kv_cache_gb300 import _build
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    nk.lib()  # builds libnk.so when it is missing
+    cuda = os.path.dirname(os.path.dirname(_build.nvcc()))
+    exe = str(tmp_path / "abi_step")
+    subprocess.run([cc, "-std=c99", "-D_POSIX_C_SOURCE=199309L", "-O1", "-Wall", "-Wextra", "-Werror", "-o", exe,
+                    os.path.join(ROOT, "tests", "abi_step.c"), "-I", _build.INCLUDE,
+                    "-I", os.path.join(cuda, "include"), "-L", os.path.dirname(_build.LIB), "-lnk",
+                    "-L", os.path.join(cuda, "lib64"), "-lcudart", "-Wl,--no-undefined"], check=True)
+    assert os.path.getsize(exe) > 0
