@@ -189,9 +189,13 @@ size_t nk_decode_workspace_bytes(int32_t B, int32_t T, int32_t num_q_heads, int3
  * default split one sequence beyond about 1.2 million keys), the split
  * kernel runs an instance that folds its fp32 accumulators every 128 pages
  * (about 2% slower), so that coarse splits keep the accuracy of fine ones.
- * The mma.sync shapes have no such instance: their error also grows with the
- * pages one CTA runs (relative L2 7e-4 against the oracle at 4,096 pages of
- * one kv-head per CTA, T = 1), and runs beyond that were not measured.
+ * The mma.sync shapes (every other tensor-core shape, and the last chunk of
+ * a chunked verify when it has too few rows for tcgen05) have no such
+ * instance, and their error grows with the keys one CTA runs: a num_ctas
+ * that could give one of their CTAs more than 262,144 keys of one kv-head
+ * (4,096 pages of 64 keys) returns NK_ERR_UNSUPPORTED before anything is
+ * launched. The default split reaches that only beyond about 10 million
+ * keys per sequence; nk_paged_decode_attn_simt has no such limit.
  */
 int nk_paged_decode_attn(const nk_kv_pool* pool, const void* q_dev, const int32_t* block_table_dev,
                          int32_t max_pages_per_seq, const int32_t* ctx_lens_dev, int32_t B, int32_t T,

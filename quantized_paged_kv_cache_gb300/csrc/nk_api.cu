@@ -49,6 +49,11 @@ int sm_count() {
   return n;
 }
 
+// The longest run of one kv-head's keys a CTA of the mma.sync decode kernels
+// may take: 4,096 pages of 64 keys measured 4.4e-4 to 7.0e-4 relative L2
+// against the oracle (16,384 pages: 1.18e-3, past the 1e-3 tolerance).
+constexpr int64_t kMaxMmaRunKeys = 262144;
+
 int64_t max_items(int32_t B, int32_t Hkv, int32_t max_ctx, int32_t P) {
   return (int64_t)B * Hkv * ((max_ctx + P - 1) / P);
 }
@@ -146,6 +151,21 @@ int prepare_decode(const nk_kv_pool* pool, const void* q, const int32_t* bt, int
                      : path == Path::kRk8v4 ? decode_rk8v4_ctas_per_sm(D, G)
                      : (simt ? decode_simt_ctas_per_sm(D, G) : decode_mma_ctas_per_sm(D, T, G));
   const int32_t n = num_ctas > 0 ? num_ctas : default_ctas(B, Hkv, max_ctx, P, per_sm);
+  // The fp32 sums of mma.sync are not rounded to nearest, and their error
+  // grows with the keys of one kv-head that a CTA runs through its
+  // accumulators. The tcgen05 kernel folds them (its FOLD instance); the
+  // mma.sync kernels do not, so a split that would give one of their CTAs
+  // more than kMaxMmaRunKeys keys of one kv-head is refused. A chunked verify
+  // runs its last chunk (fewer columns) on the mma.sync kernel when that
+  // chunk has too few rows for the tcgen05 one.
+  if (!simt || rk_tc) {
+    const int Tl = T - (T - 1) / Tc * Tc;  // columns of the last chunk
+    const bool mma_kernel =
+        rk_tc || !decode_tc_supported(fmt, D, Tc, G, P) || !decode_tc_supported(fmt, D, Tl, G, P);
+    const int64_t unit = ((int64_t)max_ctx + P - 1) / P;
+    const int64_t per_cta = (max_items(B, Hkv, max_ctx, P) + n - 1) / n;
+    if (mma_kernel && (per_cta < unit ? per_cta : unit) * P > kMaxMmaRunKeys) return NK_ERR_UNSUPPORTED;
+  }
   const size_t need = nk_decode_workspace_bytes(B, T, Hq, Hkv, D, n);
   if (need > 0 && (!workspace || workspace_bytes < need)) return NK_ERR_WORKSPACE;
   if (workspace && !aligned(workspace, 16)) return NK_ERR_WORKSPACE;

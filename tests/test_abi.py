@@ -88,6 +88,16 @@ def test_decode_rejects_bad_arguments():
     assert decode(pool(), B=2000) == 3                         # beyond the batch limit
     assert decode(pool(), B=1025) == 3                         # one past it (1,024 sequences)
     assert decode(pool(P=256, D=256), max_pages=1) == 3        # a 256-key page of head_dim 256: no two-stage ring
+    # a split giving one mma.sync CTA more than 262,144 keys of one kv-head
+    # (T = 1 at G = 6: the mma.sync kernel; 4 CTAs over a 2^20-key sequence)
+    L = nk.lib()
+    big = pool(num_pages=1 << 14, P=64, H=4, D=256)
+    assert L.nk_paged_decode_attn(ctypes.byref(big), FAKE, FAKE, 1 << 14, FAKE, 1, 1, 24, 0.0625, 1 << 20, 4,
+                                  FAKE, 1 << 40, FAKE, None, None) == 3
+    # the same split for a verify whose last column chunk runs on mma.sync
+    # (T = 13 at G = 6: chunks of 4, 4, 4 and 1 columns)
+    assert L.nk_paged_decode_attn(ctypes.byref(big), FAKE, FAKE, 1 << 14, FAKE, 1, 13, 24, 0.0625, 1 << 20, 4,
+                                  FAKE, 1 << 40, FAKE, None, None) == 3
     assert decode(pool(), B=0) == 0                            # nothing to do
     assert E.lib().nk_paged_decode_attn_simt(ctypes.byref(pool()), FAKE, FAKE, 4, FAKE, 1, 1, 16, 0.1, 64, 0,
                                              FAKE, 1 << 30, FAKE, None, None) == 3  # G > 8 on CUDA cores
